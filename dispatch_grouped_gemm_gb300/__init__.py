@@ -1,0 +1,327 @@
+"""GB300 (sm_103a) fused MoE-FFN: Python binding of libhmm.so.
+
+The functions ``hmm_*`` mirror the C entry points of ``include/hmm.h`` one to
+one and only marshal arguments (torch tensors -> device pointers and sizes,
+the current CUDA stream).  Every step of the computation runs in the CUDA
+kernels of the library; there is no Python or CPU fallback: if ``libhmm.so``
+is missing, every call raises.
+
+``moe_ffn(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight)`` is
+the autograd entry point (forward saves what the backward needs, backward
+returns one gradient per public argument and None for topk_ids), following
+the HyperMegaMoE API (§3.1) and its DFunction semantics (§3.2).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+__all__ = [
+    "HmmError", "HmmShape", "hmm_create", "hmm_destroy", "hmm_set_option",
+    "hmm_workspace_size", "hmm_route", "hmm_forward", "hmm_backward", "hmm_status",
+    "hmm_error_string", "Context", "moe_ffn", "library_path", "load_library",
+    "HMM_OPT_VALIDATE", "HMM_OPT_WAIT_BUDGET_NS", "HMM_OPT_INJECT_SKIP_READY",
+    "HMM_DTYPE_BF16", "HMM_DTYPE_F32", "HMM_STATUS_EXPERT_ID", "HMM_STATUS_TIMEOUT",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_HERE)
+_LIB_PATH = os.path.join(_HERE, "libhmm.so")
+_HEADER = os.path.join(_ROOT, "include", "hmm.h")
+
+
+def _header_constants():
+    consts = {}
+    with open(_HEADER) as f:
+        for m in re.finditer(r"#define\s+(HMM_\w+)\s+\(?(-?\w+?)u?\)?\s", f.read()):
+            try:
+                consts[m.group(1)] = int(m.group(2), 0)
+            except ValueError:
+                pass
+    return consts
+
+
+_C = _header_constants()
+HMM_OK = _C["HMM_OK"]
+HMM_ERR_TIMEOUT = _C["HMM_ERR_TIMEOUT"]
+HMM_ERR_EXPERT_ID = _C["HMM_ERR_EXPERT_ID"]
+HMM_OPT_VALIDATE = _C["HMM_OPT_VALIDATE"]
+HMM_OPT_WAIT_BUDGET_NS = _C["HMM_OPT_WAIT_BUDGET_NS"]
+HMM_OPT_INJECT_SKIP_READY = _C["HMM_OPT_INJECT_SKIP_READY"]
+HMM_DTYPE_BF16 = _C["HMM_DTYPE_BF16"]
+HMM_DTYPE_F32 = _C["HMM_DTYPE_F32"]
+HMM_STATUS_EXPERT_ID = _C["HMM_STATUS_EXPERT_ID"]
+HMM_STATUS_TIMEOUT = _C["HMM_STATUS_TIMEOUT"]
+
+
+class HmmShape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int64), ("I", ctypes.c_int64),
+                ("E", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("weights_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class HmmError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {hmm_error_string(code)} (code {code})")
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libhmm.so (raises if it was not built: there is no fallback)."""
+    global _lib
+    with _lib_lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing; build it with "
+                "`python -m dispatch_grouped_gemm_gb300.build` (nvcc, sm_103a)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+        sp = ctypes.POINTER(HmmShape)
+        sig = {
+            "hmm_create": [ctypes.POINTER(vp), i32],
+            "hmm_destroy": [vp],
+            "hmm_set_option": [vp, i32, i64],
+            "hmm_workspace_size": [sp, i32, ctypes.POINTER(sz), ctypes.POINTER(sz),
+                                   ctypes.POINTER(sz)],
+            "hmm_route": [vp, sp, vp, vp, vp, vp, vp, vp, sz, vp],
+            "hmm_forward": [vp, sp, vp, vp, vp, vp, vp, vp, vp, sz, vp, sz, vp],
+            "hmm_backward": [vp, sp, vp, vp, vp, vp, vp, sz, vp, vp, vp, vp, vp, sz, vp],
+            "hmm_status": [vp, vp, ctypes.POINTER(i32)],
+        }
+        for name, args in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = i32
+        lib.hmm_error_string.argtypes = [i32]
+        lib.hmm_error_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+# ------------------------------------------------------------ marshalling
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _nbytes(t) -> int:
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, where: str):
+    if rc != HMM_OK:
+        raise HmmError(rc, where)
+
+
+def make_shape(T, H, I, E, K, weights_dtype=HMM_DTYPE_BF16) -> HmmShape:
+    return HmmShape(int(T), int(H), int(I), int(E), int(K), int(weights_dtype), 0)
+
+
+def hmm_error_string(code: int) -> str:
+    return load_library().hmm_error_string(int(code)).decode()
+
+
+def hmm_create(device: int = 0):
+    h = ctypes.c_void_p()
+    _check(load_library().hmm_create(ctypes.byref(h), int(device)), "hmm_create")
+    return h
+
+
+def hmm_destroy(ctx):
+    _check(load_library().hmm_destroy(ctx), "hmm_destroy")
+
+
+def hmm_set_option(ctx, option: int, value: int):
+    _check(load_library().hmm_set_option(ctx, int(option), int(value)), "hmm_set_option")
+
+
+def hmm_workspace_size(shape: HmmShape, training: bool):
+    f, s, b = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load_library().hmm_workspace_size(ctypes.byref(shape), int(bool(training)),
+                                             ctypes.byref(f), ctypes.byref(s), ctypes.byref(b)),
+           "hmm_workspace_size")
+    return f.value, s.value, b.value
+
+
+def hmm_route(ctx, shape, topk_ids, counts, offsets, slot2row, row2slot, workspace, stream=None):
+    rc = load_library().hmm_route(ctx, ctypes.byref(shape), _ptr(topk_ids), _ptr(counts),
+                                  _ptr(offsets), _ptr(slot2row), _ptr(row2slot), _ptr(workspace),
+                                  _nbytes(workspace), _stream(stream))
+    _check(rc, "hmm_route")
+
+
+def hmm_forward(ctx, shape, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight, y,
+                saved, workspace, stream=None):
+    rc = load_library().hmm_forward(ctx, ctypes.byref(shape), _ptr(x), _ptr(topk_ids),
+                                    _ptr(topk_weights), _ptr(up_proj_weight),
+                                    _ptr(down_proj_weight), _ptr(y), _ptr(saved), _nbytes(saved),
+                                    _ptr(workspace), _nbytes(workspace), _stream(stream))
+    _check(rc, "hmm_forward")
+
+
+def hmm_backward(ctx, shape, dy, topk_weights, up_proj_weight, down_proj_weight, saved, dx,
+                 d_up_proj_weight, d_down_proj_weight, d_topk_weights, workspace, stream=None):
+    rc = load_library().hmm_backward(ctx, ctypes.byref(shape), _ptr(dy), _ptr(topk_weights),
+                                     _ptr(up_proj_weight), _ptr(down_proj_weight), _ptr(saved),
+                                     _nbytes(saved), _ptr(dx), _ptr(d_up_proj_weight),
+                                     _ptr(d_down_proj_weight), _ptr(d_topk_weights),
+                                     _ptr(workspace), _nbytes(workspace), _stream(stream))
+    _check(rc, "hmm_backward")
+
+
+def hmm_status(ctx, stream=None):
+    """Synchronise the stream, read and clear the device status word.
+    Returns (return code, HMM_STATUS_* bits) without raising."""
+    bits = ctypes.c_int(0)
+    rc = load_library().hmm_status(ctx, _stream(stream), ctypes.byref(bits))
+    return rc, bits.value
+
+
+# ------------------------------------------------------------ torch layer
+_WDTYPES = {torch.bfloat16: HMM_DTYPE_BF16, torch.float32: HMM_DTYPE_F32}
+
+
+def _u8(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+class Context:
+    """A library context on one device plus shape checks of torch arguments."""
+
+    _cache: dict = {}
+    _cache_lock = threading.Lock()
+
+    def __init__(self, device=None):
+        dev = torch.device("cuda", torch.cuda.current_device() if device is None else
+                           torch.device(device).index or 0)
+        self.device = dev
+        self.handle = hmm_create(dev.index)
+
+    def close(self):
+        if self.handle is not None:
+            hmm_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @classmethod
+    def for_device(cls, device) -> "Context":
+        idx = device.index if device.index is not None else torch.cuda.current_device()
+        with cls._cache_lock:
+            c = cls._cache.get(idx)
+            if c is None:
+                c = cls._cache[idx] = cls(torch.device("cuda", idx))
+            return c
+
+    def set_option(self, option: int, value: int):
+        hmm_set_option(self.handle, option, value)
+
+    @staticmethod
+    def shape_of(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight) -> HmmShape:
+        if x.dim() != 2 or topk_ids.dim() != 2 or up_proj_weight.dim() != 3:
+            raise ValueError("x [T,H], topk_ids [T,K], up_proj_weight [E,H,2I] expected")
+        T, H = x.shape
+        E, H1, I2 = up_proj_weight.shape
+        if H1 != H or I2 % 2:
+            raise ValueError(f"up_proj_weight {tuple(up_proj_weight.shape)} does not match x {tuple(x.shape)}")
+        I = I2 // 2
+        if tuple(down_proj_weight.shape) != (E, I, H):
+            raise ValueError(f"down_proj_weight must be {(E, I, H)}, got {tuple(down_proj_weight.shape)}")
+        if topk_ids.shape[0] != T or tuple(topk_weights.shape) != tuple(topk_ids.shape):
+            raise ValueError("topk_ids / topk_weights must both be [T, K]")
+        if x.dtype != torch.bfloat16 or up_proj_weight.dtype != torch.bfloat16 or \
+                down_proj_weight.dtype != torch.bfloat16:
+            raise TypeError("x, up_proj_weight and down_proj_weight must be bfloat16")
+        if topk_ids.dtype != torch.int32:
+            raise TypeError("topk_ids must be int32")
+        if topk_weights.dtype not in _WDTYPES:
+            raise TypeError("topk_weights must be bfloat16 or float32")
+        for t in (x, topk_ids, topk_weights, up_proj_weight, down_proj_weight):
+            if not t.is_cuda or not t.is_contiguous():
+                raise ValueError("all arguments must be contiguous CUDA tensors")
+        return make_shape(T, H, I, E, topk_ids.shape[1], _WDTYPES[topk_weights.dtype])
+
+    def forward(self, x, topk_ids, topk_weights, W1, W2, training: bool, stream=None):
+        shape = self.shape_of(x, topk_ids, topk_weights, W1, W2)
+        fwd, sv, _ = hmm_workspace_size(shape, training)
+        y = torch.empty_like(x)
+        ws = _u8(fwd, x.device)
+        saved = _u8(sv, x.device) if training else None
+        hmm_forward(self.handle, shape, x, topk_ids, topk_weights, W1, W2, y, saved, ws, stream)
+        return y, saved
+
+    def backward(self, dy, x, topk_ids, topk_weights, W1, W2, saved, need=(True, True, True, True),
+                 stream=None):
+        shape = self.shape_of(x, topk_ids, topk_weights, W1, W2)
+        _, _, bwd = hmm_workspace_size(shape, True)
+        dy = dy.contiguous()
+        if dy.dtype != torch.bfloat16 or tuple(dy.shape) != tuple(x.shape):
+            raise ValueError("dy must be bfloat16 with the shape of x")
+        dx = torch.empty_like(x) if need[0] else None
+        dW1 = torch.empty_like(W1) if need[1] else None
+        dW2 = torch.empty_like(W2) if need[2] else None
+        dw = torch.empty_like(topk_weights) if need[3] else None
+        ws = _u8(bwd, x.device)
+        hmm_backward(self.handle, shape, dy, topk_weights, W1, W2, saved, dx, dW1, dW2, dw, ws,
+                     stream)
+        return dx, dW1, dW2, dw
+
+
+class _MoEFFN(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, topk_ids, topk_weights, W1, W2):
+        c = Context.for_device(x.device)
+        y, saved = c.forward(x, topk_ids, topk_weights, W1, W2, training=True)
+        ctx.save_for_backward(x, topk_ids, topk_weights, W1, W2, saved)
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        x, topk_ids, topk_weights, W1, W2, saved = ctx.saved_tensors
+        need = (ctx.needs_input_grad[0], ctx.needs_input_grad[3], ctx.needs_input_grad[4],
+                ctx.needs_input_grad[2])
+        c = Context.for_device(x.device)
+        dx, dW1, dW2, dw = c.backward(dy, x, topk_ids, topk_weights, W1, W2, saved, need)
+        return dx, None, dw, dW1, dW2
+
+
+def moe_ffn(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight):
+    """y[T,H] = sum_k topk_weights[t,k] * FFN_{topk_ids[t,k]}(x[t]) with SwiGLU
+    experts (gate = first I columns of up_proj's 2I outputs).  Differentiable
+    in x, topk_weights and both weight tensors; topk_ids is not."""
+    if not (torch.is_grad_enabled() and any(
+            t.requires_grad for t in (x, topk_weights, up_proj_weight, down_proj_weight))):
+        c = Context.for_device(x.device)
+        y, _ = c.forward(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight,
+                         training=False)
+        return y
+    return _MoEFFN.apply(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight)

@@ -1,0 +1,431 @@
+// hmm_api.cu -- the C ABI of include/hmm.h: host-side validation, buffer
+// planning and the launch sequence of the forward and backward.
+//
+// [HyperMegaMoE §2.3 / §10] the operator offers a workspace query plus an
+// execute call for the forward and for the backward; [§3.3] routing offsets,
+// counters, tiling and buffers are internal; [§4.2] bad shapes, dtypes,
+// layouts and capacities are rejected at the host boundary before any
+// device work; [§5.3] buffer capacity and workspace size are computed and
+// checked on the host, and per-call event state is reset so that repeated
+// iterations never see stale counters (the routing kernel and the backward
+// dispatch kernel zero the tickets and ready counters of their call).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "hmm_internal.h"
+
+struct hmm_ctx {
+  int device = -1;
+  int num_sms = 0;
+  unsigned* status = nullptr;  // device status word
+  int validate = 0;
+  uint64_t budget_ns = 2000000000ull;
+  int inject_skip_ready = 0;
+  hmm::EncodeTiledFn encode = nullptr;
+};
+
+namespace hmm {
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int make_plan(const hmm_shape* s, bool training, Plan* p) {
+  std::memset(p, 0, sizeof(*p));
+  p->T = s->T;
+  p->H = s->H;
+  p->I = s->I;
+  p->E = s->E;
+  p->K = s->K;
+  p->TK = s->T * s->K;
+  p->training = training;
+  const int64_t TK = p->TK;
+  int64_t R = TK == 0 ? 0 : TK + std::min<int64_t>(p->E, TK) * (BM - 1);
+  R = (R + BM - 1) / BM * BM;
+  p->R = R;
+  p->max_mtiles = R / BM;
+  p->nchunks = (TK + RCHUNK - 1) / RCHUNK;
+  p->nt_dswiglu = (p->I + BN - 1) / BN;
+  const size_t A = 256;
+  size_t o = 0;
+  p->off_counts = o;    o = align_up(o + 4 * p->E, A);
+  p->off_offsets = o;   o = align_up(o + 4 * (p->E + 1), A);
+  p->off_poff = o;      o = align_up(o + 4 * (p->E + 1), A);
+  p->off_slot2prow = o; o = align_up(o + 4 * TK, A);
+  p->off_prow2slot = o; o = align_up(o + 4 * R, A);
+  p->meta_bytes = o;
+  o = 0;
+  p->off_chunk_base = o; o = align_up(o + 4 * p->nchunks * p->E, A);
+  p->off_tickets = o;
+  p->off_ready = o + 4 * NUM_TICKETS;  // contiguous with the tickets (zeroed together)
+  o = align_up(p->off_ready + 4 * p->max_mtiles, A);
+  p->ctrl_bytes = o;
+  const size_t xperm = align_up(static_cast<size_t>(R) * p->H * 2, A);
+  const size_t hbytes = align_up(static_cast<size_t>(R) * 2 * p->I * 4, A);
+  const size_t abytes = align_up(static_cast<size_t>(R) * p->I * 2, A);
+  const size_t obytes = align_up(static_cast<size_t>(R) * p->H * 2, A);
+  if (training) {
+    p->sv_meta = 0;
+    p->sv_xperm = p->meta_bytes;
+    p->sv_h = p->sv_xperm + xperm;
+    p->saved_bytes = p->sv_h + hbytes;
+    p->fw_ctrl = 0;
+    p->fw_a = p->ctrl_bytes;
+    p->fw_o = p->fw_a + abytes;
+    p->fwd_ws_bytes = p->fw_o + obytes;
+  } else {
+    p->saved_bytes = 0;
+    p->fw_ctrl = 0;
+    p->fw_meta = p->ctrl_bytes;
+    p->fw_xperm = p->fw_meta + p->meta_bytes;
+    p->fw_a = p->fw_xperm + xperm;
+    p->fw_o = p->fw_a + abytes;
+    p->fwd_ws_bytes = p->fw_o + obytes;
+  }
+  o = 0;
+  p->bw_ctrl = o;    o = align_up(o + p->ctrl_bytes, A);
+  p->bw_dyperm = o;  o = align_up(o + static_cast<size_t>(R) * p->H * 2, A);
+  p->bw_wperm = o;   o = align_up(o + static_cast<size_t>(R) * 4, A);
+  p->bw_dh = o;      o = align_up(o + static_cast<size_t>(R) * 2 * p->I * 2, A);
+  p->bw_wa = o;      o = align_up(o + static_cast<size_t>(R) * p->I * 2, A);
+  p->bw_dxperm = o;  o = align_up(o + static_cast<size_t>(R) * p->H * 2, A);
+  p->bw_dwp = o;     o = align_up(o + static_cast<size_t>(R) * p->nt_dswiglu * 4, A);
+  p->bwd_ws_bytes = o;
+  return HMM_OK;
+}
+
+MetaPtrs meta_at(const Plan& p, void* base) {
+  uint8_t* b = static_cast<uint8_t*>(base);
+  MetaPtrs m;
+  m.counts = reinterpret_cast<int32_t*>(b + p.off_counts);
+  m.offsets = reinterpret_cast<int32_t*>(b + p.off_offsets);
+  m.poff = reinterpret_cast<int32_t*>(b + p.off_poff);
+  m.slot2prow = reinterpret_cast<int32_t*>(b + p.off_slot2prow);
+  m.prow2slot = reinterpret_cast<int32_t*>(b + p.off_prow2slot);
+  return m;
+}
+
+CtrlPtrs ctrl_at(const Plan& p, void* base) {
+  uint8_t* b = static_cast<uint8_t*>(base);
+  CtrlPtrs c;
+  c.chunk_base = reinterpret_cast<int32_t*>(b + p.off_chunk_base);
+  c.tickets = reinterpret_cast<int32_t*>(b + p.off_tickets);
+  c.ready = reinterpret_cast<int32_t*>(b + p.off_ready);
+  return c;
+}
+
+}  // namespace hmm
+
+using namespace hmm;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(const hmm_shape* s) {
+  if (!s) return HMM_ERR_ARG;
+  if (s->reserved != 0) return HMM_ERR_ARG;
+  if (s->weights_dtype != HMM_DTYPE_BF16 && s->weights_dtype != HMM_DTYPE_F32)
+    return HMM_ERR_DTYPE;
+  if (s->T < 0 || s->H <= 0 || s->I <= 0 || s->E <= 0 || s->K <= 0) return HMM_ERR_SHAPE;
+  if (s->E > MAX_E || s->K > 32) return HMM_ERR_SHAPE;
+  if (s->H > (1 << 20) || s->I > (1 << 20) || s->T > (int64_t(1) << 31)) return HMM_ERR_SHAPE;
+  if (s->H % 8 != 0 || s->I % 8 != 0) return HMM_ERR_LAYOUT;
+  const int64_t TK = s->T * s->K;
+  const int64_t R = TK + std::min<int64_t>(s->E, TK) * (BM - 1) + BM;
+  if (R >= (int64_t(1) << 31) - 1) return HMM_ERR_SHAPE;
+  return HMM_OK;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) return;
+    ok = prev == dev || cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (ok && prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+GemmEnv env_of(hmm_ctx* ctx, cudaStream_t st) {
+  GemmEnv e;
+  e.encode = ctx->encode;
+  e.num_sms = ctx->num_sms;
+  e.status = ctx->status;
+  e.budget_ns = ctx->budget_ns;
+  e.stream = st;
+  return e;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? HMM_OK : HMM_ERR_CUDA; }
+
+int read_route_error(hmm_ctx* ctx, cudaStream_t st) {
+  unsigned v = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return HMM_ERR_CUDA;
+  if (cudaMemcpy(&v, ctx->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return HMM_ERR_CUDA;
+  if (v & HMM_STATUS_EXPERT_ID) {
+    const unsigned keep = v & ~HMM_STATUS_EXPERT_ID;
+    if (cudaMemcpy(ctx->status, &keep, sizeof keep, cudaMemcpyHostToDevice) != cudaSuccess)
+      return HMM_ERR_CUDA;
+    return HMM_ERR_EXPERT_ID;
+  }
+  return HMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int hmm_create(hmm_ctx** out, int device) {
+  if (!out) return HMM_ERR_ARG;
+  *out = nullptr;
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || device < 0 || device >= n) return HMM_ERR_DEVICE;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return HMM_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return HMM_ERR_DEVICE;
+  DeviceGuard g(device);
+  if (!g.ok) return HMM_ERR_CUDA;
+  hmm_ctx* c = new hmm_ctx();
+  c->device = device;
+  c->num_sms = prop.multiProcessorCount;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn) {
+    delete c;
+    return HMM_ERR_CUDA;
+  }
+  c->encode = reinterpret_cast<EncodeTiledFn>(fn);
+  if (cudaMalloc(&c->status, sizeof(unsigned)) != cudaSuccess) {
+    delete c;
+    return HMM_ERR_CUDA;
+  }
+  if (cudaMemset(c->status, 0, sizeof(unsigned)) != cudaSuccess) {
+    cudaFree(c->status);
+    delete c;
+    return HMM_ERR_CUDA;
+  }
+  *out = c;
+  return HMM_OK;
+}
+
+int hmm_destroy(hmm_ctx* ctx) {
+  if (!ctx) return HMM_OK;
+  {
+    DeviceGuard g(ctx->device);
+    if (ctx->status) cudaFree(ctx->status);
+  }
+  delete ctx;
+  return HMM_OK;
+}
+
+int hmm_set_option(hmm_ctx* ctx, int option, int64_t value) {
+  if (!ctx) return HMM_ERR_ARG;
+  switch (option) {
+    case HMM_OPT_VALIDATE:
+      ctx->validate = value != 0;
+      return HMM_OK;
+    case HMM_OPT_WAIT_BUDGET_NS:
+      if (value < 1000000 || value > 60000000000ll) return HMM_ERR_ARG;
+      ctx->budget_ns = static_cast<uint64_t>(value);
+      return HMM_OK;
+    case HMM_OPT_INJECT_SKIP_READY:
+      ctx->inject_skip_ready = value != 0;
+      return HMM_OK;
+    default:
+      return HMM_ERR_ARG;
+  }
+}
+
+int hmm_workspace_size(const hmm_shape* shape, int training, size_t* fwd, size_t* saved,
+                       size_t* bwd) {
+  const int rc = check_shape(shape);
+  if (rc != HMM_OK) return rc;
+  Plan p;
+  make_plan(shape, training != 0, &p);
+  if (fwd) *fwd = p.fwd_ws_bytes;
+  if (saved) *saved = p.saved_bytes;
+  if (bwd) *bwd = training ? p.bwd_ws_bytes : 0;
+  return HMM_OK;
+}
+
+int hmm_route(hmm_ctx* ctx, const hmm_shape* shape, const int32_t* topk_ids, int32_t* counts,
+              int32_t* offsets, int32_t* slot2row, int32_t* row2slot, void* workspace,
+              size_t workspace_bytes, void* stream) {
+  if (!ctx) return HMM_ERR_ARG;
+  int rc = check_shape(shape);
+  if (rc != HMM_OK) return rc;
+  Plan p;
+  make_plan(shape, false, &p);
+  if (!counts || !offsets || (p.TK > 0 && (!topk_ids || !slot2row || !row2slot)) || !workspace)
+    return HMM_ERR_ARG;
+  if (!aligned16(workspace)) return HMM_ERR_LAYOUT;
+  if (workspace_bytes < p.ctrl_bytes + p.meta_bytes) return HMM_ERR_CAPACITY;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return HMM_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CtrlPtrs c = ctrl_at(p, workspace);
+  MetaPtrs m = meta_at(p, static_cast<uint8_t*>(workspace) + p.ctrl_bytes);
+  rc = cuda_rc(launch_route(p, topk_ids, m, c, slot2row, row2slot, ctx->status, st));
+  if (rc != HMM_OK) return rc;
+  rc = cuda_rc(cudaMemcpyAsync(counts, m.counts, 4 * p.E, cudaMemcpyDeviceToDevice, st));
+  if (rc != HMM_OK) return rc;
+  rc = cuda_rc(cudaMemcpyAsync(offsets, m.offsets, 4 * (p.E + 1), cudaMemcpyDeviceToDevice, st));
+  if (rc != HMM_OK) return rc;
+  if (ctx->validate) return read_route_error(ctx, st);
+  return HMM_OK;
+}
+
+int hmm_forward(hmm_ctx* ctx, const hmm_shape* shape, const void* x, const int32_t* topk_ids,
+                const void* topk_weights, const void* up_proj_weight,
+                const void* down_proj_weight, void* y, void* saved, size_t saved_bytes,
+                void* workspace, size_t workspace_bytes, void* stream) {
+  if (!ctx) return HMM_ERR_ARG;
+  int rc = check_shape(shape);
+  if (rc != HMM_OK) return rc;
+  const bool training = saved != nullptr;
+  Plan p;
+  make_plan(shape, training, &p);
+  if (p.TK > 0 && (!x || !topk_ids || !topk_weights || !up_proj_weight || !down_proj_weight ||
+                   !y || !workspace))
+    return HMM_ERR_ARG;
+  if (p.TK == 0) return HMM_OK;
+  for (const void* ptr : {x, static_cast<const void*>(topk_ids), topk_weights, up_proj_weight,
+                          down_proj_weight, static_cast<const void*>(y),
+                          static_cast<const void*>(workspace)})
+    if (!aligned16(ptr)) return HMM_ERR_LAYOUT;
+  if (training && !aligned16(saved)) return HMM_ERR_LAYOUT;
+  if (workspace_bytes < p.fwd_ws_bytes) return HMM_ERR_CAPACITY;
+  if (training && saved_bytes < p.saved_bytes) return HMM_ERR_CAPACITY;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return HMM_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* sv = static_cast<uint8_t*>(saved);
+  CtrlPtrs c = ctrl_at(p, ws + p.fw_ctrl);
+  MetaPtrs m = meta_at(p, training ? sv + p.sv_meta : ws + p.fw_meta);
+  void* x_perm = training ? sv + p.sv_xperm : ws + p.fw_xperm;
+  float* h32 = training ? reinterpret_cast<float*>(sv + p.sv_h) : nullptr;
+  void* a = ws + p.fw_a;
+  void* o = ws + p.fw_o;
+
+  rc = cuda_rc(launch_route(p, topk_ids, m, c, nullptr, nullptr, ctx->status, st));
+  if (rc != HMM_OK) return rc;
+  if (ctx->validate) {
+    rc = read_route_error(ctx, st);
+    if (rc != HMM_OK) return rc;
+  }
+  rc = cuda_rc(launch_dispatch_x(p, x, m, x_perm, st));
+  if (rc != HMM_OK) return rc;
+  const bool inject = ctx->inject_skip_ready != 0;
+  ctx->inject_skip_ready = 0;
+  rc = launch_forward_gemms(env_of(ctx, st), p, m, c, x_perm, up_proj_weight, down_proj_weight, a,
+                            h32, o, inject);
+  if (rc != HMM_OK) return rc;
+  return cuda_rc(launch_combine_y(p, o, topk_weights, shape->weights_dtype, m, y, st));
+}
+
+int hmm_backward(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const void* topk_weights,
+                 const void* up_proj_weight, const void* down_proj_weight, const void* saved,
+                 size_t saved_bytes, void* dx, void* d_up_proj_weight, void* d_down_proj_weight,
+                 void* d_topk_weights, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!ctx) return HMM_ERR_ARG;
+  int rc = check_shape(shape);
+  if (rc != HMM_OK) return rc;
+  Plan p;
+  make_plan(shape, true, &p);
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return HMM_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p.TK == 0) {
+    // no token: every weight gradient is exactly zero
+    if (d_up_proj_weight) {
+      if (!aligned16(d_up_proj_weight)) return HMM_ERR_LAYOUT;
+      rc = cuda_rc(cudaMemsetAsync(d_up_proj_weight, 0, 2 * p.E * p.H * 2 * p.I, st));
+      if (rc != HMM_OK) return rc;
+    }
+    if (d_down_proj_weight) {
+      if (!aligned16(d_down_proj_weight)) return HMM_ERR_LAYOUT;
+      rc = cuda_rc(cudaMemsetAsync(d_down_proj_weight, 0, 2 * p.E * p.I * p.H, st));
+    }
+    return rc;
+  }
+  if (!dy || !topk_weights || !up_proj_weight || !down_proj_weight || !saved || !workspace)
+    return HMM_ERR_ARG;
+  for (const void* ptr : {dy, topk_weights, up_proj_weight, down_proj_weight, saved,
+                          static_cast<const void*>(workspace)})
+    if (!aligned16(ptr)) return HMM_ERR_LAYOUT;
+  for (const void* ptr : {static_cast<const void*>(dx), static_cast<const void*>(d_up_proj_weight),
+                          static_cast<const void*>(d_down_proj_weight),
+                          static_cast<const void*>(d_topk_weights)})
+    if (ptr && !aligned16(ptr)) return HMM_ERR_LAYOUT;
+  if (saved_bytes < p.saved_bytes) return HMM_ERR_CAPACITY;
+  if (workspace_bytes < p.bwd_ws_bytes) return HMM_ERR_CAPACITY;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* sv = const_cast<uint8_t*>(static_cast<const uint8_t*>(saved));
+  MetaPtrs m = meta_at(p, sv + p.sv_meta);
+  const void* x_perm = sv + p.sv_xperm;
+  const float* h32 = reinterpret_cast<const float*>(sv + p.sv_h);
+  CtrlPtrs c = ctrl_at(p, ws + p.bw_ctrl);
+  void* dy_perm = ws + p.bw_dyperm;
+  float* wperm = reinterpret_cast<float*>(ws + p.bw_wperm);
+  void* dH = ws + p.bw_dh;
+  void* wa = ws + p.bw_wa;
+  void* dx_perm = ws + p.bw_dxperm;
+  float* dwp = reinterpret_cast<float*>(ws + p.bw_dwp);
+  const GemmEnv env = env_of(ctx, st);
+
+  rc = cuda_rc(
+      launch_dispatch_dy(p, dy, topk_weights, shape->weights_dtype, m, c, dy_perm, wperm, st));
+  if (rc != HMM_OK) return rc;
+  rc = launch_backward_data_gemms(env, p, m, c, dy_perm, wperm, h32, up_proj_weight,
+                                  down_proj_weight, dH, wa, dwp, dx_perm);
+  if (rc != HMM_OK) return rc;
+  rc = launch_backward_weight_gemms(env, p, m, c, x_perm, dy_perm, dH, wa, d_up_proj_weight,
+                                    d_down_proj_weight);
+  if (rc != HMM_OK) return rc;
+  if (dx || d_topk_weights)
+    rc = cuda_rc(launch_combine_dx(p, dx_perm, dwp, m, dx, d_topk_weights, shape->weights_dtype,
+                                   st));
+  return rc;
+}
+
+int hmm_status(hmm_ctx* ctx, void* stream, int* device_error) {
+  if (!ctx) return HMM_ERR_ARG;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return HMM_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return HMM_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, ctx->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return HMM_ERR_CUDA;
+  if (cudaMemset(ctx->status, 0, sizeof v) != cudaSuccess) return HMM_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return HMM_ERR_CUDA;
+  if (device_error) *device_error = static_cast<int>(v);
+  if (v & HMM_STATUS_TIMEOUT) return HMM_ERR_TIMEOUT;
+  if (v & HMM_STATUS_EXPERT_ID) return HMM_ERR_EXPERT_ID;
+  return HMM_OK;
+}
+
+const char* hmm_error_string(int code) {
+  switch (code) {
+    case HMM_OK: return "ok";
+    case HMM_ERR_ARG: return "invalid argument (null pointer, option or context)";
+    case HMM_ERR_SHAPE: return "shape out of the supported range or inconsistent";
+    case HMM_ERR_DTYPE: return "unsupported dtype";
+    case HMM_ERR_LAYOUT: return "misaligned pointer, or H / I not a multiple of 8";
+    case HMM_ERR_CAPACITY: return "workspace or saved buffer too small";
+    case HMM_ERR_EXPERT_ID: return "a topk_id is outside [0, E)";
+    case HMM_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case HMM_ERR_CUDA: return "a CUDA call failed";
+    case HMM_ERR_DEVICE: return "no such device, or the device is not sm_103";
+    default: return "unknown error code";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,112 @@
+// hmm_internal.h -- declarations shared by the library's translation units
+// (not part of the public ABI; the public header is include/hmm.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "hmm.h"
+
+namespace hmm {
+
+// Rows of one GEMM tile (tcgen05 M).  Every expert's rows start on a multiple
+// of BM in the permuted ("padded") layout, so an M-tile never spans experts;
+// padding rows are zero.
+constexpr int BM = 128;
+constexpr int BN = 256;   // tcgen05 N per tile
+constexpr int BK = 64;    // K per pipeline stage (one 128-byte swizzle row of bf16)
+constexpr int RCHUNK = 1024;  // slots per routing warp-chunk
+constexpr int RWARPS = 8;     // warps per routing block
+constexpr int MAX_E = 1024;   // experts supported (routing keeps per-expert counters in smem)
+constexpr int NUM_TICKETS = 8;
+
+// Device-side metadata of one call (lives in `saved` when training, else in
+// the forward workspace).  All int32.
+struct MetaPtrs {
+  int32_t* counts;     // [E]
+  int32_t* offsets;    // [E+1]  unpadded exclusive prefix of counts
+  int32_t* poff;       // [E+1]  padded prefix: expert e owns rows [poff[e], poff[e+1])
+  int32_t* slot2prow;  // [TK]   padded row of slot s (-1 for an invalid id)
+  int32_t* prow2slot;  // [R]    slot of a padded row (-1 for padding)
+};
+
+// Scratch counters of one call.
+struct CtrlPtrs {
+  int32_t* chunk_base;  // [nchunks * E]
+  int32_t* tickets;     // [NUM_TICKETS]
+  int32_t* ready;       // [max_mtiles]
+};
+
+struct Plan {
+  int64_t T, H, I, E, K, TK;
+  int64_t R;            // capacity of the padded row space
+  int64_t max_mtiles;   // R / BM
+  int64_t nchunks;      // routing warp-chunks
+  int64_t nt_dswiglu;   // N tiles of the act_grad GEMM (per-row d_w partials)
+  bool training;
+  // byte offsets inside the buffers
+  size_t meta_bytes;
+  size_t off_counts, off_offsets, off_poff, off_slot2prow, off_prow2slot;  // inside meta
+  size_t ctrl_bytes;
+  size_t off_chunk_base, off_tickets, off_ready;                           // inside ctrl
+  // forward: saved = [meta | x_perm | h]      (training)
+  //          workspace = [ctrl | a | o]       (training)
+  //          workspace = [ctrl | meta | x_perm | a | o]   (inference)
+  size_t saved_bytes, fwd_ws_bytes;
+  size_t sv_meta, sv_xperm, sv_h;
+  size_t fw_ctrl, fw_meta, fw_xperm, fw_a, fw_o;
+  // backward workspace = [ctrl | dy_perm | wperm | dH | wa | dX_perm | dwp]
+  size_t bwd_ws_bytes;
+  size_t bw_ctrl, bw_dyperm, bw_wperm, bw_dh, bw_wa, bw_dxperm, bw_dwp;
+};
+
+int make_plan(const hmm_shape* s, bool training, Plan* p);
+MetaPtrs meta_at(const Plan& p, void* base);
+CtrlPtrs ctrl_at(const Plan& p, void* base);
+
+// ------------------------------------------------------------ kernel launchers
+// Each returns a cudaError_t of its launch.
+cudaError_t launch_route(const Plan& p, const int32_t* ids, MetaPtrs m, CtrlPtrs c,
+                         int32_t* slot2row, int32_t* row2slot, unsigned* status,
+                         cudaStream_t st);
+cudaError_t launch_dispatch_x(const Plan& p, const void* x, MetaPtrs m, void* x_perm,
+                              cudaStream_t st);
+cudaError_t launch_combine_y(const Plan& p, const void* o, const void* w, int w_dtype, MetaPtrs m,
+                             void* y, cudaStream_t st);
+cudaError_t launch_dispatch_dy(const Plan& p, const void* dy, const void* w, int w_dtype,
+                               MetaPtrs m, CtrlPtrs c, void* dy_perm, float* wperm,
+                               cudaStream_t st);
+cudaError_t launch_combine_dx(const Plan& p, const void* dx_perm, const float* dwp, MetaPtrs m,
+                              void* dx, void* dw, int w_dtype, cudaStream_t st);
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct GemmEnv {
+  EncodeTiledFn encode;
+  int num_sms;
+  unsigned* status;
+  uint64_t budget_ns;
+  cudaStream_t stream;
+};
+
+// forward GMM1(+SwiGLU) and GMM2 in one persistent launch with per-M-tile
+// ready counters.  h32 may be null (inference).
+int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
+                         const void* x_perm, const void* W1, const void* W2, void* a, float* h32,
+                         void* o, bool skip_ready_release);
+// backward act_grad(+SwiGLU grad, d_w partials) and input-grad GEMMs
+int launch_backward_data_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
+                               const void* dy_perm, const float* wperm, const float* h32,
+                               const void* W1, const void* W2, void* dH, void* wa, float* dwp,
+                               void* dx_perm);
+// backward weight-gradient GEMMs dW2 = wa^T dy_perm, dW1 = x_perm^T dH
+int launch_backward_weight_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
+                                 const void* x_perm, const void* dy_perm, const void* dH,
+                                 const void* wa, void* dW1, void* dW2);
+
+}  // namespace hmm

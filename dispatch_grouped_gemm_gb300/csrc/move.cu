@@ -1,0 +1,210 @@
+// move.cu -- the bandwidth-bound steps: Dispatch (permute token rows into
+// expert-contiguous padded order) and Combine (gather each token's K expert
+// rows back and merge them), forward and backward.
+//
+// [HyperMegaMoE §2.1] Dispatch -> ... -> Combine; on one GPU these are a
+// device-side permute and unpermute.  [MoE overlap explainer §6] the combine
+// merges the top-k branches of a token weighted by their gates; here it is a
+// deterministic gather: one warp per token, fp32 sums in fixed k order, a
+// single bf16 rounding, no atomics.
+//
+// All row traffic uses 16-byte vectors (H is a multiple of 8 bf16).
+#include <cuda_bf16.h>
+
+#include "hmm_internal.h"
+
+namespace hmm {
+
+namespace {
+
+__device__ __forceinline__ float ld_weight(const void* w, int64_t i, int dtype) {
+  if (dtype == HMM_DTYPE_F32) return static_cast<const float*>(w)[i];
+  const uint16_t b = static_cast<const uint16_t*>(w)[i];
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ void st_weight(void* w, int64_t i, int dtype, float v) {
+  if (dtype == HMM_DTYPE_F32) {
+    static_cast<float*>(w)[i] = v;
+  } else {
+    static_cast<__nv_bfloat16*>(w)[i] = __float2bfloat16_rn(v);
+  }
+}
+
+__device__ __forceinline__ void acc8(float (&acc)[8], const uint4& v, float s) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    acc[2 * j] = fmaf(s, __uint_as_float(u[j] << 16), acc[2 * j]);
+    acc[2 * j + 1] = fmaf(s, __uint_as_float(u[j] & 0xFFFF0000u), acc[2 * j + 1]);
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&acc)[8]) {
+  uint4 r;
+  uint32_t* u = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+    u[j] = *reinterpret_cast<uint32_t*>(&p);
+  }
+  return r;
+}
+
+constexpr int MOVE_THREADS = 256;
+constexpr int MOVE_WARPS = MOVE_THREADS / 32;
+constexpr int UNROLL = 4;
+
+}  // namespace
+
+// Dispatch: token t's row of src goes to the padded rows of its K slots; the
+// warps past T zero the padding rows of each expert (so every padded row of
+// the GEMM operands is defined).  Optionally also scatters the routing weight
+// of every slot to its padded row (wperm, 0 on padding rows).
+__global__ void __launch_bounds__(MOVE_THREADS) dispatch_rows_kernel(
+    const uint4* __restrict__ src, int64_t T, int64_t K, int64_t H8, MetaPtrs m, int E,
+    uint4* __restrict__ dst, const void* w, int w_dtype, float* wperm, int32_t* zero_ptr,
+    int64_t zero_count) {
+  const int lane = threadIdx.x & 31;
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * MOVE_WARPS + (threadIdx.x >> 5);
+  if (zero_ptr) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * MOVE_THREADS + threadIdx.x;
+         i < zero_count; i += static_cast<int64_t>(gridDim.x) * MOVE_THREADS)
+      zero_ptr[i] = 0;
+  }
+  if (g < T) {
+    int32_t prow_l = -1;
+    if (lane < K) prow_l = m.slot2prow[g * K + lane];
+    if (wperm && lane < K && prow_l >= 0) wperm[prow_l] = ld_weight(w, g * K + lane, w_dtype);
+    const uint4* s = src + g * H8;
+    for (int64_t c0 = lane; c0 < H8; c0 += 32 * UNROLL) {
+      uint4 v[UNROLL];
+#pragma unroll
+      for (int u = 0; u < UNROLL; ++u) {
+        const int64_t c = c0 + 32 * u;
+        if (c < H8) v[u] = s[c];
+      }
+      for (int k = 0; k < K; ++k) {
+        const int32_t prow = __shfl_sync(0xffffffffu, prow_l, k);
+        if (prow < 0) continue;
+        uint4* d = dst + static_cast<int64_t>(prow) * H8;
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+          const int64_t c = c0 + 32 * u;
+          if (c < H8) d[c] = v[u];
+        }
+      }
+    }
+  } else {
+    const int64_t q = g - T;
+    const int64_t e = q / BM;
+    if (e >= E) return;
+    const int32_t row = m.poff[e] + m.counts[e] + static_cast<int32_t>(q % BM);
+    if (row >= m.poff[e + 1]) return;
+    if (wperm && lane == 0) wperm[row] = 0.0f;
+    uint4* d = dst + static_cast<int64_t>(row) * H8;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int64_t c = lane; c < H8; c += 32) d[c] = z;
+  }
+}
+
+// Combine: out[t] = sum_k scale_k * rows[slot2prow[t*K+k]], fp32 in k order,
+// one bf16 rounding.  scale_k = topk_weights[t,k] (forward) or 1 (dX).
+// With dwp != null (backward) lane k also writes
+//   d_topk_weights[t,k] = sum over the act_grad N tiles of the per-row
+//   partial dot products <G_s, a_s> (fixed order).
+template <bool WEIGHTED>
+__global__ void __launch_bounds__(MOVE_THREADS) combine_rows_kernel(
+    const uint4* __restrict__ rows, const void* w, int w_dtype, int64_t T, int64_t K, int64_t H8,
+    const int32_t* __restrict__ slot2prow, uint4* __restrict__ out, const float* dwp,
+    int64_t dwp_ld, void* dw) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * MOVE_WARPS + (threadIdx.x >> 5);
+  if (t >= T) return;
+  int32_t prow_l = -1;
+  float w_l = 0.0f;
+  if (lane < K) {
+    prow_l = slot2prow[t * K + lane];
+    w_l = WEIGHTED ? ld_weight(w, t * K + lane, w_dtype) : 1.0f;
+  }
+  if (dwp && lane < K) {
+    float d = 0.0f;
+    if (prow_l >= 0)
+      for (int64_t j = 0; j < dwp_ld; ++j) d += dwp[static_cast<int64_t>(prow_l) * dwp_ld + j];
+    st_weight(dw, t * K + lane, w_dtype, d);
+  }
+  if (!out) return;
+  for (int64_t c0 = lane; c0 < H8; c0 += 32 * UNROLL) {
+    float acc[UNROLL][8];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[u][j] = 0.0f;
+    for (int k = 0; k < K; ++k) {
+      const int32_t prow = __shfl_sync(0xffffffffu, prow_l, k);
+      const float s = __shfl_sync(0xffffffffu, w_l, k);
+      if (prow < 0) continue;
+      const uint4* r = rows + static_cast<int64_t>(prow) * H8;
+      uint4 v[UNROLL];
+#pragma unroll
+      for (int u = 0; u < UNROLL; ++u) {
+        const int64_t c = c0 + 32 * u;
+        if (c < H8) v[u] = r[c];
+      }
+#pragma unroll
+      for (int u = 0; u < UNROLL; ++u) {
+        const int64_t c = c0 + 32 * u;
+        if (c < H8) acc8(acc[u], v[u], s);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int64_t c = c0 + 32 * u;
+      if (c < H8) out[t * H8 + c] = pack8(acc[u]);
+    }
+  }
+}
+
+static int move_grid(int64_t warps) {
+  return static_cast<int>((warps + MOVE_WARPS - 1) / MOVE_WARPS);
+}
+
+cudaError_t launch_dispatch_x(const Plan& p, const void* x, MetaPtrs m, void* x_perm,
+                              cudaStream_t st) {
+  const int64_t warps = p.T + p.E * BM;
+  dispatch_rows_kernel<<<move_grid(warps), MOVE_THREADS, 0, st>>>(
+      static_cast<const uint4*>(x), p.T, p.K, p.H / 8, m, static_cast<int>(p.E),
+      static_cast<uint4*>(x_perm), nullptr, 0, nullptr, nullptr, 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_dy(const Plan& p, const void* dy, const void* w, int w_dtype,
+                               MetaPtrs m, CtrlPtrs c, void* dy_perm, float* wperm,
+                               cudaStream_t st) {
+  const int64_t warps = p.T + p.E * BM;
+  // also zero the backward launch counters (tickets and ready flags are
+  // contiguous in the control block)
+  const int64_t nzero = NUM_TICKETS + p.max_mtiles;
+  dispatch_rows_kernel<<<move_grid(warps), MOVE_THREADS, 0, st>>>(
+      static_cast<const uint4*>(dy), p.T, p.K, p.H / 8, m, static_cast<int>(p.E),
+      static_cast<uint4*>(dy_perm), w, w_dtype, wperm, c.tickets, nzero);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_y(const Plan& p, const void* o, const void* w, int w_dtype, MetaPtrs m,
+                             void* y, cudaStream_t st) {
+  combine_rows_kernel<true><<<move_grid(p.T), MOVE_THREADS, 0, st>>>(
+      static_cast<const uint4*>(o), w, w_dtype, p.T, p.K, p.H / 8, m.slot2prow,
+      static_cast<uint4*>(y), nullptr, 0, nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_dx(const Plan& p, const void* dx_perm, const float* dwp, MetaPtrs m,
+                              void* dx, void* dw, int w_dtype, cudaStream_t st) {
+  combine_rows_kernel<false><<<move_grid(p.T), MOVE_THREADS, 0, st>>>(
+      static_cast<const uint4*>(dx_perm), nullptr, w_dtype, p.T, p.K, p.H / 8, m.slot2prow,
+      static_cast<uint4*>(dx), dw ? dwp : nullptr, p.nt_dswiglu, dw);
+  return cudaGetLastError();
+}
+
+}  // namespace hmm

@@ -1,0 +1,177 @@
+/*
+ * hmm.h -- C ABI of the GB300 (sm_103a) fused MoE-FFN library (libhmm.so).
+ *
+ * The operation is the single-GPU form of the fused MoE-FFN of the
+ * HyperMegaMoE issue (hyper-parallel #312):
+ *
+ *   forward  [HyperMegaMoE §2.1, §3.1, §4.1]
+ *     Dispatch -> GMM1/up_proj -> SwiGLU -> GMM2/down_proj -> Combine
+ *     y[t] = sum_k topk_weights[t,k] * FFN_{topk_ids[t,k]}(x[t])
+ *     FFN_e(v) = (silu(v . W1[e][:, :I]) * (v . W1[e][:, I:])) . W2[e]
+ *   backward [HyperMegaMoE §2.2]
+ *     dx, d_up_proj_weight, d_down_proj_weight, d_topk_weights
+ *     (topk_ids has no gradient).
+ *
+ * On one GPU "Dispatch" and "Combine" are a device-side permute (token rows
+ * gathered into expert-contiguous order) and unpermute (the K expert rows of
+ * a token gathered back and merged with its routing weights).  There is no
+ * all-to-all and no inter-GPU traffic.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Tensors are dense, row-major (C order), on the device of the context,
+ *   with 16-byte-aligned base addresses.  Shapes (T, H, I, E, K as in
+ *   HyperMegaMoE §3.1):
+ *     x, y, dy, dx              bf16   [T, H]
+ *     topk_ids                  int32  [T, K]   global expert ids in [0, E)
+ *     topk_weights, d_topk_w    bf16 or fp32 [T, K] (hmm_shape.weights_dtype)
+ *     up_proj_weight, d_up      bf16   [E, H, 2I]  columns 0..I-1 = gate,
+ *                                                  I..2I-1 = up
+ *     down_proj_weight, d_down  bf16   [E, I, H]
+ *   H and I must be multiples of 8 (16-byte rows).
+ * - The caller owns every buffer: inputs, outputs, the per-call workspace and
+ *   the "saved" buffer that carries routing metadata and activations from a
+ *   forward to its backward.  Sizes come from hmm_workspace_size().  The
+ *   library never allocates per call; hmm_create() allocates one small
+ *   device status word.
+ * - Every call is asynchronous on `stream` (a cudaStream_t, passed as
+ *   void*).  Inputs must stay valid and unmodified until the stream reaches
+ *   the end of the call.
+ * - Returns HMM_OK (0) or a negative HMM_ERR_* code.  Shape, dtype, layout
+ *   and capacity are checked on the host before anything is launched
+ *   [HyperMegaMoE §4.2: bad input is rejected at the host boundary, not in a
+ *   device kernel].  Conditions only the device can see (an expert id out of
+ *   range, a bounded wait that ran out) set bits of the context's device
+ *   status word, which hmm_status() reads; with HMM_OPT_VALIDATE set,
+ *   hmm_forward() and hmm_route() synchronise after the routing step and
+ *   return HMM_ERR_EXPERT_ID before any GEMM runs.  Outputs are unspecified
+ *   after an error.
+ * - Gradients are written, not accumulated (d_up / d_down of an expert that
+ *   receives no token are written as exact zeros).
+ * - A context may be used from one host thread at a time.  Concurrent calls
+ *   on different streams need distinct workspace and saved buffers.
+ */
+#ifndef HMM_H_
+#define HMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* return codes */
+#define HMM_OK 0
+#define HMM_ERR_ARG (-1)       /* null pointer / bad option / bad context */
+#define HMM_ERR_SHAPE (-2)     /* dimension out of range or inconsistent */
+#define HMM_ERR_DTYPE (-3)     /* unsupported dtype code */
+#define HMM_ERR_LAYOUT (-4)    /* misaligned pointer or H, I not multiples of 8 */
+#define HMM_ERR_CAPACITY (-5)  /* workspace or saved buffer smaller than required */
+#define HMM_ERR_EXPERT_ID (-6) /* a topk_id outside [0, E) (device-detected) */
+#define HMM_ERR_TIMEOUT (-7)   /* a bounded device wait ran out (device-detected) */
+#define HMM_ERR_CUDA (-8)      /* a CUDA runtime/driver call failed */
+#define HMM_ERR_DEVICE (-9)    /* device is not sm_103 / no such device */
+
+/* bits of the device status word (hmm_status) */
+#define HMM_STATUS_EXPERT_ID 1u
+#define HMM_STATUS_TIMEOUT 2u
+
+/* dtype codes */
+#define HMM_DTYPE_BF16 0
+#define HMM_DTYPE_F32 1
+
+typedef struct hmm_ctx hmm_ctx;
+
+typedef struct hmm_shape {
+  int64_t T;             /* tokens (may be 0) */
+  int64_t H;             /* hidden size, multiple of 8 */
+  int64_t I;             /* expert intermediate size, multiple of 8 */
+  int64_t E;             /* experts, >= 1 */
+  int64_t K;             /* experts per token, >= 1 */
+  int32_t weights_dtype; /* HMM_DTYPE_BF16 or HMM_DTYPE_F32 for topk_weights */
+  int32_t reserved;      /* must be 0 */
+} hmm_shape;
+
+/* Create a context bound to CUDA device `device` (must be sm_103).  Allocates
+ * the device status word.  *out is NULL on failure. */
+int hmm_create(hmm_ctx** out, int device);
+
+/* Destroy a context (frees the status word).  NULL is accepted. */
+int hmm_destroy(hmm_ctx* ctx);
+
+/* Context options.
+ *   HMM_OPT_VALIDATE      0/1: hmm_forward/hmm_route synchronise after routing
+ *                         and return HMM_ERR_EXPERT_ID for a bad id (default 0).
+ *   HMM_OPT_WAIT_BUDGET_NS  budget of every bounded device wait, in ns
+ *                         (default 1e9; range 1e6 .. 6e10).
+ *   HMM_OPT_INJECT_SKIP_READY  test-only fault injection on the host side: when
+ *                         1, the next hmm_forward launches its GMM1 tiles
+ *                         without releasing the GMM2 ready counters, so every
+ *                         GMM2 tile's bounded wait runs out and the call
+ *                         reports HMM_STATUS_TIMEOUT.  Cleared after one call. */
+#define HMM_OPT_VALIDATE 1
+#define HMM_OPT_WAIT_BUDGET_NS 2
+#define HMM_OPT_INJECT_SKIP_READY 3
+int hmm_set_option(hmm_ctx* ctx, int option, int64_t value);
+
+/* Buffer sizes in bytes for a shape.  training != 0: the forward keeps its
+ * activations in `saved` for the backward; training == 0: they live in the
+ * forward workspace and *saved_bytes is 0.  Any output pointer may be NULL. */
+int hmm_workspace_size(const hmm_shape* shape, int training,
+                       size_t* fwd_workspace_bytes, size_t* saved_bytes,
+                       size_t* bwd_workspace_bytes);
+
+/* Routing metadata alone [HyperMegaMoE §3.3 offset/size/group list, §4.1
+ * expansion of each token into K slots s = t*K + k; MoE overlap explainer §5:
+ * counts, prefix sums, offsets and the token permutation on the device]:
+ *   counts[e]   number of slots routed to expert e                  int32 [E]
+ *   offsets[e]  exclusive prefix sum of counts, offsets[E] = T*K    int32 [E+1]
+ *   slot2row[s] position of slot s in expert-sorted order, stable
+ *               (ties by ascending s)                               int32 [T*K]
+ *   row2slot[r] inverse permutation                                 int32 [T*K]
+ * workspace: at least the forward workspace size of the same shape.
+ * No host round trip unless HMM_OPT_VALIDATE is set. */
+int hmm_route(hmm_ctx* ctx, const hmm_shape* shape, const int32_t* topk_ids,
+              int32_t* counts, int32_t* offsets, int32_t* slot2row,
+              int32_t* row2slot, void* workspace, size_t workspace_bytes,
+              void* stream);
+
+/* Fused forward [HyperMegaMoE §2.1]: y = Combine(GMM2(SwiGLU(GMM1(Dispatch(x))))).
+ * saved == NULL: inference (the [., 2I] pre-activation is never written to
+ * memory).  Otherwise saved (saved_bytes from hmm_workspace_size with
+ * training=1) receives what hmm_backward needs: routing metadata, permuted x,
+ * gate/up pre-activations, SwiGLU outputs and expert outputs. */
+int hmm_forward(hmm_ctx* ctx, const hmm_shape* shape, const void* x,
+                const int32_t* topk_ids, const void* topk_weights,
+                const void* up_proj_weight, const void* down_proj_weight,
+                void* y, void* saved, size_t saved_bytes, void* workspace,
+                size_t workspace_bytes, void* stream);
+
+/* Fused backward [HyperMegaMoE §2.2]: from dy and the `saved` buffer of the
+ * matching hmm_forward (same shape, same topk_ids, weights unchanged) writes
+ *   dx               bf16 [T, H]
+ *   d_up_proj_weight bf16 [E, H, 2I]
+ *   d_down_proj_weight bf16 [E, I, H]
+ *   d_topk_weights   [T, K] in shape->weights_dtype
+ * Any of the four outputs may be NULL to skip it. */
+int hmm_backward(hmm_ctx* ctx, const hmm_shape* shape, const void* dy,
+                 const void* topk_weights, const void* up_proj_weight,
+                 const void* down_proj_weight, const void* saved,
+                 size_t saved_bytes, void* dx, void* d_up_proj_weight,
+                 void* d_down_proj_weight, void* d_topk_weights,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronise `stream`, then read and clear the device status word.
+ * *device_error receives the HMM_STATUS_* bits.  Returns HMM_OK, or
+ * HMM_ERR_EXPERT_ID / HMM_ERR_TIMEOUT if the corresponding bit was set. */
+int hmm_status(hmm_ctx* ctx, void* stream, int* device_error);
+
+/* Static description of a return code. */
+const char* hmm_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HMM_H_ */
