@@ -1,0 +1,456 @@
+#!/usr/bin/env python
+"""Benchmark of the fused MoE-FFN hot path on GB300.
+
+One step = one full pass of the path over one batch: hmm_forward (training:
+routing, dispatch, GMM1+SwiGLU, GMM2, combine) + hmm_backward (dispatch of
+dy, act_grad + SwiGLU grad, input-grad GMM, W1Grad/W2Grad, combine of dx and
+d_topk_weights), on the prefill-shaped workload T=4096, H=2048, I=1408, E=64,
+K=6 (bf16, uniform top-6 routing, seeded synthetic inputs).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is whole-job tokens/s (tokens of all
+ranks / max-over-ranks time of the K timed steps), inputs resident in HBM, L2
+flushed (256 MiB write) before every timed step; `e2e` is the same metric
+with host inputs copied in and results copied out inside the timed region.
+`--impl reference` times the CPU oracle (the baseline arm) on a bounded
+token sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = dict(T=4096, H=2048, I=1408, E=64, K=6)
+WORKLOAD_NAME = "prefill-shaped MoE-FFN fwd+bwd: T=4096 H=2048 I=1408 E=64 K=6"
+METRIC = "MoE-FFN tokens/s (fused fwd+bwd step)"
+KERNELS_PER_STEP = 10  # route 3, dispatch_x, gemm_fwd, combine_y, dispatch_dy, 2 bwd gemms, combine_dx
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-sample", type=int, default=256,
+                    help="tokens of the oracle's CPU-baseline sample")
+    ap.add_argument("--ref-sample", type=int, default=48,
+                    help="tokens per step of the reference (oracle) arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------- distributed
+class Dist:
+    def __init__(self, want: int):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if _cuda_ok() else "gloo"
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+        dev = torch.device("cuda", self.local_rank) if _cuda_ok() else torch.device("cpu")
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def _cuda_ok():
+    import torch
+    return torch.cuda.is_available()
+
+
+# ------------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dispatch_grouped_gemm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_hash") != source_hash():
+        return None
+    v = d.get("kernels", {}).get(kernel)
+    return None if v is None else float(v)
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [r for r in csv.reader(io.StringIO(self.out.read())) if len(r) >= 9]
+        self.out.close()
+        os.unlink(self.out.name)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def emit(d):
+    print(json.dumps(d), flush=True)
+
+
+# ------------------------------------------------------------ CPU baseline
+def cpu_step(prob, W1, W2, tok):
+    """One oracle pass (fwd + bwd, all four gradients) over a token sample:
+    y, dx, d_topk_weights of the sampled tokens and the weight gradients of
+    every expert restricted to the sampled slots."""
+    import oracle
+    x, ids, w, dy = prob.x[tok], prob.topk_ids[tok], prob.topk_weights[tok], prob.dy[tok]
+    oracle.forward(x, ids, w, W1, W2)
+    oracle.backward_tokens(x, ids, w, W1, W2, dy)
+    for e in np.unique(ids):
+        oracle.weight_grad(int(e), x, ids, w, W1, W2, dy)
+
+
+def cpu_baseline(prob, n_tok: int, seed: int = 0):
+    import oracle
+    oracle.build()
+    W1, W2 = prob.W1, prob.W2
+    tok = np.sort(np.random.default_rng(seed).choice(prob.shape.T, n_tok, replace=False))
+    t0 = time.perf_counter()
+    cpu_step(prob, W1, W2, tok)
+    dt = time.perf_counter() - t0
+    return {"value": n_tok / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"{n_tok} random tokens of the workload: fp64 forward + backward "
+                      f"(y, dx, d_topk_weights, weight grads over the sampled slots)"}
+
+
+def run_reference(args, dist: Dist):
+    """The baseline arm: the fp64 CPU oracle, as it stands, on bounded samples."""
+    if dist.rank != 0:
+        return
+    import moe_inputs as mi
+    import oracle
+    oracle.build()
+    prob = mi.make("backward")
+    W1, W2 = prob.W1, prob.W2
+    rng = np.random.default_rng(1)
+    n = args.ref_sample
+    for _ in range(args.warmup):
+        cpu_step(prob, W1, W2, np.sort(rng.choice(prob.shape.T, n, replace=False)))
+    times = []
+    for _ in range(args.steps):
+        tok = np.sort(rng.choice(prob.shape.T, n, replace=False))
+        t0 = time.perf_counter()
+        cpu_step(prob, W1, W2, tok)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = n / (ms / 1e3)
+    sample = f"{n} random tokens per step of the workload, fp64 fwd+bwd"
+    emit({"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+          "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+          "data": "synthetic (seeded)",
+          "config": {"workload": WORKLOAD_NAME, **WORKLOAD, "sample_tokens_per_step": n},
+          "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
+                           "kind": "oracle", "sample": sample},
+          "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                  "d2h_bytes_per_step": 0}})
+
+
+# -------------------------------------------------------------------- GPU arm
+def run_ours(args, dist: Dist):
+    import torch
+
+    import dispatch_grouped_gemm_gb300 as hmm
+    import moe_inputs as mi
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    T, H, I, E, K = (WORKLOAD[k] for k in ("T", "H", "I", "E", "K"))
+    prob = mi.make("backward")
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+    x = bf16(prob.x).to(dev)
+    ids = torch.from_numpy(prob.topk_ids).to(dev)
+    w = bf16(prob.topk_weights).to(dev)
+    dy = bf16(prob.dy).to(dev)
+    W1 = torch.empty((E, H, 2 * I), dtype=torch.bfloat16, device=dev)
+    W2 = torch.empty((E, I, H), dtype=torch.bfloat16, device=dev)
+    for e in range(E):
+        W1[e].copy_(bf16(prob.expert_W1(e)))
+        W2[e].copy_(bf16(prob.expert_W2(e)))
+
+    ctx = hmm.Context.for_device(dev)
+    shape = hmm.Context.shape_of(x, ids, w, W1, W2)
+    fws, svb, bws = hmm.hmm_workspace_size(shape, True)
+    y = torch.empty_like(x)
+    saved = torch.empty(svb, dtype=torch.uint8, device=dev)
+    fwork = torch.empty(fws, dtype=torch.uint8, device=dev)
+    bwork = torch.empty(bws, dtype=torch.uint8, device=dev)
+    dx = torch.empty_like(x)
+    dW1 = torch.empty_like(W1)
+    dW2 = torch.empty_like(W2)
+    dw = torch.empty_like(w)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(xx=x, ii=ids, ww=w, dd=dy):
+        hmm.hmm_forward(ctx.handle, shape, xx, ii, ww, W1, W2, y, saved, fwork, stream)
+        hmm.hmm_backward(ctx.handle, shape, dd, ww, W1, W2, saved, dx, dW1, dW2, dw, bwork, stream)
+
+    # first call (module load, tensor maps, attribute setup) vs steady state
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host = time.perf_counter()
+    e0.record(stream)
+    step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    first_call_ms = e0.elapsed_time(e1)
+    first_call_host_ms = 1e3 * (time.perf_counter() - t_host)
+    for _ in range(max(args.warmup, 3)):
+        step()
+    rc, bits = hmm.hmm_status(ctx.handle)
+    if rc != 0:
+        raise RuntimeError(f"device status after warm-up: {rc} bits={bits}")
+
+    # ---------------------------------------------------------- timed region
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    ctx.set_option(hmm.HMM_OPT_PROFILE, 1)
+    hmm.hmm_profile_read(ctx.handle)  # reset
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    dist.barrier()
+    torch.cuda.synchronize()
+    for s, e in ev:
+        flush.zero_()
+        s.record(stream)
+        step()
+        e.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clocks = sampler.stop()
+    prof = hmm.hmm_profile_read(ctx.handle)
+    ctx.set_option(hmm.HMM_OPT_PROFILE, 0)
+    step_ms = sum(s.elapsed_time(e) for s, e in ev) / args.steps
+    step_ms_max = dist.max(step_ms)
+    value = dist.world * T / (step_ms_max / 1e3)
+    rc, bits = hmm.hmm_status(ctx.handle)
+    if rc != 0:
+        raise RuntimeError(f"device status after timed region: {rc} bits={bits}")
+
+    # per-phase algorithmic work and roofline of the dominant kernel
+    TK = T * K
+    F = 2.0 * TK * H * I  # one "unit": 2*TK*H*I flops
+    algo = {
+        "route": ("hbm", 3 * TK * 4.0),
+        "dispatch_x": ("hbm", (T * H + TK * H) * 2.0),
+        "gemm_fwd": ("tensor", 3 * F),
+        "combine_y": ("hbm", (TK * H + T * H) * 2.0 + TK * 2.0),
+        "dispatch_dy": ("hbm", (T * H + TK * H) * 2.0),
+        "gemm_bwd_data": ("tensor", 3 * F),
+        "gemm_bwd_weight": ("tensor", 3 * F),
+        "combine_dx": ("hbm", (TK * H + T * H) * 2.0),
+    }
+    peaks, peak_src = load_peaks()
+    phases = {}
+    for name, (ms, launches) in prof.items():
+        n_calls = args.steps
+        per_ms = ms / n_calls if n_calls else 0.0
+        bound, work = algo[name]
+        if bound == "tensor":
+            ach = work / (per_ms / 1e3) / 1e12
+            peak = peaks["bf16_tflops_sustained"]
+            unit = "TFLOP/s"
+        else:
+            ach = work / (per_ms / 1e3) / 1e9
+            peak = peaks["hbm_gbs"]
+            unit = "GB/s"
+        phases[name] = {"ms": per_ms, "share": ms / max(1e-9, sum(v[0] for v in prof.values())),
+                        "bound": bound, "achieved": ach, "unit": unit, "frac": ach / peak,
+                        "launches": launches}
+    dom = max(phases, key=lambda k: phases[k]["ms"])
+    dp = phases[dom]
+    roofline = {"kernel": dom, "bound": dp["bound"], "achieved": dp["achieved"],
+                "peak": peaks["bf16_tflops_sustained"] if dp["bound"] == "tensor"
+                else peaks["hbm_gbs"],
+                "unit": dp["unit"], "frac": dp["frac"], "traffic": load_traffic(dom),
+                "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if dp['bound'] == 'tensor' else 'hbm_gbs'})"}
+
+    fwd_ms = sum(phases[k]["ms"] for k in ("route", "dispatch_x", "gemm_fwd", "combine_y"))
+    bwd_ms = sum(phases[k]["ms"] for k in ("dispatch_dy", "gemm_bwd_data", "gemm_bwd_weight",
+                                            "combine_dx"))
+    gemm_flops = 9 * F  # 6 TK H I forward + 12 TK H I backward
+    gemm_ms = sum(phases[k]["ms"] for k in ("gemm_fwd", "gemm_bwd_data", "gemm_bwd_weight"))
+
+    # ------------------------------------------------------------------ e2e
+    e2e = None
+    if not args.no_e2e:
+        hx = bf16(prob.x).pin_memory()
+        hids = torch.from_numpy(prob.topk_ids).pin_memory()
+        hw = bf16(prob.topk_weights).pin_memory()
+        hdy = bf16(prob.dy).pin_memory()
+        oy = torch.empty_like(hx).pin_memory()
+        odx = torch.empty_like(hx).pin_memory()
+        odw = torch.empty_like(hw).pin_memory()
+        dx_in = torch.empty_like(x)
+        di_in = torch.empty_like(ids)
+        dw_in = torch.empty_like(w)
+        ddy_in = torch.empty_like(dy)
+        h2d = sum(t.numel() * t.element_size() for t in (hx, hids, hw, hdy))
+        d2h = sum(t.numel() * t.element_size() for t in (oy, odx, odw))
+
+        def e2e_step():
+            dx_in.copy_(hx, non_blocking=True)
+            di_in.copy_(hids, non_blocking=True)
+            dw_in.copy_(hw, non_blocking=True)
+            ddy_in.copy_(hdy, non_blocking=True)
+            step(dx_in, di_in, dw_in, ddy_in)
+            oy.copy_(y, non_blocking=True)
+            odx.copy_(dx, non_blocking=True)
+            odw.copy_(dw, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        dist.barrier()
+        torch.cuda.synchronize()
+        for s, e in ev2:
+            flush.zero_()
+            s.record(stream)
+            e2e_step()
+            e.record(stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+        e2e_ms = dist.max(sum(s.elapsed_time(e) for s, e in ev2) / args.steps)
+        e2e = {"value": dist.world * T / (e2e_ms / 1e3), "unit": "tokens/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded normal inputs, uniform top-6 routing)",
+        "config": {"workload": WORKLOAD_NAME, **WORKLOAD, "l2": "256 MiB flush before each step",
+                   "parallelism": f"replicas x{dist.world}"},
+        "grouped_gemm_tflops": gemm_flops / (gemm_ms / 1e3) / 1e12 if gemm_ms else None,
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+        "first_call_ms": first_call_ms, "first_call_host_ms": first_call_host_ms,
+        "roofline": roofline,
+        "phases": phases,
+        "e2e": e2e,
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches_traced": int(sum(v[1] for v in prof.values())),
+        "clocks": clocks,
+    }
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(prob, args.cpu_sample)
+    if dist.rank == 0:
+        emit(out)
+
+
+def main():
+    args = parse()
+    dist = Dist(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist)
+        else:
+            run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

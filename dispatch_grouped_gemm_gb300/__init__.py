@@ -24,7 +24,8 @@ __all__ = [
     "HmmError", "HmmShape", "hmm_create", "hmm_destroy", "hmm_set_option",
     "hmm_workspace_size", "hmm_route", "hmm_forward", "hmm_backward", "hmm_status",
     "hmm_error_string", "Context", "moe_ffn", "library_path", "load_library",
-    "HMM_OPT_VALIDATE", "HMM_OPT_WAIT_BUDGET_NS", "HMM_OPT_INJECT_SKIP_READY",
+    "hmm_profile_read", "hmm_phase_name",
+    "HMM_OPT_VALIDATE", "HMM_OPT_WAIT_BUDGET_NS", "HMM_OPT_INJECT_SKIP_READY", "HMM_OPT_PROFILE",
     "HMM_DTYPE_BF16", "HMM_DTYPE_F32", "HMM_STATUS_EXPERT_ID", "HMM_STATUS_TIMEOUT",
 ]
 
@@ -52,6 +53,7 @@ HMM_ERR_EXPERT_ID = _C["HMM_ERR_EXPERT_ID"]
 HMM_OPT_VALIDATE = _C["HMM_OPT_VALIDATE"]
 HMM_OPT_WAIT_BUDGET_NS = _C["HMM_OPT_WAIT_BUDGET_NS"]
 HMM_OPT_INJECT_SKIP_READY = _C["HMM_OPT_INJECT_SKIP_READY"]
+HMM_OPT_PROFILE = _C["HMM_OPT_PROFILE"]
 HMM_DTYPE_BF16 = _C["HMM_DTYPE_BF16"]
 HMM_DTYPE_F32 = _C["HMM_DTYPE_F32"]
 HMM_STATUS_EXPERT_ID = _C["HMM_STATUS_EXPERT_ID"]
@@ -101,6 +103,8 @@ def load_library():
             "hmm_forward": [vp, sp, vp, vp, vp, vp, vp, vp, vp, sz, vp, sz, vp],
             "hmm_backward": [vp, sp, vp, vp, vp, vp, vp, sz, vp, vp, vp, vp, vp, sz, vp],
             "hmm_status": [vp, vp, ctypes.POINTER(i32)],
+            "hmm_profile_read": [vp, i32, ctypes.POINTER(ctypes.c_double),
+                                 ctypes.POINTER(ctypes.c_int64)],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -108,6 +112,8 @@ def load_library():
             fn.restype = i32
         lib.hmm_error_string.argtypes = [i32]
         lib.hmm_error_string.restype = ctypes.c_char_p
+        lib.hmm_phase_name.argtypes = [i32]
+        lib.hmm_phase_name.restype = ctypes.c_char_p
         _lib = lib
         return lib
 
@@ -200,6 +206,20 @@ def hmm_status(ctx, stream=None):
     bits = ctypes.c_int(0)
     rc = load_library().hmm_status(ctx, _stream(stream), ctypes.byref(bits))
     return rc, bits.value
+
+
+def hmm_phase_name(phase: int):
+    r = load_library().hmm_phase_name(int(phase))
+    return None if r is None else r.decode()
+
+
+def hmm_profile_read(ctx):
+    """{phase name: (GPU ms, kernel launches)} since the previous read."""
+    n = _C["HMM_NUM_PHASES"]
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    _check(load_library().hmm_profile_read(ctx, n, ms, cnt), "hmm_profile_read")
+    return {hmm_phase_name(i): (ms[i], cnt[i]) for i in range(n)}
 
 
 # ------------------------------------------------------------ torch layer

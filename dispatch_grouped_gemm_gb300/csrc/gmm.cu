@@ -65,6 +65,9 @@ struct Prob {
   int64_t ld_out2;
   void* out3;
   int64_t ld_out3;
+  void* out4;           // SwiGLU grad: low bf16 half of dH (same layout as out)
+  void* out5;           // SwiGLU grad: low bf16 half of w*a (same layout as out2)
+  int split;            // wgrad: 0 none, 1 A operand given as hi+lo, 2 B operand hi+lo
   const void* aux;
   int64_t ld_aux;
   const float* rowscale;
@@ -108,7 +111,7 @@ __device__ void decode_tile(const Params& P, const Prob& pr, int u, TileInfo& ti
     ti.m0 = (r / pr.n_tiles) * BM;
     ti.n0 = (r % pr.n_tiles) * BN;
     ti.krow0 = P.poff[e];
-    ti.kb = (P.poff[e + 1] - P.poff[e]) / BK;
+    ti.kb = (P.poff[e + 1] - P.poff[e]) / BK * (pr.split ? 2 : 1);
   } else {
     // largest e with n_tiles * poff[e]/BM <= u (empty experts own no tiles)
     int lo = 0, hi = P.E - 1;
@@ -136,14 +139,22 @@ __device__ void decode_tile(const Params& P, const Prob& pr, int u, TileInfo& ti
 template <class C>
 __device__ __forceinline__ void load_stage(const Prob& pr, const TileInfo& ti, int kb,
                                            const CUtensorMap* tA, const CUtensorMap* tB,
-                                           uint8_t* sA, uint8_t* sB, uint64_t* bar) {
+                                           const CUtensorMap* tS, uint8_t* sA, uint8_t* sB,
+                                           uint64_t* bar) {
   if constexpr (C::WGRAD) {
-    const int k = ti.krow0 + kb * BK;
-    tma_load_2d(sA, tA, bar, ti.m0, k);
-    tma_load_2d(sA + 8192, tA, bar, ti.m0 + 64, k);
+    // with a split operand the K loop runs twice over the expert's rows:
+    // first against the high bf16 half, then against the low half
+    const int nk = pr.split ? ti.kb / 2 : ti.kb;
+    const bool lo = kb >= nk;
+    const int k = ti.krow0 + (lo ? kb - nk : kb) * BK;
+    const CUtensorMap* a = (pr.split == 1 && lo) ? tS : tA;
+    const CUtensorMap* b = (pr.split == 2 && lo) ? tS : tB;
+    tma_load_2d(sA, a, bar, ti.m0, k);
+    tma_load_2d(sA + 8192, a, bar, ti.m0 + 64, k);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * 8192, tB, bar, ti.n0 + 64 * j, k);
+    for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * 8192, b, bar, ti.n0 + 64 * j, k);
   } else {
+    (void)tS;
     const int k = kb * BK;
     tma_load_2d(sA, tA, bar, k, ti.m0);
     if constexpr (C::B_MN) {
@@ -194,6 +205,20 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v
       d[q] = u;
     }
   }
+}
+
+// v = hi + lo with hi = bf16(v), lo = bf16(v - hi): the pair carries about
+// 16 significant bits, enough for the weight-gradient GEMMs that consume it.
+__device__ __forceinline__ void store_bf16x32_split(__nv_bfloat16* hi, __nv_bfloat16* lo,
+                                                    const float* v, int valid) {
+  float h[32], l[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    h[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
+    l[j] = v[j] - h[j];
+  }
+  store_bf16x32(hi, h, valid);
+  store_bf16x32(lo, l, valid);
 }
 
 __device__ __forceinline__ void store_f32x32(float* dst, const float* v, int valid) {
@@ -280,6 +305,8 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
     const float* h_row = static_cast<const float*>(pr.aux) + row * pr.ld_aux;
     __nv_bfloat16* dh_row = static_cast<__nv_bfloat16*>(pr.out) + row * pr.ld_out;
     __nv_bfloat16* wa_row = static_cast<__nv_bfloat16*>(pr.out2) + row * pr.ld_out2;
+    __nv_bfloat16* dh_lo = static_cast<__nv_bfloat16*>(pr.out4) + row * pr.ld_out;
+    __nv_bfloat16* wa_lo = static_cast<__nv_bfloat16*>(pr.out5) + row * pr.ld_out2;
     const float w = pr.rowscale[row];
     float dwp = 0.0f;
 #pragma unroll 1
@@ -306,9 +333,9 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
         du[j] = dA * g * s;
         wa[j] = w * a;
       }
-      store_bf16x32(dh_row + col, dg, valid);
-      store_bf16x32(dh_row + pr.half + col, du, valid);
-      store_bf16x32(wa_row + col, wa, valid);
+      store_bf16x32_split(dh_row + col, dh_lo + col, dg, valid);
+      store_bf16x32_split(dh_row + pr.half + col, dh_lo + pr.half + col, du, valid);
+      store_bf16x32_split(wa_row + col, wa_lo + col, wa, valid);
     }
     static_cast<float*>(pr.out3)[row * pr.ld_out3 + ti.n0 / BN] = dwp;
   }
@@ -340,8 +367,9 @@ __device__ __noinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t
 template <class C0, class C1>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gmm_kernel(const __grid_constant__ Params P, const __grid_constant__ CUtensorMap tA0,
-               const __grid_constant__ CUtensorMap tB0, const __grid_constant__ CUtensorMap tA1,
-               const __grid_constant__ CUtensorMap tB1) {
+               const __grid_constant__ CUtensorMap tB0, const __grid_constant__ CUtensorMap tS0,
+               const __grid_constant__ CUtensorMap tA1, const __grid_constant__ CUtensorMap tB1,
+               const __grid_constant__ CUtensorMap tS1) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -393,9 +421,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ------------------------------------------------------- TMA producer
       tma_prefetch_desc(&tA0);
       tma_prefetch_desc(&tB0);
+      if (P.p[0].split) tma_prefetch_desc(&tS0);
       if (P.nprob > 1) {
         tma_prefetch_desc(&tA1);
         tma_prefetch_desc(&tB1);
+        if (P.p[1].split) tma_prefetch_desc(&tS1);
       }
       const int T0 = tiles_of(P, P.p[0], C0::WGRAD);
       const int T1 = P.nprob > 1 ? tiles_of(P, P.p[1], C1::WGRAD) : 0;
@@ -443,9 +473,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint8_t* sB = sA + A_BYTES;
           mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
           if (ti.prob == 0)
-            load_stage<C0>(pr, ti, kb, &tA0, &tB0, sA, sB, &full[stage]);
+            load_stage<C0>(pr, ti, kb, &tA0, &tB0, &tS0, sA, sB, &full[stage]);
           else
-            load_stage<C1>(pr, ti, kb, &tA1, &tB1, sA, sB, &full[stage]);
+            load_stage<C1>(pr, ti, kb, &tA1, &tB1, &tS1, sA, sB, &full[stage]);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -607,7 +637,8 @@ int map_w(const GemmEnv& env, CUtensorMap* m, const void* base, int64_t E, int64
 
 template <class C0, class C1>
 int launch(const GemmEnv& env, Params& P, const CUtensorMap& a0, const CUtensorMap& b0,
-           const CUtensorMap& a1, const CUtensorMap& b1, int64_t max_tiles) {
+           const CUtensorMap& s0, const CUtensorMap& a1, const CUtensorMap& b1,
+           const CUtensorMap& s1, int64_t max_tiles) {
   if (max_tiles <= 0) return HMM_OK;
   auto kern = gmm_kernel<C0, C1>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
@@ -616,7 +647,7 @@ int launch(const GemmEnv& env, Params& P, const CUtensorMap& a0, const CUtensorM
   const int grid = static_cast<int>(std::min<int64_t>(env.num_sms, max_tiles));
   P.status = env.status;
   P.budget_ns = env.budget_ns;
-  kern<<<grid, NUM_THREADS, SMEM_BYTES, env.stream>>>(P, a0, b0, a1, b1);
+  kern<<<grid, NUM_THREADS, SMEM_BYTES, env.stream>>>(P, a0, b0, s0, a1, b1, s1);
   return cudaGetLastError() == cudaSuccess ? HMM_OK : HMM_ERR_CUDA;
 }
 
@@ -663,19 +694,19 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
   g2.wait = c.ready;
   g2.wait_target = 4 * g1.n_tiles;
   const int64_t max_tiles = p.max_mtiles * (g1.n_tiles + g2.n_tiles);
-  return launch<CfgGmm1, CfgGmm2>(env, P, tA0, tB0, tA1, tB1, max_tiles);
+  return launch<CfgGmm1, CfgGmm2>(env, P, tA0, tB0, tA0, tA1, tB1, tA1, max_tiles);
 }
 
 int launch_backward_data_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
                                const void* dy_perm, const float* wperm, const float* h32,
-                               const void* W1, const void* W2, void* dH, void* wa, float* dwp,
-                               void* dx_perm) {
+                               const void* W1, const void* W2, void* dH, void* dH_lo, void* wa,
+                               void* wa_lo, float* dwp, void* dx_perm) {
   const int64_t H = p.H, I = p.I, E = p.E, R = p.R;
   CUtensorMap tA0, tB0, tA1, tB1;
   int rc = HMM_OK;
   rc |= map_act(env, &tA0, dy_perm, R, H, BM);       // dy_perm [R, H], K = H
   rc |= map_w(env, &tB0, W2, E, I, H, BN);           // W2 [E, I, H] = (W2^T) K-major, N = I
-  rc |= map_act(env, &tA1, dH, R, 2 * I, BM);        // dH [R, 2I], K = 2I
+  rc |= map_act(env, &tA1, dH, R, 2 * I, BM);        // dH [R, 2I] (high half), K = 2I
   rc |= map_w(env, &tB1, W1, E, H, 2 * I, BN);       // W1 [E, H, 2I] = (W1^T) K-major, N = H
   if (rc != HMM_OK) return HMM_ERR_CUDA;
   Params P{};
@@ -694,6 +725,8 @@ int launch_backward_data_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, Ct
   ag.ld_out2 = I;
   ag.out3 = dwp;
   ag.ld_out3 = p.nt_dswiglu;
+  ag.out4 = dH_lo;
+  ag.out5 = wa_lo;
   ag.aux = h32;
   ag.ld_aux = 2 * I;
   ag.rowscale = wperm;
@@ -707,58 +740,67 @@ int launch_backward_data_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, Ct
   ig.wait = c.ready;
   ig.wait_target = 4 * ag.n_tiles;
   const int64_t max_tiles = p.max_mtiles * (ag.n_tiles + ig.n_tiles);
-  return launch<CfgActGrad, CfgInGrad>(env, P, tA0, tB0, tA1, tB1, max_tiles);
+  return launch<CfgActGrad, CfgInGrad>(env, P, tA0, tB0, tA0, tA1, tB1, tA1, max_tiles);
 }
 
 int launch_backward_weight_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
                                  const void* x_perm, const void* dy_perm, const void* dH,
-                                 const void* wa, void* dW1, void* dW2) {
+                                 const void* dH_lo, const void* wa, const void* wa_lo, void* dW1,
+                                 void* dW2) {
   const int64_t H = p.H, I = p.I, E = p.E, R = p.R;
-  CUtensorMap tA0, tB0, tA1, tB1;
+  // dW2[e] = (wa_hi + wa_lo)^T . dy_perm : [I, rows] x [rows, H]
+  // dW1[e] = x_perm^T . (dH_hi + dH_lo)  : [H, rows] x [rows, 2I]
+  CUtensorMap w2A, w2B, w2S, w1A, w1B, w1S;
   int rc = HMM_OK;
-  // dW2[e] = wa^T . dy_perm : [I, rows] x [rows, H]
-  rc |= map_act(env, &tA0, wa, R, I, 64);
-  rc |= map_act(env, &tB0, dy_perm, R, H, 64);
-  // dW1[e] = x_perm^T . dH : [H, rows] x [rows, 2I]
-  rc |= map_act(env, &tA1, x_perm, R, H, 64);
-  rc |= map_act(env, &tB1, dH, R, 2 * I, 64);
+  rc |= map_act(env, &w2A, wa, R, I, 64);
+  rc |= map_act(env, &w2B, dy_perm, R, H, 64);
+  rc |= map_act(env, &w2S, wa_lo, R, I, 64);
+  rc |= map_act(env, &w1A, x_perm, R, H, 64);
+  rc |= map_act(env, &w1B, dH, R, 2 * I, 64);
+  rc |= map_act(env, &w1S, dH_lo, R, 2 * I, 64);
   if (rc != HMM_OK) return HMM_ERR_CUDA;
+  Prob w2{}, w1{};
+  w2.M = static_cast<int>(I);
+  w2.N = static_cast<int>(H);
+  w2.m_tiles = static_cast<int>((I + BM - 1) / BM);
+  w2.n_tiles = static_cast<int>((H + BN - 1) / BN);
+  w2.out = dW2;
+  w2.ld_out = H;
+  w2.out_estride = I * H;
+  w2.split = 1;
+  w1.M = static_cast<int>(H);
+  w1.N = static_cast<int>(2 * I);
+  w1.m_tiles = static_cast<int>((H + BM - 1) / BM);
+  w1.n_tiles = static_cast<int>((2 * I + BN - 1) / BN);
+  w1.out = dW1;
+  w1.ld_out = 2 * I;
+  w1.out_estride = H * 2 * I;
+  w1.split = 2;
   Params P{};
-  P.nprob = 0;
   P.poff = m.poff;
   P.E = static_cast<int>(E);
   P.ticket = c.tickets + 2;
-  Prob pr[2]{};
-  int n = 0;
-  if (dW2) {
-    Prob& w2 = pr[n++];
-    w2.M = static_cast<int>(I);
-    w2.N = static_cast<int>(H);
-    w2.m_tiles = static_cast<int>((I + BM - 1) / BM);
-    w2.n_tiles = static_cast<int>((H + BN - 1) / BN);
-    w2.out = dW2;
-    w2.ld_out = H;
-    w2.out_estride = I * H;
+  if (dW2 && dW1) {
+    // dW1 first: its tiles are the larger share, dW2 tiles fill the tail
+    P.nprob = 2;
+    P.p[0] = w1;
+    P.p[1] = w2;
+    const int64_t max_tiles = E * (w1.m_tiles * w1.n_tiles + w2.m_tiles * w2.n_tiles);
+    return launch<CfgWGrad, CfgWGrad>(env, P, w1A, w1B, w1S, w2A, w2B, w2S, max_tiles);
   }
   if (dW1) {
-    Prob& w1 = pr[n++];
-    w1.M = static_cast<int>(H);
-    w1.N = static_cast<int>(2 * I);
-    w1.m_tiles = static_cast<int>((H + BM - 1) / BM);
-    w1.n_tiles = static_cast<int>((2 * I + BN - 1) / BN);
-    w1.out = dW1;
-    w1.ld_out = 2 * I;
-    w1.out_estride = H * 2 * I;
+    P.nprob = 1;
+    P.p[0] = w1;
+    return launch<CfgWGrad, CfgWGrad>(env, P, w1A, w1B, w1S, w1A, w1B, w1S,
+                                      E * w1.m_tiles * w1.n_tiles);
   }
-  if (n == 0) return HMM_OK;
-  P.nprob = n;
-  P.p[0] = pr[0];
-  P.p[1] = pr[1];
-  int64_t max_tiles = 0;
-  for (int i = 0; i < n; ++i) max_tiles += E * P.p[i].m_tiles * P.p[i].n_tiles;
-  const CUtensorMap& a0 = dW2 ? tA0 : tA1;
-  const CUtensorMap& b0 = dW2 ? tB0 : tB1;
-  return launch<CfgWGrad, CfgWGrad>(env, P, a0, b0, tA1, tB1, max_tiles);
+  if (dW2) {
+    P.nprob = 1;
+    P.p[0] = w2;
+    return launch<CfgWGrad, CfgWGrad>(env, P, w2A, w2B, w2S, w2A, w2B, w2S,
+                                      E * w2.m_tiles * w2.n_tiles);
+  }
+  return HMM_OK;
 }
 
 }  // namespace hmm

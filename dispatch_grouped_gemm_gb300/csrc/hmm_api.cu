@@ -14,8 +14,31 @@
 
 #include <algorithm>
 #include <cstring>
+#include <vector>
 
 #include "hmm_internal.h"
+
+namespace {
+
+struct PhaseInfo {
+  const char* name;
+  int kernels;
+};
+constexpr PhaseInfo kPhases[HMM_NUM_PHASES] = {
+    {"route", 3},         {"dispatch_x", 1},      {"gemm_fwd", 1},
+    {"combine_y", 1},     {"dispatch_dy", 1},     {"gemm_bwd_data", 1},
+    {"gemm_bwd_weight", 1}, {"combine_dx", 1}};
+enum Phase {
+  PH_ROUTE = 0, PH_DISPATCH_X, PH_GEMM_FWD, PH_COMBINE_Y, PH_DISPATCH_DY,
+  PH_GEMM_BWD_DATA, PH_GEMM_BWD_WEIGHT, PH_COMBINE_DX
+};
+
+struct ProfRec {
+  int phase;
+  cudaEvent_t begin, end;
+};
+
+}  // namespace
 
 struct hmm_ctx {
   int device = -1;
@@ -24,8 +47,48 @@ struct hmm_ctx {
   int validate = 0;
   uint64_t budget_ns = 2000000000ull;
   int inject_skip_ready = 0;
+  int profile = 0;
+  std::vector<ProfRec> recs;
+  std::vector<cudaEvent_t> pool;
   hmm::EncodeTiledFn encode = nullptr;
 };
+
+namespace {
+
+cudaEvent_t take_event(hmm_ctx* c) {
+  if (!c->pool.empty()) {
+    cudaEvent_t e = c->pool.back();
+    c->pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Brackets one launch phase with events on the launching stream when
+// profiling is on.
+struct PhaseScope {
+  hmm_ctx* c;
+  int phase;
+  cudaStream_t st;
+  cudaEvent_t begin = nullptr;
+  PhaseScope(hmm_ctx* ctx, int ph, cudaStream_t s) : c(ctx), phase(ph), st(s) {
+    if (c->profile && (begin = take_event(c)) != nullptr) cudaEventRecord(begin, st);
+  }
+  ~PhaseScope() {
+    if (!begin) return;
+    cudaEvent_t end = take_event(c);
+    if (!end) {
+      c->pool.push_back(begin);
+      return;
+    }
+    cudaEventRecord(end, st);
+    c->recs.push_back({phase, begin, end});
+  }
+};
+
+}  // namespace
 
 namespace hmm {
 
@@ -88,7 +151,9 @@ int make_plan(const hmm_shape* s, bool training, Plan* p) {
   p->bw_dyperm = o;  o = align_up(o + static_cast<size_t>(R) * p->H * 2, A);
   p->bw_wperm = o;   o = align_up(o + static_cast<size_t>(R) * 4, A);
   p->bw_dh = o;      o = align_up(o + static_cast<size_t>(R) * 2 * p->I * 2, A);
+  p->bw_dhlo = o;    o = align_up(o + static_cast<size_t>(R) * 2 * p->I * 2, A);
   p->bw_wa = o;      o = align_up(o + static_cast<size_t>(R) * p->I * 2, A);
+  p->bw_walo = o;    o = align_up(o + static_cast<size_t>(R) * p->I * 2, A);
   p->bw_dxperm = o;  o = align_up(o + static_cast<size_t>(R) * p->H * 2, A);
   p->bw_dwp = o;     o = align_up(o + static_cast<size_t>(R) * p->nt_dswiglu * 4, A);
   p->bwd_ws_bytes = o;
@@ -219,6 +284,12 @@ int hmm_destroy(hmm_ctx* ctx) {
   if (!ctx) return HMM_OK;
   {
     DeviceGuard g(ctx->device);
+    for (auto& r : ctx->recs) {
+      cudaEventSynchronize(r.end);
+      cudaEventDestroy(r.begin);
+      cudaEventDestroy(r.end);
+    }
+    for (cudaEvent_t e : ctx->pool) cudaEventDestroy(e);
     if (ctx->status) cudaFree(ctx->status);
   }
   delete ctx;
@@ -237,6 +308,9 @@ int hmm_set_option(hmm_ctx* ctx, int option, int64_t value) {
       return HMM_OK;
     case HMM_OPT_INJECT_SKIP_READY:
       ctx->inject_skip_ready = value != 0;
+      return HMM_OK;
+    case HMM_OPT_PROFILE:
+      ctx->profile = value != 0;
       return HMM_OK;
     default:
       return HMM_ERR_ARG;
@@ -315,19 +389,29 @@ int hmm_forward(hmm_ctx* ctx, const hmm_shape* shape, const void* x, const int32
   void* a = ws + p.fw_a;
   void* o = ws + p.fw_o;
 
-  rc = cuda_rc(launch_route(p, topk_ids, m, c, nullptr, nullptr, ctx->status, st));
+  {
+    PhaseScope ps(ctx, PH_ROUTE, st);
+    rc = cuda_rc(launch_route(p, topk_ids, m, c, nullptr, nullptr, ctx->status, st));
+  }
   if (rc != HMM_OK) return rc;
   if (ctx->validate) {
     rc = read_route_error(ctx, st);
     if (rc != HMM_OK) return rc;
   }
-  rc = cuda_rc(launch_dispatch_x(p, x, m, x_perm, st));
+  {
+    PhaseScope ps(ctx, PH_DISPATCH_X, st);
+    rc = cuda_rc(launch_dispatch_x(p, x, m, x_perm, st));
+  }
   if (rc != HMM_OK) return rc;
   const bool inject = ctx->inject_skip_ready != 0;
   ctx->inject_skip_ready = 0;
-  rc = launch_forward_gemms(env_of(ctx, st), p, m, c, x_perm, up_proj_weight, down_proj_weight, a,
-                            h32, o, inject);
+  {
+    PhaseScope ps(ctx, PH_GEMM_FWD, st);
+    rc = launch_forward_gemms(env_of(ctx, st), p, m, c, x_perm, up_proj_weight, down_proj_weight,
+                              a, h32, o, inject);
+  }
   if (rc != HMM_OK) return rc;
+  PhaseScope ps(ctx, PH_COMBINE_Y, st);
   return cuda_rc(launch_combine_y(p, o, topk_weights, shape->weights_dtype, m, y, st));
 }
 
@@ -376,23 +460,36 @@ int hmm_backward(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const voi
   void* dy_perm = ws + p.bw_dyperm;
   float* wperm = reinterpret_cast<float*>(ws + p.bw_wperm);
   void* dH = ws + p.bw_dh;
+  void* dH_lo = ws + p.bw_dhlo;
   void* wa = ws + p.bw_wa;
+  void* wa_lo = ws + p.bw_walo;
   void* dx_perm = ws + p.bw_dxperm;
   float* dwp = reinterpret_cast<float*>(ws + p.bw_dwp);
   const GemmEnv env = env_of(ctx, st);
 
-  rc = cuda_rc(
-      launch_dispatch_dy(p, dy, topk_weights, shape->weights_dtype, m, c, dy_perm, wperm, st));
+  {
+    PhaseScope ps(ctx, PH_DISPATCH_DY, st);
+    rc = cuda_rc(
+        launch_dispatch_dy(p, dy, topk_weights, shape->weights_dtype, m, c, dy_perm, wperm, st));
+  }
   if (rc != HMM_OK) return rc;
-  rc = launch_backward_data_gemms(env, p, m, c, dy_perm, wperm, h32, up_proj_weight,
-                                  down_proj_weight, dH, wa, dwp, dx_perm);
+  {
+    PhaseScope ps(ctx, PH_GEMM_BWD_DATA, st);
+    rc = launch_backward_data_gemms(env, p, m, c, dy_perm, wperm, h32, up_proj_weight,
+                                    down_proj_weight, dH, dH_lo, wa, wa_lo, dwp, dx_perm);
+  }
   if (rc != HMM_OK) return rc;
-  rc = launch_backward_weight_gemms(env, p, m, c, x_perm, dy_perm, dH, wa, d_up_proj_weight,
-                                    d_down_proj_weight);
+  if (d_up_proj_weight || d_down_proj_weight) {
+    PhaseScope ps(ctx, PH_GEMM_BWD_WEIGHT, st);
+    rc = launch_backward_weight_gemms(env, p, m, c, x_perm, dy_perm, dH, dH_lo, wa, wa_lo,
+                                      d_up_proj_weight, d_down_proj_weight);
+  }
   if (rc != HMM_OK) return rc;
-  if (dx || d_topk_weights)
+  if (dx || d_topk_weights) {
+    PhaseScope ps(ctx, PH_COMBINE_DX, st);
     rc = cuda_rc(launch_combine_dx(p, dx_perm, dwp, m, dx, d_topk_weights, shape->weights_dtype,
                                    st));
+  }
   return rc;
 }
 
@@ -410,6 +507,36 @@ int hmm_status(hmm_ctx* ctx, void* stream, int* device_error) {
   if (v & HMM_STATUS_TIMEOUT) return HMM_ERR_TIMEOUT;
   if (v & HMM_STATUS_EXPERT_ID) return HMM_ERR_EXPERT_ID;
   return HMM_OK;
+}
+
+int hmm_profile_read(hmm_ctx* ctx, int n, double* ms, int64_t* launches) {
+  if (!ctx || n < 0) return HMM_ERR_ARG;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return HMM_ERR_CUDA;
+  double acc[HMM_NUM_PHASES] = {0};
+  int64_t cnt[HMM_NUM_PHASES] = {0};
+  int rc = HMM_OK;
+  for (auto& r : ctx->recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.end) != cudaSuccess ||
+        cudaEventElapsedTime(&t, r.begin, r.end) != cudaSuccess)
+      rc = HMM_ERR_CUDA;
+    acc[r.phase] += t;
+    cnt[r.phase] += kPhases[r.phase].kernels;
+    ctx->pool.push_back(r.begin);
+    ctx->pool.push_back(r.end);
+  }
+  ctx->recs.clear();
+  for (int i = 0; i < n && i < HMM_NUM_PHASES; ++i) {
+    if (ms) ms[i] = acc[i];
+    if (launches) launches[i] = cnt[i];
+  }
+  return rc;
+}
+
+const char* hmm_phase_name(int phase) {
+  if (phase < 0 || phase >= HMM_NUM_PHASES) return nullptr;
+  return kPhases[phase].name;
 }
 
 const char* hmm_error_string(int code) {

@@ -57,9 +57,10 @@ struct Plan {
   size_t saved_bytes, fwd_ws_bytes;
   size_t sv_meta, sv_xperm, sv_h;
   size_t fw_ctrl, fw_meta, fw_xperm, fw_a, fw_o;
-  // backward workspace = [ctrl | dy_perm | wperm | dH | wa | dX_perm | dwp]
+  // backward workspace =
+  //   [ctrl | dy_perm | wperm | dH | dH_lo | wa | wa_lo | dX_perm | dwp]
   size_t bwd_ws_bytes;
-  size_t bw_ctrl, bw_dyperm, bw_wperm, bw_dh, bw_wa, bw_dxperm, bw_dwp;
+  size_t bw_ctrl, bw_dyperm, bw_wperm, bw_dh, bw_dhlo, bw_wa, bw_walo, bw_dxperm, bw_dwp;
 };
 
 int make_plan(const hmm_shape* s, bool training, Plan* p);
@@ -100,13 +101,16 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
                          const void* x_perm, const void* W1, const void* W2, void* a, float* h32,
                          void* o, bool skip_ready_release);
 // backward act_grad(+SwiGLU grad, d_w partials) and input-grad GEMMs
+// (dH and w*a are written as two bf16 halves, hi + lo)
 int launch_backward_data_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
                                const void* dy_perm, const float* wperm, const float* h32,
-                               const void* W1, const void* W2, void* dH, void* wa, float* dwp,
-                               void* dx_perm);
-// backward weight-gradient GEMMs dW2 = wa^T dy_perm, dW1 = x_perm^T dH
+                               const void* W1, const void* W2, void* dH, void* dH_lo, void* wa,
+                               void* wa_lo, float* dwp, void* dx_perm);
+// backward weight-gradient GEMMs dW2 = (wa_hi + wa_lo)^T dy_perm,
+// dW1 = x_perm^T (dH_hi + dH_lo)
 int launch_backward_weight_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
                                  const void* x_perm, const void* dy_perm, const void* dH,
-                                 const void* wa, void* dW1, void* dW2);
+                                 const void* dH_lo, const void* wa, const void* wa_lo, void* dW1,
+                                 void* dW2);
 
 }  // namespace hmm

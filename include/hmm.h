@@ -104,7 +104,7 @@ int hmm_destroy(hmm_ctx* ctx);
  *   HMM_OPT_VALIDATE      0/1: hmm_forward/hmm_route synchronise after routing
  *                         and return HMM_ERR_EXPERT_ID for a bad id (default 0).
  *   HMM_OPT_WAIT_BUDGET_NS  budget of every bounded device wait, in ns
- *                         (default 1e9; range 1e6 .. 6e10).
+ *                         (default 2e9; range 1e6 .. 6e10).
  *   HMM_OPT_INJECT_SKIP_READY  test-only fault injection on the host side: when
  *                         1, the next hmm_forward launches its GMM1 tiles
  *                         without releasing the GMM2 ready counters, so every
@@ -113,7 +113,27 @@ int hmm_destroy(hmm_ctx* ctx);
 #define HMM_OPT_VALIDATE 1
 #define HMM_OPT_WAIT_BUDGET_NS 2
 #define HMM_OPT_INJECT_SKIP_READY 3
+/*   HMM_OPT_PROFILE       0/1: bracket every launch phase with CUDA events
+ *                         recorded on the call's stream (read them with
+ *                         hmm_profile_read).  Default 0. */
+#define HMM_OPT_PROFILE 4
 int hmm_set_option(hmm_ctx* ctx, int option, int64_t value);
+
+/* Launch phases timed under HMM_OPT_PROFILE (index = phase id):
+ *   0 route (3 kernels)    1 dispatch_x      2 gemm_fwd (GMM1+SwiGLU, GMM2)
+ *   3 combine_y            4 dispatch_dy     5 gemm_bwd_data (act_grad +
+ *   SwiGLU grad, input-grad)                 6 gemm_bwd_weight (W1Grad,
+ *   W2Grad)                7 combine_dx (+ d_topk_weights)              */
+#define HMM_NUM_PHASES 8
+
+/* Tracing: waits for every event recorded since the previous read, then
+ * writes, for each phase id < n, the summed GPU time in ms (ms[i]) and the
+ * number of kernel launches (launches[i]) recorded since that read, and
+ * resets the counters.  Either array may be NULL. */
+int hmm_profile_read(hmm_ctx* ctx, int n, double* ms, int64_t* launches);
+
+/* Name of a phase id ("route", "gemm_fwd", ...), or NULL if out of range. */
+const char* hmm_phase_name(int phase);
 
 /* Buffer sizes in bytes for a shape.  training != 0: the forward keeps its
  * activations in `saved` for the backward; training == 0: they live in the
