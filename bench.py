@@ -45,16 +45,22 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-sample", type=int, default=256,
+    ap.add_argument("--cpu-sample", type=int, default=1024,
                     help="tokens of the oracle's CPU-baseline sample")
     ap.add_argument("--ref-sample", type=int, default=48,
                     help="tokens per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--shape", default=None,
+                    help="T,H,I,E,K override (profiling of a smaller case; not a bench line)")
+    a = ap.parse_args()
+    if a.shape:
+        T, H, I, E, K = (int(v) for v in a.shape.split(","))
+        WORKLOAD.update(T=T, H=H, I=I, E=E, K=K)
+    return a
 
 
 # --------------------------------------------------------------- distributed
@@ -104,25 +110,25 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_hash() -> str:
+def source_hash(files) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dispatch_grouped_gemm_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in files:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def load_traffic(kernel: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current sources of that kernel (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
+        if d.get("source_hash") != source_hash(d["files"]):
+            return None
     except Exception:
-        return None
-    if d.get("source_hash") != source_hash():
         return None
     v = d.get("kernels", {}).get(kernel)
     return None if v is None else float(v)
@@ -253,7 +259,10 @@ def run_ours(args, dist: Dist):
     dev = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(dev)
     T, H, I, E, K = (WORKLOAD[k] for k in ("T", "H", "I", "E", "K"))
-    prob = mi.make("backward")
+    if args.shape:
+        prob = mi.make_shape(T, H, I, E, K, seed=1004)
+    else:
+        prob = mi.make("backward")
 
     def bf16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
@@ -434,6 +443,8 @@ def run_ours(args, dist: Dist):
         "gpu_launches_traced": int(sum(v[1] for v in prof.values())),
         "clocks": clocks,
     }
+    if args.shape:
+        out["config"]["workload"] = f"profiling case T={T} H={H} I={I} E={E} K={K}"
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(prob, args.cpu_sample)
     if dist.rank == 0:
