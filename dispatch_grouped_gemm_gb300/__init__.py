@@ -22,7 +22,7 @@ import torch
 
 __all__ = [
     "HmmError", "HmmShape", "hmm_create", "hmm_destroy", "hmm_set_option",
-    "hmm_workspace_size", "hmm_route", "hmm_forward", "hmm_backward", "hmm_status",
+    "hmm_workspace_size", "hmm_route", "hmm_route_static", "hmm_forward", "hmm_backward", "hmm_status",
     "hmm_error_string", "Context", "moe_ffn", "library_path", "load_library",
     "hmm_profile_read", "hmm_phase_name",
     "HMM_OPT_VALIDATE", "HMM_OPT_WAIT_BUDGET_NS", "HMM_OPT_INJECT_SKIP_READY", "HMM_OPT_PROFILE",
@@ -100,6 +100,7 @@ def load_library():
             "hmm_workspace_size": [sp, i32, ctypes.POINTER(sz), ctypes.POINTER(sz),
                                    ctypes.POINTER(sz)],
             "hmm_route": [vp, sp, vp, vp, vp, vp, vp, vp, sz, vp],
+            "hmm_route_static": [sp, vp, vp, vp, vp, vp, vp],
             "hmm_forward": [vp, sp, vp, vp, vp, vp, vp, vp, vp, sz, vp, sz, vp],
             "hmm_backward": [vp, sp, vp, vp, vp, vp, vp, sz, vp, vp, vp, vp, vp, sz, vp],
             "hmm_status": [vp, vp, ctypes.POINTER(i32)],
@@ -179,6 +180,15 @@ def hmm_route(ctx, shape, topk_ids, counts, offsets, slot2row, row2slot, workspa
                                   _ptr(offsets), _ptr(slot2row), _ptr(row2slot), _ptr(workspace),
                                   _nbytes(workspace), _stream(stream))
     _check(rc, "hmm_route")
+
+
+def hmm_route_static(shape, topk_ids, counts, offsets, slot2row, row2slot, stream=None):
+    """Routing on the current device with the library's static scratch (no
+    allocation, no context); see include/hmm.h."""
+    rc = load_library().hmm_route_static(ctypes.byref(shape), _ptr(topk_ids), _ptr(counts),
+                                         _ptr(offsets), _ptr(slot2row), _ptr(row2slot),
+                                         _stream(stream))
+    _check(rc, "hmm_route_static")
 
 
 def hmm_forward(ctx, shape, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight, y,

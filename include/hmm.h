@@ -157,6 +157,31 @@ int hmm_route(hmm_ctx* ctx, const hmm_shape* shape, const int32_t* topk_ids,
               int32_t* row2slot, void* workspace, size_t workspace_bytes,
               void* stream);
 
+/* Routing with no allocation and no context.  The paper has no counterpart
+ * of this entry point; it exists for callers that cannot allocate device
+ * memory (an engine whose memory pool owns the whole device, a plug-in whose
+ * host gives it no allocator or workspace).
+ *
+ * Computes exactly what hmm_route computes (same kernels, same outputs, same
+ * argument meaning and layout), on the current CUDA device, asynchronously
+ * on `stream`.  Its scratch is one 8 MiB device array inside the library
+ * (held by every GPU that loads the library until the process exits); it
+ * calls no cudaMalloc, cudaFree or other allocating routine.
+ * - The first call on each device looks up the array's device address (and
+ *   checks that the device is sm_103); make that first call before any stream
+ *   capture on that device.
+ * - Every call shares the one array: calls whose GPU work overlaps (on two
+ *   streams, or from two host threads) race and give undefined results.
+ *   Serialise them on one stream.
+ * - A shape whose scratch exceeds the array returns HMM_ERR_CAPACITY before
+ *   any device work; the scratch grows with T*K and E (about 12 bytes per
+ *   slot plus 4*E bytes per 1024 slots).
+ * - Ids outside [0, E) are left out: their slot2row is -1 and
+ *   offsets[E] < T*K (there is no status word to read). */
+int hmm_route_static(const hmm_shape* shape, const int32_t* topk_ids,
+                     int32_t* counts, int32_t* offsets, int32_t* slot2row,
+                     int32_t* row2slot, void* stream);
+
 /* Fused forward [HyperMegaMoE §2.1]: y = Combine(GMM2(SwiGLU(GMM1(Dispatch(x))))).
  * saved == NULL: inference (the [., 2I] pre-activation is never written to
  * memory).  Otherwise saved (saved_bytes from hmm_workspace_size with
