@@ -38,7 +38,7 @@ sys.path.insert(0, ROOT)
 WORKLOAD = dict(T=4096, H=2048, I=1408, E=64, K=6)
 WORKLOAD_NAME = "prefill-shaped MoE-FFN fwd+bwd: T=4096 H=2048 I=1408 E=64 K=6"
 METRIC = "MoE-FFN tokens/s (fused fwd+bwd step)"
-KERNELS_PER_STEP = 10  # route 3, dispatch_x, gemm_fwd, combine_y, dispatch_dy, 2 bwd gemms, combine_dx
+KERNELS_PER_STEP = 9  # route 3, dispatch_x, gemm_fwd, combine_y, dispatch_dy, gemm_bwd, combine_dx
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -54,9 +54,19 @@ def parse():
                     help="tokens per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", choices=["prefill_fwd_bwd", "skewed_fwd", "decode_fwd"],
+                    default="prefill_fwd_bwd",
+                    help="prefill_fwd_bwd is the benchmark line; the forward-only modes "
+                         "measure the skewed and decode workloads")
+    ap.add_argument("--bwd-data-sms", type=int, default=0,
+                    help="SMs for the data-gradient GEMMs of the backward (0: automatic)")
     ap.add_argument("--shape", default=None,
                     help="T,H,I,E,K override (profiling of a smaller case; not a bench line)")
     a = ap.parse_args()
+    if a.workload == "skewed_fwd":
+        WORKLOAD.update(T=16384, H=7168, I=2048, E=32, K=8)
+    elif a.workload == "decode_fwd":
+        WORKLOAD.update(T=128, H=7168, I=2048, E=256, K=8)
     if a.shape:
         T, H, I, E, K = (int(v) for v in a.shape.split(","))
         WORKLOAD.update(T=T, H=H, I=I, E=E, K=K)
@@ -259,8 +269,13 @@ def run_ours(args, dist: Dist):
     dev = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(dev)
     T, H, I, E, K = (WORKLOAD[k] for k in ("T", "H", "I", "E", "K"))
+    fwd_only = args.workload != "prefill_fwd_bwd"
     if args.shape:
         prob = mi.make_shape(T, H, I, E, K, seed=1004)
+    elif args.workload == "skewed_fwd":
+        prob = mi.make("skewed")
+    elif args.workload == "decode_fwd":
+        prob = mi.make("decode")
     else:
         prob = mi.make("backward")
 
@@ -273,27 +288,33 @@ def run_ours(args, dist: Dist):
     dy = bf16(prob.dy).to(dev)
     W1 = torch.empty((E, H, 2 * I), dtype=torch.bfloat16, device=dev)
     W2 = torch.empty((E, I, H), dtype=torch.bfloat16, device=dev)
-    for e in range(E):
-        W1[e].copy_(bf16(prob.expert_W1(e)))
-        W2[e].copy_(bf16(prob.expert_W2(e)))
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        for e, w1, w2 in ex.map(lambda e: (e, prob.expert_W1(e), prob.expert_W2(e)), range(E)):
+            W1[e].copy_(bf16(w1))
+            W2[e].copy_(bf16(w2))
 
     ctx = hmm.Context.for_device(dev)
+    if args.bwd_data_sms:
+        ctx.set_option(hmm.HMM_OPT_BWD_DATA_SMS, args.bwd_data_sms)
     shape = hmm.Context.shape_of(x, ids, w, W1, W2)
-    fws, svb, bws = hmm.hmm_workspace_size(shape, True)
+    fws, svb, bws = hmm.hmm_workspace_size(shape, not fwd_only)
     y = torch.empty_like(x)
-    saved = torch.empty(svb, dtype=torch.uint8, device=dev)
+    saved = torch.empty(svb, dtype=torch.uint8, device=dev) if not fwd_only else None
     fwork = torch.empty(fws, dtype=torch.uint8, device=dev)
-    bwork = torch.empty(bws, dtype=torch.uint8, device=dev)
+    bwork = torch.empty(bws, dtype=torch.uint8, device=dev) if not fwd_only else None
     dx = torch.empty_like(x)
-    dW1 = torch.empty_like(W1)
-    dW2 = torch.empty_like(W2)
+    dW1 = torch.empty_like(W1) if not fwd_only else None
+    dW2 = torch.empty_like(W2) if not fwd_only else None
     dw = torch.empty_like(w)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def step(xx=x, ii=ids, ww=w, dd=dy):
         hmm.hmm_forward(ctx.handle, shape, xx, ii, ww, W1, W2, y, saved, fwork, stream)
-        hmm.hmm_backward(ctx.handle, shape, dd, ww, W1, W2, saved, dx, dW1, dW2, dw, bwork, stream)
+        if not fwd_only:
+            hmm.hmm_backward(ctx.handle, shape, dd, ww, W1, W2, saved, dx, dW1, dW2, dw, bwork,
+                             stream)
 
     # first call (module load, tensor maps, attribute setup) vs steady state
     torch.cuda.synchronize()
@@ -347,13 +368,17 @@ def run_ours(args, dist: Dist):
         "gemm_fwd": ("tensor", 3 * F),
         "combine_y": ("hbm", (TK * H + T * H) * 2.0 + TK * 2.0),
         "dispatch_dy": ("hbm", (T * H + TK * H) * 2.0),
-        "gemm_bwd_data": ("tensor", 3 * F),
-        "gemm_bwd_weight": ("tensor", 3 * F),
+        "gemm_bwd": ("tensor", 6 * F),
         "combine_dx": ("hbm", (TK * H + T * H) * 2.0),
     }
+    if args.workload == "decode_fwd":
+        touched = int(np.unique(prob.topk_ids).size)
+        algo["gemm_fwd"] = ("hbm", touched * (H * 2 * I + I * H) * 2.0 + (T * K) * (H + I) * 4.0)
     peaks, peak_src = load_peaks()
     phases = {}
     for name, (ms, launches) in prof.items():
+        if launches == 0:
+            continue
         n_calls = args.steps
         per_ms = ms / n_calls if n_calls else 0.0
         bound, work = algo[name]
@@ -377,14 +402,14 @@ def run_ours(args, dist: Dist):
                 "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if dp['bound'] == 'tensor' else 'hbm_gbs'})"}
 
     fwd_ms = sum(phases[k]["ms"] for k in ("route", "dispatch_x", "gemm_fwd", "combine_y"))
-    bwd_ms = sum(phases[k]["ms"] for k in ("dispatch_dy", "gemm_bwd_data", "gemm_bwd_weight",
-                                            "combine_dx"))
-    gemm_flops = 9 * F  # 6 TK H I forward + 12 TK H I backward
-    gemm_ms = sum(phases[k]["ms"] for k in ("gemm_fwd", "gemm_bwd_data", "gemm_bwd_weight"))
+    bwd_ms = sum(phases[k]["ms"] for k in ("dispatch_dy", "gemm_bwd", "combine_dx")
+                 if k in phases)
+    gemm_flops = 3 * F if fwd_only else 9 * F  # 6 TK H I forward + 12 TK H I backward
+    gemm_ms = sum(phases[k]["ms"] for k in ("gemm_fwd", "gemm_bwd") if k in phases)
 
     # ------------------------------------------------------------------ e2e
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not fwd_only:
         hx = bf16(prob.x).pin_memory()
         hids = torch.from_numpy(prob.topk_ids).pin_memory()
         hw = bf16(prob.topk_weights).pin_memory()
@@ -443,9 +468,13 @@ def run_ours(args, dist: Dist):
         "gpu_launches_traced": int(sum(v[1] for v in prof.values())),
         "clocks": clocks,
     }
+    if fwd_only:
+        out["metric"] = "MoE-FFN tokens/s (fused forward, inference)"
+        out["config"]["workload"] = f"{args.workload}: T={T} H={H} I={I} E={E} K={K}"
+        out["gpu_launches"] = 6 * args.steps
     if args.shape:
         out["config"]["workload"] = f"profiling case T={T} H={H} I={I} E={E} K={K}"
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and not fwd_only:
         out["cpu_baseline"] = cpu_baseline(prob, args.cpu_sample)
     if dist.rank == 0:
         emit(out)

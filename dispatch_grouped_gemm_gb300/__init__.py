@@ -26,6 +26,7 @@ __all__ = [
     "hmm_error_string", "Context", "moe_ffn", "library_path", "load_library",
     "hmm_profile_read", "hmm_phase_name",
     "HMM_OPT_VALIDATE", "HMM_OPT_WAIT_BUDGET_NS", "HMM_OPT_INJECT_SKIP_READY", "HMM_OPT_PROFILE",
+    "HMM_OPT_BWD_DATA_SMS",
     "HMM_DTYPE_BF16", "HMM_DTYPE_F32", "HMM_STATUS_EXPERT_ID", "HMM_STATUS_TIMEOUT",
 ]
 
@@ -54,6 +55,7 @@ HMM_OPT_VALIDATE = _C["HMM_OPT_VALIDATE"]
 HMM_OPT_WAIT_BUDGET_NS = _C["HMM_OPT_WAIT_BUDGET_NS"]
 HMM_OPT_INJECT_SKIP_READY = _C["HMM_OPT_INJECT_SKIP_READY"]
 HMM_OPT_PROFILE = _C["HMM_OPT_PROFILE"]
+HMM_OPT_BWD_DATA_SMS = _C["HMM_OPT_BWD_DATA_SMS"]
 HMM_DTYPE_BF16 = _C["HMM_DTYPE_BF16"]
 HMM_DTYPE_F32 = _C["HMM_DTYPE_F32"]
 HMM_STATUS_EXPERT_ID = _C["HMM_STATUS_EXPERT_ID"]

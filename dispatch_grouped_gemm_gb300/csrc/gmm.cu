@@ -10,17 +10,22 @@
 //   wgrad mode  out[e] = A[rows of e]^T . B[rows of e]     (contraction over
 //               the expert's padded rows; A, B: activations, MN-major)
 //
-// One launch may hold two problems.  Tiles are handed out through a global
-// atomic ticket, all tiles of problem 0 before those of problem 1.  A tile of
-// problem 1 may wait on a per-M-tile ready counter that the epilogues of
-// problem 0 release [HyperMegaMoE §2.1: tasks split by token/expert tile,
-// event counts release downstream tasks, no global barrier].  Because every
-// producer tile has a smaller ticket, it was already taken by a running CTA
-// when its consumer spins, so the wait cannot deadlock; it is bounded anyway.
+// One launch holds up to four problems.  Tiles are handed out through a global
+// atomic ticket in "schedule steps": step j holds, for every problem p, the
+// tiles of expert j - lag_p.  A consumer problem runs a few experts behind its
+// producer and waits on a ready counter (per M-tile, or per expert for the
+// weight gradients) that the producer's epilogues release [HyperMegaMoE §2.1:
+// tasks split by token/expert tile, event counts release downstream tasks, no
+// global barrier; §2.2 / §5.2: W2Grad interleaved with the act_grad branch,
+// W1Grad overlapped with the input gradient].  Interleaving experts mixes
+// memory-bound and tensor-bound tiles in flight.  Every producer tile has a
+// smaller ticket than its consumers, so it was already taken by a running CTA
+// when a consumer spins: the wait cannot deadlock (and is bounded anyway).
 //
-// CTA = 6 warps: warp 0 issues TMA loads (one thread), warp 1 allocates TMEM
-// and issues tcgen05.mma (one thread), warps 2..5 drain the accumulators
-// (each owns the 32 TMEM lanes of its warp id mod 4).  Two 128x256 fp32
+// CTA = 7 warps: warp 6 schedules tiles (tickets, decoding, dependency waits,
+// about one tile ahead), warp 0 issues TMA loads (one thread), warp 1
+// allocates TMEM and issues tcgen05.mma (one thread), warps 2..5 drain the
+// accumulators (each owns the 32 TMEM lanes of its warp id mod 4).  Two 128x256 fp32
 // accumulators in TMEM (512 columns) let the epilogue of one tile overlap the
 // MMAs of the next; a 4-stage ring of 48 KB smem stages feeds the MMAs.
 #include <cuda_bf16.h>
@@ -46,9 +51,10 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int TI_DEPTH = 4;
-constexpr int NUM_THREADS = 192;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 1024;
+constexpr int TI_DEPTH = 3;
+constexpr int NUM_THREADS = 224;  // 7 warps
+// alignment slack + stages + barriers, tile-info ring and schedule prefix table
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 512 + 4 * (3 * MAX_E + 8 + 1) + 256;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 
 struct Prob {
@@ -68,22 +74,38 @@ struct Prob {
   void* out4;           // SwiGLU grad: low bf16 half of dH (same layout as out)
   void* out5;           // SwiGLU grad: low bf16 half of w*a (same layout as out2)
   int split;            // wgrad: 0 none, 1 A operand given as hi+lo, 2 B operand hi+lo
+  int wgrad;            // 1: contraction over the expert's rows (tile count fixed per expert)
+  int lag;              // the tiles of expert e are issued at schedule step e + lag
+  int group;            // CTA group whose ticket queue holds this problem's tiles
   const void* aux;
   int64_t ld_aux;
   const float* rowscale;
-  int* signal;       // per-M-tile counters released after a tile's stores
-  const int* wait;   // per-M-tile counters acquired before a tile's A loads
-  int wait_target;
+  int* signal_m;        // per-M-tile counters released after a tile's stores
+  int* signal_e;        // per-expert counters released after a tile's stores
+  const int* wait_m;    // per-M-tile counter acquired before a tile's loads
+  const int* wait_e;    // per-expert counter acquired before a tile's loads
+  int wait_unit;        // target: wait_unit (per M-tile) or wait_unit * M-tiles of e
 };
 
+constexpr int MAX_PROB = 4;
+constexpr int MAX_STEPS = 3 * MAX_E + 8;
+
 struct Params {
-  Prob p[2];
+  Prob p[MAX_PROB];
   int nprob;
+  int steps[2];         // per CTA group: E + largest lag of its problems
+  int group_split;      // CTAs [0, group_split) serve group 0, the rest group 1
+                        // (0: one group)
   const int32_t* poff;
+  const int32_t* counts;
   int E;
   int* ticket;
   unsigned* status;
   unsigned long long budget_ns;
+};
+
+struct Maps {
+  CUtensorMap m[MAX_PROB][3];  // A, B, and the low half of a split operand
 };
 
 struct TileInfo {
@@ -96,39 +118,83 @@ struct TileInfo {
 };
 
 // ----------------------------------------------------------------- scheduler
-__device__ __forceinline__ int tiles_of(const Params& P, const Prob& pr, bool wgrad) {
-  if (wgrad) return P.E * pr.m_tiles * pr.n_tiles;
-  return (P.poff[P.E] / BM) * pr.n_tiles;
+__device__ __forceinline__ int mtiles_of(const Params& P, int e) {
+  return (P.poff[e + 1] - P.poff[e]) / BM;
+}
+
+__device__ __forceinline__ int tiles_of(const Params& P, const Prob& pr, int e) {
+  if (e < 0 || e >= P.E) return 0;
+  if (pr.wgrad) return pr.m_tiles * pr.n_tiles;
+  return mtiles_of(P, e) * pr.n_tiles;
+}
+
+// Prefix sums of the tile counts of group g's schedule steps (one warp, into
+// smem).
+__device__ void build_schedule(const Params& P, int g, int* pref) {
+  const int lane = threadIdx.x & 31;
+  const int steps = P.steps[g];
+  int carry = 0;
+  if (lane == 0) pref[0] = 0;
+  for (int base = 0; base < steps; base += 32) {
+    const int j = base + lane;
+    int v = 0;
+    if (j < steps)
+      for (int q = 0; q < P.nprob; ++q)
+        if (P.p[q].group == g) v += tiles_of(P, P.p[q], j - P.p[q].lag);
+    int inc = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, inc, d);
+      if (lane >= d) inc += n;
+    }
+    if (j < steps) pref[j + 1] = carry + inc;
+    carry += __shfl_sync(0xffffffffu, inc, 31);
+  }
+  __syncwarp();
+}
+
+// Ticket t of group g -> (problem, expert, local tile index).  Returns false
+// past the end.
+__device__ bool locate_tile(const Params& P, int g, const int* pref, int t, int& prob, int& e,
+                            int& r) {
+  const int steps = P.steps[g];
+  if (t >= pref[steps]) return false;
+  int lo = 0, hi = steps - 1;  // largest step j with pref[j] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pref[mid] <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  r = t - pref[lo];
+  for (int q = 0; q < P.nprob; ++q) {
+    if (P.p[q].group != g) continue;
+    const int eq = lo - P.p[q].lag;
+    const int c = tiles_of(P, P.p[q], eq);
+    if (r < c) {
+      prob = q;
+      e = eq;
+      return true;
+    }
+    r -= c;
+  }
+  return false;  // not reached
 }
 
 template <class C>
-__device__ void decode_tile(const Params& P, const Prob& pr, int u, TileInfo& ti) {
+__device__ void decode_tile(const Params& P, const Prob& pr, int e, int r, TileInfo& ti) {
+  ti.e = e;
   if constexpr (C::WGRAD) {
-    const int per = pr.m_tiles * pr.n_tiles;
-    const int e = u / per;
-    const int r = u - e * per;
-    ti.e = e;
     ti.m0 = (r / pr.n_tiles) * BM;
     ti.n0 = (r % pr.n_tiles) * BN;
     ti.krow0 = P.poff[e];
-    ti.kb = (P.poff[e + 1] - P.poff[e]) / BK * (pr.split ? 2 : 1);
+    // rows past counts[e] are zero padding: skip whole zero K blocks
+    ti.kb = (P.counts[e] + BK - 1) / BK * (pr.split ? 2 : 1);
   } else {
-    // largest e with n_tiles * poff[e]/BM <= u (empty experts own no tiles)
-    int lo = 0, hi = P.E - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if ((P.poff[mid] / BM) * pr.n_tiles <= u)
-        lo = mid;
-      else
-        hi = mid - 1;
-    }
-    const int e = lo;
-    const int mt0 = P.poff[e] / BM;
-    const int nm = P.poff[e + 1] / BM - mt0;
-    const int local = u - mt0 * pr.n_tiles;
-    const int nb = local / nm;
-    ti.e = e;
-    ti.m0 = (mt0 + (local - nb * nm)) * BM;
+    const int nm = mtiles_of(P, e);
+    const int nb = r / nm;  // M tiles innermost: a weight tile is reused from L2
+    ti.m0 = P.poff[e] + (r - nb * nm) * BM;
     ti.n0 = nb * (C::EPI == EPI_SWIGLU ? BN / 2 : BN);
     ti.krow0 = 0;
     ti.kb = (pr.K + BK - 1) / BK;
@@ -136,11 +202,19 @@ __device__ void decode_tile(const Params& P, const Prob& pr, int u, TileInfo& ti
 }
 
 // ----------------------------------------------------------------- producer
+// Loads the operand boxes of K block kb of a tile into one smem stage.  Every
+// box starts at an inner coordinate that is a multiple of 8 elements (16 bytes).
 template <class C>
-__device__ __forceinline__ void load_stage(const Prob& pr, const TileInfo& ti, int kb,
-                                           const CUtensorMap* tA, const CUtensorMap* tB,
-                                           const CUtensorMap* tS, uint8_t* sA, uint8_t* sB,
-                                           uint64_t* bar) {
+__device__ __forceinline__ void stage_boxes(const Prob& pr, const TileInfo& ti, int kb,
+                                            const CUtensorMap* tA, const CUtensorMap* tB,
+                                            const CUtensorMap* tS, uint8_t* sA, uint8_t* sB,
+                                            uint64_t* bar) {
+  auto ld2 = [&](void* dst, const CUtensorMap* m, int c0, int c1) {
+    tma_load_2d(dst, m, bar, c0, c1);
+  };
+  auto ld3 = [&](void* dst, const CUtensorMap* m, int c0, int c1, int c2) {
+    tma_load_3d(dst, m, bar, c0, c1, c2);
+  };
   if constexpr (C::WGRAD) {
     // with a split operand the K loop runs twice over the expert's rows:
     // first against the high bf16 half, then against the low half
@@ -149,28 +223,36 @@ __device__ __forceinline__ void load_stage(const Prob& pr, const TileInfo& ti, i
     const int k = ti.krow0 + (lo ? kb - nk : kb) * BK;
     const CUtensorMap* a = (pr.split == 1 && lo) ? tS : tA;
     const CUtensorMap* b = (pr.split == 2 && lo) ? tS : tB;
-    tma_load_2d(sA, a, bar, ti.m0, k);
-    tma_load_2d(sA + 8192, a, bar, ti.m0 + 64, k);
+    ld2(sA, a, ti.m0, k);
+    ld2(sA + 8192, a, ti.m0 + 64, k);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * 8192, b, bar, ti.n0 + 64 * j, k);
+    for (int j = 0; j < 4; ++j) ld2(sB + j * 8192, b, ti.n0 + 64 * j, k);
   } else {
     (void)tS;
     const int k = kb * BK;
-    tma_load_2d(sA, tA, bar, k, ti.m0);
+    ld2(sA, tA, k, ti.m0);
     if constexpr (C::B_MN) {
       if constexpr (C::EPI == EPI_SWIGLU) {
-        tma_load_3d(sB, tB, bar, ti.n0, k, ti.e);
-        tma_load_3d(sB + 8192, tB, bar, ti.n0 + 64, k, ti.e);
-        tma_load_3d(sB + 16384, tB, bar, pr.half + ti.n0, k, ti.e);
-        tma_load_3d(sB + 24576, tB, bar, pr.half + ti.n0 + 64, k, ti.e);
+        ld3(sB, tB, ti.n0, k, ti.e);
+        ld3(sB + 8192, tB, ti.n0 + 64, k, ti.e);
+        ld3(sB + 16384, tB, pr.half + ti.n0, k, ti.e);
+        ld3(sB + 24576, tB, pr.half + ti.n0 + 64, k, ti.e);
       } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) tma_load_3d(sB + j * 8192, tB, bar, ti.n0 + 64 * j, k, ti.e);
+        for (int j = 0; j < 4; ++j) ld3(sB + j * 8192, tB, ti.n0 + 64 * j, k, ti.e);
       }
     } else {
-      tma_load_3d(sB, tB, bar, k, ti.n0, ti.e);
+      ld3(sB, tB, k, ti.n0, ti.e);
     }
   }
+}
+
+template <class C>
+__device__ __forceinline__ void load_stage(const Prob& pr, const TileInfo& ti, int kb,
+                                           const CUtensorMap* tA, const CUtensorMap* tB,
+                                           const CUtensorMap* tS, uint8_t* sA, uint8_t* sB,
+                                           uint64_t* bar) {
+  stage_boxes<C>(pr, ti, kb, tA, tB, tS, sA, sB, bar);
 }
 
 // ---------------------------------------------------------------------- MMA
@@ -364,12 +446,17 @@ __device__ __noinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t
 }
 
 // ------------------------------------------------------------------- kernel
-template <class C0, class C1>
+#define HMM_BY_PROB(q, F, ...)       \
+  switch (q) {                       \
+    case 0: F<C0>(__VA_ARGS__); break; \
+    case 1: F<C1>(__VA_ARGS__); break; \
+    case 2: F<C2>(__VA_ARGS__); break; \
+    default: F<C3>(__VA_ARGS__); break; \
+  }
+
+template <class C0, class C1, class C2, class C3>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gmm_kernel(const __grid_constant__ Params P, const __grid_constant__ CUtensorMap tA0,
-               const __grid_constant__ CUtensorMap tB0, const __grid_constant__ CUtensorMap tS0,
-               const __grid_constant__ CUtensorMap tA1, const __grid_constant__ CUtensorMap tB1,
-               const __grid_constant__ CUtensorMap tS1) {
+    gmm_kernel(const __grid_constant__ Params P, const __grid_constant__ Maps maps) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -385,6 +472,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   TileInfo* s_ti = reinterpret_cast<TileInfo*>(mma_done + 1);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_ti + TI_DEPTH);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  int* s_pref = reinterpret_cast<int*>(s_tmem + 2);  // [steps + 1]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -400,7 +488,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < TI_DEPTH; ++i) {
       mbar_init(&ti_full[i], 1);
-      mbar_init(&ti_empty[i], 5);
+      mbar_init(&ti_empty[i], 6);  // TMA producer, MMA issuer, 4 epilogue warps
     }
     mbar_init(mma_done, 1);
     *s_abort = 0;
@@ -416,39 +504,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *s_tmem;
   const WaitCtl wc{s_abort, P.status, P.budget_ns};
 
-  if (warp == 0) {
+  const int group = (P.group_split > 0 && static_cast<int>(blockIdx.x) >= P.group_split) ? 1 : 0;
+  if (warp == 6) {
+    // --------------------------------------------------------- tile scheduler
+    // Fetches tickets, decodes them and waits for each tile's dependencies
+    // about one tile ahead of the TMA producer, so neither the ticket atomic
+    // nor a ready-counter poll sits on the load path.  (A deeper lookahead
+    // spreads the M tiles that share a weight tile over time and costs L2
+    // reuse of the weights.)
+    build_schedule(P, group, s_pref);
     if (lane == 0) {
-      // ------------------------------------------------------- TMA producer
-      tma_prefetch_desc(&tA0);
-      tma_prefetch_desc(&tB0);
-      if (P.p[0].split) tma_prefetch_desc(&tS0);
-      if (P.nprob > 1) {
-        tma_prefetch_desc(&tA1);
-        tma_prefetch_desc(&tB1);
-        if (P.p[1].split) tma_prefetch_desc(&tS1);
-      }
-      const int T0 = tiles_of(P, P.p[0], C0::WGRAD);
-      const int T1 = P.nprob > 1 ? tiles_of(P, P.p[1], C1::WGRAD) : 0;
-      uint32_t stage = 0, sphase = 0;
       int ti_slot = 0;
       uint32_t ti_phase = 0;
-      uint32_t issued = 0;  // k-blocks issued by this CTA
-      bool ok = true;
+      int t = atomicAdd(P.ticket + group, 1);
       for (;;) {
-        const int t = atomicAdd(P.ticket, 1);
         TileInfo ti;
         ti.prob = -1;
-        if (t < T0) {
-          ti.prob = 0;
-          decode_tile<C0>(P, P.p[0], t, ti);
-        } else if (t < T0 + T1) {
-          ti.prob = 1;
-          decode_tile<C1>(P, P.p[1], t - T0, ti);
+        int q = 0, e = 0, r = 0;
+        if (locate_tile(P, group, s_pref, t, q, e, r)) {
+          ti.prob = q;
+          HMM_BY_PROB(q, decode_tile, P, P.p[q], e, r, ti);
         }
-        if (!mbar_wait(&ti_empty[ti_slot], ti_phase ^ 1u, wc)) {
-          ok = false;
-          break;
+        if (ti.prob >= 0) t = atomicAdd(P.ticket + group, 1);  // next ticket, early
+        if (ti.prob >= 0) {
+          const Prob& pr = P.p[ti.prob];
+          if (pr.wait_m || pr.wait_e) {
+            const bool got =
+                pr.wait_m ? counter_wait(&pr.wait_m[ti.m0 / BM], pr.wait_unit, wc)
+                          : counter_wait(&pr.wait_e[ti.e], pr.wait_unit * mtiles_of(P, ti.e), wc);
+            if (!got) break;
+          }
         }
+        if (!mbar_wait(&ti_empty[ti_slot], ti_phase ^ 1u, wc)) break;
         s_ti[ti_slot] = ti;
         mbar_arrive(&ti_full[ti_slot]);
         if (++ti_slot == TI_DEPTH) {
@@ -456,14 +543,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ti_phase ^= 1u;
         }
         if (ti.prob < 0) break;
-        const Prob& pr = P.p[ti.prob];
-        if (pr.wait) {
-          if (!counter_wait(&pr.wait[ti.m0 / BM], pr.wait_target, wc)) {
-            ok = false;
-            break;
-          }
-          fence_proxy_async_global();
+      }
+    }
+  } else if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------- TMA producer
+      for (int q = 0; q < P.nprob; ++q) {
+        tma_prefetch_desc(&maps.m[q][0]);
+        tma_prefetch_desc(&maps.m[q][1]);
+        if (P.p[q].split) tma_prefetch_desc(&maps.m[q][2]);
+      }
+      uint32_t stage = 0, sphase = 0;
+      int ti_slot = 0;
+      uint32_t ti_phase = 0;
+      uint32_t issued = 0;  // k-blocks issued by this CTA
+      bool ok = true;
+      for (;;) {
+        if (!mbar_wait(&ti_full[ti_slot], ti_phase, wc)) {
+          ok = false;
+          break;
         }
+        const TileInfo ti = s_ti[ti_slot];
+        mbar_arrive(&ti_empty[ti_slot]);
+        if (++ti_slot == TI_DEPTH) {
+          ti_slot = 0;
+          ti_phase ^= 1u;
+        }
+        if (ti.prob < 0) break;
+        const Prob& pr = P.p[ti.prob];
+        // the scheduler acquired this tile's ready counter (gpu scope) before
+        // publishing it; order that with the async-proxy loads below
+        if (pr.wait_m || pr.wait_e) fence_proxy_async_global();
+        const CUtensorMap* mp = maps.m[ti.prob];
         for (int kb = 0; kb < ti.kb; ++kb) {
           if (!mbar_wait(&empty[stage], sphase ^ 1u, wc)) {
             ok = false;
@@ -472,10 +583,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint8_t* sA = stages + stage * STAGE_BYTES;
           uint8_t* sB = sA + A_BYTES;
           mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-          if (ti.prob == 0)
-            load_stage<C0>(pr, ti, kb, &tA0, &tB0, &tS0, sA, sB, &full[stage]);
-          else
-            load_stage<C1>(pr, ti, kb, &tA1, &tB1, &tS1, sA, sB, &full[stage]);
+          HMM_BY_PROB(ti.prob, load_stage, pr, ti, kb, &mp[0], &mp[1], &mp[2], sA, sB,
+                      &full[stage]);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -519,10 +628,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t a_base = smem_u32(stages + stage * STAGE_BYTES);
           const uint32_t b_base = a_base + A_BYTES;
-          if (ti.prob == 0)
-            mma_stage<C0>(d_tmem, a_base, b_base, kb == 0);
-          else
-            mma_stage<C1>(d_tmem, a_base, b_base, kb == 0);
+          HMM_BY_PROB(ti.prob, mma_stage, d_tmem, a_base, b_base, kb == 0);
           umma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
@@ -538,7 +644,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       umma_commit(mma_done);
       drain_wait(mma_done, 0, P.budget_ns);
     }
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------- epilogue
     const int q = warp & 3;
     const int row_in_tile = q * 32 + lane;
@@ -561,10 +667,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (ti.prob < 0) break;
       const Prob& pr = P.p[ti.prob];
       if (ti.kb == 0) {
-        if (ti.prob == 0)
-          epilogue_zero<C0>(pr, ti, row_in_tile);
-        else
-          epilogue_zero<C1>(pr, ti, row_in_tile);
+        HMM_BY_PROB(ti.prob, epilogue_zero, pr, ti, row_in_tile);
         continue;
       }
       if (lane == 0) got = mbar_wait(&tfull[acc], acc_phase, wc);
@@ -573,17 +676,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!got) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      if (ti.prob == 0)
-        epilogue_tile<C0>(pr, ti, taddr, row_in_tile);
-      else
-        epilogue_tile<C1>(pr, ti, taddr, row_in_tile);
+      HMM_BY_PROB(ti.prob, epilogue_tile, pr, ti, taddr, row_in_tile);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
-      if (pr.signal) {
+      if (pr.signal_m || pr.signal_e) {
         fence_proxy_async_global();
         __syncwarp();
-        if (lane == 0) red_release_add(&pr.signal[ti.m0 / BM], 1);
+        if (lane == 0) {
+          if (pr.signal_m) red_release_add(&pr.signal_m[ti.m0 / BM], 1);
+          if (pr.signal_e) red_release_add(&pr.signal_e[ti.e], 1);
+        }
       }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
@@ -635,19 +738,30 @@ int map_w(const GemmEnv& env, CUtensorMap* m, const void* base, int64_t E, int64
   return encode(env, m, base, 3, dims, str, box);
 }
 
-template <class C0, class C1>
-int launch(const GemmEnv& env, Params& P, const CUtensorMap& a0, const CUtensorMap& b0,
-           const CUtensorMap& s0, const CUtensorMap& a1, const CUtensorMap& b1,
-           const CUtensorMap& s1, int64_t max_tiles) {
-  if (max_tiles <= 0) return HMM_OK;
-  auto kern = gmm_kernel<C0, C1>;
+template <class C0, class C1, class C2, class C3>
+int launch(const GemmEnv& env, Params& P, const Maps& maps, int64_t max_tiles) {
+  if (max_tiles <= 0 || P.nprob == 0) return HMM_OK;
+  auto kern = gmm_kernel<C0, C1, C2, C3>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
       cudaSuccess)
     return HMM_ERR_CUDA;
-  const int grid = static_cast<int>(std::min<int64_t>(env.num_sms, max_tiles));
+  int max_lag[2] = {-1, -1};
+  for (int q = 0; q < P.nprob; ++q)
+    max_lag[P.p[q].group] = std::max(max_lag[P.p[q].group], P.p[q].lag);
+  for (int g = 0; g < 2; ++g) {
+    P.steps[g] = max_lag[g] < 0 ? 0 : P.E + max_lag[g];
+    if (P.steps[g] > MAX_STEPS) return HMM_ERR_SHAPE;
+  }
+  int grid = static_cast<int>(std::min<int64_t>(env.num_sms, max_tiles));
+  if (max_lag[1] < 0) P.group_split = 0;
+  if (P.group_split > 0) {
+    // both groups need CTAs: the grid is every SM, the split inside it
+    grid = env.num_sms;
+    P.group_split = std::min(std::max(P.group_split, 1), grid - 1);
+  }
   P.status = env.status;
   P.budget_ns = env.budget_ns;
-  kern<<<grid, NUM_THREADS, SMEM_BYTES, env.stream>>>(P, a0, b0, s0, a1, b1, s1);
+  kern<<<grid, NUM_THREADS, SMEM_BYTES, env.stream>>>(P, maps);
   return cudaGetLastError() == cudaSuccess ? HMM_OK : HMM_ERR_CUDA;
 }
 
@@ -663,16 +777,19 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
                          const void* x_perm, const void* W1, const void* W2, void* a, float* h32,
                          void* o, bool skip_ready_release) {
   const int64_t H = p.H, I = p.I, E = p.E, R = p.R;
-  CUtensorMap tA0, tB0, tA1, tB1;
+  Maps maps;
   int rc = HMM_OK;
-  rc |= map_act(env, &tA0, x_perm, R, H, BM);        // x_perm [R, H], K = H
-  rc |= map_w(env, &tB0, W1, E, H, 2 * I, 64);       // W1 [E, H, 2I]: MN-major B
-  rc |= map_act(env, &tA1, a, R, I, BM);             // a [R, I], K = I
-  rc |= map_w(env, &tB1, W2, E, I, H, 64);           // W2 [E, I, H]: MN-major B
+  rc |= map_act(env, &maps.m[0][0], x_perm, R, H, BM);   // x_perm [R, H], K = H
+  rc |= map_w(env, &maps.m[0][1], W1, E, H, 2 * I, 64);  // W1 [E, H, 2I]: MN-major B
+  rc |= map_act(env, &maps.m[1][0], a, R, I, BM);        // a [R, I], K = I
+  rc |= map_w(env, &maps.m[1][1], W2, E, I, H, 64);      // W2 [E, I, H]: MN-major B
   if (rc != HMM_OK) return HMM_ERR_CUDA;
+  maps.m[0][2] = maps.m[0][0];
+  maps.m[1][2] = maps.m[1][0];
   Params P{};
   P.nprob = 2;
   P.poff = m.poff;
+  P.counts = m.counts;
   P.E = static_cast<int>(E);
   P.ticket = c.tickets + 0;
   Prob& g1 = P.p[0];
@@ -684,34 +801,52 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
   g1.ld_out = I;
   g1.out2 = h32;
   g1.ld_out2 = 2 * I;
-  g1.signal = skip_ready_release ? nullptr : c.ready;
+  g1.signal_m = skip_ready_release ? nullptr : c.ready;
   Prob& g2 = P.p[1];
   g2.K = static_cast<int>(I);
   g2.N = static_cast<int>(H);
   g2.n_tiles = static_cast<int>((H + BN - 1) / BN);
   g2.out = o;
   g2.ld_out = H;
-  g2.wait = c.ready;
-  g2.wait_target = 4 * g1.n_tiles;
+  // GMM2 after every GMM1 tile has been handed out: its ready waits then only
+  // meet the last wave of GMM1 tiles
+  g2.lag = static_cast<int>(E);
+  g2.wait_m = c.ready;
+  g2.wait_unit = 4 * g1.n_tiles;  // the 4 epilogue warps of every GMM1 tile of the M tile
   const int64_t max_tiles = p.max_mtiles * (g1.n_tiles + g2.n_tiles);
-  return launch<CfgGmm1, CfgGmm2>(env, P, tA0, tB0, tA0, tA1, tB1, tA1, max_tiles);
+  return launch<CfgGmm1, CfgGmm2, CfgGmm2, CfgGmm2>(env, P, maps, max_tiles);
 }
 
-int launch_backward_data_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
-                               const void* dy_perm, const float* wperm, const float* h32,
-                               const void* W1, const void* W2, void* dH, void* dH_lo, void* wa,
-                               void* wa_lo, float* dwp, void* dx_perm) {
+int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
+                          const void* x_perm, const void* dy_perm, const float* wperm,
+                          const float* h32, const void* W1, const void* W2, void* dH,
+                          void* dH_lo, void* wa, void* wa_lo, float* dwp, void* dx_perm,
+                          void* dW1, void* dW2) {
   const int64_t H = p.H, I = p.I, E = p.E, R = p.R;
-  CUtensorMap tA0, tB0, tA1, tB1;
+  Maps maps;
   int rc = HMM_OK;
-  rc |= map_act(env, &tA0, dy_perm, R, H, BM);       // dy_perm [R, H], K = H
-  rc |= map_w(env, &tB0, W2, E, I, H, BN);           // W2 [E, I, H] = (W2^T) K-major, N = I
-  rc |= map_act(env, &tA1, dH, R, 2 * I, BM);        // dH [R, 2I] (high half), K = 2I
-  rc |= map_w(env, &tB1, W1, E, H, 2 * I, BN);       // W1 [E, H, 2I] = (W1^T) K-major, N = H
+  // act_grad: G = dy_perm . W2^T   (B = W2 [E, I, H] read K-major, N = I)
+  rc |= map_act(env, &maps.m[0][0], dy_perm, R, H, BM);
+  rc |= map_w(env, &maps.m[0][1], W2, E, I, H, BN);
+  // input-grad: dX_perm = dH . W1^T (B = W1 [E, H, 2I] read K-major, N = H)
+  rc |= map_act(env, &maps.m[1][0], dH, R, 2 * I, BM);
+  rc |= map_w(env, &maps.m[1][1], W1, E, H, 2 * I, BN);
+  // W2Grad: dW2[e] = (wa_hi + wa_lo)^T . dy_perm    [I, rows] x [rows, H]
+  rc |= map_act(env, &maps.m[2][0], wa, R, I, 64);
+  rc |= map_act(env, &maps.m[2][1], dy_perm, R, H, 64);
+  rc |= map_act(env, &maps.m[2][2], wa_lo, R, I, 64);
+  // W1Grad: dW1[e] = x_perm^T . (dH_hi + dH_lo)     [H, rows] x [rows, 2I]
+  rc |= map_act(env, &maps.m[3][0], x_perm, R, H, 64);
+  rc |= map_act(env, &maps.m[3][1], dH, R, 2 * I, 64);
+  rc |= map_act(env, &maps.m[3][2], dH_lo, R, 2 * I, 64);
   if (rc != HMM_OK) return HMM_ERR_CUDA;
+  const CUtensorMap map_w2[3] = {maps.m[2][0], maps.m[2][1], maps.m[2][2]};
+  const CUtensorMap map_w1[3] = {maps.m[3][0], maps.m[3][1], maps.m[3][2]};
+  maps.m[0][2] = maps.m[0][0];
+  maps.m[1][2] = maps.m[1][0];
   Params P{};
-  P.nprob = 2;
   P.poff = m.poff;
+  P.counts = m.counts;
   P.E = static_cast<int>(E);
   P.ticket = c.tickets + 1;
   Prob& ag = P.p[0];
@@ -730,35 +865,16 @@ int launch_backward_data_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, Ct
   ag.aux = h32;
   ag.ld_aux = 2 * I;
   ag.rowscale = wperm;
-  ag.signal = c.ready;
+  ag.signal_m = c.ready;
+  ag.signal_e = c.eready;
   Prob& ig = P.p[1];
   ig.K = static_cast<int>(2 * I);
   ig.N = static_cast<int>(H);
   ig.n_tiles = static_cast<int>((H + BN - 1) / BN);
   ig.out = dx_perm;
   ig.ld_out = H;
-  ig.wait = c.ready;
-  ig.wait_target = 4 * ag.n_tiles;
-  const int64_t max_tiles = p.max_mtiles * (ag.n_tiles + ig.n_tiles);
-  return launch<CfgActGrad, CfgInGrad>(env, P, tA0, tB0, tA0, tA1, tB1, tA1, max_tiles);
-}
-
-int launch_backward_weight_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
-                                 const void* x_perm, const void* dy_perm, const void* dH,
-                                 const void* dH_lo, const void* wa, const void* wa_lo, void* dW1,
-                                 void* dW2) {
-  const int64_t H = p.H, I = p.I, E = p.E, R = p.R;
-  // dW2[e] = (wa_hi + wa_lo)^T . dy_perm : [I, rows] x [rows, H]
-  // dW1[e] = x_perm^T . (dH_hi + dH_lo)  : [H, rows] x [rows, 2I]
-  CUtensorMap w2A, w2B, w2S, w1A, w1B, w1S;
-  int rc = HMM_OK;
-  rc |= map_act(env, &w2A, wa, R, I, 64);
-  rc |= map_act(env, &w2B, dy_perm, R, H, 64);
-  rc |= map_act(env, &w2S, wa_lo, R, I, 64);
-  rc |= map_act(env, &w1A, x_perm, R, H, 64);
-  rc |= map_act(env, &w1B, dH, R, 2 * I, 64);
-  rc |= map_act(env, &w1S, dH_lo, R, 2 * I, 64);
-  if (rc != HMM_OK) return HMM_ERR_CUDA;
+  ig.wait_m = c.ready;
+  ig.wait_unit = 4 * ag.n_tiles;
   Prob w2{}, w1{};
   w2.M = static_cast<int>(I);
   w2.N = static_cast<int>(H);
@@ -776,31 +892,58 @@ int launch_backward_weight_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, 
   w1.ld_out = 2 * I;
   w1.out_estride = H * 2 * I;
   w1.split = 2;
-  Params P{};
-  P.poff = m.poff;
-  P.E = static_cast<int>(E);
-  P.ticket = c.tickets + 2;
-  if (dW2 && dW1) {
-    // dW1 first: its tiles are the larger share, dW2 tiles fill the tail
-    P.nprob = 2;
-    P.p[0] = w1;
-    P.p[1] = w2;
-    const int64_t max_tiles = E * (w1.m_tiles * w1.n_tiles + w2.m_tiles * w2.n_tiles);
-    return launch<CfgWGrad, CfgWGrad>(env, P, w1A, w1B, w1S, w2A, w2B, w2S, max_tiles);
+  for (Prob* w : {&w2, &w1}) {
+    w->wgrad = 1;
+    w->wait_e = c.eready;
+    w->wait_unit = 4 * ag.n_tiles;  // every act_grad tile of every M tile of the expert
   }
-  if (dW1) {
-    P.nprob = 1;
-    P.p[0] = w1;
-    return launch<CfgWGrad, CfgWGrad>(env, P, w1A, w1B, w1S, w1A, w1B, w1S,
-                                      E * w1.m_tiles * w1.n_tiles);
+  ig.lag = static_cast<int>(E);  // input-grad after every act_grad tile is handed out
+  const int64_t data_tiles = p.max_mtiles * (ag.n_tiles + ig.n_tiles);
+  const int64_t w_tiles = (dW2 ? E * w2.m_tiles * w2.n_tiles : 0) +
+                          (dW1 ? E * w1.m_tiles * w1.n_tiles : 0);
+  const int nw = (dW2 ? 1 : 0) + (dW1 ? 1 : 0);
+  auto add_wgrad = [&](Params& Q, int first, int group) {
+    int q = first;
+    if (dW2) {
+      Q.p[q] = w2;
+      Q.p[q].group = group;
+      maps.m[q][0] = map_w2[0];
+      maps.m[q][1] = map_w2[1];
+      maps.m[q][2] = map_w2[2];
+      ++q;
+    }
+    if (dW1) {
+      Q.p[q] = w1;
+      Q.p[q].group = group;
+      maps.m[q][0] = map_w1[0];
+      maps.m[q][1] = map_w1[1];
+      maps.m[q][2] = map_w1[2];
+      ++q;
+    }
+    Q.nprob = q;
+  };
+  if (env.bwd_data_sms > 0 && nw > 0) {
+    // Two CTA groups in one launch: env.bwd_data_sms SMs run act_grad and
+    // input-grad, the others the weight gradients, trailing act_grad expert by
+    // expert.
+    add_wgrad(P, 2, 1);
+    P.group_split = env.bwd_data_sms;
+    return launch<CfgActGrad, CfgInGrad, CfgWGrad, CfgWGrad>(env, P, maps,
+                                                            data_tiles + w_tiles);
   }
-  if (dW2) {
-    P.nprob = 1;
-    P.p[0] = w2;
-    return launch<CfgWGrad, CfgWGrad>(env, P, w2A, w2B, w2S, w2A, w2B, w2S,
-                                      E * w2.m_tiles * w2.n_tiles);
-  }
-  return HMM_OK;
+  // Default: two launches.  The data gradients first; then the weight
+  // gradients, whose per-expert waits are already satisfied.
+  P.nprob = 2;
+  rc = launch<CfgActGrad, CfgInGrad, CfgInGrad, CfgInGrad>(env, P, maps, data_tiles);
+  if (rc != HMM_OK || nw == 0) return rc;
+  Params W{};
+  W.poff = m.poff;
+  W.counts = m.counts;
+  W.E = static_cast<int>(E);
+  W.ticket = c.tickets + 3;
+  add_wgrad(W, 0, 0);
+  for (int q = 0; q < W.nprob; ++q) W.p[q].wait_e = nullptr;  // act_grad has completed
+  return launch<CfgWGrad, CfgWGrad, CfgWGrad, CfgWGrad>(env, W, maps, w_tiles);
 }
 
 }  // namespace hmm

@@ -25,12 +25,11 @@ struct PhaseInfo {
   int kernels;
 };
 constexpr PhaseInfo kPhases[HMM_NUM_PHASES] = {
-    {"route", 3},         {"dispatch_x", 1},      {"gemm_fwd", 1},
-    {"combine_y", 1},     {"dispatch_dy", 1},     {"gemm_bwd_data", 1},
-    {"gemm_bwd_weight", 1}, {"combine_dx", 1}};
+    {"route", 3},     {"dispatch_x", 1},  {"gemm_fwd", 1}, {"combine_y", 1},
+    {"dispatch_dy", 1}, {"gemm_bwd", 1},  {"combine_dx", 1}};
 enum Phase {
-  PH_ROUTE = 0, PH_DISPATCH_X, PH_GEMM_FWD, PH_COMBINE_Y, PH_DISPATCH_DY,
-  PH_GEMM_BWD_DATA, PH_GEMM_BWD_WEIGHT, PH_COMBINE_DX
+  PH_ROUTE = 0, PH_DISPATCH_X, PH_GEMM_FWD, PH_COMBINE_Y, PH_DISPATCH_DY, PH_GEMM_BWD,
+  PH_COMBINE_DX
 };
 
 struct ProfRec {
@@ -48,6 +47,7 @@ struct hmm_ctx {
   uint64_t budget_ns = 2000000000ull;
   int inject_skip_ready = 0;
   int profile = 0;
+  int bwd_data_sms = 0;
   std::vector<ProfRec> recs;
   std::vector<cudaEvent_t> pool;
   hmm::EncodeTiledFn encode = nullptr;
@@ -121,8 +121,10 @@ int make_plan(const hmm_shape* s, bool training, Plan* p) {
   o = 0;
   p->off_chunk_base = o; o = align_up(o + 4 * p->nchunks * p->E, A);
   p->off_tickets = o;
-  p->off_ready = o + 4 * NUM_TICKETS;  // contiguous with the tickets (zeroed together)
-  o = align_up(p->off_ready + 4 * p->max_mtiles, A);
+  p->off_ready = o + 4 * NUM_TICKETS;  // tickets, ready, eready contiguous (zeroed together)
+  p->off_eready = p->off_ready + 4 * p->max_mtiles;
+  p->ctrl_zero_count = NUM_TICKETS + p->max_mtiles + p->E;
+  o = align_up(p->off_eready + 4 * p->E, A);
   p->ctrl_bytes = o;
   const size_t xperm = align_up(static_cast<size_t>(R) * p->H * 2, A);
   const size_t hbytes = align_up(static_cast<size_t>(R) * 2 * p->I * 4, A);
@@ -177,6 +179,7 @@ CtrlPtrs ctrl_at(const Plan& p, void* base) {
   c.chunk_base = reinterpret_cast<int32_t*>(b + p.off_chunk_base);
   c.tickets = reinterpret_cast<int32_t*>(b + p.off_tickets);
   c.ready = reinterpret_cast<int32_t*>(b + p.off_ready);
+  c.eready = reinterpret_cast<int32_t*>(b + p.off_eready);
   return c;
 }
 
@@ -219,6 +222,7 @@ GemmEnv env_of(hmm_ctx* ctx, cudaStream_t st) {
   GemmEnv e;
   e.encode = ctx->encode;
   e.num_sms = ctx->num_sms;
+  e.bwd_data_sms = ctx->bwd_data_sms;
   e.status = ctx->status;
   e.budget_ns = ctx->budget_ns;
   e.stream = st;
@@ -311,6 +315,10 @@ int hmm_set_option(hmm_ctx* ctx, int option, int64_t value) {
       return HMM_OK;
     case HMM_OPT_PROFILE:
       ctx->profile = value != 0;
+      return HMM_OK;
+    case HMM_OPT_BWD_DATA_SMS:
+      if (value < 0 || value >= ctx->num_sms) return HMM_ERR_ARG;
+      ctx->bwd_data_sms = static_cast<int>(value);
       return HMM_OK;
     default:
       return HMM_ERR_ARG;
@@ -474,15 +482,10 @@ int hmm_backward(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const voi
   }
   if (rc != HMM_OK) return rc;
   {
-    PhaseScope ps(ctx, PH_GEMM_BWD_DATA, st);
-    rc = launch_backward_data_gemms(env, p, m, c, dy_perm, wperm, h32, up_proj_weight,
-                                    down_proj_weight, dH, dH_lo, wa, wa_lo, dwp, dx_perm);
-  }
-  if (rc != HMM_OK) return rc;
-  if (d_up_proj_weight || d_down_proj_weight) {
-    PhaseScope ps(ctx, PH_GEMM_BWD_WEIGHT, st);
-    rc = launch_backward_weight_gemms(env, p, m, c, x_perm, dy_perm, dH, dH_lo, wa, wa_lo,
-                                      d_up_proj_weight, d_down_proj_weight);
+    PhaseScope ps(ctx, PH_GEMM_BWD, st);
+    rc = launch_backward_gemms(env, p, m, c, x_perm, dy_perm, wperm, h32, up_proj_weight,
+                               down_proj_weight, dH, dH_lo, wa, wa_lo, dwp, dx_perm,
+                               d_up_proj_weight, d_down_proj_weight);
   }
   if (rc != HMM_OK) return rc;
   if (dx || d_topk_weights) {

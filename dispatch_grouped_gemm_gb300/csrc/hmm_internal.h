@@ -35,8 +35,9 @@ struct MetaPtrs {
 // Scratch counters of one call.
 struct CtrlPtrs {
   int32_t* chunk_base;  // [nchunks * E]
-  int32_t* tickets;     // [NUM_TICKETS]
-  int32_t* ready;       // [max_mtiles]
+  int32_t* tickets;     // [NUM_TICKETS]      } contiguous: zeroed together
+  int32_t* ready;       // [max_mtiles]       } at the start of every call
+  int32_t* eready;      // [E]                }
 };
 
 struct Plan {
@@ -50,7 +51,8 @@ struct Plan {
   size_t meta_bytes;
   size_t off_counts, off_offsets, off_poff, off_slot2prow, off_prow2slot;  // inside meta
   size_t ctrl_bytes;
-  size_t off_chunk_base, off_tickets, off_ready;                           // inside ctrl
+  size_t off_chunk_base, off_tickets, off_ready, off_eready;               // inside ctrl
+  int64_t ctrl_zero_count;  // int32 counters from off_tickets that each call zeroes
   // forward: saved = [meta | x_perm | h]      (training)
   //          workspace = [ctrl | a | o]       (training)
   //          workspace = [ctrl | meta | x_perm | a | o]   (inference)
@@ -90,6 +92,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 struct GemmEnv {
   EncodeTiledFn encode;
   int num_sms;
+  int bwd_data_sms;  // SMs for the data-gradient group of the backward (0: automatic)
   unsigned* status;
   uint64_t budget_ns;
   cudaStream_t stream;
@@ -101,16 +104,14 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
                          const void* x_perm, const void* W1, const void* W2, void* a, float* h32,
                          void* o, bool skip_ready_release);
 // backward act_grad(+SwiGLU grad, d_w partials) and input-grad GEMMs
-// (dH and w*a are written as two bf16 halves, hi + lo)
-int launch_backward_data_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
-                               const void* dy_perm, const float* wperm, const float* h32,
-                               const void* W1, const void* W2, void* dH, void* dH_lo, void* wa,
-                               void* wa_lo, float* dwp, void* dx_perm);
-// backward weight-gradient GEMMs dW2 = (wa_hi + wa_lo)^T dy_perm,
-// dW1 = x_perm^T (dH_hi + dH_lo)
-int launch_backward_weight_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
-                                 const void* x_perm, const void* dy_perm, const void* dH,
-                                 const void* dH_lo, const void* wa, const void* wa_lo, void* dW1,
-                                 void* dW2);
+// backward GEMMs in one persistent launch, interleaved per expert:
+//   act_grad (+SwiGLU grad, d_w partials; dH and w*a written as bf16 hi + lo),
+//   input-grad (per-M-tile release), W2Grad and W1Grad (per-expert release,
+//   reading the hi + lo halves).  dW1 / dW2 may be null.
+int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
+                          const void* x_perm, const void* dy_perm, const float* wperm,
+                          const float* h32, const void* W1, const void* W2, void* dH,
+                          void* dH_lo, void* wa, void* wa_lo, float* dwp, void* dx_perm,
+                          void* dW1, void* dW2);
 
 }  // namespace hmm

@@ -73,7 +73,7 @@ __device__ int32_t block_exclusive_scan(int32_t v, int32_t* warp_tot, int32_t* t
 }
 
 __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int64_t nchunks, MetaPtrs m,
-                                                          CtrlPtrs c, int64_t max_mtiles) {
+                                                          CtrlPtrs c, int64_t zero_count) {
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t tot_cnt, tot_pad;
   const int e = threadIdx.x;
@@ -99,8 +99,8 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int64_t nchunks
     m.offsets[E] = tot_cnt;
     m.poff[E] = tot_pad;
   }
-  for (int i = e; i < NUM_TICKETS; i += blockDim.x) c.tickets[i] = 0;
-  for (int64_t i = e; i < max_mtiles; i += blockDim.x) c.ready[i] = 0;
+  // tickets, per-M-tile and per-expert ready counters of this call
+  for (int64_t i = e; i < zero_count; i += blockDim.x) c.tickets[i] = 0;
 }
 
 __global__ void __launch_bounds__(RWARPS * 32) route_rank_kernel(
@@ -152,7 +152,7 @@ cudaError_t launch_route(const Plan& p, const int32_t* ids, MetaPtrs m, CtrlPtrs
     route_count_kernel<<<blocks, RWARPS * 32, smem, st>>>(ids, p.TK, E, p.nchunks, c.chunk_base,
                                                           status);
   }
-  route_scan_kernel<<<1, 1024, 0, st>>>(E, p.nchunks, m, c, p.max_mtiles);
+  route_scan_kernel<<<1, 1024, 0, st>>>(E, p.nchunks, m, c, p.ctrl_zero_count);
   if (p.nchunks > 0) {
     route_rank_kernel<<<blocks, RWARPS * 32, smem, st>>>(ids, p.TK, E, p.nchunks, m,
                                                          c.chunk_base, slot2row, row2slot);

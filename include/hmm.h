@@ -117,14 +117,19 @@ int hmm_destroy(hmm_ctx* ctx);
  *                         recorded on the call's stream (read them with
  *                         hmm_profile_read).  Default 0. */
 #define HMM_OPT_PROFILE 4
+/*   HMM_OPT_BWD_DATA_SMS  0 (default): the backward GEMMs run as phases of one
+ *                         queue (act_grad, input-grad, then the weight
+ *                         gradients).  n > 0: n SMs run the data-gradient
+ *                         GEMMs while the others run the weight-gradient
+ *                         GEMMs concurrently, trailing act_grad per expert. */
+#define HMM_OPT_BWD_DATA_SMS 5
 int hmm_set_option(hmm_ctx* ctx, int option, int64_t value);
 
 /* Launch phases timed under HMM_OPT_PROFILE (index = phase id):
- *   0 route (3 kernels)    1 dispatch_x      2 gemm_fwd (GMM1+SwiGLU, GMM2)
- *   3 combine_y            4 dispatch_dy     5 gemm_bwd_data (act_grad +
- *   SwiGLU grad, input-grad)                 6 gemm_bwd_weight (W1Grad,
- *   W2Grad)                7 combine_dx (+ d_topk_weights)              */
-#define HMM_NUM_PHASES 8
+ *   0 route (3 kernels)  1 dispatch_x  2 gemm_fwd (GMM1+SwiGLU, GMM2)
+ *   3 combine_y          4 dispatch_dy 5 gemm_bwd (act_grad + SwiGLU grad,
+ *   input-grad, W2Grad, W1Grad)        6 combine_dx (+ d_topk_weights)   */
+#define HMM_NUM_PHASES 7
 
 /* Tracing: waits for every event recorded since the previous read, then
  * writes, for each phase id < n, the summed GPU time in ms (ms[i]) and the
