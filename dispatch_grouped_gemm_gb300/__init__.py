@@ -24,7 +24,7 @@ __all__ = [
     "HmmError", "HmmShape", "hmm_create", "hmm_destroy", "hmm_set_option",
     "hmm_workspace_size", "hmm_route", "hmm_route_static", "hmm_forward", "hmm_backward", "hmm_status",
     "hmm_error_string", "Context", "moe_ffn", "library_path", "load_library",
-    "hmm_profile_read", "hmm_phase_name",
+    "hmm_profile_read", "hmm_phase_name", "hmm_set_trace",
     "HMM_OPT_VALIDATE", "HMM_OPT_WAIT_BUDGET_NS", "HMM_OPT_INJECT_SKIP_READY", "HMM_OPT_PROFILE",
     "HMM_OPT_BWD_DATA_SMS",
     "HMM_DTYPE_BF16", "HMM_DTYPE_F32", "HMM_STATUS_EXPERT_ID", "HMM_STATUS_TIMEOUT",
@@ -108,6 +108,7 @@ def load_library():
             "hmm_status": [vp, vp, ctypes.POINTER(i32)],
             "hmm_profile_read": [vp, i32, ctypes.POINTER(ctypes.c_double),
                                  ctypes.POINTER(ctypes.c_int64)],
+            "hmm_set_trace": [vp, vp, sz, i32],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -232,6 +233,14 @@ def hmm_profile_read(ctx):
     cnt = (ctypes.c_int64 * n)()
     _check(load_library().hmm_profile_read(ctx, n, ms, cnt), "hmm_profile_read")
     return {hmm_phase_name(i): (ms[i], cnt[i]) for i in range(n)}
+
+
+def hmm_set_trace(ctx, buffer, which: int):
+    """Record the per-tile timeline of the next GEMM launch of kind `which`
+    (0 forward, 1 backward data, 2 backward weight) into `buffer` (a device
+    tensor; None disables)."""
+    _check(load_library().hmm_set_trace(ctx, _ptr(buffer), _nbytes(buffer), int(which)),
+           "hmm_set_trace")
 
 
 # ------------------------------------------------------------ torch layer

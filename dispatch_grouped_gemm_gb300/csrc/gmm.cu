@@ -52,7 +52,14 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TI_DEPTH = 3;
-constexpr int NUM_THREADS = 224;  // 7 warps
+// Warp roles: 0 TMA producer, 1 MMA issuer, 2..5 epilogue (one per TMEM lane
+// quarter), 6 tile scheduler.  (Eight epilogue warps, two per quarter on
+// alternate column chunks, were measured slower: more scattered epilogue
+// traffic in flight slows the TMA operand feed of the same SM.)
+constexpr int EPI_WARPS = 4;
+constexpr int CH_SPLIT = EPI_WARPS / 4;  // warps sharing a lane quarter
+constexpr int SCHED_WARP = 2 + EPI_WARPS;
+constexpr int NUM_THREADS = 32 * (SCHED_WARP + 1);  // 11 warps
 // alignment slack + stages + barriers, tile-info ring and schedule prefix table
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 512 + 4 * (3 * MAX_E + 8 + 1) + 256;
 constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -102,6 +109,8 @@ struct Params {
   int* ticket;
   unsigned* status;
   unsigned long long budget_ns;
+  uint64_t* trace;      // per-tile timeline records (null: off)
+  int trace_cap;
 };
 
 struct Maps {
@@ -116,6 +125,17 @@ struct TileInfo {
   int kb;     // K blocks (0: empty wgrad tile -> zeros)
   int krow0;  // wgrad: first padded row of the expert
 };
+
+// ------------------------------------------------------------------ tracing
+__device__ __forceinline__ uint64_t* trace_rec(const Params& P, int lt) {
+  if (P.trace == nullptr || lt >= P.trace_cap) return nullptr;
+  return P.trace + (static_cast<int64_t>(blockIdx.x) * P.trace_cap + lt) * 8;
+}
+__device__ __forceinline__ uint32_t sm_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
 
 // ----------------------------------------------------------------- scheduler
 __device__ __forceinline__ int mtiles_of(const Params& P, int e) {
@@ -215,6 +235,7 @@ __device__ __forceinline__ void stage_boxes(const Prob& pr, const TileInfo& ti, 
   auto ld3 = [&](void* dst, const CUtensorMap* m, int c0, int c1, int c2) {
     tma_load_3d(dst, m, bar, c0, c1, c2);
   };
+
   if constexpr (C::WGRAD) {
     // with a split operand the K loop runs twice over the expert's rows:
     // first against the high bf16 half, then against the low half
@@ -261,21 +282,26 @@ __device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t a_base, uint
                                           bool first) {
 #pragma unroll
   for (int kk = 0; kk < BK / 16; ++kk) {
-    const uint64_t ad = C::A_MN ? sw128_desc(a_base + kk * 2048, 8192, 1024)
-                                : sw128_desc(a_base + kk * 32, 16, 1024);
-    const uint64_t bd = C::B_MN ? sw128_desc(b_base + kk * 2048, 8192, 1024)
-                                : sw128_desc(b_base + kk * 32, 16, 1024);
+    const uint64_t ad = C::A_MN ? smem_desc(a_base + kk * 2048, 8192, 1024, LAYOUT_SW128)
+                                : smem_desc(a_base + kk * 32, 16, 1024, LAYOUT_SW128);
+    const uint64_t bd = C::B_MN ? smem_desc(b_base + kk * 2048, 8192, 1024, LAYOUT_SW128)
+                                : smem_desc(b_base + kk * 32, 16, 1024, LAYOUT_SW128);
     umma_bf16(d_tmem, ad, bd, C::IDESC, (first && kk == 0) ? 0u : 1u);
   }
 }
 
 // ----------------------------------------------------------------- epilogue
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
-__device__ __forceinline__ float sigmoid_f(float g) { return 1.0f / (1.0f + __expf(-g)); }
+// sigma(g) = 1 / (1 + exp(-g)) with the fast exponential and division
+// intrinsics (a few ulp in fp32, far inside the bf16 output rounding).
+// For g -> -inf the denominator overflows to inf and the quotient is 0.
+__device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
+__device__ __forceinline__ float silu_f(float g) { return g * sigmoid_f(g); }
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v, int valid) {
+// 16-byte groups of one row segment: group q of the 32 columns at p + q * gs
+// bytes (gs = 16: contiguous).
+__device__ __forceinline__ void store_bf16x32(void* dst, int64_t gs, const float* v, int valid) {
   // valid: number of the 32 columns inside the output (multiple of 8)
-  uint4* d = reinterpret_cast<uint4*>(dst);
+  char* d = static_cast<char*>(dst);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     if (q * 8 < valid) {
@@ -284,14 +310,14 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v
       u.y = pack_bf16(v[q * 8 + 2], v[q * 8 + 3]);
       u.z = pack_bf16(v[q * 8 + 4], v[q * 8 + 5]);
       u.w = pack_bf16(v[q * 8 + 6], v[q * 8 + 7]);
-      d[q] = u;
+      *reinterpret_cast<uint4*>(d + q * gs) = u;
     }
   }
 }
 
 // v = hi + lo with hi = bf16(v), lo = bf16(v - hi): the pair carries about
 // 16 significant bits, enough for the weight-gradient GEMMs that consume it.
-__device__ __forceinline__ void store_bf16x32_split(__nv_bfloat16* hi, __nv_bfloat16* lo,
+__device__ __forceinline__ void store_bf16x32_split(void* hi, void* lo, int64_t gs,
                                                     const float* v, int valid) {
   float h[32], l[32];
 #pragma unroll
@@ -299,23 +325,41 @@ __device__ __forceinline__ void store_bf16x32_split(__nv_bfloat16* hi, __nv_bflo
     h[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
     l[j] = v[j] - h[j];
   }
-  store_bf16x32(hi, h, valid);
-  store_bf16x32(lo, l, valid);
+  store_bf16x32(hi, gs, h, valid);
+  store_bf16x32(lo, gs, l, valid);
 }
 
-__device__ __forceinline__ void store_f32x32(float* dst, const float* v, int valid) {
-  float4* d = reinterpret_cast<float4*>(dst);
+__device__ __forceinline__ void store_bf16x8_split(__nv_bfloat16* hi, __nv_bfloat16* lo,
+                                                   const float* v) {
+  uint4 h, l;
+  uint32_t* hp = reinterpret_cast<uint32_t*>(&h);
+  uint32_t* lp = reinterpret_cast<uint32_t*>(&l);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float h0 = __bfloat162float(__float2bfloat16_rn(v[2 * j]));
+    const float h1 = __bfloat162float(__float2bfloat16_rn(v[2 * j + 1]));
+    hp[j] = pack_bf16(h0, h1);
+    lp[j] = pack_bf16(v[2 * j] - h0, v[2 * j + 1] - h1);
+  }
+  *reinterpret_cast<uint4*>(hi) = h;
+  *reinterpret_cast<uint4*>(lo) = l;
+}
+
+__device__ __forceinline__ void store_f32x32(void* dst, int64_t gs, const float* v, int valid) {
+  char* d = static_cast<char*>(dst);
 #pragma unroll
   for (int q = 0; q < 8; ++q)
-    if (q * 4 < valid) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    if (q * 4 < valid)
+      *reinterpret_cast<float4*>(d + q * gs) =
+          make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
-__device__ __forceinline__ void load_f32x32(const float* src, float* v, int valid) {
-  const float4* s = reinterpret_cast<const float4*>(src);
+__device__ __forceinline__ void load_f32x32(const void* src, int64_t gs, float* v, int valid) {
+  const char* s = static_cast<const char*>(src);
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (q * 4 < valid) f = s[q];
+    if (q * 4 < valid) f = *reinterpret_cast<const float4*>(s + q * gs);
     v[4 * q] = f.x;
     v[4 * q + 1] = f.y;
     v[4 * q + 2] = f.z;
@@ -324,18 +368,17 @@ __device__ __forceinline__ void load_f32x32(const float* src, float* v, int vali
 }
 
 // Drains the accumulator of one tile; taddr addresses this warp's lanes.
+// ch: which warp of the lane quarter (chunks ch, ch + CH_SPLIT, ...).
 template <class C>
 __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti, uint32_t taddr,
-                                              int row_in_tile) {
-  const int lane = threadIdx.x & 31;
-  (void)lane;
+                                              int row_in_tile, int ch) {
   if constexpr (C::EPI == EPI_SWIGLU) {
     // cols [0,128): gate of n0..n0+127, [128,256): up of the same columns
     const int64_t row = ti.m0 + row_in_tile;
     __nv_bfloat16* a_row = static_cast<__nv_bfloat16*>(pr.out) + row * pr.ld_out;
     float* h_row = pr.out2 ? static_cast<float*>(pr.out2) + row * pr.ld_out2 : nullptr;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = ch; c < 4; c += CH_SPLIT) {
       const int col = ti.n0 + c * 32;
       if (col >= pr.N) break;
       const int valid = min(32, pr.N - col);
@@ -349,10 +392,10 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
         const float gf = __uint_as_float(g[j]), uf = __uint_as_float(u[j]);
         av[j] = silu_f(gf) * uf;
       }
-      store_bf16x32(a_row + col, av, valid);
+      store_bf16x32(a_row + col, 16, av, valid);
       if (h_row) {
-        store_f32x32(h_row + col, reinterpret_cast<const float*>(g), valid);
-        store_f32x32(h_row + pr.half + col, reinterpret_cast<const float*>(u), valid);
+        store_f32x32(h_row + col, 16, reinterpret_cast<const float*>(g), valid);
+        store_f32x32(h_row + pr.half + col, 16, reinterpret_cast<const float*>(u), valid);
       }
     }
   } else if constexpr (C::EPI == EPI_STORE) {
@@ -368,13 +411,14 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
     const bool row_ok = !C::WGRAD || row < pr.M;
     __nv_bfloat16* orow = base + row * pr.ld_out;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = ch; c < BN / 32; c += CH_SPLIT) {
       const int col = ti.n0 + c * 32;
       if (col >= pr.N) break;
       uint32_t r[32];
       tmem_ld32(taddr + c * 32, r);
       tmem_ld_wait();
-      if (row_ok) store_bf16x32(orow + col, reinterpret_cast<const float*>(r), min(32, pr.N - col));
+      if (row_ok)
+        store_bf16x32(orow + col, 16, reinterpret_cast<const float*>(r), min(32, pr.N - col));
     }
   } else {  // EPI_DSWIGLU
     // acc = G = dy_perm . W2^T for columns n0..n0+255 of I.  With the saved
@@ -392,47 +436,58 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
     const float w = pr.rowscale[row];
     float dwp = 0.0f;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = ch; c < BN / 32; c += CH_SPLIT) {
       const int col = ti.n0 + c * 32;
       if (col >= pr.N) break;
       const int valid = min(32, pr.N - col);
       uint32_t r[32];
       tmem_ld32(taddr + c * 32, r);
       float gv[32], uv[32];
-      load_f32x32(h_row + col, gv, valid);
-      load_f32x32(h_row + pr.half + col, uv, valid);
+      load_f32x32(h_row + col, 16, gv, valid);
+      load_f32x32(h_row + pr.half + col, 16, uv, valid);
       tmem_ld_wait();
-      float dg[32], du[32], wa[32];
+      // eight columns at a time: compute, split into bf16 hi + lo, store
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float G = __uint_as_float(r[j]);
-        const float g = gv[j], u = uv[j];
-        const float s = sigmoid_f(g);
-        const float a = g * s * u;
-        dwp = fmaf(G, a, dwp);
-        const float dA = w * G;
-        dg[j] = dA * u * s * (1.0f + g * (1.0f - s));
-        du[j] = dA * g * s;
-        wa[j] = w * a;
+      for (int q = 0; q < 4; ++q) {
+        if (q * 8 < valid) {
+          float dg[8], du[8], wa[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float G = __uint_as_float(r[q * 8 + j]);
+            const float g = gv[q * 8 + j], u = uv[q * 8 + j];
+            const float sg = sigmoid_f(g);
+            const float a = g * sg * u;
+            dwp = fmaf(G, a, dwp);
+            const float dA = w * G;
+            dg[j] = dA * u * sg * (1.0f + g * (1.0f - sg));
+            du[j] = dA * g * sg;
+            wa[j] = w * a;
+          }
+          const int cq = col + q * 8;
+          store_bf16x8_split(dh_row + cq, dh_lo + cq, dg);
+          store_bf16x8_split(dh_row + pr.half + cq, dh_lo + pr.half + cq, du);
+          store_bf16x8_split(wa_row + cq, wa_lo + cq, wa);
+        }
       }
-      store_bf16x32_split(dh_row + col, dh_lo + col, dg, valid);
-      store_bf16x32_split(dh_row + pr.half + col, dh_lo + pr.half + col, du, valid);
-      store_bf16x32_split(wa_row + col, wa_lo + col, wa, valid);
     }
-    static_cast<float*>(pr.out3)[row * pr.ld_out3 + ti.n0 / BN] = dwp;
+    // one partial per (column block, warp of the quarter); the combine sums
+    // them in order
+    static_cast<float*>(pr.out3)[row * pr.ld_out3 + (ti.n0 / BN) * CH_SPLIT + ch] = dwp;
   }
 }
 
 template <class C>
-__device__ __forceinline__ void epilogue_zero(const Prob& pr, const TileInfo& ti, int row_in_tile) {
+__device__ __forceinline__ void epilogue_zero(const Prob& pr, const TileInfo& ti, int row_in_tile,
+                                              int ch) {
   // wgrad tile of an expert with no rows: the gradient is exactly zero
   const int64_t row = ti.m0 + row_in_tile;
   if (row >= pr.M) return;
   __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(pr.out) +
                         static_cast<int64_t>(ti.e) * pr.out_estride + row * pr.ld_out;
   const uint4 z = make_uint4(0, 0, 0, 0);
-  for (int col = ti.n0; col < min(ti.n0 + BN, pr.N); col += 8)
-    *reinterpret_cast<uint4*>(orow + col) = z;
+  for (int c = ch; c < BN / 32; c += CH_SPLIT)
+    for (int col = ti.n0 + c * 32; col < min(ti.n0 + c * 32 + 32, pr.N); col += 8)
+      *reinterpret_cast<uint4*>(orow + col) = z;
 }
 
 // Bounded wait that ignores the abort flag (used only to drain in-flight
@@ -484,11 +539,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], EPI_WARPS);
     }
     for (int i = 0; i < TI_DEPTH; ++i) {
       mbar_init(&ti_full[i], 1);
-      mbar_init(&ti_empty[i], 6);  // TMA producer, MMA issuer, 4 epilogue warps
+      mbar_init(&ti_empty[i], 2 + EPI_WARPS);  // TMA producer, MMA issuer, epilogue warps
     }
     mbar_init(mma_done, 1);
     *s_abort = 0;
@@ -505,45 +560,67 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const WaitCtl wc{s_abort, P.status, P.budget_ns};
 
   const int group = (P.group_split > 0 && static_cast<int>(blockIdx.x) >= P.group_split) ? 1 : 0;
-  if (warp == 6) {
+  if (warp == SCHED_WARP) {
     // --------------------------------------------------------- tile scheduler
     // Fetches tickets, decodes them and waits for each tile's dependencies
     // about one tile ahead of the TMA producer, so neither the ticket atomic
     // nor a ready-counter poll sits on the load path.  (A deeper lookahead
     // spreads the M tiles that share a weight tile over time and costs L2
-    // reuse of the weights.)
+    // reuse of the weights.)  Lane 0 does the bookkeeping.
     build_schedule(P, group, s_pref);
-    if (lane == 0) {
-      int ti_slot = 0;
-      uint32_t ti_phase = 0;
-      int t = atomicAdd(P.ticket + group, 1);
-      for (;;) {
-        TileInfo ti;
-        ti.prob = -1;
+    int ti_slot = 0;
+    uint32_t ti_phase = 0;
+    int lt = 0;  // tiles of this CTA so far (trace index)
+    int t = 0;
+    if (lane == 0) t = atomicAdd(P.ticket + group, 1);
+    for (;;) {
+      TileInfo ti;
+      ti.prob = -1;
+      ti.e = ti.m0 = ti.n0 = ti.kb = ti.krow0 = 0;
+      bool ok = true;
+      if (lane == 0) {
         int q = 0, e = 0, r = 0;
         if (locate_tile(P, group, s_pref, t, q, e, r)) {
           ti.prob = q;
           HMM_BY_PROB(q, decode_tile, P, P.p[q], e, r, ti);
+          t = atomicAdd(P.ticket + group, 1);  // next ticket, early
+          const Prob& pr = P.p[q];
+          if (pr.wait_m || pr.wait_e)
+            ok = pr.wait_m ? counter_wait(&pr.wait_m[ti.m0 / BM], pr.wait_unit, wc)
+                           : counter_wait(&pr.wait_e[ti.e], pr.wait_unit * mtiles_of(P, ti.e),
+                                          wc);
         }
-        if (ti.prob >= 0) t = atomicAdd(P.ticket + group, 1);  // next ticket, early
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      ti.prob = __shfl_sync(0xffffffffu, ti.prob, 0);
+      ti.e = __shfl_sync(0xffffffffu, ti.e, 0);
+      ti.m0 = __shfl_sync(0xffffffffu, ti.m0, 0);
+      ti.n0 = __shfl_sync(0xffffffffu, ti.n0, 0);
+      ti.kb = __shfl_sync(0xffffffffu, ti.kb, 0);
+      ti.krow0 = __shfl_sync(0xffffffffu, ti.krow0, 0);
+      bool got = false;
+      if (lane == 0) got = mbar_wait(&ti_empty[ti_slot], ti_phase ^ 1u, wc);
+      if (!__shfl_sync(0xffffffffu, got, 0)) break;
+      if (lane == 0) {
         if (ti.prob >= 0) {
-          const Prob& pr = P.p[ti.prob];
-          if (pr.wait_m || pr.wait_e) {
-            const bool got =
-                pr.wait_m ? counter_wait(&pr.wait_m[ti.m0 / BM], pr.wait_unit, wc)
-                          : counter_wait(&pr.wait_e[ti.e], pr.wait_unit * mtiles_of(P, ti.e), wc);
-            if (!got) break;
+          if (uint64_t* rec = trace_rec(P, lt)) {
+            rec[0] = (static_cast<uint64_t>(sm_id()) << 48) |
+                     (static_cast<uint64_t>(ti.prob) << 40) |
+                     (static_cast<uint64_t>(ti.e & 0xFFFFF) << 20) |
+                     static_cast<uint64_t>(ti.kb & 0xFFFFF);
+            rec[1] = globaltimer_ns();
           }
         }
-        if (!mbar_wait(&ti_empty[ti_slot], ti_phase ^ 1u, wc)) break;
         s_ti[ti_slot] = ti;
         mbar_arrive(&ti_full[ti_slot]);
-        if (++ti_slot == TI_DEPTH) {
-          ti_slot = 0;
-          ti_phase ^= 1u;
-        }
-        if (ti.prob < 0) break;
       }
+      __syncwarp();
+      ++lt;
+      if (++ti_slot == TI_DEPTH) {
+        ti_slot = 0;
+        ti_phase ^= 1u;
+      }
+      if (ti.prob < 0) break;
     }
   } else if (warp == 0) {
     if (lane == 0) {
@@ -558,6 +635,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t ti_phase = 0;
       uint32_t issued = 0;  // k-blocks issued by this CTA
       bool ok = true;
+      int lt = 0;
       for (;;) {
         if (!mbar_wait(&ti_full[ti_slot], ti_phase, wc)) {
           ok = false;
@@ -575,11 +653,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // publishing it; order that with the async-proxy loads below
         if (pr.wait_m || pr.wait_e) fence_proxy_async_global();
         const CUtensorMap* mp = maps.m[ti.prob];
+        uint64_t* rec = trace_rec(P, lt++);
         for (int kb = 0; kb < ti.kb; ++kb) {
           if (!mbar_wait(&empty[stage], sphase ^ 1u, wc)) {
             ok = false;
             break;
           }
+          if (rec && kb == 0) rec[2] = globaltimer_ns();
           uint8_t* sA = stages + stage * STAGE_BYTES;
           uint8_t* sB = sA + A_BYTES;
           mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
@@ -591,6 +671,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             sphase ^= 1u;
           }
         }
+        if (rec && ok) rec[3] = globaltimer_ns();
         if (!ok) break;
       }
       if (!ok) {
@@ -606,6 +687,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int ti_slot = 0;
       uint32_t ti_phase = 0;
       uint32_t acc = 0, acc_phase = 0;
+      int lt = 0;
       for (;;) {
         if (!mbar_wait(&ti_full[ti_slot], ti_phase, wc)) break;
         const TileInfo ti = s_ti[ti_slot];
@@ -615,9 +697,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ti_phase ^= 1u;
         }
         if (ti.prob < 0) break;
+        uint64_t* rec = trace_rec(P, lt++);
         if (ti.kb == 0) continue;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, wc)) break;
         tc_fence_after();
+        if (rec) rec[4] = globaltimer_ns();
         const uint32_t d_tmem = tmem_base + acc * BN;
         bool ok = true;
         for (int kb = 0; kb < ti.kb; ++kb) {
@@ -637,6 +721,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (!ok) break;
         umma_commit(&tfull[acc]);
+        if (rec) rec[5] = globaltimer_ns();
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
@@ -644,13 +729,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       umma_commit(mma_done);
       drain_wait(mma_done, 0, P.budget_ns);
     }
-  } else if (warp >= 2 && warp <= 5) {
+  } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
     // ------------------------------------------------------------- epilogue
     const int q = warp & 3;
+    const int ch = (warp - 2) / 4;  // which warp of the lane quarter
     const int row_in_tile = q * 32 + lane;
     int ti_slot = 0;
     uint32_t ti_phase = 0;
     uint32_t acc = 0, acc_phase = 0;
+    int lt = 0;
     for (;;) {
       bool got = false;
       if (lane == 0) got = mbar_wait(&ti_full[ti_slot], ti_phase, wc);
@@ -666,8 +753,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (ti.prob < 0) break;
       const Prob& pr = P.p[ti.prob];
+      uint64_t* rec = (warp == 2 && lane == 0) ? trace_rec(P, lt) : nullptr;  // one warp reports
+      ++lt;
       if (ti.kb == 0) {
-        HMM_BY_PROB(ti.prob, epilogue_zero, pr, ti, row_in_tile);
+        HMM_BY_PROB(ti.prob, epilogue_zero, pr, ti, row_in_tile, ch);
         continue;
       }
       if (lane == 0) got = mbar_wait(&tfull[acc], acc_phase, wc);
@@ -675,11 +764,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) break;
       tc_fence_after();
+      if (rec) rec[6] = globaltimer_ns();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      HMM_BY_PROB(ti.prob, epilogue_tile, pr, ti, taddr, row_in_tile);
+      HMM_BY_PROB(ti.prob, epilogue_tile, pr, ti, taddr, row_in_tile, ch);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (rec) rec[7] = globaltimer_ns();
       if (pr.signal_m || pr.signal_e) {
         fence_proxy_async_global();
         __syncwarp();
@@ -739,8 +830,12 @@ int map_w(const GemmEnv& env, CUtensorMap* m, const void* base, int64_t E, int64
 }
 
 template <class C0, class C1, class C2, class C3>
-int launch(const GemmEnv& env, Params& P, const Maps& maps, int64_t max_tiles) {
+int launch(const GemmEnv& env, Params& P, const Maps& maps, int64_t max_tiles, int kind) {
   if (max_tiles <= 0 || P.nprob == 0) return HMM_OK;
+  if (env.trace && env.trace_which == kind) {
+    P.trace = env.trace;
+    P.trace_cap = env.trace_cap;
+  }
   auto kern = gmm_kernel<C0, C1, C2, C3>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
       cudaSuccess)
@@ -771,7 +866,8 @@ using CfgGmm1 = Cfg<EPI_SWIGLU, false, true>;
 using CfgGmm2 = Cfg<EPI_STORE, false, true>;
 using CfgActGrad = Cfg<EPI_DSWIGLU, false, false>;
 using CfgInGrad = Cfg<EPI_STORE, false, false>;
-using CfgWGrad = Cfg<EPI_STORE, true, true>;
+using CfgW2Grad = Cfg<EPI_STORE, true, true>;
+using CfgW1Grad = Cfg<EPI_STORE, true, true>;
 
 int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
                          const void* x_perm, const void* W1, const void* W2, void* a, float* h32,
@@ -812,9 +908,9 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
   // meet the last wave of GMM1 tiles
   g2.lag = static_cast<int>(E);
   g2.wait_m = c.ready;
-  g2.wait_unit = 4 * g1.n_tiles;  // the 4 epilogue warps of every GMM1 tile of the M tile
+  g2.wait_unit = EPI_WARPS * g1.n_tiles;  // every epilogue warp of every GMM1 tile of the M tile
   const int64_t max_tiles = p.max_mtiles * (g1.n_tiles + g2.n_tiles);
-  return launch<CfgGmm1, CfgGmm2, CfgGmm2, CfgGmm2>(env, P, maps, max_tiles);
+  return launch<CfgGmm1, CfgGmm2, CfgGmm2, CfgGmm2>(env, P, maps, max_tiles, 0);
 }
 
 int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
@@ -859,7 +955,8 @@ int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtr
   ag.out2 = wa;
   ag.ld_out2 = I;
   ag.out3 = dwp;
-  ag.ld_out3 = p.nt_dswiglu;
+  static_assert(CH_SPLIT == 1, "the d_w partial buffer holds one entry per act_grad N tile");
+  ag.ld_out3 = p.dwp_ld;
   ag.out4 = dH_lo;
   ag.out5 = wa_lo;
   ag.aux = h32;
@@ -874,7 +971,7 @@ int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtr
   ig.out = dx_perm;
   ig.ld_out = H;
   ig.wait_m = c.ready;
-  ig.wait_unit = 4 * ag.n_tiles;
+  ig.wait_unit = EPI_WARPS * ag.n_tiles;
   Prob w2{}, w1{};
   w2.M = static_cast<int>(I);
   w2.N = static_cast<int>(H);
@@ -895,32 +992,25 @@ int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtr
   for (Prob* w : {&w2, &w1}) {
     w->wgrad = 1;
     w->wait_e = c.eready;
-    w->wait_unit = 4 * ag.n_tiles;  // every act_grad tile of every M tile of the expert
+    w->wait_unit = EPI_WARPS * ag.n_tiles;  // every act_grad tile of every M tile of the expert
   }
   ig.lag = static_cast<int>(E);  // input-grad after every act_grad tile is handed out
   const int64_t data_tiles = p.max_mtiles * (ag.n_tiles + ig.n_tiles);
   const int64_t w_tiles = (dW2 ? E * w2.m_tiles * w2.n_tiles : 0) +
                           (dW1 ? E * w1.m_tiles * w1.n_tiles : 0);
   const int nw = (dW2 ? 1 : 0) + (dW1 ? 1 : 0);
+  if (!dW2) w2.m_tiles = 0;  // fixed problem slots: W2Grad, then W1Grad
+  if (!dW1) w1.m_tiles = 0;
   auto add_wgrad = [&](Params& Q, int first, int group) {
-    int q = first;
-    if (dW2) {
-      Q.p[q] = w2;
-      Q.p[q].group = group;
-      maps.m[q][0] = map_w2[0];
-      maps.m[q][1] = map_w2[1];
-      maps.m[q][2] = map_w2[2];
-      ++q;
+    Q.p[first] = w2;
+    Q.p[first].group = group;
+    Q.p[first + 1] = w1;
+    Q.p[first + 1].group = group;
+    for (int j = 0; j < 3; ++j) {
+      maps.m[first][j] = map_w2[j];
+      maps.m[first + 1][j] = map_w1[j];
     }
-    if (dW1) {
-      Q.p[q] = w1;
-      Q.p[q].group = group;
-      maps.m[q][0] = map_w1[0];
-      maps.m[q][1] = map_w1[1];
-      maps.m[q][2] = map_w1[2];
-      ++q;
-    }
-    Q.nprob = q;
+    Q.nprob = first + 2;
   };
   if (env.bwd_data_sms > 0 && nw > 0) {
     // Two CTA groups in one launch: env.bwd_data_sms SMs run act_grad and
@@ -928,13 +1018,13 @@ int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtr
     // expert.
     add_wgrad(P, 2, 1);
     P.group_split = env.bwd_data_sms;
-    return launch<CfgActGrad, CfgInGrad, CfgWGrad, CfgWGrad>(env, P, maps,
-                                                            data_tiles + w_tiles);
+    return launch<CfgActGrad, CfgInGrad, CfgW2Grad, CfgW1Grad>(env, P, maps,
+                                                              data_tiles + w_tiles, 1);
   }
   // Default: two launches.  The data gradients first; then the weight
   // gradients, whose per-expert waits are already satisfied.
   P.nprob = 2;
-  rc = launch<CfgActGrad, CfgInGrad, CfgInGrad, CfgInGrad>(env, P, maps, data_tiles);
+  rc = launch<CfgActGrad, CfgInGrad, CfgInGrad, CfgInGrad>(env, P, maps, data_tiles, 1);
   if (rc != HMM_OK || nw == 0) return rc;
   Params W{};
   W.poff = m.poff;
@@ -943,7 +1033,7 @@ int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtr
   W.ticket = c.tickets + 3;
   add_wgrad(W, 0, 0);
   for (int q = 0; q < W.nprob; ++q) W.p[q].wait_e = nullptr;  // act_grad has completed
-  return launch<CfgWGrad, CfgWGrad, CfgWGrad, CfgWGrad>(env, W, maps, w_tiles);
+  return launch<CfgW2Grad, CfgW1Grad, CfgW1Grad, CfgW1Grad>(env, W, maps, w_tiles, 2);
 }
 
 }  // namespace hmm

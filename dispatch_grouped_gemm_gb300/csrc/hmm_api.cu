@@ -48,6 +48,9 @@ struct hmm_ctx {
   int inject_skip_ready = 0;
   int profile = 0;
   int bwd_data_sms = 0;
+  uint64_t* trace = nullptr;
+  size_t trace_bytes = 0;
+  int trace_which = 0;
   std::vector<ProfRec> recs;
   std::vector<cudaEvent_t> pool;
   hmm::EncodeTiledFn encode = nullptr;
@@ -110,6 +113,7 @@ int make_plan(const hmm_shape* s, bool training, Plan* p) {
   p->max_mtiles = R / BM;
   p->nchunks = (TK + RCHUNK - 1) / RCHUNK;
   p->nt_dswiglu = (p->I + BN - 1) / BN;
+  p->dwp_ld = p->nt_dswiglu;  // one d_w partial per act_grad N tile and row
   const size_t A = 256;
   size_t o = 0;
   p->off_counts = o;    o = align_up(o + 4 * p->E, A);
@@ -157,7 +161,7 @@ int make_plan(const hmm_shape* s, bool training, Plan* p) {
   p->bw_wa = o;      o = align_up(o + static_cast<size_t>(R) * p->I * 2, A);
   p->bw_walo = o;    o = align_up(o + static_cast<size_t>(R) * p->I * 2, A);
   p->bw_dxperm = o;  o = align_up(o + static_cast<size_t>(R) * p->H * 2, A);
-  p->bw_dwp = o;     o = align_up(o + static_cast<size_t>(R) * p->nt_dswiglu * 4, A);
+  p->bw_dwp = o;     o = align_up(o + static_cast<size_t>(R) * p->dwp_ld * 4, A);
   p->bwd_ws_bytes = o;
   return HMM_OK;
 }
@@ -223,6 +227,9 @@ GemmEnv env_of(hmm_ctx* ctx, cudaStream_t st) {
   e.encode = ctx->encode;
   e.num_sms = ctx->num_sms;
   e.bwd_data_sms = ctx->bwd_data_sms;
+  e.trace = ctx->trace;
+  e.trace_cap = ctx->trace ? static_cast<int>(ctx->trace_bytes / (64 * ctx->num_sms)) : 0;
+  e.trace_which = ctx->trace_which;
   e.status = ctx->status;
   e.budget_ns = ctx->budget_ns;
   e.stream = st;
@@ -535,6 +542,16 @@ int hmm_profile_read(hmm_ctx* ctx, int n, double* ms, int64_t* launches) {
     if (launches) launches[i] = cnt[i];
   }
   return rc;
+}
+
+int hmm_set_trace(hmm_ctx* ctx, void* buffer, size_t bytes, int which) {
+  if (!ctx || which < 0 || which > 2) return HMM_ERR_ARG;
+  if (buffer && (reinterpret_cast<uintptr_t>(buffer) & 15u)) return HMM_ERR_LAYOUT;
+  if (buffer && bytes < static_cast<size_t>(64) * ctx->num_sms) return HMM_ERR_CAPACITY;
+  ctx->trace = static_cast<uint64_t*>(buffer);
+  ctx->trace_bytes = buffer ? bytes : 0;
+  ctx->trace_which = which;
+  return HMM_OK;
 }
 
 const char* hmm_phase_name(int phase) {

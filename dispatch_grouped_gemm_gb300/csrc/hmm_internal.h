@@ -45,7 +45,8 @@ struct Plan {
   int64_t R;            // capacity of the padded row space
   int64_t max_mtiles;   // R / BM
   int64_t nchunks;      // routing warp-chunks
-  int64_t nt_dswiglu;   // N tiles of the act_grad GEMM (per-row d_w partials)
+  int64_t nt_dswiglu;   // N tiles of the act_grad GEMM
+  int64_t dwp_ld;       // per-row d_w partials (one per act_grad N tile)
   bool training;
   // byte offsets inside the buffers
   size_t meta_bytes;
@@ -92,6 +93,9 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 struct GemmEnv {
   EncodeTiledFn encode;
   int num_sms;
+  uint64_t* trace;   // tile timeline buffer of the traced launch (null: off)
+  int trace_cap;     // records per CTA
+  int trace_which;   // which GEMM launch kind is traced
   int bwd_data_sms;  // SMs for the data-gradient group of the backward (0: automatic)
   unsigned* status;
   uint64_t budget_ns;

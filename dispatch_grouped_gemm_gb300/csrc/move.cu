@@ -203,7 +203,7 @@ cudaError_t launch_combine_dx(const Plan& p, const void* dx_perm, const float* d
                               void* dx, void* dw, int w_dtype, cudaStream_t st) {
   combine_rows_kernel<false><<<move_grid(p.T), MOVE_THREADS, 0, st>>>(
       static_cast<const uint4*>(dx_perm), nullptr, w_dtype, p.T, p.K, p.H / 8, m.slot2prow,
-      static_cast<uint4*>(dx), dw ? dwp : nullptr, p.nt_dswiglu, dw);
+      static_cast<uint4*>(dx), dw ? dwp : nullptr, p.dwp_ld, dw);
   return cudaGetLastError();
 }
 

@@ -208,16 +208,21 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor for a 128-byte-swizzled operand tile
-// (sm_100-family descriptor: version field 1, layout SWIZZLE_128B).
-//   lbo: leading-dimension byte offset, sbo: stride-dimension byte offset.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor of an operand tile (sm_100-family
+// descriptor: version field 1).  lbo / sbo: leading / stride dimension byte
+// offsets; layout: LAYOUT_SW128 (128-byte swizzle) or LAYOUT_NONE (8-row x
+// 16-byte core matrices, where lbo is the core-matrix stride along K and sbo
+// the stride along M or N).
+constexpr uint32_t LAYOUT_NONE = 0;
+constexpr uint32_t LAYOUT_SW128 = 2;
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
   d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
+  d |= static_cast<uint64_t>(layout & 7u) << 61;
   return d;
 }
 

@@ -140,6 +140,20 @@ int hmm_profile_read(hmm_ctx* ctx, int n, double* ms, int64_t* launches);
 /* Name of a phase id ("route", "gemm_fwd", ...), or NULL if out of range. */
 const char* hmm_phase_name(int phase);
 
+/* Per-tile timeline of one GEMM launch (tracing).  buffer (device memory
+ * owned by the caller, 16-byte aligned) receives, for the next launch of GEMM
+ * kind `which` (0: forward GEMMs, 1: backward data-gradient GEMMs, 2:
+ * backward weight-gradient GEMMs), one record of 8 uint64 per tile and CTA:
+ *   [0] (sm id << 48) | (problem << 40) | (expert << 20) | K blocks
+ *   [1] scheduler published the tile   [2] first TMA load issued
+ *   [3] last TMA load issued           [4] first MMA issued
+ *   [5] last MMA committed             [6] epilogue saw the accumulator
+ *   [7] epilogue done (one warp)       (globaltimer ns; 0 = not reached)
+ * laid out as records[cta * cap + i] with cap = bytes / (64 * grid), where
+ * grid is the number of SMs.  Slots a launch does not reach stay as they were.
+ * NULL disables tracing. */
+int hmm_set_trace(hmm_ctx* ctx, void* buffer, size_t bytes, int which);
+
 /* Buffer sizes in bytes for a shape.  training != 0: the forward keeps its
  * activations in `saved` for the backward; training == 0: they live in the
  * forward workspace and *saved_bytes is 0.  Any output pointer may be NULL. */
