@@ -1022,10 +1022,13 @@ int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtr
                                                               data_tiles + w_tiles, 1);
   }
   // Default: two launches.  The data gradients first; then the weight
-  // gradients, whose per-expert waits are already satisfied.
+  // gradients, whose per-expert waits are already satisfied: on CTA pairs
+  // (2-SM MMAs) unless disabled, else on single CTAs.
   P.nprob = 2;
   rc = launch<CfgActGrad, CfgInGrad, CfgInGrad, CfgInGrad>(env, P, maps, data_tiles, 1);
   if (rc != HMM_OK || nw == 0) return rc;
+  if (env.pair_wgrad)
+    return launch_wgrad_pair(env, p, m, x_perm, dy_perm, dH, dH_lo, wa, wa_lo, dW1, dW2);
   Params W{};
   W.poff = m.poff;
   W.counts = m.counts;

@@ -1,0 +1,433 @@
+// gmm_pair.cu -- the weight-gradient GEMMs on CTA pairs (tcgen05 cta_group::2).
+//
+// [HyperMegaMoE §2.2 W2Grad, W1Grad]
+//   dW2[e] = (wa_hi + wa_lo)^T . dy_perm      [I, rows of e] x [rows of e, H]
+//   dW1[e] = x_perm^T . (dH_hi + dH_lo)       [H, rows of e] x [rows of e, 2I]
+// (the rounded operand is read as a bf16 hi + lo pair, so the K loop runs over
+// the expert's rows twice).
+//
+// Two CTAs of a cluster compute one 256 x 256 output tile with 2-SM MMAs:
+// each CTA loads its 128 rows of A and its 128 of the 256 columns of B, and
+// each accumulates its 128 rows x 256 columns in its own TMEM.  Per SM that is
+// 32 KB of operands per 64-deep K step instead of 48 KB for a 1-SM 128 x 256
+// tile, a third less smem and L2 traffic for the same MMA work.
+//
+// Roles per CTA: warp 0 issues TMA (both CTAs, one thread), warp 1 issues the
+// MMAs (even CTA only), warps 2..5 drain TMEM (both CTAs).  The even CTA's
+// full barriers count the bytes of both CTAs; the MMA commits arrive on the
+// empty / accumulator-full barriers of both CTAs; both CTAs' epilogues release
+// the even CTA's accumulator-empty barrier.  Tiles are assigned statically
+// (cluster c takes tiles c, c + #clusters, ...): these GEMMs depend on nothing
+// inside the launch.  Every wait is bounded.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "ptx.cuh"
+
+namespace hmm {
+
+namespace {
+
+constexpr int PSTAGES = 6;
+constexpr int PA_BYTES = 128 * 64 * 2;  // this CTA's 128 rows of A, 64 deep
+constexpr int PB_BYTES = 128 * 64 * 2;  // this CTA's 128 columns of B, 64 deep
+constexpr int PSTAGE = PA_BYTES + PB_BYTES;
+constexpr int P_THREADS = 192;
+constexpr int P_SMEM = 1024 + PSTAGES * PSTAGE + 512;
+constexpr uint32_t P_TMEM_COLS = 512;
+constexpr uint32_t IDESC_PAIR = idesc_bf16_f32(256, 256, 1, 1);  // both MN-major
+
+struct PairProb {
+  int M, N;      // output [M, N] per expert
+  int mpairs;    // 256-row tile pairs along M
+  int n_tiles;   // 256-column tiles along N
+  int split;     // 1: A given as hi + lo, 2: B given as hi + lo
+  __nv_bfloat16* out;
+  int64_t ld_out;
+  int64_t out_estride;
+};
+
+struct PairParams {
+  PairProb p[2];
+  int nprob;
+  const int32_t* poff;
+  const int32_t* counts;
+  int E;
+  unsigned* status;
+  unsigned long long budget_ns;
+  uint64_t* trace;  // per-tile timeline records of the even CTA (null: off)
+  int trace_cap;
+};
+
+struct PairMaps {
+  CUtensorMap m[2][3];  // A, B, low half of the split operand
+};
+
+struct PairTile {
+  int prob, e, m0, n0, kb, krow0;
+};
+
+__device__ __forceinline__ int pair_tiles(const PairParams& P, int q) {
+  return P.E * P.p[q].mpairs * P.p[q].n_tiles;
+}
+
+__device__ __forceinline__ void pair_decode(const PairParams& P, int u, PairTile& t) {
+  int q = 0;
+  while (q + 1 < P.nprob && u >= pair_tiles(P, q)) {
+    u -= pair_tiles(P, q);
+    ++q;
+  }
+  const PairProb& pr = P.p[q];
+  const int per = pr.mpairs * pr.n_tiles;
+  t.prob = q;
+  t.e = u / per;
+  const int r = u - t.e * per;
+  t.m0 = (r / pr.n_tiles) * 256;
+  t.n0 = (r % pr.n_tiles) * 256;
+  t.krow0 = P.poff[t.e];
+  // rows past counts[e] are zero padding: skip whole zero K blocks
+  t.kb = (P.counts[t.e] + 63) / 64 * (pr.split ? 2 : 1);
+}
+
+// Timeline record of this CTA's lt-th tile (even CTA of the pair only).
+__device__ __forceinline__ uint64_t* pair_rec(const PairParams& P, bool leader, int lt) {
+  if (!leader || P.trace == nullptr || lt >= P.trace_cap) return nullptr;
+  return P.trace + (static_cast<int64_t>(blockIdx.x) * P.trace_cap + lt) * 8;
+}
+
+__device__ __noinline__ void pair_drain_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < (1u << 28); ++it) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((it & 31u) == 31u && globaltimer_ns() - t0 > budget_ns) return;
+  }
+}
+
+__device__ __noinline__ void pair_pause_ns(uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < ns) __nanosleep(1000);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
+    wgrad_pair_kernel(const __grid_constant__ PairParams P, const __grid_constant__ PairMaps maps) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* stages = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PSTAGES * PSTAGE);
+  uint64_t* full = bars;               // used in the even CTA
+  uint64_t* empty = bars + PSTAGES;    // both CTAs
+  uint64_t* tfull = empty + PSTAGES;   // both CTAs
+  uint64_t* tempty = tfull + 2;        // even CTA
+  uint64_t* mma_done = tempty + 2;     // even CTA
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PSTAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 8);  // 4 epilogue warps in each CTA of the pair
+    }
+    mbar_init(mma_done, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  cluster_sync_all();  // the peer's barriers are initialised before any remote arrive
+  if (warp == 1) {
+    tmem_alloc_pair(s_tmem, P_TMEM_COLS);  // collective: one warp in each CTA of the pair
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const WaitCtl wc{s_abort, P.status, P.budget_ns};
+
+  int total = 0;
+  for (int q = 0; q < P.nprob; ++q) total += pair_tiles(P, q);
+  const int first = static_cast<int>(cluster_id_x());
+  const int stride = static_cast<int>(ncluster_x());
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------- TMA producer
+      for (int q = 0; q < P.nprob; ++q)
+        for (int j = 0; j < 3; ++j) tma_prefetch_desc(&maps.m[q][j]);
+      uint32_t stage = 0, sphase = 0;
+      uint32_t issued = 0;
+      bool ok = true;
+      int lt = 0;
+      for (int u = first; u < total && ok; u += stride) {
+        PairTile t;
+        pair_decode(P, u, t);
+        const PairProb& pr = P.p[t.prob];
+        const CUtensorMap* mp = maps.m[t.prob];
+        uint64_t* rec = pair_rec(P, leader, lt++);
+        if (rec) {
+          uint32_t smid;
+          asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+          rec[0] = (static_cast<uint64_t>(smid) << 48) | (static_cast<uint64_t>(t.prob) << 40) |
+                   (static_cast<uint64_t>(t.e & 0xFFFFF) << 20) |
+                   static_cast<uint64_t>(t.kb & 0xFFFFF);
+          rec[1] = globaltimer_ns();
+        }
+        const int nk = pr.split ? t.kb / 2 : t.kb;
+        const int ma = t.m0 + 128 * static_cast<int>(rank);  // this CTA's rows of the output
+        const int nbc = t.n0 + 128 * static_cast<int>(rank);  // this CTA's half of B's columns
+        for (int kb = 0; kb < t.kb; ++kb) {
+          if (!mbar_wait(&empty[stage], sphase ^ 1u, wc)) {
+            ok = false;
+            break;
+          }
+          if (rec && kb == 0) rec[2] = globaltimer_ns();
+          const bool lo = kb >= nk;
+          const int k = t.krow0 + (lo ? kb - nk : kb) * 64;
+          const CUtensorMap* a = (pr.split == 1 && lo) ? &mp[2] : &mp[0];
+          const CUtensorMap* b = (pr.split == 2 && lo) ? &mp[2] : &mp[1];
+          uint8_t* sA = stages + stage * PSTAGE;
+          uint8_t* sB = sA + PA_BYTES;
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * PSTAGE);
+          const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
+          tma_load_2d_pair(sA, a, bar, ma, k);
+          tma_load_2d_pair(sA + 8192, a, bar, ma + 64, k);
+          tma_load_2d_pair(sB, b, bar, nbc, k);
+          tma_load_2d_pair(sB + 8192, b, bar, nbc + 64, k);
+          ++issued;
+          if (++stage == PSTAGES) {
+            stage = 0;
+            sphase ^= 1u;
+          }
+        }
+        if (rec && ok) rec[3] = globaltimer_ns();
+      }
+      if (!ok) {
+        if (leader) {
+          for (uint32_t s = 0; s < PSTAGES; ++s)
+            if (issued > s)
+              pair_drain_wait(&full[s], ((issued - 1 - s) / PSTAGES) & 1u, P.budget_ns);
+        } else {
+          pair_pause_ns(200000);  // the even CTA counts our bytes; give copies time to land
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------------------ MMA issue
+      uint32_t stage = 0, sphase = 0;
+      uint32_t acc = 0, acc_phase = 0;
+      bool ok = true;
+      int lt = 0;
+      for (int u = first; u < total && ok; u += stride) {
+        PairTile t;
+        pair_decode(P, u, t);
+        uint64_t* rec = pair_rec(P, leader, lt++);
+        if (t.kb == 0) continue;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, wc)) break;
+        tc_fence_after();
+        if (rec) rec[4] = globaltimer_ns();
+        const uint32_t d_tmem = tmem_base + acc * 256;
+        for (int kb = 0; kb < t.kb; ++kb) {
+          if (!mbar_wait(&full[stage], sphase, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(stages + stage * PSTAGE);
+          const uint32_t b_base = a_base + PA_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // MN-major halves: two 64-wide chunks 8 KB apart, 8-row groups 1 KB
+            const uint64_t ad = smem_desc(a_base + kk * 2048, 8192, 1024, LAYOUT_SW128);
+            const uint64_t bd = smem_desc(b_base + kk * 2048, 8192, 1024, LAYOUT_SW128);
+            umma_bf16_pair(d_tmem, ad, bd, IDESC_PAIR, (kb == 0 && kk == 0) ? 0u : 1u);
+          }
+          umma_commit_pair(&empty[stage], 0x3);
+          if (++stage == PSTAGES) {
+            stage = 0;
+            sphase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair(&tfull[acc], 0x3);
+        if (rec) rec[5] = globaltimer_ns();
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      umma_commit_pair(mma_done, 0x1);
+      pair_drain_wait(mma_done, 0, P.budget_ns);
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int q4 = warp & 3;
+    const int row_in_half = q4 * 32 + lane;
+    uint32_t acc = 0, acc_phase = 0;
+    const uint32_t tempty_cl[2] = {mapa_shared(smem_u32(&tempty[0]), 0),
+                                   mapa_shared(smem_u32(&tempty[1]), 0)};
+    int lt = 0;
+    for (int u = first; u < total; u += stride) {
+      PairTile t;
+      pair_decode(P, u, t);
+      const PairProb& pr = P.p[t.prob];
+      uint64_t* rec = (warp == 2 && lane == 0) ? pair_rec(P, leader, lt) : nullptr;
+      ++lt;
+      const int64_t row = t.m0 + 128 * static_cast<int>(rank) + row_in_half;
+      __nv_bfloat16* orow = pr.out + static_cast<int64_t>(t.e) * pr.out_estride + row * pr.ld_out;
+      if (t.kb == 0) {
+        // an expert with no rows: its weight gradient is exactly zero
+        if (row < pr.M)
+          for (int col = t.n0; col < min(t.n0 + 256, pr.N); col += 8)
+            *reinterpret_cast<uint4*>(orow + col) = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      bool got = false;
+      if (lane == 0) got = mbar_wait(&tfull[acc], acc_phase, wc);
+      __syncwarp();
+      if (!__shfl_sync(0xffffffffu, got, 0)) break;
+      tc_fence_after();
+      if (rec) rec[6] = globaltimer_ns();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + acc * 256;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        const int col = t.n0 + c * 32;
+        if (col >= pr.N) break;
+        uint32_t r[32];
+        tmem_ld32(taddr + c * 32, r);
+        tmem_ld_wait();
+        if (row < pr.M) {
+          const int valid = min(32, pr.N - col);
+          uint4* d = reinterpret_cast<uint4*>(orow + col);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            if (g * 8 < valid) {
+              const float* v = reinterpret_cast<const float*>(r) + g * 8;
+              d[g] = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]),
+                                pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(&tempty[acc]);
+        else
+          mbar_arrive_cluster(tempty_cl[acc]);
+      }
+      if (rec) rec[7] = globaltimer_ns();
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // no peer access to our smem or TMEM after this point
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, P_TMEM_COLS);  // collective, like the allocation
+  }
+}
+
+int encode2d(const GemmEnv& env, CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+  const cuuint64_t gd[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t gs[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t bx[2] = {64, 64};
+  const cuuint32_t es[2] = {1, 1};
+  CUresult r = env.encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gd, gs,
+                          bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? HMM_OK : HMM_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, const void* x_perm,
+                      const void* dy_perm, const void* dH, const void* dH_lo, const void* wa,
+                      const void* wa_lo, void* dW1, void* dW2) {
+  const int64_t H = p.H, I = p.I, E = p.E, R = p.R;
+  if (!dW1 && !dW2) return HMM_OK;
+  PairMaps maps;
+  PairParams P{};
+  P.poff = m.poff;
+  P.counts = m.counts;
+  P.E = static_cast<int>(E);
+  P.status = env.status;
+  P.budget_ns = env.budget_ns;
+  if (env.trace && env.trace_which == 2) {
+    P.trace = env.trace;
+    P.trace_cap = env.trace_cap;
+  }
+  int rc = HMM_OK;
+  int q = 0;
+  if (dW2) {
+    rc |= encode2d(env, &maps.m[q][0], wa, R, I);
+    rc |= encode2d(env, &maps.m[q][1], dy_perm, R, H);
+    rc |= encode2d(env, &maps.m[q][2], wa_lo, R, I);
+    PairProb& w = P.p[q++];
+    w.M = static_cast<int>(I);
+    w.N = static_cast<int>(H);
+    w.mpairs = static_cast<int>((I + 255) / 256);
+    w.n_tiles = static_cast<int>((H + 255) / 256);
+    w.split = 1;
+    w.out = static_cast<__nv_bfloat16*>(dW2);
+    w.ld_out = H;
+    w.out_estride = I * H;
+  }
+  if (dW1) {
+    rc |= encode2d(env, &maps.m[q][0], x_perm, R, H);
+    rc |= encode2d(env, &maps.m[q][1], dH, R, 2 * I);
+    rc |= encode2d(env, &maps.m[q][2], dH_lo, R, 2 * I);
+    PairProb& w = P.p[q++];
+    w.M = static_cast<int>(H);
+    w.N = static_cast<int>(2 * I);
+    w.mpairs = static_cast<int>((H + 255) / 256);
+    w.n_tiles = static_cast<int>((2 * I + 255) / 256);
+    w.split = 2;
+    w.out = static_cast<__nv_bfloat16*>(dW1);
+    w.ld_out = 2 * I;
+    w.out_estride = H * 2 * I;
+  }
+  if (rc != HMM_OK) return HMM_ERR_CUDA;
+  P.nprob = q;
+  int64_t total = 0;
+  for (int i = 0; i < q; ++i) total += E * P.p[i].mpairs * P.p[i].n_tiles;
+  if (total <= 0) return HMM_OK;
+  if (cudaFuncSetAttribute(wgrad_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           P_SMEM) != cudaSuccess)
+    return HMM_ERR_CUDA;
+  // as many pairs as can be resident at once (tiles are assigned statically)
+  int clusters = env.num_sms / 2;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+    cfg.blockDim = dim3(P_THREADS);
+    cfg.dynamicSmemBytes = P_SMEM;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, wgrad_pair_kernel, &cfg) == cudaSuccess &&
+        active > 0)
+      clusters = std::min(clusters, active);
+  }
+  clusters = static_cast<int>(std::min<int64_t>(clusters, total));
+  wgrad_pair_kernel<<<2 * clusters, P_THREADS, P_SMEM, env.stream>>>(P, maps);
+  return cudaGetLastError() == cudaSuccess ? HMM_OK : HMM_ERR_CUDA;
+}
+
+}  // namespace hmm

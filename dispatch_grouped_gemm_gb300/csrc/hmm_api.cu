@@ -48,6 +48,7 @@ struct hmm_ctx {
   int inject_skip_ready = 0;
   int profile = 0;
   int bwd_data_sms = 0;
+  int pair_wgrad = 1;
   uint64_t* trace = nullptr;
   size_t trace_bytes = 0;
   int trace_which = 0;
@@ -227,6 +228,7 @@ GemmEnv env_of(hmm_ctx* ctx, cudaStream_t st) {
   e.encode = ctx->encode;
   e.num_sms = ctx->num_sms;
   e.bwd_data_sms = ctx->bwd_data_sms;
+  e.pair_wgrad = ctx->pair_wgrad;
   e.trace = ctx->trace;
   e.trace_cap = ctx->trace ? static_cast<int>(ctx->trace_bytes / (64 * ctx->num_sms)) : 0;
   e.trace_which = ctx->trace_which;
@@ -322,6 +324,9 @@ int hmm_set_option(hmm_ctx* ctx, int option, int64_t value) {
       return HMM_OK;
     case HMM_OPT_PROFILE:
       ctx->profile = value != 0;
+      return HMM_OK;
+    case HMM_OPT_PAIR_WGRAD:
+      ctx->pair_wgrad = value != 0;
       return HMM_OK;
     case HMM_OPT_BWD_DATA_SMS:
       if (value < 0 || value >= ctx->num_sms) return HMM_ERR_ARG;

@@ -97,6 +97,7 @@ struct GemmEnv {
   int trace_cap;     // records per CTA
   int trace_which;   // which GEMM launch kind is traced
   int bwd_data_sms;  // SMs for the data-gradient group of the backward (0: automatic)
+  int pair_wgrad;    // weight gradients on CTA pairs (2-SM MMA)
   unsigned* status;
   uint64_t budget_ns;
   cudaStream_t stream;
@@ -117,5 +118,10 @@ int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtr
                           const float* h32, const void* W1, const void* W2, void* dH,
                           void* dH_lo, void* wa, void* wa_lo, float* dwp, void* dx_perm,
                           void* dW1, void* dW2);
+
+// weight-gradient GEMMs on CTA pairs (tcgen05 cta_group::2), 256 x 256 tiles
+int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, const void* x_perm,
+                      const void* dy_perm, const void* dH, const void* dH_lo, const void* wa,
+                      const void* wa_lo, void* dW1, void* dW2);
 
 }  // namespace hmm

@@ -123,6 +123,10 @@ int hmm_destroy(hmm_ctx* ctx);
  *                         GEMMs while the others run the weight-gradient
  *                         GEMMs concurrently, trailing act_grad per expert. */
 #define HMM_OPT_BWD_DATA_SMS 5
+/*   HMM_OPT_PAIR_WGRAD    1 (default): the weight-gradient GEMMs run on CTA
+ *                         pairs with 2-SM MMAs (256 x 256 tiles); 0: on single
+ *                         CTAs (128 x 256 tiles). */
+#define HMM_OPT_PAIR_WGRAD 6
 int hmm_set_option(hmm_ctx* ctx, int option, int64_t value);
 
 /* Launch phases timed under HMM_OPT_PROFILE (index = phase id):
