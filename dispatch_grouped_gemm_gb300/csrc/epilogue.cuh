@@ -1,0 +1,51 @@
+// epilogue.cuh -- moving a tcgen05 accumulator block out of TMEM.
+#pragma once
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace hmm {
+
+// tcgen05.ld (32x32b) hands a warp its 32 TMEM lanes one row per thread.
+// Written out in that form, every 16-byte store of the warp lands in 32
+// different rows.  Instead each warp passes its 32x32 fp32 block through a
+// padded shared-memory buffer and continues with lane l owning the eight
+// columns 8*(l & 3) .. +7 of the rows (l >> 2) + 8k, k = 0..3: a warp-wide
+// 16-byte access then covers 8 rows x 64 contiguous bytes.
+//
+// Buffer: 32 rows with a stride of XS floats (16-byte aligned rows; both the
+// row-wise writes and the column-group reads below are free of bank
+// conflicts).
+constexpr int XS = 36;
+constexpr int XBUF_BYTES = 32 * XS * 4;  // per epilogue warp
+
+__device__ __forceinline__ void xpose(float* buf, int lane, const uint32_t (&r)[32],
+                                      float (&o)[4][8]) {
+  float4* d = reinterpret_cast<float4*>(buf + lane * XS);
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    d[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                       __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+  __syncwarp();
+  const float* s = buf + (lane >> 2) * XS + (lane & 3) * 8;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float4 a = *reinterpret_cast<const float4*>(s + k * 8 * XS);
+    const float4 b = *reinterpret_cast<const float4*>(s + k * 8 * XS + 4);
+    o[k][0] = a.x; o[k][1] = a.y; o[k][2] = a.z; o[k][3] = a.w;
+    o[k][4] = b.x; o[k][5] = b.y; o[k][6] = b.z; o[k][7] = b.w;
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
+  uint4 u;
+  u.x = pack_bf16(v[0], v[1]);
+  u.y = pack_bf16(v[2], v[3]);
+  u.z = pack_bf16(v[4], v[5]);
+  u.w = pack_bf16(v[6], v[7]);
+  return u;
+}
+
+}  // namespace hmm

@@ -32,6 +32,7 @@
 
 #include <algorithm>
 
+#include "epilogue.cuh"
 #include "ptx.cuh"
 
 namespace hmm {
@@ -45,12 +46,21 @@ struct Cfg {
   static constexpr bool A_MN = WGRAD_;  // activations transposed in the wgrad mode
   static constexpr bool B_MN = B_MN_;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+  // 2-SM MMA of a CTA pair: M = 256 rows (128 per CTA), the same N
+  static constexpr uint32_t IDESC2 = idesc_bf16_f32(2 * BM, BN, A_MN ? 1 : 0, B_MN ? 1 : 0);
 };
 
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+// CTA pairs: each CTA stages its 128 rows of A and 128 of the 256 columns of
+// B, 32 KB per K block, in six stages (the same 192 KB)
+constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_B_BYTES = (BN / 2) * BK * 2;  // 16 KB
+constexpr int PAIR_STAGE_BYTES = A_BYTES + PAIR_B_BYTES;
+constexpr int MAX_STAGES = PAIR_STAGES;
+static_assert(PAIR_STAGES * PAIR_STAGE_BYTES <= STAGES * STAGE_BYTES, "pair stages");
 constexpr int TI_DEPTH = 3;
 // Warp roles: 0 TMA producer, 1 MMA issuer, 2..5 epilogue (one per TMEM lane
 // quarter), 6 tile scheduler.  (Eight epilogue warps, two per quarter on
@@ -60,8 +70,11 @@ constexpr int EPI_WARPS = 4;
 constexpr int CH_SPLIT = EPI_WARPS / 4;  // warps sharing a lane quarter
 constexpr int SCHED_WARP = 2 + EPI_WARPS;
 constexpr int NUM_THREADS = 32 * (SCHED_WARP + 1);  // 11 warps
-// alignment slack + stages + barriers, tile-info ring and schedule prefix table
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 512 + 4 * (3 * MAX_E + 8 + 1) + 256;
+// alignment slack + stages + epilogue buffers + barriers, tile-info ring and
+// schedule prefix table
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_WARPS * XBUF_BYTES + 512 +
+                           4 * (3 * MAX_E + 8 + 1) + 256;
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 constexpr uint32_t TMEM_COLS = 2 * BN;
 
 struct Prob {
@@ -100,6 +113,7 @@ constexpr int MAX_STEPS = 3 * MAX_E + 8;
 struct Params {
   Prob p[MAX_PROB];
   int nprob;
+  int pair;             // rows mode on CTA pairs: a tile is two M tiles of one expert
   int steps[2];         // per CTA group: E + largest lag of its problems
   int group_split;      // CTAs [0, group_split) serve group 0, the rest group 1
                         // (0: one group)
@@ -124,6 +138,7 @@ struct TileInfo {
   int n0;     // first output column
   int kb;     // K blocks (0: empty wgrad tile -> zeros)
   int krow0;  // wgrad: first padded row of the expert
+  int ph;     // pair tile whose second M tile lies past the expert (odd M-tile count)
 };
 
 // ------------------------------------------------------------------ tracing
@@ -145,7 +160,8 @@ __device__ __forceinline__ int mtiles_of(const Params& P, int e) {
 __device__ __forceinline__ int tiles_of(const Params& P, const Prob& pr, int e) {
   if (e < 0 || e >= P.E) return 0;
   if (pr.wgrad) return pr.m_tiles * pr.n_tiles;
-  return mtiles_of(P, e) * pr.n_tiles;
+  const int nm = mtiles_of(P, e);
+  return (P.pair ? (nm + 1) / 2 : nm) * pr.n_tiles;
 }
 
 // Prefix sums of the tile counts of group g's schedule steps (one warp, into
@@ -213,8 +229,11 @@ __device__ void decode_tile(const Params& P, const Prob& pr, int e, int r, TileI
     ti.kb = (P.counts[e] + BK - 1) / BK * (pr.split ? 2 : 1);
   } else {
     const int nm = mtiles_of(P, e);
-    const int nb = r / nm;  // M tiles innermost: a weight tile is reused from L2
-    ti.m0 = P.poff[e] + (r - nb * nm) * BM;
+    const int nu = P.pair ? (nm + 1) / 2 : nm;  // M tiles or M-tile pairs
+    const int nb = r / nu;  // M innermost: a weight tile is reused from L2
+    const int mu = r - nb * nu;
+    ti.m0 = P.poff[e] + mu * BM * (P.pair ? 2 : 1);
+    ti.ph = P.pair && 2 * mu + 1 >= nm;
     ti.n0 = nb * (C::EPI == EPI_SWIGLU ? BN / 2 : BN);
     ti.krow0 = 0;
     ti.kb = (pr.K + BK - 1) / BK;
@@ -268,6 +287,30 @@ __device__ __forceinline__ void stage_boxes(const Prob& pr, const TileInfo& ti, 
   }
 }
 
+// CTA pair: this CTA's share of K block kb (its 128 rows of A unless it is
+// the empty half of the pair; its 128 columns of B) into its own smem, counted
+// on the even CTA's full barrier (bar: shared::cluster address).
+template <class C>
+__device__ __forceinline__ void stage_boxes_pair(const Prob& pr, const TileInfo& ti, int kb,
+                                                 const CUtensorMap* tA, const CUtensorMap* tB,
+                                                 uint8_t* sA, uint8_t* sB, uint32_t bar,
+                                                 uint32_t rank) {
+  static_assert(!C::WGRAD, "CTA pairs serve the rows-mode GEMMs");
+  const int k = kb * BK;
+  if (rank == 0 || !ti.ph) tma_load_2d_pair(sA, tA, bar, k, ti.m0 + BM * static_cast<int>(rank));
+  if constexpr (C::B_MN) {
+    int c;
+    if constexpr (C::EPI == EPI_SWIGLU)
+      c = (rank == 0 ? 0 : pr.half) + ti.n0;  // gate columns | up columns
+    else
+      c = ti.n0 + (BN / 2) * static_cast<int>(rank);
+    tma_load_3d_pair(sB, tB, bar, c, k, ti.e);
+    tma_load_3d_pair(sB + 8192, tB, bar, c + 64, k, ti.e);
+  } else {
+    tma_load_3d_pair(sB, tB, bar, k, ti.n0 + (BN / 2) * static_cast<int>(rank), ti.e);
+  }
+}
+
 template <class C>
 __device__ __forceinline__ void load_stage(const Prob& pr, const TileInfo& ti, int kb,
                                            const CUtensorMap* tA, const CUtensorMap* tB,
@@ -290,6 +333,19 @@ __device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t a_base, uint
   }
 }
 
+template <class C>
+__device__ __forceinline__ void mma_stage_pair(uint32_t d_tmem, uint32_t a_base, uint32_t b_base,
+                                               bool first) {
+#pragma unroll
+  for (int kk = 0; kk < BK / 16; ++kk) {
+    const uint64_t ad = C::A_MN ? smem_desc(a_base + kk * 2048, 8192, 1024, LAYOUT_SW128)
+                                : smem_desc(a_base + kk * 32, 16, 1024, LAYOUT_SW128);
+    const uint64_t bd = C::B_MN ? smem_desc(b_base + kk * 2048, 8192, 1024, LAYOUT_SW128)
+                                : smem_desc(b_base + kk * 32, 16, 1024, LAYOUT_SW128);
+    umma_bf16_pair(d_tmem, ad, bd, C::IDESC2, (first && kk == 0) ? 0u : 1u);
+  }
+}
+
 // ----------------------------------------------------------------- epilogue
 // sigma(g) = 1 / (1 + exp(-g)) with the fast exponential and division
 // intrinsics (a few ulp in fp32, far inside the bf16 output rounding).
@@ -297,119 +353,68 @@ __device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t a_base, uint
 __device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 __device__ __forceinline__ float silu_f(float g) { return g * sigmoid_f(g); }
 
-// 16-byte groups of one row segment: group q of the 32 columns at p + q * gs
-// bytes (gs = 16: contiguous).
-__device__ __forceinline__ void store_bf16x32(void* dst, int64_t gs, const float* v, int valid) {
-  // valid: number of the 32 columns inside the output (multiple of 8)
-  char* d = static_cast<char*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    if (q * 8 < valid) {
-      uint4 u;
-      u.x = pack_bf16(v[q * 8 + 0], v[q * 8 + 1]);
-      u.y = pack_bf16(v[q * 8 + 2], v[q * 8 + 3]);
-      u.z = pack_bf16(v[q * 8 + 4], v[q * 8 + 5]);
-      u.w = pack_bf16(v[q * 8 + 6], v[q * 8 + 7]);
-      *reinterpret_cast<uint4*>(d + q * gs) = u;
-    }
-  }
-}
-
 // v = hi + lo with hi = bf16(v), lo = bf16(v - hi): the pair carries about
 // 16 significant bits, enough for the weight-gradient GEMMs that consume it.
-__device__ __forceinline__ void store_bf16x32_split(void* hi, void* lo, int64_t gs,
-                                                    const float* v, int valid) {
-  float h[32], l[32];
+__device__ __forceinline__ void store_bf16x8_split(__nv_bfloat16* hi, __nv_bfloat16* lo,
+                                                   const float* v) {
+  float h[8], l[8];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
+  for (int j = 0; j < 8; ++j) {
     h[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
     l[j] = v[j] - h[j];
   }
-  store_bf16x32(hi, gs, h, valid);
-  store_bf16x32(lo, gs, l, valid);
+  *reinterpret_cast<uint4*>(hi) = pack_bf16x8(h);
+  *reinterpret_cast<uint4*>(lo) = pack_bf16x8(l);
 }
 
-__device__ __forceinline__ void store_bf16x8_split(__nv_bfloat16* hi, __nv_bfloat16* lo,
-                                                   const float* v) {
-  uint4 h, l;
-  uint32_t* hp = reinterpret_cast<uint32_t*>(&h);
-  uint32_t* lp = reinterpret_cast<uint32_t*>(&l);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float h0 = __bfloat162float(__float2bfloat16_rn(v[2 * j]));
-    const float h1 = __bfloat162float(__float2bfloat16_rn(v[2 * j + 1]));
-    hp[j] = pack_bf16(h0, h1);
-    lp[j] = pack_bf16(v[2 * j] - h0, v[2 * j + 1] - h1);
-  }
-  *reinterpret_cast<uint4*>(hi) = h;
-  *reinterpret_cast<uint4*>(lo) = l;
+__device__ __forceinline__ void store_f32x8(float* dst, const float* v) {
+  reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
 
-__device__ __forceinline__ void store_f32x32(void* dst, int64_t gs, const float* v, int valid) {
-  char* d = static_cast<char*>(dst);
-#pragma unroll
-  for (int q = 0; q < 8; ++q)
-    if (q * 4 < valid)
-      *reinterpret_cast<float4*>(d + q * gs) =
-          make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-}
-
-__device__ __forceinline__ void load_f32x32(const void* src, int64_t gs, float* v, int valid) {
-  const char* s = static_cast<const char*>(src);
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (q * 4 < valid) f = *reinterpret_cast<const float4*>(s + q * gs);
-    v[4 * q] = f.x;
-    v[4 * q + 1] = f.y;
-    v[4 * q + 2] = f.z;
-    v[4 * q + 3] = f.w;
-  }
-}
-
-// Drains the accumulator of one tile; taddr addresses this warp's lanes.
-// ch: which warp of the lane quarter (chunks ch, ch + CH_SPLIT, ...).
+// Drains the accumulator of one tile.  taddr addresses this warp's TMEM lane
+// quarter, whose rows are r0 .. r0 + 31 of the output (r0 = m0 + 32 * quarter);
+// ch: which warp of the lane quarter (column chunks ch, ch + CH_SPLIT, ...).
+// Column chunks are skipped per lane with plain conditionals, never an early
+// continue: the next chunk's TMEM load is a warp-wide instruction.
 template <class C>
 __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti, uint32_t taddr,
-                                              int row_in_tile, int ch) {
+                                              int64_t r0, int lane, int ch, float* xbuf) {
+  const int cg = (lane & 3) * 8;        // this lane's first column within a 32-column chunk
+  const int64_t rl = r0 + (lane >> 2);  // this lane's rows: rl + 8k
   if constexpr (C::EPI == EPI_SWIGLU) {
     // cols [0,128): gate of n0..n0+127, [128,256): up of the same columns
-    const int64_t row = ti.m0 + row_in_tile;
-    __nv_bfloat16* a_row = static_cast<__nv_bfloat16*>(pr.out) + row * pr.ld_out;
-    float* h_row = pr.out2 ? static_cast<float*>(pr.out2) + row * pr.ld_out2 : nullptr;
 #pragma unroll 1
     for (int c = ch; c < 4; c += CH_SPLIT) {
       const int col = ti.n0 + c * 32;
       if (col >= pr.N) break;
-      const int valid = min(32, pr.N - col);
       uint32_t g[32], u[32];
       tmem_ld32(taddr + c * 32, g);
       tmem_ld32(taddr + 128 + c * 32, u);
       tmem_ld_wait();
-      float av[32];
+      float gv[4][8], uv[4][8];
+      xpose(xbuf, lane, g, gv);
+      xpose(xbuf, lane, u, uv);
+      if (col + cg < pr.N) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float gf = __uint_as_float(g[j]), uf = __uint_as_float(u[j]);
-        av[j] = silu_f(gf) * uf;
-      }
-      store_bf16x32(a_row + col, 16, av, valid);
-      if (h_row) {
-        store_f32x32(h_row + col, 16, reinterpret_cast<const float*>(g), valid);
-        store_f32x32(h_row + pr.half + col, 16, reinterpret_cast<const float*>(u), valid);
+        for (int k = 0; k < 4; ++k) {
+          const int64_t row = rl + 8 * k;
+          float av[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) av[j] = silu_f(gv[k][j]) * uv[k][j];
+          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(pr.out) + row * pr.ld_out + col +
+                                    cg) = pack_bf16x8(av);
+          if (pr.out2) {
+            float* h_row = static_cast<float*>(pr.out2) + row * pr.ld_out2;
+            store_f32x8(h_row + col + cg, gv[k]);
+            store_f32x8(h_row + pr.half + col + cg, uv[k]);
+          }
+        }
       }
     }
   } else if constexpr (C::EPI == EPI_STORE) {
-    int64_t row;
-    __nv_bfloat16* base;
-    if constexpr (C::WGRAD) {
-      row = ti.m0 + row_in_tile;
-      base = static_cast<__nv_bfloat16*>(pr.out) + static_cast<int64_t>(ti.e) * pr.out_estride;
-    } else {
-      row = ti.m0 + row_in_tile;
-      base = static_cast<__nv_bfloat16*>(pr.out);
-    }
-    const bool row_ok = !C::WGRAD || row < pr.M;
-    __nv_bfloat16* orow = base + row * pr.ld_out;
+    __nv_bfloat16* base = static_cast<__nv_bfloat16*>(pr.out);
+    if constexpr (C::WGRAD) base += static_cast<int64_t>(ti.e) * pr.out_estride;
 #pragma unroll 1
     for (int c = ch; c < BN / 32; c += CH_SPLIT) {
       const int col = ti.n0 + c * 32;
@@ -417,62 +422,109 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
       uint32_t r[32];
       tmem_ld32(taddr + c * 32, r);
       tmem_ld_wait();
-      if (row_ok)
-        store_bf16x32(orow + col, 16, reinterpret_cast<const float*>(r), min(32, pr.N - col));
+      float v[4][8];
+      xpose(xbuf, lane, r, v);
+      if (col + cg < pr.N) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int64_t row = rl + 8 * k;
+          if (!C::WGRAD || row < pr.M)
+            *reinterpret_cast<uint4*>(base + row * pr.ld_out + col + cg) = pack_bf16x8(v[k]);
+        }
+      }
     }
   } else {  // EPI_DSWIGLU
     // acc = G = dy_perm . W2^T for columns n0..n0+255 of I.  With the saved
     // fp32 pre-activations g, u and the slot's routing weight w:
     //   a = silu(g) u,  dA = w G,
     //   dgate = dA u s (1 + g (1 - s)),  dup = dA g s     (s = sigmoid(g))
-    // writes dH = [dgate | dup] (bf16), wa = w a (bf16, the W2Grad operand)
-    // and the partial d_w = sum_j G_j a_j of this column block (fp32).
-    const int64_t row = ti.m0 + row_in_tile;
-    const float* h_row = static_cast<const float*>(pr.aux) + row * pr.ld_aux;
-    __nv_bfloat16* dh_row = static_cast<__nv_bfloat16*>(pr.out) + row * pr.ld_out;
-    __nv_bfloat16* wa_row = static_cast<__nv_bfloat16*>(pr.out2) + row * pr.ld_out2;
-    __nv_bfloat16* dh_lo = static_cast<__nv_bfloat16*>(pr.out4) + row * pr.ld_out;
-    __nv_bfloat16* wa_lo = static_cast<__nv_bfloat16*>(pr.out5) + row * pr.ld_out2;
-    const float w = pr.rowscale[row];
-    float dwp = 0.0f;
+    // writes dH = [dgate | dup] (bf16 hi + lo), wa = w a (bf16 hi + lo, the
+    // W2Grad operand) and the partial d_w = sum_j G_j a_j of this column
+    // block (fp32).  The pre-activations of the next chunk are loaded while
+    // the current one is computed.
+    const float* hb = static_cast<const float*>(pr.aux);
+    float w[4], dwp[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      w[k] = pr.rowscale[rl + 8 * k];
+      dwp[k] = 0.0f;
+    }
+    float4 gn[4][2], un[4][2];
+    auto load_h = [&](int col) {
+      const bool ok = col + cg < pr.N;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4* p =
+            reinterpret_cast<const float4*>(hb + (rl + 8 * k) * pr.ld_aux + col + cg);
+        const float4* pu =
+            reinterpret_cast<const float4*>(hb + (rl + 8 * k) * pr.ld_aux + pr.half + col + cg);
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        gn[k][0] = ok ? __ldg(p) : z;
+        gn[k][1] = ok ? __ldg(p + 1) : z;
+        un[k][0] = ok ? __ldg(pu) : z;
+        un[k][1] = ok ? __ldg(pu + 1) : z;
+      }
+    };
+    if (ti.n0 + ch * 32 < pr.N) load_h(ti.n0 + ch * 32);
 #pragma unroll 1
     for (int c = ch; c < BN / 32; c += CH_SPLIT) {
       const int col = ti.n0 + c * 32;
       if (col >= pr.N) break;
-      const int valid = min(32, pr.N - col);
+      float gv[4][8], uv[4][8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        gv[k][0] = gn[k][0].x; gv[k][1] = gn[k][0].y; gv[k][2] = gn[k][0].z; gv[k][3] = gn[k][0].w;
+        gv[k][4] = gn[k][1].x; gv[k][5] = gn[k][1].y; gv[k][6] = gn[k][1].z; gv[k][7] = gn[k][1].w;
+        uv[k][0] = un[k][0].x; uv[k][1] = un[k][0].y; uv[k][2] = un[k][0].z; uv[k][3] = un[k][0].w;
+        uv[k][4] = un[k][1].x; uv[k][5] = un[k][1].y; uv[k][6] = un[k][1].z; uv[k][7] = un[k][1].w;
+      }
+      const int ncol = col + 32 * CH_SPLIT;
+      if (c + CH_SPLIT < BN / 32 && ncol < pr.N) load_h(ncol);
       uint32_t r[32];
       tmem_ld32(taddr + c * 32, r);
-      float gv[32], uv[32];
-      load_f32x32(h_row + col, 16, gv, valid);
-      load_f32x32(h_row + pr.half + col, 16, uv, valid);
       tmem_ld_wait();
-      // eight columns at a time: compute, split into bf16 hi + lo, store
+      float Gv[4][8];
+      xpose(xbuf, lane, r, Gv);
+      if (col + cg < pr.N) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (q * 8 < valid) {
+        for (int k = 0; k < 4; ++k) {
+          const int64_t row = rl + 8 * k;
           float dg[8], du[8], wa[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float G = __uint_as_float(r[q * 8 + j]);
-            const float g = gv[q * 8 + j], u = uv[q * 8 + j];
+            const float G = Gv[k][j], g = gv[k][j], u = uv[k][j];
             const float sg = sigmoid_f(g);
             const float a = g * sg * u;
-            dwp = fmaf(G, a, dwp);
-            const float dA = w * G;
+            dwp[k] = fmaf(G, a, dwp[k]);
+            const float dA = w[k] * G;
             dg[j] = dA * u * sg * (1.0f + g * (1.0f - sg));
             du[j] = dA * g * sg;
-            wa[j] = w * a;
+            wa[j] = w[k] * a;
           }
-          const int cq = col + q * 8;
-          store_bf16x8_split(dh_row + cq, dh_lo + cq, dg);
-          store_bf16x8_split(dh_row + pr.half + cq, dh_lo + pr.half + cq, du);
-          store_bf16x8_split(wa_row + cq, wa_lo + cq, wa);
+          __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(pr.out) + row * pr.ld_out + col + cg;
+          __nv_bfloat16* dl = static_cast<__nv_bfloat16*>(pr.out4) + row * pr.ld_out + col + cg;
+          store_bf16x8_split(dh, dl, dg);
+          store_bf16x8_split(dh + pr.half, dl + pr.half, du);
+          store_bf16x8_split(static_cast<__nv_bfloat16*>(pr.out2) + row * pr.ld_out2 + col + cg,
+                             static_cast<__nv_bfloat16*>(pr.out5) + row * pr.ld_out2 + col + cg,
+                             wa);
         }
       }
     }
-    // one partial per (column block, warp of the quarter); the combine sums
-    // them in order
-    static_cast<float*>(pr.out3)[row * pr.ld_out3 + (ti.n0 / BN) * CH_SPLIT + ch] = dwp;
+    // one partial per (row, column block, warp of the quarter): the four
+    // lanes of a row add theirs in a fixed tree, the combine sums the blocks
+    // in order
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      dwp[k] += __shfl_xor_sync(0xffffffffu, dwp[k], 1);
+      dwp[k] += __shfl_xor_sync(0xffffffffu, dwp[k], 2);
+    }
+    if (cg == 0) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        static_cast<float*>(pr.out3)[(rl + 8 * k) * pr.ld_out3 + (ti.n0 / BN) * CH_SPLIT + ch] =
+            dwp[k];
+    }
   }
 }
 
@@ -500,6 +552,11 @@ __device__ __noinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t
   }
 }
 
+__device__ __noinline__ void pause_ns(uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < ns) __nanosleep(1000);
+}
+
 // ------------------------------------------------------------------- kernel
 #define HMM_BY_PROB(q, F, ...)       \
   switch (q) {                       \
@@ -509,20 +566,24 @@ __device__ __noinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t
     default: F<C3>(__VA_ARGS__); break; \
   }
 
-template <class C0, class C1, class C2, class C3>
+template <bool PAIR, class C0, class C1, class C2, class C3>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gmm_kernel(const __grid_constant__ Params P, const __grid_constant__ Maps maps) {
+  constexpr int NST = PAIR ? PAIR_STAGES : STAGES;
+  constexpr int SBYTES = PAIR ? PAIR_STAGE_BYTES : STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + STAGES;
-  uint64_t* tfull = bars + 2 * STAGES;
-  uint64_t* tempty = tfull + 2;
+  float* xbufs = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + EPI_WARPS * XBUF_BYTES);
+  uint64_t* full = bars;                    // [NST]; in a pair: the even CTA's counts both CTAs
+  uint64_t* empty = bars + MAX_STAGES;      // [NST]
+  uint64_t* tfull = bars + 2 * MAX_STAGES;  // [2]
+  uint64_t* tempty = tfull + 2;             // [2]; in a pair: the even CTA's, both CTAs arrive
   uint64_t* ti_full = tempty + 2;
-  uint64_t* ti_empty = ti_full + TI_DEPTH;
+  uint64_t* ti_empty = ti_full + TI_DEPTH;  // in a pair: the even CTA's, both CTAs arrive
   uint64_t* mma_done = ti_empty + TI_DEPTH;
   TileInfo* s_ti = reinterpret_cast<TileInfo*>(mma_done + 1);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_ti + TI_DEPTH);
@@ -531,33 +592,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], EPI_WARPS);
+      mbar_init(&tempty[a], PAIR ? 2 * EPI_WARPS : EPI_WARPS);
     }
     for (int i = 0; i < TI_DEPTH; ++i) {
       mbar_init(&ti_full[i], 1);
-      mbar_init(&ti_empty[i], 2 + EPI_WARPS);  // TMA producer, MMA issuer, epilogue warps
+      // consumers: TMA producer, MMA issuer, epilogue warps (+ the odd CTA's
+      // producer and epilogue warps in a pair)
+      mbar_init(&ti_empty[i], PAIR ? 2 * (1 + EPI_WARPS) + 1 : 2 + EPI_WARPS);
     }
     mbar_init(mma_done, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
+  if constexpr (PAIR) cluster_sync_all();  // barriers initialised before any remote arrive
   if (warp == 1) {
-    tmem_alloc(s_tmem, TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(s_tmem, TMEM_COLS);  // collective: one warp in each CTA of the pair
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(s_tmem, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
   const WaitCtl wc{s_abort, P.status, P.budget_ns};
+  // in a pair the odd CTA's consumers release the even CTA's tile-info slots
+  auto ti_release = [&](int slot) {
+    if (!PAIR || leader)
+      mbar_arrive(&ti_empty[slot]);
+    else
+      mbar_arrive_cluster(mapa_shared(smem_u32(&ti_empty[slot]), 0));
+  };
 
   const int group = (P.group_split > 0 && static_cast<int>(blockIdx.x) >= P.group_split) ? 1 : 0;
   if (warp == SCHED_WARP) {
@@ -566,61 +644,77 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // about one tile ahead of the TMA producer, so neither the ticket atomic
     // nor a ready-counter poll sits on the load path.  (A deeper lookahead
     // spreads the M tiles that share a weight tile over time and costs L2
-    // reuse of the weights.)  Lane 0 does the bookkeeping.
-    build_schedule(P, group, s_pref);
-    int ti_slot = 0;
-    uint32_t ti_phase = 0;
-    int lt = 0;  // tiles of this CTA so far (trace index)
-    int t = 0;
-    if (lane == 0) t = atomicAdd(P.ticket + group, 1);
-    for (;;) {
-      TileInfo ti;
-      ti.prob = -1;
-      ti.e = ti.m0 = ti.n0 = ti.kb = ti.krow0 = 0;
-      bool ok = true;
-      if (lane == 0) {
-        int q = 0, e = 0, r = 0;
-        if (locate_tile(P, group, s_pref, t, q, e, r)) {
-          ti.prob = q;
-          HMM_BY_PROB(q, decode_tile, P, P.p[q], e, r, ti);
-          t = atomicAdd(P.ticket + group, 1);  // next ticket, early
-          const Prob& pr = P.p[q];
-          if (pr.wait_m || pr.wait_e)
-            ok = pr.wait_m ? counter_wait(&pr.wait_m[ti.m0 / BM], pr.wait_unit, wc)
-                           : counter_wait(&pr.wait_e[ti.e], pr.wait_unit * mtiles_of(P, ti.e),
-                                          wc);
-        }
-      }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      ti.prob = __shfl_sync(0xffffffffu, ti.prob, 0);
-      ti.e = __shfl_sync(0xffffffffu, ti.e, 0);
-      ti.m0 = __shfl_sync(0xffffffffu, ti.m0, 0);
-      ti.n0 = __shfl_sync(0xffffffffu, ti.n0, 0);
-      ti.kb = __shfl_sync(0xffffffffu, ti.kb, 0);
-      ti.krow0 = __shfl_sync(0xffffffffu, ti.krow0, 0);
-      bool got = false;
-      if (lane == 0) got = mbar_wait(&ti_empty[ti_slot], ti_phase ^ 1u, wc);
-      if (!__shfl_sync(0xffffffffu, got, 0)) break;
-      if (lane == 0) {
-        if (ti.prob >= 0) {
-          if (uint64_t* rec = trace_rec(P, lt)) {
-            rec[0] = (static_cast<uint64_t>(sm_id()) << 48) |
-                     (static_cast<uint64_t>(ti.prob) << 40) |
-                     (static_cast<uint64_t>(ti.e & 0xFFFFF) << 20) |
-                     static_cast<uint64_t>(ti.kb & 0xFFFFF);
-            rec[1] = globaltimer_ns();
+    // reuse of the weights.)  Lane 0 does the bookkeeping.  In a pair only
+    // the even CTA schedules; it writes each tile into both CTAs' rings.
+    if (!PAIR || leader) {
+      build_schedule(P, group, s_pref);
+      int ti_slot = 0;
+      uint32_t ti_phase = 0;
+      int lt = 0;  // tiles of this CTA so far (trace index)
+      int t = 0;
+      if (lane == 0) t = atomicAdd(P.ticket + group, 1);
+      for (;;) {
+        TileInfo ti;
+        ti.prob = -1;
+        ti.e = ti.m0 = ti.n0 = ti.kb = ti.krow0 = ti.ph = 0;
+        bool ok = true;
+        if (lane == 0) {
+          int q = 0, e = 0, r = 0;
+          if (locate_tile(P, group, s_pref, t, q, e, r)) {
+            ti.prob = q;
+            HMM_BY_PROB(q, decode_tile, P, P.p[q], e, r, ti);
+            t = atomicAdd(P.ticket + group, 1);  // next ticket, early
+            const Prob& pr = P.p[q];
+            if (pr.wait_m) {
+              ok = counter_wait(&pr.wait_m[ti.m0 / BM], pr.wait_unit, wc);
+              if (ok && PAIR && !ti.ph)
+                ok = counter_wait(&pr.wait_m[ti.m0 / BM + 1], pr.wait_unit, wc);
+            } else if (pr.wait_e) {
+              ok = counter_wait(&pr.wait_e[ti.e], pr.wait_unit * mtiles_of(P, ti.e), wc);
+            }
           }
         }
-        s_ti[ti_slot] = ti;
-        mbar_arrive(&ti_full[ti_slot]);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        // every lane leaves the loop with lane 0 (end marker below)
+        ti.prob = __shfl_sync(0xffffffffu, ti.prob, 0);
+        ti.e = __shfl_sync(0xffffffffu, ti.e, 0);
+        ti.m0 = __shfl_sync(0xffffffffu, ti.m0, 0);
+        ti.n0 = __shfl_sync(0xffffffffu, ti.n0, 0);
+        ti.kb = __shfl_sync(0xffffffffu, ti.kb, 0);
+        ti.krow0 = __shfl_sync(0xffffffffu, ti.krow0, 0);
+        ti.ph = __shfl_sync(0xffffffffu, ti.ph, 0);
+        bool got = false;
+        if (lane == 0) got = mbar_wait<PAIR>(&ti_empty[ti_slot], ti_phase ^ 1u, wc);
+        if (!__shfl_sync(0xffffffffu, got, 0)) break;
+        if (lane == 0) {
+          if (ti.prob >= 0) {
+            if (uint64_t* rec = trace_rec(P, lt)) {
+              rec[0] = (static_cast<uint64_t>(sm_id()) << 48) |
+                       (static_cast<uint64_t>(ti.prob) << 40) |
+                       (static_cast<uint64_t>(ti.e & 0xFFFFF) << 20) |
+                       static_cast<uint64_t>(ti.kb & 0xFFFFF);
+              rec[1] = globaltimer_ns();
+            }
+          }
+          s_ti[ti_slot] = ti;
+          if constexpr (PAIR) {
+            const uint32_t dst = mapa_shared(smem_u32(&s_ti[ti_slot]), 1);
+            const int* src = reinterpret_cast<const int*>(&ti);
+#pragma unroll
+            for (int j = 0; j < static_cast<int>(sizeof(TileInfo) / 4); ++j)
+              st_shared_cluster(dst + 4 * j, src[j]);
+            mbar_arrive_cluster(mapa_shared(smem_u32(&ti_full[ti_slot]), 1));
+          }
+          mbar_arrive(&ti_full[ti_slot]);
+        }
+        __syncwarp();
+        ++lt;
+        if (++ti_slot == TI_DEPTH) {
+          ti_slot = 0;
+          ti_phase ^= 1u;
+        }
+        if (ti.prob < 0) break;
       }
-      __syncwarp();
-      ++lt;
-      if (++ti_slot == TI_DEPTH) {
-        ti_slot = 0;
-        ti_phase ^= 1u;
-      }
-      if (ti.prob < 0) break;
     }
   } else if (warp == 0) {
     if (lane == 0) {
@@ -637,12 +731,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       int lt = 0;
       for (;;) {
-        if (!mbar_wait(&ti_full[ti_slot], ti_phase, wc)) {
+        if (!mbar_wait<PAIR>(&ti_full[ti_slot], ti_phase, wc)) {
           ok = false;
           break;
         }
         const TileInfo ti = s_ti[ti_slot];
-        mbar_arrive(&ti_empty[ti_slot]);
+        ti_release(ti_slot);
         if (++ti_slot == TI_DEPTH) {
           ti_slot = 0;
           ti_phase ^= 1u;
@@ -653,20 +747,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // publishing it; order that with the async-proxy loads below
         if (pr.wait_m || pr.wait_e) fence_proxy_async_global();
         const CUtensorMap* mp = maps.m[ti.prob];
-        uint64_t* rec = trace_rec(P, lt++);
+        uint64_t* rec = (!PAIR || leader) ? trace_rec(P, lt) : nullptr;
+        ++lt;
         for (int kb = 0; kb < ti.kb; ++kb) {
           if (!mbar_wait(&empty[stage], sphase ^ 1u, wc)) {
             ok = false;
             break;
           }
           if (rec && kb == 0) rec[2] = globaltimer_ns();
-          uint8_t* sA = stages + stage * STAGE_BYTES;
-          uint8_t* sB = sA + A_BYTES;
-          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-          HMM_BY_PROB(ti.prob, load_stage, pr, ti, kb, &mp[0], &mp[1], &mp[2], sA, sB,
-                      &full[stage]);
+          uint8_t* sA = stages + stage * SBYTES;
+          if constexpr (PAIR) {
+            uint8_t* sB = sA + A_BYTES;
+            if (leader)
+              mbar_arrive_expect_tx(&full[stage], (ti.ph ? 1 : 2) * A_BYTES + 2 * PAIR_B_BYTES);
+            const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
+            HMM_BY_PROB(ti.prob, stage_boxes_pair, pr, ti, kb, &mp[0], &mp[1], sA, sB, bar, rank);
+          } else {
+            uint8_t* sB = sA + A_BYTES;
+            mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+            HMM_BY_PROB(ti.prob, load_stage, pr, ti, kb, &mp[0], &mp[1], &mp[2], sA, sB,
+                        &full[stage]);
+          }
           ++issued;
-          if (++stage == STAGES) {
+          if (++stage == NST) {
             stage = 0;
             sphase ^= 1u;
           }
@@ -676,12 +779,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (!ok) {
         // wait (bounded) for the copies still in flight before leaving
-        for (uint32_t s = 0; s < STAGES; ++s)
-          if (issued > s) drain_wait(&full[s], ((issued - 1 - s) / STAGES) & 1u, P.budget_ns);
+        if (!PAIR || leader) {
+          for (uint32_t s = 0; s < NST; ++s)
+            if (issued > s) drain_wait(&full[s], ((issued - 1 - s) / NST) & 1u, P.budget_ns);
+        } else {
+          pause_ns(200000);  // the even CTA counts our bytes; give the copies time to land
+        }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && (!PAIR || leader)) {
       // ------------------------------------------------------------ MMA issue
       uint32_t stage = 0, sphase = 0;
       int ti_slot = 0;
@@ -699,7 +806,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (ti.prob < 0) break;
         uint64_t* rec = trace_rec(P, lt++);
         if (ti.kb == 0) continue;
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, wc)) break;
+        if (!mbar_wait<PAIR>(&tempty[acc], acc_phase ^ 1u, wc)) break;
         tc_fence_after();
         if (rec) rec[4] = globaltimer_ns();
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -710,23 +817,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(stages + stage * STAGE_BYTES);
+          const uint32_t a_base = smem_u32(stages + stage * SBYTES);
           const uint32_t b_base = a_base + A_BYTES;
-          HMM_BY_PROB(ti.prob, mma_stage, d_tmem, a_base, b_base, kb == 0);
-          umma_commit(&empty[stage]);
-          if (++stage == STAGES) {
+          if constexpr (PAIR) {
+            HMM_BY_PROB(ti.prob, mma_stage_pair, d_tmem, a_base, b_base, kb == 0);
+            umma_commit_pair(&empty[stage], 0x3);
+          } else {
+            HMM_BY_PROB(ti.prob, mma_stage, d_tmem, a_base, b_base, kb == 0);
+            umma_commit(&empty[stage]);
+          }
+          if (++stage == NST) {
             stage = 0;
             sphase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(&tfull[acc]);
+        if constexpr (PAIR)
+          umma_commit_pair(&tfull[acc], 0x3);
+        else
+          umma_commit(&tfull[acc]);
         if (rec) rec[5] = globaltimer_ns();
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
       // every MMA issued by this thread completes before TMEM is released
-      umma_commit(mma_done);
+      if constexpr (PAIR)
+        umma_commit_pair(mma_done, 0x1);
+      else
+        umma_commit(mma_done);
       drain_wait(mma_done, 0, P.budget_ns);
     }
   } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
@@ -734,26 +852,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;
     const int ch = (warp - 2) / 4;  // which warp of the lane quarter
     const int row_in_tile = q * 32 + lane;
+    float* xbuf = xbufs + (warp - 2) * (XBUF_BYTES / 4);
+    const uint32_t tempty_cl[2] = {PAIR ? mapa_shared(smem_u32(&tempty[0]), 0) : 0u,
+                                   PAIR ? mapa_shared(smem_u32(&tempty[1]), 0) : 0u};
     int ti_slot = 0;
     uint32_t ti_phase = 0;
     uint32_t acc = 0, acc_phase = 0;
     int lt = 0;
     for (;;) {
       bool got = false;
-      if (lane == 0) got = mbar_wait(&ti_full[ti_slot], ti_phase, wc);
+      if (lane == 0) got = mbar_wait<PAIR>(&ti_full[ti_slot], ti_phase, wc);
       __syncwarp();
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) break;
-      const TileInfo ti = s_ti[ti_slot];
+      TileInfo ti = s_ti[ti_slot];
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ti_empty[ti_slot]);
+      if (lane == 0) ti_release(ti_slot);
       if (++ti_slot == TI_DEPTH) {
         ti_slot = 0;
         ti_phase ^= 1u;
       }
       if (ti.prob < 0) break;
       const Prob& pr = P.p[ti.prob];
-      uint64_t* rec = (warp == 2 && lane == 0) ? trace_rec(P, lt) : nullptr;  // one warp reports
+      // one warp of the (even) CTA reports
+      uint64_t* rec = (warp == 2 && lane == 0 && leader) ? trace_rec(P, lt) : nullptr;
       ++lt;
       if (ti.kb == 0) {
         HMM_BY_PROB(ti.prob, epilogue_zero, pr, ti, row_in_tile, ch);
@@ -765,13 +887,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!got) break;
       tc_fence_after();
       if (rec) rec[6] = globaltimer_ns();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      HMM_BY_PROB(ti.prob, epilogue_tile, pr, ti, taddr, row_in_tile, ch);
+      // this CTA's 128 rows of a pair tile; the odd CTA's half of the last
+      // pair of an expert with an odd number of M tiles holds no rows
+      const bool real = !PAIR || leader || !ti.ph;
+      ti.m0 += PAIR ? BM * static_cast<int>(rank) : 0;
+      if (real) {
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+        HMM_BY_PROB(ti.prob, epilogue_tile, pr, ti, taddr, ti.m0 + q * 32, lane, ch, xbuf);
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) {
+        if (!PAIR || leader)
+          mbar_arrive(&tempty[acc]);
+        else
+          mbar_arrive_cluster(tempty_cl[acc]);
+      }
       if (rec) rec[7] = globaltimer_ns();
-      if (pr.signal_m || pr.signal_e) {
+      if (real && (pr.signal_m || pr.signal_e)) {
         fence_proxy_async_global();
         __syncwarp();
         if (lane == 0) {
@@ -786,9 +919,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // no peer access to our smem or TMEM after this
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -829,14 +966,14 @@ int map_w(const GemmEnv& env, CUtensorMap* m, const void* base, int64_t E, int64
   return encode(env, m, base, 3, dims, str, box);
 }
 
-template <class C0, class C1, class C2, class C3>
+template <bool PAIR, class C0, class C1, class C2, class C3>
 int launch(const GemmEnv& env, Params& P, const Maps& maps, int64_t max_tiles, int kind) {
   if (max_tiles <= 0 || P.nprob == 0) return HMM_OK;
   if (env.trace && env.trace_which == kind) {
     P.trace = env.trace;
     P.trace_cap = env.trace_cap;
   }
-  auto kern = gmm_kernel<C0, C1, C2, C3>;
+  auto kern = gmm_kernel<PAIR, C0, C1, C2, C3>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
       cudaSuccess)
     return HMM_ERR_CUDA;
@@ -856,8 +993,34 @@ int launch(const GemmEnv& env, Params& P, const Maps& maps, int64_t max_tiles, i
   }
   P.status = env.status;
   P.budget_ns = env.budget_ns;
-  kern<<<grid, NUM_THREADS, SMEM_BYTES, env.stream>>>(P, maps);
-  return cudaGetLastError() == cudaSuccess ? HMM_OK : HMM_ERR_CUDA;
+  P.pair = PAIR ? 1 : 0;
+  if constexpr (PAIR) {
+    // clusters of two CTAs, as many as can be resident at once (the tile
+    // dependencies inside the launch need every CTA running)
+    if (P.group_split > 0) return HMM_ERR_ARG;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = env.stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int clusters = env.num_sms / 2;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active <= 0)
+      return HMM_ERR_CUDA;
+    clusters = static_cast<int>(std::min<int64_t>(std::min(clusters, active), max_tiles));
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+    return cudaLaunchKernelEx(&cfg, kern, P, maps) == cudaSuccess ? HMM_OK : HMM_ERR_CUDA;
+  } else {
+    kern<<<grid, NUM_THREADS, SMEM_BYTES, env.stream>>>(P, maps);
+    return cudaGetLastError() == cudaSuccess ? HMM_OK : HMM_ERR_CUDA;
+  }
 }
 
 }  // namespace
@@ -910,7 +1073,9 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
   g2.wait_m = c.ready;
   g2.wait_unit = EPI_WARPS * g1.n_tiles;  // every epilogue warp of every GMM1 tile of the M tile
   const int64_t max_tiles = p.max_mtiles * (g1.n_tiles + g2.n_tiles);
-  return launch<CfgGmm1, CfgGmm2, CfgGmm2, CfgGmm2>(env, P, maps, max_tiles, 0);
+  if (env.pair_rows)
+    return launch<true, CfgGmm1, CfgGmm2, CfgGmm2, CfgGmm2>(env, P, maps, max_tiles, 0);
+  return launch<false, CfgGmm1, CfgGmm2, CfgGmm2, CfgGmm2>(env, P, maps, max_tiles, 0);
 }
 
 int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
@@ -921,12 +1086,15 @@ int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtr
   const int64_t H = p.H, I = p.I, E = p.E, R = p.R;
   Maps maps;
   int rc = HMM_OK;
+  // data gradients on CTA pairs: each CTA loads 128 of the 256 B rows
+  const bool pair = env.pair_rows && env.bwd_data_sms <= 0;
+  const uint32_t b_rows = pair ? BN / 2 : BN;
   // act_grad: G = dy_perm . W2^T   (B = W2 [E, I, H] read K-major, N = I)
   rc |= map_act(env, &maps.m[0][0], dy_perm, R, H, BM);
-  rc |= map_w(env, &maps.m[0][1], W2, E, I, H, BN);
+  rc |= map_w(env, &maps.m[0][1], W2, E, I, H, b_rows);
   // input-grad: dX_perm = dH . W1^T (B = W1 [E, H, 2I] read K-major, N = H)
   rc |= map_act(env, &maps.m[1][0], dH, R, 2 * I, BM);
-  rc |= map_w(env, &maps.m[1][1], W1, E, H, 2 * I, BN);
+  rc |= map_w(env, &maps.m[1][1], W1, E, H, 2 * I, b_rows);
   // W2Grad: dW2[e] = (wa_hi + wa_lo)^T . dy_perm    [I, rows] x [rows, H]
   rc |= map_act(env, &maps.m[2][0], wa, R, I, 64);
   rc |= map_act(env, &maps.m[2][1], dy_perm, R, H, 64);
@@ -1018,14 +1186,16 @@ int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtr
     // expert.
     add_wgrad(P, 2, 1);
     P.group_split = env.bwd_data_sms;
-    return launch<CfgActGrad, CfgInGrad, CfgW2Grad, CfgW1Grad>(env, P, maps,
-                                                              data_tiles + w_tiles, 1);
+    return launch<false, CfgActGrad, CfgInGrad, CfgW2Grad, CfgW1Grad>(env, P, maps,
+                                                                     data_tiles + w_tiles, 1);
   }
   // Default: two launches.  The data gradients first; then the weight
   // gradients, whose per-expert waits are already satisfied: on CTA pairs
   // (2-SM MMAs) unless disabled, else on single CTAs.
   P.nprob = 2;
-  rc = launch<CfgActGrad, CfgInGrad, CfgInGrad, CfgInGrad>(env, P, maps, data_tiles, 1);
+  rc = pair ? launch<true, CfgActGrad, CfgInGrad, CfgInGrad, CfgInGrad>(env, P, maps, data_tiles, 1)
+            : launch<false, CfgActGrad, CfgInGrad, CfgInGrad, CfgInGrad>(env, P, maps, data_tiles,
+                                                                        1);
   if (rc != HMM_OK || nw == 0) return rc;
   if (env.pair_wgrad)
     return launch_wgrad_pair(env, p, m, x_perm, dy_perm, dH, dH_lo, wa, wa_lo, dW1, dW2);
@@ -1036,7 +1206,7 @@ int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtr
   W.ticket = c.tickets + 3;
   add_wgrad(W, 0, 0);
   for (int q = 0; q < W.nprob; ++q) W.p[q].wait_e = nullptr;  // act_grad has completed
-  return launch<CfgW2Grad, CfgW1Grad, CfgW1Grad, CfgW1Grad>(env, W, maps, w_tiles, 2);
+  return launch<false, CfgW2Grad, CfgW1Grad, CfgW1Grad, CfgW1Grad>(env, W, maps, w_tiles, 2);
 }
 
 }  // namespace hmm

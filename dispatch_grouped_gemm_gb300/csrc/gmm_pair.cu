@@ -3,14 +3,15 @@
 // [HyperMegaMoE §2.2 W2Grad, W1Grad]
 //   dW2[e] = (wa_hi + wa_lo)^T . dy_perm      [I, rows of e] x [rows of e, H]
 //   dW1[e] = x_perm^T . (dH_hi + dH_lo)       [H, rows of e] x [rows of e, 2I]
-// (the rounded operand is read as a bf16 hi + lo pair, so the K loop runs over
-// the expert's rows twice).
+// (the rounded operand is read as a bf16 hi + lo pair: every 64-row K step
+// stages A, B and the low half of the split operand together and issues two
+// MMAs on them, so the unsplit operand is loaded once).
 //
 // Two CTAs of a cluster compute one 256 x 256 output tile with 2-SM MMAs:
 // each CTA loads its 128 rows of A and its 128 of the 256 columns of B, and
 // each accumulates its 128 rows x 256 columns in its own TMEM.  Per SM that is
-// 32 KB of operands per 64-deep K step instead of 48 KB for a 1-SM 128 x 256
-// tile, a third less smem and L2 traffic for the same MMA work.
+// 48 KB of operands per 64-deep K step (two MMAs) instead of 96 KB for 1-SM
+// 128 x 256 tiles that reload the unsplit operand for the low half.
 //
 // Roles per CTA: warp 0 issues TMA (both CTAs, one thread), warp 1 issues the
 // MMAs (even CTA only), warps 2..5 drain TMEM (both CTAs).  The even CTA's
@@ -23,18 +24,22 @@
 
 #include <algorithm>
 
+#include "epilogue.cuh"
 #include "ptx.cuh"
 
 namespace hmm {
 
 namespace {
 
-constexpr int PSTAGES = 6;
+constexpr int PSTAGES = 4;
 constexpr int PA_BYTES = 128 * 64 * 2;  // this CTA's 128 rows of A, 64 deep
 constexpr int PB_BYTES = 128 * 64 * 2;  // this CTA's 128 columns of B, 64 deep
-constexpr int PSTAGE = PA_BYTES + PB_BYTES;
+constexpr int PX_BYTES = 128 * 64 * 2;  // the low half of the split one of them
+constexpr int PSTAGE = PA_BYTES + PB_BYTES + PX_BYTES;
 constexpr int P_THREADS = 192;
-constexpr int P_SMEM = 1024 + PSTAGES * PSTAGE + 512;
+constexpr int P_EPI_WARPS = 4;
+constexpr int P_SMEM = 1024 + PSTAGES * PSTAGE + P_EPI_WARPS * XBUF_BYTES + 512;
+static_assert(P_SMEM <= 232448, "shared memory per CTA");
 constexpr uint32_t P_TMEM_COLS = 512;
 constexpr uint32_t IDESC_PAIR = idesc_bf16_f32(256, 256, 1, 1);  // both MN-major
 
@@ -87,7 +92,7 @@ __device__ __forceinline__ void pair_decode(const PairParams& P, int u, PairTile
   t.n0 = (r % pr.n_tiles) * 256;
   t.krow0 = P.poff[t.e];
   // rows past counts[e] are zero padding: skip whole zero K blocks
-  t.kb = (P.counts[t.e] + 63) / 64 * (pr.split ? 2 : 1);
+  t.kb = (P.counts[t.e] + 63) / 64;
 }
 
 // Timeline record of this CTA's lt-th tile (even CTA of the pair only).
@@ -115,7 +120,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PSTAGES * PSTAGE);
+  float* xbufs = reinterpret_cast<float*>(smem + PSTAGES * PSTAGE);
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(smem + PSTAGES * PSTAGE + P_EPI_WARPS * XBUF_BYTES);
   uint64_t* full = bars;               // used in the even CTA
   uint64_t* empty = bars + PSTAGES;    // both CTAs
   uint64_t* tfull = empty + PSTAGES;   // both CTAs
@@ -181,7 +188,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                    static_cast<uint64_t>(t.kb & 0xFFFFF);
           rec[1] = globaltimer_ns();
         }
-        const int nk = pr.split ? t.kb / 2 : t.kb;
         const int ma = t.m0 + 128 * static_cast<int>(rank);  // this CTA's rows of the output
         const int nbc = t.n0 + 128 * static_cast<int>(rank);  // this CTA's half of B's columns
         for (int kb = 0; kb < t.kb; ++kb) {
@@ -190,18 +196,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             break;
           }
           if (rec && kb == 0) rec[2] = globaltimer_ns();
-          const bool lo = kb >= nk;
-          const int k = t.krow0 + (lo ? kb - nk : kb) * 64;
-          const CUtensorMap* a = (pr.split == 1 && lo) ? &mp[2] : &mp[0];
-          const CUtensorMap* b = (pr.split == 2 && lo) ? &mp[2] : &mp[1];
+          const int k = t.krow0 + kb * 64;
           uint8_t* sA = stages + stage * PSTAGE;
           uint8_t* sB = sA + PA_BYTES;
+          uint8_t* sX = sB + PB_BYTES;
+          const int xc = pr.split == 1 ? ma : nbc;  // the low half's columns
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * PSTAGE);
           const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
-          tma_load_2d_pair(sA, a, bar, ma, k);
-          tma_load_2d_pair(sA + 8192, a, bar, ma + 64, k);
-          tma_load_2d_pair(sB, b, bar, nbc, k);
-          tma_load_2d_pair(sB + 8192, b, bar, nbc + 64, k);
+          tma_load_2d_pair(sA, &mp[0], bar, ma, k);
+          tma_load_2d_pair(sA + 8192, &mp[0], bar, ma + 64, k);
+          tma_load_2d_pair(sB, &mp[1], bar, nbc, k);
+          tma_load_2d_pair(sB + 8192, &mp[1], bar, nbc + 64, k);
+          tma_load_2d_pair(sX, &mp[2], bar, xc, k);
+          tma_load_2d_pair(sX + 8192, &mp[2], bar, xc + 64, k);
           ++issued;
           if (++stage == PSTAGES) {
             stage = 0;
@@ -230,6 +237,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       for (int u = first; u < total && ok; u += stride) {
         PairTile t;
         pair_decode(P, u, t);
+        const int split = P.p[t.prob].split;
         uint64_t* rec = pair_rec(P, leader, lt++);
         if (t.kb == 0) continue;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, wc)) break;
@@ -244,12 +252,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
           tc_fence_after();
           const uint32_t a_base = smem_u32(stages + stage * PSTAGE);
           const uint32_t b_base = a_base + PA_BYTES;
+          const uint32_t x_base = b_base + PB_BYTES;
+          // second MMA of each K=16 step: the low half against the other operand
+          const uint32_t a2_base = split == 1 ? x_base : a_base;
+          const uint32_t b2_base = split == 1 ? b_base : x_base;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             // MN-major halves: two 64-wide chunks 8 KB apart, 8-row groups 1 KB
             const uint64_t ad = smem_desc(a_base + kk * 2048, 8192, 1024, LAYOUT_SW128);
             const uint64_t bd = smem_desc(b_base + kk * 2048, 8192, 1024, LAYOUT_SW128);
             umma_bf16_pair(d_tmem, ad, bd, IDESC_PAIR, (kb == 0 && kk == 0) ? 0u : 1u);
+            const uint64_t ad2 = smem_desc(a2_base + kk * 2048, 8192, 1024, LAYOUT_SW128);
+            const uint64_t bd2 = smem_desc(b2_base + kk * 2048, 8192, 1024, LAYOUT_SW128);
+            umma_bf16_pair(d_tmem, ad2, bd2, IDESC_PAIR, 1u);
           }
           umma_commit_pair(&empty[stage], 0x3);
           if (++stage == PSTAGES) {
@@ -270,6 +285,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     // ------------------------------------------------------------- epilogue
     const int q4 = warp & 3;
     const int row_in_half = q4 * 32 + lane;
+    float* xbuf = xbufs + (warp - 2) * (XBUF_BYTES / 4);
+    const int cg = (lane & 3) * 8;  // this lane's columns within a 32-column chunk
     uint32_t acc = 0, acc_phase = 0;
     const uint32_t tempty_cl[2] = {mapa_shared(smem_u32(&tempty[0]), 0),
                                    mapa_shared(smem_u32(&tempty[1]), 0)};
@@ -296,6 +313,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       tc_fence_after();
       if (rec) rec[6] = globaltimer_ns();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + acc * 256;
+      // this lane's rows after the transposition: rl + 8k
+      const int64_t rl = t.m0 + 128 * static_cast<int>(rank) + q4 * 32 + (lane >> 2);
+      __nv_bfloat16* obase = pr.out + static_cast<int64_t>(t.e) * pr.out_estride;
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         const int col = t.n0 + c * 32;
@@ -303,17 +323,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         uint32_t r[32];
         tmem_ld32(taddr + c * 32, r);
         tmem_ld_wait();
-        if (row < pr.M) {
-          const int valid = min(32, pr.N - col);
-          uint4* d = reinterpret_cast<uint4*>(orow + col);
+        float v[4][8];
+        xpose(xbuf, lane, r, v);
+        if (col + cg < pr.N) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            if (g * 8 < valid) {
-              const float* v = reinterpret_cast<const float*>(r) + g * 8;
-              d[g] = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]),
-                                pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
-            }
-          }
+          for (int k = 0; k < 4; ++k)
+            if (rl + 8 * k < pr.M)
+              *reinterpret_cast<uint4*>(obase + (rl + 8 * k) * pr.ld_out + col + cg) =
+                  pack_bf16x8(v[k]);
         }
       }
       tc_fence_before();

@@ -49,6 +49,7 @@ struct hmm_ctx {
   int profile = 0;
   int bwd_data_sms = 0;
   int pair_wgrad = 1;
+  int pair_rows = 2;  // 0 off, 1 on, 2 automatic
   uint64_t* trace = nullptr;
   size_t trace_bytes = 0;
   int trace_which = 0;
@@ -223,12 +224,14 @@ struct DeviceGuard {
   }
 };
 
-GemmEnv env_of(hmm_ctx* ctx, cudaStream_t st) {
+GemmEnv env_of(hmm_ctx* ctx, const Plan& p, cudaStream_t st) {
   GemmEnv e;
   e.encode = ctx->encode;
   e.num_sms = ctx->num_sms;
   e.bwd_data_sms = ctx->bwd_data_sms;
   e.pair_wgrad = ctx->pair_wgrad;
+  // pairs pay off when most experts have two or more 128-row tiles
+  e.pair_rows = ctx->pair_rows == 2 ? (p.TK >= 2 * BM * p.E ? 1 : 0) : ctx->pair_rows;
   e.trace = ctx->trace;
   e.trace_cap = ctx->trace ? static_cast<int>(ctx->trace_bytes / (64 * ctx->num_sms)) : 0;
   e.trace_which = ctx->trace_which;
@@ -327,6 +330,10 @@ int hmm_set_option(hmm_ctx* ctx, int option, int64_t value) {
       return HMM_OK;
     case HMM_OPT_PAIR_WGRAD:
       ctx->pair_wgrad = value != 0;
+      return HMM_OK;
+    case HMM_OPT_PAIR_ROWS:
+      if (value < 0 || value > 2) return HMM_ERR_ARG;
+      ctx->pair_rows = static_cast<int>(value);
       return HMM_OK;
     case HMM_OPT_BWD_DATA_SMS:
       if (value < 0 || value >= ctx->num_sms) return HMM_ERR_ARG;
@@ -427,7 +434,7 @@ int hmm_forward(hmm_ctx* ctx, const hmm_shape* shape, const void* x, const int32
   ctx->inject_skip_ready = 0;
   {
     PhaseScope ps(ctx, PH_GEMM_FWD, st);
-    rc = launch_forward_gemms(env_of(ctx, st), p, m, c, x_perm, up_proj_weight, down_proj_weight,
+    rc = launch_forward_gemms(env_of(ctx, p, st), p, m, c, x_perm, up_proj_weight, down_proj_weight,
                               a, h32, o, inject);
   }
   if (rc != HMM_OK) return rc;
@@ -485,7 +492,7 @@ int hmm_backward(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const voi
   void* wa_lo = ws + p.bw_walo;
   void* dx_perm = ws + p.bw_dxperm;
   float* dwp = reinterpret_cast<float*>(ws + p.bw_dwp);
-  const GemmEnv env = env_of(ctx, st);
+  const GemmEnv env = env_of(ctx, p, st);
 
   {
     PhaseScope ps(ctx, PH_DISPATCH_DY, st);

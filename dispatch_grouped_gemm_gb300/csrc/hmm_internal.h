@@ -98,6 +98,7 @@ struct GemmEnv {
   int trace_which;   // which GEMM launch kind is traced
   int bwd_data_sms;  // SMs for the data-gradient group of the backward (0: automatic)
   int pair_wgrad;    // weight gradients on CTA pairs (2-SM MMA)
+  int pair_rows;     // forward and data-gradient GEMMs on CTA pairs (2-SM MMA)
   unsigned* status;
   uint64_t budget_ns;
   cudaStream_t stream;

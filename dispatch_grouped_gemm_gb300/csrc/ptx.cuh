@@ -55,6 +55,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The same with cluster-scope acquire: for phases completed by arrivals with
+// release.cluster from the other CTA of a pair, whose shared-memory writes
+// must be visible after the wait.
+__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], "
+      "%2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+template <bool CL>
+__device__ __forceinline__ bool mbar_try_wait_s(uint64_t* bar, uint32_t parity) {
+  if constexpr (CL)
+    return mbar_try_wait_cl(bar, parity);
+  else
+    return mbar_try_wait(bar, parity);
+}
 
 // Abort state shared by the roles of one CTA.
 struct WaitCtl {
@@ -70,10 +90,12 @@ __device__ __forceinline__ void raise_timeout(const WaitCtl& w) {
 
 // Slow path of a bounded wait: true when the barrier phase completed, false
 // after the budget ran out, the CTA aborted, or another CTA reported a timeout.
+// CL: cluster-scope acquire (see mbar_try_wait_cl).
+template <bool CL = false>
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1; it < (1u << 30); ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_s<CL>(bar, parity)) return true;
     if ((it & 31u) == 0) {
       if (*w.abort) return false;
       if (*reinterpret_cast<volatile unsigned*>(w.status) & HMM_STATUS_TIMEOUT) {
@@ -90,9 +112,10 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
   return false;
 }
 
+template <bool CL = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, w);
+  if (mbar_try_wait_s<CL>(bar, parity)) return true;
+  return mbar_wait_slow<CL>(bar, parity, w);
 }
 
 // Acquire-poll a global counter until it reaches `target` (bounded).
@@ -247,6 +270,18 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar_cl)
       : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m, uint32_t bar_cl,
+                                                 int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cl)
+      : "memory");
+}
+// Store to a shared variable given by its shared::cluster address.
+__device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, int v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(

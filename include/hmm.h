@@ -127,6 +127,13 @@ int hmm_destroy(hmm_ctx* ctx);
  *                         pairs with 2-SM MMAs (256 x 256 tiles); 0: on single
  *                         CTAs (128 x 256 tiles). */
 #define HMM_OPT_PAIR_WGRAD 6
+/*   HMM_OPT_PAIR_ROWS     2 (default): automatic; the forward GEMMs and the
+ *                         data-gradient GEMMs run on CTA pairs with 2-SM MMAs
+ *                         (two 128-row tiles of one expert per 256 x 256 tile)
+ *                         when the routed rows average at least two 128-row
+ *                         tiles per expert (T * K >= 256 * E), else on single
+ *                         CTAs.  1: always on CTA pairs; 0: never. */
+#define HMM_OPT_PAIR_ROWS 7
 int hmm_set_option(hmm_ctx* ctx, int option, int64_t value);
 
 /* Launch phases timed under HMM_OPT_PROFILE (index = phase id):

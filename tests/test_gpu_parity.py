@@ -96,14 +96,28 @@ def _scenarios():
     yield "one_token", gu.problem(1, 128, 64, 4, 2, seed=12)
     yield "ragged_small", gu.problem(37, 136, 72, 6, 4, seed=13, ids=r.integers(0, 6, size=(37, 4)))
     yield "tiny_config", gu.problem(64, 128, 64, 8, 2, seed=1000)
+    # skewed top-4 of 6 experts (Gumbel top-k): 6, 5, 5, 4, 3 and 2 tiles of 128
+    # rows, so CTA pairs with and without an empty second half; K (H = 264)
+    # and N (I = 200) ragged
+    g = np.log([5, 3, 2, 1, 1, 0.5]) + np.random.default_rng(15).gumbel(size=(700, 6))
+    yield "multi_tile", gu.problem(700, 264, 200, 6, 4, seed=14,
+                                   ids=np.argsort(-g, axis=1)[:, :4].astype(np.int32))
 
 
 SCEN = list(_scenarios())
 
 
+@pytest.fixture(params=[0, 1], ids=["cta", "pair"])
+def rows_mode(run, request):
+    """Rows-mode GEMMs on single CTAs or on CTA pairs (2-SM MMAs)."""
+    hmm.hmm_set_option(run.ctx.handle, hmm.HMM_OPT_PAIR_ROWS, request.param)
+    yield request.param
+    hmm.hmm_set_option(run.ctx.handle, hmm.HMM_OPT_PAIR_ROWS, 2)
+
+
 @pytest.mark.parametrize("training", [True, False])
 @pytest.mark.parametrize("case", SCEN, ids=lambda c: c[0])
-def test_forward_matches_oracle(run, case, training):
+def test_forward_matches_oracle(run, case, training, rows_mode):
     _, p = case
     d = gu.upload(p)
     y, _ = run.forward(d, training=training)
@@ -114,7 +128,7 @@ def test_forward_matches_oracle(run, case, training):
 
 
 @pytest.mark.parametrize("case", SCEN, ids=lambda c: c[0])
-def test_backward_matches_oracle(run, case):
+def test_backward_matches_oracle(run, case, rows_mode):
     _, p = case
     d = gu.upload(p)
     y, saved = run.forward(d)
@@ -144,8 +158,8 @@ def test_fp32_routing_weights(run):
     gu.check("dw", gu.f64(dw), rdw)
 
 
-def test_repeated_calls_bit_identical(run):
-    p = gu.problem(300, 264, 200, 10, 3, seed=11)
+def test_repeated_calls_bit_identical(run, rows_mode):
+    p = dict(SCEN)["multi_tile"]
     d = gu.upload(p)
     outs = []
     for _ in range(3):
