@@ -14,10 +14,24 @@
 //
 // Three launches: per-warp-chunk histograms -> one-block scan -> per-chunk
 // stable ranks (warp match_any groups equal ids inside each 32-slot step, so
-// the order inside a chunk follows s).
+// the order inside a chunk follows s).  Each warp loads its whole chunk of
+// ids into registers before the first step, so the steps do not wait on
+// global loads one after another.
 #include "hmm_internal.h"
 
 namespace hmm {
+
+constexpr int RSTEPS = RCHUNK / 32;  // 32-slot steps per chunk
+
+// ids of slots s0 + 32 j + lane, j < RSTEPS (-2 past s1: "no slot")
+__device__ __forceinline__ void load_chunk_ids(const int32_t* __restrict__ ids, int64_t s0,
+                                               int64_t s1, int lane, int (&v)[RSTEPS]) {
+#pragma unroll
+  for (int j = 0; j < RSTEPS; ++j) {
+    const int64_t s = s0 + 32 * j + lane;
+    v[j] = s < s1 ? __ldg(ids + s) : -2;
+  }
+}
 
 __global__ void __launch_bounds__(RWARPS * 32) route_count_kernel(const int32_t* __restrict__ ids,
                                                                   int64_t TK, int E,
@@ -33,12 +47,15 @@ __global__ void __launch_bounds__(RWARPS * 32) route_count_kernel(const int32_t*
   __syncwarp();
   const int64_t s0 = chunk * RCHUNK;
   const int64_t s1 = (s0 + RCHUNK < TK ? s0 + RCHUNK : TK);
+  int v[RSTEPS];
+  load_chunk_ids(ids, s0, s1, lane, v);
   bool bad = false;
-  for (int64_t s = s0 + lane; s < s1; s += 32) {
-    const int e = ids[s];
+#pragma unroll
+  for (int j = 0; j < RSTEPS; ++j) {
+    const int e = v[j];
     if (static_cast<unsigned>(e) < static_cast<unsigned>(E))
       atomicAdd(&cnt[e], 1);
-    else
+    else if (e != -2)
       bad = true;
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(status, HMM_STATUS_EXPERT_ID);
@@ -77,12 +94,17 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int64_t nchunks
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t tot_cnt, tot_pad;
   const int e = threadIdx.x;
+  // counts of expert e over the chunks, loaded eight chunks at a time
+  constexpr int CB = 8;
   int32_t cnt = 0;
   if (e < E) {
-    for (int64_t ch = 0; ch < nchunks; ++ch) {
-      const int32_t v = c.chunk_base[ch * E + e];
-      c.chunk_base[ch * E + e] = cnt;
-      cnt += v;
+    for (int64_t ch0 = 0; ch0 < nchunks; ch0 += CB) {
+      int32_t v[CB];
+#pragma unroll
+      for (int j = 0; j < CB; ++j)
+        v[j] = ch0 + j < nchunks ? c.chunk_base[(ch0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < CB; ++j) cnt += v[j];
     }
   }
   const int32_t padded = (cnt + BM - 1) / BM * BM;
@@ -92,7 +114,19 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int64_t nchunks
     m.counts[e] = cnt;
     m.offsets[e] = off;
     m.poff[e] = poff;
-    for (int64_t ch = 0; ch < nchunks; ++ch) c.chunk_base[ch * E + e] += off;
+    // chunk counts -> first row of each chunk's slots of e
+    int32_t run = off;
+    for (int64_t ch0 = 0; ch0 < nchunks; ch0 += CB) {
+      int32_t v[CB];
+#pragma unroll
+      for (int j = 0; j < CB; ++j)
+        v[j] = ch0 + j < nchunks ? c.chunk_base[(ch0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < CB; ++j) {
+        if (ch0 + j < nchunks) c.chunk_base[(ch0 + j) * E + e] = run;
+        run += v[j];
+      }
+    }
     for (int32_t r = poff + cnt; r < poff + padded; ++r) m.prow2slot[r] = -1;
   }
   if (e == 0) {
@@ -111,33 +145,40 @@ __global__ void __launch_bounds__(RWARPS * 32) route_rank_kernel(
   int32_t* cnt = sh + warp * E;
   const int64_t chunk = static_cast<int64_t>(blockIdx.x) * RWARPS + warp;
   if (chunk >= nchunks) return;
-  for (int e = lane; e < E; e += 32) cnt[e] = chunk_base[chunk * E + e];
+  // cursor of each expert: the padded row of its next slot in this chunk
+  for (int e = lane; e < E; e += 32)
+    cnt[e] = chunk_base[chunk * E + e] + (m.poff[e] - m.offsets[e]);
   __syncwarp();
   const int64_t s0 = chunk * RCHUNK;
   const int64_t s1 = (s0 + RCHUNK < TK ? s0 + RCHUNK : TK);
-  for (int64_t base = s0; base < s1; base += 32) {
-    const int64_t s = base + lane;
-    const bool in = s < s1;
-    const int e = in ? ids[s] : -1;
-    const bool ok = in && static_cast<unsigned>(e) < static_cast<unsigned>(E);
-    const int key = ok ? e : -1 - lane;  // invalid lanes never group
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    int32_t row = 0;
-    if (ok) row = cnt[e] + __popc(peers & ((1u << lane) - 1u));
-    __syncwarp();
-    if (ok && lane == 31 - __clz(peers)) cnt[e] += __popc(peers);
-    __syncwarp();
-    if (ok) {
-      const int32_t prow = m.poff[e] + (row - m.offsets[e]);
-      m.slot2prow[s] = prow;
-      m.prow2slot[prow] = static_cast<int32_t>(s);
-      if (slot2row) {
-        slot2row[s] = row;
-        row2slot[row] = static_cast<int32_t>(s);
+  int v[RSTEPS];
+  load_chunk_ids(ids, s0, s1, lane, v);
+#pragma unroll
+  for (int j = 0; j < RSTEPS; ++j) {
+    if (s0 + 32 * j < s1) {  // warp-uniform
+      const int64_t s = s0 + 32 * j + lane;
+      const bool in = s < s1;
+      const int e = v[j];
+      const bool ok = in && static_cast<unsigned>(e) < static_cast<unsigned>(E);
+      const int key = ok ? e : -1 - lane;  // invalid lanes never group
+      const unsigned peers = __match_any_sync(0xffffffffu, key);
+      int32_t prow = 0;
+      if (ok) prow = cnt[e] + __popc(peers & ((1u << lane) - 1u));
+      __syncwarp();
+      if (ok && lane == 31 - __clz(peers)) cnt[e] += __popc(peers);
+      __syncwarp();
+      if (ok) {
+        m.slot2prow[s] = prow;
+        m.prow2slot[prow] = static_cast<int32_t>(s);
+        if (slot2row) {
+          const int32_t row = prow - (m.poff[e] - m.offsets[e]);
+          slot2row[s] = row;
+          row2slot[row] = static_cast<int32_t>(s);
+        }
+      } else if (in) {
+        m.slot2prow[s] = -1;
+        if (slot2row) slot2row[s] = -1;
       }
-    } else if (in) {
-      m.slot2prow[s] = -1;
-      if (slot2row) slot2row[s] = -1;
     }
   }
 }
