@@ -1082,7 +1082,7 @@ int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtr
                           const void* x_perm, const void* dy_perm, const float* wperm,
                           const float* h32, const void* W1, const void* W2, void* dH,
                           void* dH_lo, void* wa, void* wa_lo, float* dwp, void* dx_perm,
-                          void* dW1, void* dW2) {
+                          void* dW1, void* dW2, int part) {
   const int64_t H = p.H, I = p.I, E = p.E, R = p.R;
   Maps maps;
   int rc = HMM_OK;
@@ -1183,7 +1183,8 @@ int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtr
   if (env.bwd_data_sms > 0 && nw > 0) {
     // Two CTA groups in one launch: env.bwd_data_sms SMs run act_grad and
     // input-grad, the others the weight gradients, trailing act_grad expert by
-    // expert.
+    // expert.  (All of it is part 1.)
+    if (part != 1) return HMM_OK;
     add_wgrad(P, 2, 1);
     P.group_split = env.bwd_data_sms;
     return launch<false, CfgActGrad, CfgInGrad, CfgW2Grad, CfgW1Grad>(env, P, maps,
@@ -1193,10 +1194,12 @@ int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtr
   // gradients, whose per-expert waits are already satisfied: on CTA pairs
   // (2-SM MMAs) unless disabled, else on single CTAs.
   P.nprob = 2;
-  rc = pair ? launch<true, CfgActGrad, CfgInGrad, CfgInGrad, CfgInGrad>(env, P, maps, data_tiles, 1)
-            : launch<false, CfgActGrad, CfgInGrad, CfgInGrad, CfgInGrad>(env, P, maps, data_tiles,
-                                                                        1);
-  if (rc != HMM_OK || nw == 0) return rc;
+  if (part == 1)
+    return pair ? launch<true, CfgActGrad, CfgInGrad, CfgInGrad, CfgInGrad>(env, P, maps,
+                                                                            data_tiles, 1)
+                : launch<false, CfgActGrad, CfgInGrad, CfgInGrad, CfgInGrad>(env, P, maps,
+                                                                             data_tiles, 1);
+  if (nw == 0) return HMM_OK;
   if (env.pair_wgrad)
     return launch_wgrad_pair(env, p, m, x_perm, dy_perm, dH, dH_lo, wa, wa_lo, dW1, dW2);
   Params W{};

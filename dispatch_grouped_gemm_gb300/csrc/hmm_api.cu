@@ -25,11 +25,11 @@ struct PhaseInfo {
   int kernels;
 };
 constexpr PhaseInfo kPhases[HMM_NUM_PHASES] = {
-    {"route", 3},     {"dispatch_x", 1},  {"gemm_fwd", 1}, {"combine_y", 1},
-    {"dispatch_dy", 1}, {"gemm_bwd", 1},  {"combine_dx", 1}};
+    {"route", 3},       {"dispatch_x", 1},    {"gemm_fwd", 1},        {"combine_y", 1},
+    {"dispatch_dy", 1}, {"gemm_bwd_data", 1}, {"gemm_bwd_weight", 1}, {"combine_dx", 1}};
 enum Phase {
-  PH_ROUTE = 0, PH_DISPATCH_X, PH_GEMM_FWD, PH_COMBINE_Y, PH_DISPATCH_DY, PH_GEMM_BWD,
-  PH_COMBINE_DX
+  PH_ROUTE = 0, PH_DISPATCH_X, PH_GEMM_FWD, PH_COMBINE_Y, PH_DISPATCH_DY, PH_GEMM_BWD_DATA,
+  PH_GEMM_BWD_WEIGHT, PH_COMBINE_DX
 };
 
 struct ProfRec {
@@ -56,6 +56,11 @@ struct hmm_ctx {
   std::vector<ProfRec> recs;
   std::vector<cudaEvent_t> pool;
   hmm::EncodeTiledFn encode = nullptr;
+  // second stream of the backward: the dx / d_topk_weights combine runs there
+  // beside the weight-gradient GEMMs (fork and join events on the caller's
+  // stream)
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
 };
 
 namespace {
@@ -287,7 +292,12 @@ int hmm_create(hmm_ctx** out, int device) {
     delete c;
     return HMM_ERR_CUDA;
   }
-  if (cudaMemset(c->status, 0, sizeof(unsigned)) != cudaSuccess) {
+  if (cudaMemset(c->status, 0, sizeof(unsigned)) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->join, cudaEventDisableTiming) != cudaSuccess) {
+    if (c->side) cudaStreamDestroy(c->side);
+    if (c->fork) cudaEventDestroy(c->fork);
     cudaFree(c->status);
     delete c;
     return HMM_ERR_CUDA;
@@ -306,6 +316,12 @@ int hmm_destroy(hmm_ctx* ctx) {
       cudaEventDestroy(r.end);
     }
     for (cudaEvent_t e : ctx->pool) cudaEventDestroy(e);
+    if (ctx->side) {
+      cudaStreamSynchronize(ctx->side);
+      cudaStreamDestroy(ctx->side);
+    }
+    if (ctx->fork) cudaEventDestroy(ctx->fork);
+    if (ctx->join) cudaEventDestroy(ctx->join);
     if (ctx->status) cudaFree(ctx->status);
   }
   delete ctx;
@@ -500,18 +516,42 @@ int hmm_backward(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const voi
         launch_dispatch_dy(p, dy, topk_weights, shape->weights_dtype, m, c, dy_perm, wperm, st));
   }
   if (rc != HMM_OK) return rc;
+  auto gemms = [&](int part) {
+    return launch_backward_gemms(env, p, m, c, x_perm, dy_perm, wperm, h32, up_proj_weight,
+                                 down_proj_weight, dH, dH_lo, wa, wa_lo, dwp, dx_perm,
+                                 d_up_proj_weight, d_down_proj_weight, part);
+  };
   {
-    PhaseScope ps(ctx, PH_GEMM_BWD, st);
-    rc = launch_backward_gemms(env, p, m, c, x_perm, dy_perm, wperm, h32, up_proj_weight,
-                               down_proj_weight, dH, dH_lo, wa, wa_lo, dwp, dx_perm,
-                               d_up_proj_weight, d_down_proj_weight);
+    PhaseScope ps(ctx, PH_GEMM_BWD_DATA, st);
+    rc = gemms(1);
   }
   if (rc != HMM_OK) return rc;
-  if (dx || d_topk_weights) {
-    PhaseScope ps(ctx, PH_COMBINE_DX, st);
-    rc = cuda_rc(launch_combine_dx(p, dx_perm, dwp, m, dx, d_topk_weights, shape->weights_dtype,
-                                   st));
+  // dx and d_topk_weights need only part 1: combine them on the side stream
+  // while part 2 (the weight gradients) runs; the caller's stream waits for
+  // both before anything queued after this call.
+  const bool combine = dx || d_topk_weights;
+  if (combine) {
+    rc = cuda_rc(cudaEventRecord(ctx->fork, st));
+    if (rc == HMM_OK) rc = cuda_rc(cudaStreamWaitEvent(ctx->side, ctx->fork, 0));
+    if (rc != HMM_OK) return rc;
+    {
+      PhaseScope pc(ctx, PH_COMBINE_DX, ctx->side);
+      rc = cuda_rc(launch_combine_dx(p, dx_perm, dwp, m, dx, d_topk_weights,
+                                     shape->weights_dtype, ctx->side));
+    }
+    const int rj = cuda_rc(cudaEventRecord(ctx->join, ctx->side));
+    if (rc == HMM_OK) rc = rj;
   }
+  int r2 = rc;
+  if (rc == HMM_OK && (d_up_proj_weight || d_down_proj_weight) && ctx->bwd_data_sms == 0) {
+    PhaseScope ps(ctx, PH_GEMM_BWD_WEIGHT, st);
+    r2 = gemms(2);
+  }
+  if (combine) {
+    const int rw = cuda_rc(cudaStreamWaitEvent(st, ctx->join, 0));
+    if (rc == HMM_OK) rc = rw;
+  }
+  if (rc == HMM_OK) rc = r2;
   return rc;
 }
 

@@ -109,16 +109,17 @@ struct GemmEnv {
 int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
                          const void* x_perm, const void* W1, const void* W2, void* a, float* h32,
                          void* o, bool skip_ready_release);
-// backward act_grad(+SwiGLU grad, d_w partials) and input-grad GEMMs
-// backward GEMMs in one persistent launch, interleaved per expert:
-//   act_grad (+SwiGLU grad, d_w partials; dH and w*a written as bf16 hi + lo),
-//   input-grad (per-M-tile release), W2Grad and W1Grad (per-expert release,
-//   reading the hi + lo halves).  dW1 / dW2 may be null.
+// backward GEMMs.  part 1: act_grad (+SwiGLU grad, d_w partials; dH and w*a
+// written as bf16 hi + lo) and input-grad (per-M-tile release) in one
+// persistent launch.  part 2: W2Grad and W1Grad (reading the hi + lo halves),
+// which need nothing from input-grad.  With env.bwd_data_sms > 0 all four run
+// in part 1 (two CTA groups, the weight gradients trailing act_grad per
+// expert) and part 2 does nothing.  dW1 / dW2 may be null.
 int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
                           const void* x_perm, const void* dy_perm, const float* wperm,
                           const float* h32, const void* W1, const void* W2, void* dH,
                           void* dH_lo, void* wa, void* wa_lo, float* dwp, void* dx_perm,
-                          void* dW1, void* dW2);
+                          void* dW1, void* dW2, int part);
 
 // weight-gradient GEMMs on CTA pairs (tcgen05 cta_group::2), 256 x 256 tiles
 int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, const void* x_perm,

@@ -138,9 +138,12 @@ int hmm_set_option(hmm_ctx* ctx, int option, int64_t value);
 
 /* Launch phases timed under HMM_OPT_PROFILE (index = phase id):
  *   0 route (3 kernels)  1 dispatch_x  2 gemm_fwd (GMM1+SwiGLU, GMM2)
- *   3 combine_y          4 dispatch_dy 5 gemm_bwd (act_grad + SwiGLU grad,
- *   input-grad, W2Grad, W1Grad)        6 combine_dx (+ d_topk_weights)   */
-#define HMM_NUM_PHASES 7
+ *   3 combine_y          4 dispatch_dy
+ *   5 gemm_bwd_data (act_grad + SwiGLU grad, input-grad; with
+ *     HMM_OPT_BWD_DATA_SMS > 0 also W2Grad, W1Grad)
+ *   6 gemm_bwd_weight (W2Grad, W1Grad)
+ *   7 combine_dx (+ d_topk_weights; on a second stream, beside phase 6)  */
+#define HMM_NUM_PHASES 8
 
 /* Tracing: waits for every event recorded since the previous read, then
  * writes, for each phase id < n, the summed GPU time in ms (ms[i]) and the
