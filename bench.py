@@ -130,14 +130,14 @@ def source_hash(files) -> str:
     return h.hexdigest()[:16]
 
 
-def load_traffic(kernel: str):
+def load_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current sources of that kernel (else None)."""
+    this workload and on the current sources of that kernel (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        if d.get("source_hash") != source_hash(d["files"]):
+        if d.get("workload") != workload or d.get("source_hash") != source_hash(d["files"]):
             return None
     except Exception:
         return None
@@ -401,7 +401,7 @@ def run_ours(args, dist: Dist):
     roofline = {"kernel": dom, "bound": dp["bound"], "achieved": dp["achieved"],
                 "peak": peaks["bf16_tflops_sustained"] if dp["bound"] == "tensor"
                 else peaks["hbm_gbs"],
-                "unit": dp["unit"], "frac": dp["frac"], "traffic": load_traffic(dom),
+                "unit": dp["unit"], "frac": dp["frac"], "traffic": None if args.shape else load_traffic(dom, args.workload),
                 "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if dp['bound'] == 'tensor' else 'hbm_gbs'})"}
 
     fwd_ms = sum(phases[k]["ms"] for k in ("route", "dispatch_x", "gemm_fwd", "combine_y"))
