@@ -22,7 +22,8 @@ import torch
 
 __all__ = [
     "HmmError", "HmmShape", "hmm_create", "hmm_destroy", "hmm_set_option",
-    "hmm_workspace_size", "hmm_route", "hmm_route_static", "hmm_forward", "hmm_backward", "hmm_status",
+    "hmm_workspace_size", "hmm_route", "hmm_route_static", "hmm_forward", "hmm_backward",
+    "hmm_backward_dx", "hmm_backward_dw", "hmm_status",
     "hmm_error_string", "Context", "moe_ffn", "library_path", "load_library",
     "hmm_profile_read", "hmm_phase_name", "hmm_set_trace",
     "HMM_OPT_VALIDATE", "HMM_OPT_WAIT_BUDGET_NS", "HMM_OPT_INJECT_SKIP_READY", "HMM_OPT_PROFILE",
@@ -107,6 +108,8 @@ def load_library():
             "hmm_route_static": [sp, vp, vp, vp, vp, vp, vp],
             "hmm_forward": [vp, sp, vp, vp, vp, vp, vp, vp, vp, sz, vp, sz, vp],
             "hmm_backward": [vp, sp, vp, vp, vp, vp, vp, sz, vp, vp, vp, vp, vp, sz, vp],
+            "hmm_backward_dx": [vp, sp, vp, vp, vp, vp, vp, sz, vp, vp, vp, sz, vp],
+            "hmm_backward_dw": [vp, sp, vp, sz, vp, vp, vp, sz, vp],
             "hmm_status": [vp, vp, ctypes.POINTER(i32)],
             "hmm_profile_read": [vp, i32, ctypes.POINTER(ctypes.c_double),
                                  ctypes.POINTER(ctypes.c_int64)],
@@ -213,6 +216,24 @@ def hmm_backward(ctx, shape, dy, topk_weights, up_proj_weight, down_proj_weight,
                                      _ptr(d_down_proj_weight), _ptr(d_topk_weights),
                                      _ptr(workspace), _nbytes(workspace), _stream(stream))
     _check(rc, "hmm_backward")
+
+
+def hmm_backward_dx(ctx, shape, dy, topk_weights, up_proj_weight, down_proj_weight, saved, dx,
+                    d_topk_weights, workspace, stream=None):
+    rc = load_library().hmm_backward_dx(ctx, ctypes.byref(shape), _ptr(dy), _ptr(topk_weights),
+                                        _ptr(up_proj_weight), _ptr(down_proj_weight),
+                                        _ptr(saved), _nbytes(saved), _ptr(dx),
+                                        _ptr(d_topk_weights), _ptr(workspace), _nbytes(workspace),
+                                        _stream(stream))
+    _check(rc, "hmm_backward_dx")
+
+
+def hmm_backward_dw(ctx, shape, saved, d_up_proj_weight, d_down_proj_weight, workspace,
+                    stream=None):
+    rc = load_library().hmm_backward_dw(ctx, ctypes.byref(shape), _ptr(saved), _nbytes(saved),
+                                        _ptr(d_up_proj_weight), _ptr(d_down_proj_weight),
+                                        _ptr(workspace), _nbytes(workspace), _stream(stream))
+    _check(rc, "hmm_backward_dw")
 
 
 def hmm_status(ctx, stream=None):

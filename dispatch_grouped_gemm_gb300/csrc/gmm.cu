@@ -1089,12 +1089,16 @@ int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtr
   // data gradients on CTA pairs: each CTA loads 128 of the 256 B rows
   const bool pair = env.pair_rows && env.bwd_data_sms <= 0;
   const uint32_t b_rows = pair ? BN / 2 : BN;
-  // act_grad: G = dy_perm . W2^T   (B = W2 [E, I, H] read K-major, N = I)
-  rc |= map_act(env, &maps.m[0][0], dy_perm, R, H, BM);
-  rc |= map_w(env, &maps.m[0][1], W2, E, I, H, b_rows);
-  // input-grad: dX_perm = dH . W1^T (B = W1 [E, H, 2I] read K-major, N = H)
-  rc |= map_act(env, &maps.m[1][0], dH, R, 2 * I, BM);
-  rc |= map_w(env, &maps.m[1][1], W1, E, H, 2 * I, b_rows);
+  if (part == 1) {  // (part 2 needs neither W1 nor W2)
+    // act_grad: G = dy_perm . W2^T   (B = W2 [E, I, H] read K-major, N = I)
+    rc |= map_act(env, &maps.m[0][0], dy_perm, R, H, BM);
+    rc |= map_w(env, &maps.m[0][1], W2, E, I, H, b_rows);
+    // input-grad: dX_perm = dH . W1^T (B = W1 [E, H, 2I] read K-major, N = H)
+    rc |= map_act(env, &maps.m[1][0], dH, R, 2 * I, BM);
+    rc |= map_w(env, &maps.m[1][1], W1, E, H, 2 * I, b_rows);
+    maps.m[0][2] = maps.m[0][0];
+    maps.m[1][2] = maps.m[1][0];
+  }
   // W2Grad: dW2[e] = (wa_hi + wa_lo)^T . dy_perm    [I, rows] x [rows, H]
   rc |= map_act(env, &maps.m[2][0], wa, R, I, 64);
   rc |= map_act(env, &maps.m[2][1], dy_perm, R, H, 64);
@@ -1106,8 +1110,6 @@ int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtr
   if (rc != HMM_OK) return HMM_ERR_CUDA;
   const CUtensorMap map_w2[3] = {maps.m[2][0], maps.m[2][1], maps.m[2][2]};
   const CUtensorMap map_w1[3] = {maps.m[3][0], maps.m[3][1], maps.m[3][2]};
-  maps.m[0][2] = maps.m[0][0];
-  maps.m[1][2] = maps.m[1][0];
   Params P{};
   P.poff = m.poff;
   P.counts = m.counts;

@@ -458,13 +458,24 @@ int hmm_forward(hmm_ctx* ctx, const hmm_shape* shape, const void* x, const int32
   return cuda_rc(launch_combine_y(p, o, topk_weights, shape->weights_dtype, m, y, st));
 }
 
-int hmm_backward(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const void* topk_weights,
-                 const void* up_proj_weight, const void* down_proj_weight, const void* saved,
-                 size_t saved_bytes, void* dx, void* d_up_proj_weight, void* d_down_proj_weight,
-                 void* d_topk_weights, void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+enum BackwardMode { BWD_FULL = 0, BWD_DX = 1, BWD_DW = 2 };
+
+// hmm_backward, hmm_backward_dx and hmm_backward_dw.  BWD_DX runs everything
+// but the weight gradients and leaves their operands (dy_perm, dH and w*a as
+// bf16 hi + lo) in the workspace; BWD_DW runs only the weight gradients from
+// them.
+int backward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const void* topk_weights,
+                  const void* up_proj_weight, const void* down_proj_weight, const void* saved,
+                  size_t saved_bytes, void* dx, void* d_up_proj_weight, void* d_down_proj_weight,
+                  void* d_topk_weights, void* workspace, size_t workspace_bytes, void* stream,
+                  BackwardMode mode) {
   if (!ctx) return HMM_ERR_ARG;
   int rc = check_shape(shape);
   if (rc != HMM_OK) return rc;
+  if (mode == BWD_DX) d_up_proj_weight = d_down_proj_weight = nullptr;
+  if (mode == BWD_DW) dx = d_topk_weights = nullptr;
   Plan p;
   make_plan(shape, true, &p);
   DeviceGuard g(ctx->device);
@@ -483,12 +494,12 @@ int hmm_backward(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const voi
     }
     return rc;
   }
-  if (!dy || !topk_weights || !up_proj_weight || !down_proj_weight || !saved || !workspace)
+  if (!saved || !workspace) return HMM_ERR_ARG;
+  if (mode != BWD_DW && (!dy || !topk_weights || !up_proj_weight || !down_proj_weight))
     return HMM_ERR_ARG;
   for (const void* ptr : {dy, topk_weights, up_proj_weight, down_proj_weight, saved,
-                          static_cast<const void*>(workspace)})
-    if (!aligned16(ptr)) return HMM_ERR_LAYOUT;
-  for (const void* ptr : {static_cast<const void*>(dx), static_cast<const void*>(d_up_proj_weight),
+                          static_cast<const void*>(workspace), static_cast<const void*>(dx),
+                          static_cast<const void*>(d_up_proj_weight),
                           static_cast<const void*>(d_down_proj_weight),
                           static_cast<const void*>(d_topk_weights)})
     if (ptr && !aligned16(ptr)) return HMM_ERR_LAYOUT;
@@ -508,7 +519,20 @@ int hmm_backward(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const voi
   void* wa_lo = ws + p.bw_walo;
   void* dx_perm = ws + p.bw_dxperm;
   float* dwp = reinterpret_cast<float*>(ws + p.bw_dwp);
-  const GemmEnv env = env_of(ctx, p, st);
+  GemmEnv env = env_of(ctx, p, st);
+  // the deferred weight gradients read what a two-launch data phase left
+  if (mode == BWD_DW) env.bwd_data_sms = 0;
+  auto gemms = [&](int part) {
+    return launch_backward_gemms(env, p, m, c, x_perm, dy_perm, wperm, h32, up_proj_weight,
+                                 down_proj_weight, dH, dH_lo, wa, wa_lo, dwp, dx_perm,
+                                 d_up_proj_weight, d_down_proj_weight, part);
+  };
+  const bool weights = (d_up_proj_weight || d_down_proj_weight) && env.bwd_data_sms == 0;
+  if (mode == BWD_DW) {
+    if (!weights) return HMM_OK;
+    PhaseScope ps(ctx, PH_GEMM_BWD_WEIGHT, st);
+    return gemms(2);
+  }
 
   {
     PhaseScope ps(ctx, PH_DISPATCH_DY, st);
@@ -516,11 +540,6 @@ int hmm_backward(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const voi
         launch_dispatch_dy(p, dy, topk_weights, shape->weights_dtype, m, c, dy_perm, wperm, st));
   }
   if (rc != HMM_OK) return rc;
-  auto gemms = [&](int part) {
-    return launch_backward_gemms(env, p, m, c, x_perm, dy_perm, wperm, h32, up_proj_weight,
-                                 down_proj_weight, dH, dH_lo, wa, wa_lo, dwp, dx_perm,
-                                 d_up_proj_weight, d_down_proj_weight, part);
-  };
   {
     PhaseScope ps(ctx, PH_GEMM_BWD_DATA, st);
     rc = gemms(1);
@@ -543,7 +562,7 @@ int hmm_backward(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const voi
     if (rc == HMM_OK) rc = rj;
   }
   int r2 = rc;
-  if (rc == HMM_OK && (d_up_proj_weight || d_down_proj_weight) && ctx->bwd_data_sms == 0) {
+  if (rc == HMM_OK && weights) {
     PhaseScope ps(ctx, PH_GEMM_BWD_WEIGHT, st);
     r2 = gemms(2);
   }
@@ -553,6 +572,34 @@ int hmm_backward(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const voi
   }
   if (rc == HMM_OK) rc = r2;
   return rc;
+}
+
+}  // namespace
+
+int hmm_backward(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const void* topk_weights,
+                 const void* up_proj_weight, const void* down_proj_weight, const void* saved,
+                 size_t saved_bytes, void* dx, void* d_up_proj_weight, void* d_down_proj_weight,
+                 void* d_topk_weights, void* workspace, size_t workspace_bytes, void* stream) {
+  return backward_impl(ctx, shape, dy, topk_weights, up_proj_weight, down_proj_weight, saved,
+                       saved_bytes, dx, d_up_proj_weight, d_down_proj_weight, d_topk_weights,
+                       workspace, workspace_bytes, stream, BWD_FULL);
+}
+
+int hmm_backward_dx(hmm_ctx* ctx, const hmm_shape* shape, const void* dy,
+                    const void* topk_weights, const void* up_proj_weight,
+                    const void* down_proj_weight, const void* saved, size_t saved_bytes, void* dx,
+                    void* d_topk_weights, void* workspace, size_t workspace_bytes, void* stream) {
+  return backward_impl(ctx, shape, dy, topk_weights, up_proj_weight, down_proj_weight, saved,
+                       saved_bytes, dx, nullptr, nullptr, d_topk_weights, workspace,
+                       workspace_bytes, stream, BWD_DX);
+}
+
+int hmm_backward_dw(hmm_ctx* ctx, const hmm_shape* shape, const void* saved, size_t saved_bytes,
+                    void* d_up_proj_weight, void* d_down_proj_weight, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  return backward_impl(ctx, shape, nullptr, nullptr, nullptr, nullptr, saved, saved_bytes,
+                       nullptr, d_up_proj_weight, d_down_proj_weight, nullptr, workspace,
+                       workspace_bytes, stream, BWD_DW);
 }
 
 int hmm_status(hmm_ctx* ctx, void* stream, int* device_error) {

@@ -240,6 +240,34 @@ int hmm_backward(hmm_ctx* ctx, const hmm_shape* shape, const void* dy,
                  void* d_down_proj_weight, void* d_topk_weights,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/* The backward split into its data and weight halves, for schedulers that
+ * defer the weight gradients [EP overlap issue §2.3 (W/D split, deferred W
+ * queue), §4.5: separate D-only and W-only backward entry points].
+ *
+ * hmm_backward_dx: what hmm_backward does without the weight gradients
+ *   (dispatch dY, act_grad + SwiGLU grad, input-grad, combine dX and
+ *   d_topk_weights; dx or d_topk_weights may be NULL).  It leaves in
+ *   `workspace` the operands of the weight gradients: dY permuted, dH and
+ *   w*a (bf16 hi + lo halves).
+ * hmm_backward_dw: d_up_proj_weight and d_down_proj_weight (either may be
+ *   NULL) from those operands and `saved`.  Call it on the same stream, after
+ *   the hmm_backward_dx of the same shape, `saved` and `workspace`; nothing
+ *   else may write that workspace or `saved` in between.  The workspace is
+ *   held until then: that is the memory cost of deferring W.
+ *
+ * Together the two write exactly what one hmm_backward call writes (the
+ * same kernels on the same inputs: bit-identical results).  Errors as for
+ * hmm_backward; hmm_backward_dw checks only shape, saved and workspace. */
+int hmm_backward_dx(hmm_ctx* ctx, const hmm_shape* shape, const void* dy,
+                    const void* topk_weights, const void* up_proj_weight,
+                    const void* down_proj_weight, const void* saved,
+                    size_t saved_bytes, void* dx, void* d_topk_weights,
+                    void* workspace, size_t workspace_bytes, void* stream);
+int hmm_backward_dw(hmm_ctx* ctx, const hmm_shape* shape, const void* saved,
+                    size_t saved_bytes, void* d_up_proj_weight,
+                    void* d_down_proj_weight, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
 /* Synchronise `stream`, then read and clear the device status word.
  * *device_error receives the HMM_STATUS_* bits.  Returns HMM_OK, or
  * HMM_ERR_EXPERT_ID / HMM_ERR_TIMEOUT if the corresponding bit was set. */

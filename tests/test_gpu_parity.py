@@ -234,3 +234,35 @@ def test_autograd_and_grad_accumulation(run):
     with torch.no_grad():
         y2 = hmm.moe_ffn(d.x, d.ids, d.w, d.W1, d.W2)
     assert torch.equal(y2.view(torch.int16), y.detach().view(torch.int16))
+
+
+def test_backward_split_dx_then_dw_is_bit_identical(run, rows_mode):
+    """hmm_backward_dx followed by hmm_backward_dw (the deferred weight
+    gradients of the EP overlap issue's W/D split, §2.3) writes what one
+    hmm_backward call writes, bit for bit; the weight half can also write
+    one of the two weight gradients alone."""
+    p = dict(SCEN)["multi_tile"]
+    d = gu.upload(p)
+    y, saved = run.forward(d)
+    dx, dW1, dW2, dw = run.backward(d, saved)
+    sh = run.shape(d)
+    _, _, bwd = hmm.hmm_workspace_size(sh, True)
+    ws = torch.empty(bwd, dtype=torch.uint8, device=gu.dev())
+    dx2 = torch.empty_like(dx)
+    dw2 = torch.empty_like(dw)
+    dW1b = torch.full_like(dW1, float("nan"))
+    dW2b = torch.full_like(dW2, float("nan"))
+    hmm.hmm_backward_dx(run.ctx.handle, sh, d.dy, d.w, d.W1, d.W2, saved, dx2, dw2, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(dx.view(torch.int16), dx2.view(torch.int16))
+    assert torch.equal(dw.view(torch.int16), dw2.view(torch.int16))
+    hmm.hmm_backward_dw(run.ctx.handle, sh, saved, dW1b, dW2b, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(dW1.view(torch.int16), dW1b.view(torch.int16))
+    assert torch.equal(dW2.view(torch.int16), dW2b.view(torch.int16))
+    # one weight gradient only
+    dW2c = torch.full_like(dW2, float("nan"))
+    hmm.hmm_backward_dw(run.ctx.handle, sh, saved, None, dW2c, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(dW2.view(torch.int16), dW2c.view(torch.int16))
+    assert run.status() == (0, 0)
