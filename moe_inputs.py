@@ -34,6 +34,7 @@ import numpy as np
 
 # sub-stream tags
 _TAG_X, _TAG_IDS, _TAG_W, _TAG_DY, _TAG_W1, _TAG_W2, _TAG_PERM = 1, 2, 3, 4, 5, 6, 7
+_TAG_SW1, _TAG_SW2 = 8, 9  # the optional shared expert
 
 
 @dataclass(frozen=True)
@@ -151,6 +152,17 @@ class Problem:
         """down_proj_weight[e], bf16 bits [I, H]."""
         s = self.shape
         return normal_bf16(_rng(self.seed, _TAG_W2, e), (s.I, s.H), 1.0 / np.sqrt(s.I))
+
+    def shared_W1(self) -> np.ndarray:
+        """Optional shared expert's up_proj weight, bf16 bits [H, 2I] (drawn like a
+        routed expert's, from its own sub-stream)."""
+        s = self.shape
+        return normal_bf16(_rng(self.seed, _TAG_SW1), (s.H, 2 * s.I), 1.0 / np.sqrt(s.H))
+
+    def shared_W2(self) -> np.ndarray:
+        """Optional shared expert's down_proj weight, bf16 bits [I, H]."""
+        s = self.shape
+        return normal_bf16(_rng(self.seed, _TAG_SW2), (s.I, s.H), 1.0 / np.sqrt(s.I))
 
     def _all(self, fn, shape_tail):
         s = self.shape

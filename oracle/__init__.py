@@ -66,6 +66,11 @@ def _load():
         lib.oracle_expert_ffn.restype = None
         lib.oracle_expert_ffn.argtypes = [i64, i64, ctypes.c_int, vp, i64, vp,
                                           i64, vp, i64, vp, vp, vp]
+        lib.oracle_shared_forward.restype = None
+        lib.oracle_shared_forward.argtypes = [i64, i64, i64, ctypes.c_int, vp, vp, vp, vp]
+        lib.oracle_shared_backward.restype = None
+        lib.oracle_shared_backward.argtypes = [i64, i64, i64, ctypes.c_int, vp, vp, vp, vp,
+                                               vp, vp, vp]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         _lib = lib
@@ -185,3 +190,30 @@ def backward(x, topk_ids, topk_weights, W1, W2, dy):
     for e in range(E):
         dW1[e], dW2[e] = weight_grad(e, x, topk_ids, topk_weights, W1, W2, dy)
     return dx, dW1, dW2, dw
+
+
+def shared_forward(x, Ws1, Ws2):
+    """The shared expert's term of y (float64 [T,H]): FFN_s(x[t]) for every
+    token, unit weight [HyperMegaMoE §6.1]."""
+    dt, (x, Ws1, Ws2) = _fp([x, Ws1, Ws2])
+    T, H = x.shape
+    H1, I2 = Ws1.shape
+    I = I2 // 2
+    assert H1 == H and Ws2.shape == (I, H)
+    ys = np.zeros((T, H), np.float64)
+    _load().oracle_shared_forward(T, H, I, dt, _ptr(x), _ptr(Ws1), _ptr(Ws2), _ptr(ys))
+    return ys
+
+
+def shared_backward(x, Ws1, Ws2, dy):
+    """The shared expert's part of dx and its weight gradients:
+    (dx_s [T,H], dWs1 [H,2I], dWs2 [I,H]) in float64."""
+    dt, (x, Ws1, Ws2, dy) = _fp([x, Ws1, Ws2, dy])
+    T, H = x.shape
+    I = Ws1.shape[1] // 2
+    dxs = np.zeros((T, H), np.float64)
+    dWs1 = np.zeros((H, 2 * I), np.float64)
+    dWs2 = np.zeros((I, H), np.float64)
+    _load().oracle_shared_backward(T, H, I, dt, _ptr(x), _ptr(Ws1), _ptr(Ws2), _ptr(dy),
+                                   _ptr(dxs), _ptr(dWs1), _ptr(dWs2))
+    return dxs, dWs1, dWs2

@@ -334,3 +334,86 @@ int64_t oracle_weight_grad(int64_t T, int64_t H, int64_t I, int64_t E,
   free(DH);
   return 0;
 }
+
+/*
+ * Optional shared expert [HyperMegaMoE §6.1: shared-expert weights whose
+ * GMM1 -> SwiGLU -> GMM2 run beside the routed experts and whose output is
+ * merged at Combine].  Reading where the page is silent: every token goes
+ * through the shared expert with unit weight (no gate), so
+ *   y[t] += FFN_s(x[t])
+ * with FFN_s the expert FFN above on Ws1 [H, 2I], Ws2 [I, H].  ys is double
+ * [T, H] (the shared term alone).
+ */
+void oracle_shared_forward(int64_t T, int64_t H, int64_t I, int dt,
+                           const void* x, const void* Ws1, const void* Ws2,
+                           double* ys) {
+#pragma omp parallel
+  {
+    double* h = (double*)malloc(sizeof(double) * (size_t)(2 * I));
+    double* a = (double*)malloc(sizeof(double) * (size_t)I);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t t = 0; t < T; ++t)
+      oracle_expert_ffn(H, I, dt, x, t * H, Ws1, 0, Ws2, 0, h, a, ys + t * H);
+    free(h);
+    free(a);
+  }
+}
+
+/*
+ * Backward of the shared term (the chain rule through y[t] += FFN_s(x[t]),
+ * unit weight):
+ *   dA_t = dy_t . Ws2^T,  dH_t = SwiGLU grad,  dxs[t] = dH_t . Ws1^T
+ *   dWs2 = sum_t a_t^T (outer) dy_t          [I, H]
+ *   dWs1 = sum_t x_t^T (outer) dH_t          [H, 2I]
+ * summed over tokens in ascending t.  dxs is double [T, H] (the shared
+ * term's part of dx alone).
+ */
+void oracle_shared_backward(int64_t T, int64_t H, int64_t I, int dt,
+                            const void* x, const void* Ws1, const void* Ws2,
+                            const void* dy, double* dxs, double* dWs1,
+                            double* dWs2) {
+  double* A = (double*)malloc(sizeof(double) * (size_t)(T * I));
+  double* DH = (double*)malloc(sizeof(double) * (size_t)(T * 2 * I));
+#pragma omp parallel
+  {
+    double* h = (double*)malloc(sizeof(double) * (size_t)(2 * I));
+    double* o = (double*)malloc(sizeof(double) * (size_t)H);
+    double* dO = (double*)malloc(sizeof(double) * (size_t)H);
+    double* dA = (double*)malloc(sizeof(double) * (size_t)I);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t t = 0; t < T; ++t) {
+      oracle_expert_ffn(H, I, dt, x, t * H, Ws1, 0, Ws2, 0, h, A + t * I, o);
+      slot_backward(H, I, dt, Ws2, 0, h, 1.0, dy, t * H, dO, dA,
+                    DH + t * 2 * I);
+      double* dxt = dxs + t * H;
+      for (int64_t i = 0; i < H; ++i) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < 2 * I; ++j)
+          acc += DH[t * 2 * I + j] * ld(Ws1, i * 2 * I + j, dt);
+        dxt[i] = acc;
+      }
+    }
+    free(h);
+    free(o);
+    free(dO);
+    free(dA);
+  }
+  for (int64_t i = 0; i < H * 2 * I; ++i) dWs1[i] = 0.0;
+  for (int64_t i = 0; i < I * H; ++i) dWs2[i] = 0.0;
+#pragma omp parallel for schedule(static)
+  for (int64_t j = 0; j < I; ++j)
+    for (int64_t t = 0; t < T; ++t) {
+      double aj = A[t * I + j];
+      for (int64_t c = 0; c < H; ++c)
+        dWs2[j * H + c] += aj * ld(dy, t * H + c, dt);
+    }
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < H; ++i)
+    for (int64_t t = 0; t < T; ++t) {
+      double xi = ld(x, t * H + i, dt);
+      for (int64_t j = 0; j < 2 * I; ++j)
+        dWs1[i * 2 * I + j] += xi * DH[t * 2 * I + j];
+    }
+  free(A);
+  free(DH);
+}

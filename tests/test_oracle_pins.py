@@ -286,3 +286,79 @@ def test_backward_zero_weight_slot_contributes_no_dx_dW():
     np.testing.assert_allclose(dx, dx1, rtol=1e-13, atol=1e-15)
     np.testing.assert_allclose(dW1, dW1_1, rtol=1e-13, atol=1e-15)
     np.testing.assert_allclose(dW2, dW2_1, rtol=1e-13, atol=1e-15)
+
+
+# ------------------------------------------------------------ shared expert
+# [HyperMegaMoE §6.1] optional shared expert, merged at Combine with unit
+# weight (the reading: no gate, every token).
+
+def _shared_f64(T=6, H=8, I=5, seed=7):
+    r = np.random.default_rng(seed)
+    x = r.standard_normal((T, H))
+    Ws1 = r.standard_normal((H, 2 * I)) / math.sqrt(H)
+    Ws2 = r.standard_normal((I, H)) / math.sqrt(I)
+    dy = r.standard_normal((T, H))
+    return x, Ws1, Ws2, dy
+
+
+def test_shared_forward_is_a_dense_swiglu_ffn_torch():
+    """Library special case: the shared term is silu(x Wg) (x Wu) Wd for
+    every token, as torch computes it in fp64."""
+    torch = pytest.importorskip("torch")
+    x, Ws1, Ws2, _ = _shared_f64()
+    I = Ws2.shape[0]
+    xt, W1t, W2t = (torch.from_numpy(a) for a in (x, Ws1, Ws2))
+    ref = (torch.nn.functional.silu(xt @ W1t[:, :I]) * (xt @ W1t[:, I:])) @ W2t
+    np.testing.assert_allclose(oracle.shared_forward(x, Ws1, Ws2), ref.numpy(),
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_shared_backward_matches_torch_autograd():
+    """dx_s, dWs1, dWs2 of L = <dy, FFN_s(x)> against torch fp64 autograd."""
+    torch = pytest.importorskip("torch")
+    x, Ws1, Ws2, dy = _shared_f64()
+    I = Ws2.shape[0]
+    xt, W1t, W2t = (torch.from_numpy(a).clone().requires_grad_(True) for a in (x, Ws1, Ws2))
+    y = (torch.nn.functional.silu(xt @ W1t[:, :I]) * (xt @ W1t[:, I:])) @ W2t
+    (y * torch.from_numpy(dy)).sum().backward()
+    dxs, dWs1, dWs2 = oracle.shared_backward(x, Ws1, Ws2, dy)
+    np.testing.assert_allclose(dxs, xt.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dWs1, W1t.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dWs2, W2t.grad.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_shared_backward_finite_differences():
+    """Central differences of L = <dy, FFN_s(x)> in fp64 for sampled entries."""
+    x, Ws1, Ws2, dy = _shared_f64(T=4, H=6, I=3, seed=9)
+    dxs, dWs1, dWs2 = oracle.shared_backward(x, Ws1, Ws2, dy)
+    loss = lambda x_, a_, b_: float((oracle.shared_forward(x_, a_, b_) * dy).sum())
+    eps = 1e-6
+    r = np.random.default_rng(1)
+    for arr, grad, which in ((x, dxs, 0), (Ws1, dWs1, 1), (Ws2, dWs2, 2)):
+        for _ in range(6):
+            idx = tuple(r.integers(0, n) for n in arr.shape)
+            p, m = arr.copy(), arr.copy()
+            p[idx] += eps
+            m[idx] -= eps
+            args_p = [x, Ws1, Ws2]
+            args_m = [x, Ws1, Ws2]
+            args_p[which], args_m[which] = p, m
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (which, idx, fd, grad[idx])
+
+
+def test_shared_expert_equals_a_routed_expert_with_unit_weight():
+    """The shared expert is the routed forward/backward of an E=1, K=1 layer
+    with every routing weight 1 (the routed oracle is pinned above)."""
+    x, Ws1, Ws2, dy = _shared_f64(T=7, seed=11)
+    T = x.shape[0]
+    ids = np.zeros((T, 1), np.int32)
+    w = np.ones((T, 1))
+    np.testing.assert_allclose(oracle.shared_forward(x, Ws1, Ws2),
+                               oracle.forward(x, ids, w, Ws1[None], Ws2[None]),
+                               rtol=1e-13, atol=1e-13)
+    dxs, dWs1, dWs2 = oracle.shared_backward(x, Ws1, Ws2, dy)
+    rdx, rdW1, rdW2, _ = oracle.backward(x, ids, w, Ws1[None], Ws2[None], dy)
+    np.testing.assert_allclose(dxs, rdx, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dWs1, rdW1[0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dWs2, rdW2[0], rtol=1e-12, atol=1e-12)
