@@ -59,8 +59,6 @@ def parse():
                     default="prefill_fwd_bwd",
                     help="prefill_fwd_bwd is the benchmark line; the forward-only modes "
                          "measure the skewed and decode workloads")
-    ap.add_argument("--bwd-data-sms", type=int, default=0,
-                    help="SMs for the data-gradient GEMMs of the backward (0: automatic)")
     ap.add_argument("--shape", default=None,
                     help="T,H,I,E,K override (profiling of a smaller case; not a bench line)")
     a = ap.parse_args()
@@ -296,8 +294,6 @@ def run_ours(args, dist: Dist):
             W2[e].copy_(bf16(w2))
 
     ctx = hmm.Context.for_device(dev)
-    if args.bwd_data_sms:
-        ctx.set_option(hmm.HMM_OPT_BWD_DATA_SMS, args.bwd_data_sms)
     shape = hmm.Context.shape_of(x, ids, w, W1, W2)
     fws, svb, bws = hmm.hmm_workspace_size(shape, not fwd_only)
     y = torch.empty_like(x)

@@ -23,11 +23,12 @@ import torch
 __all__ = [
     "HmmError", "HmmShape", "hmm_create", "hmm_destroy", "hmm_set_option",
     "hmm_workspace_size", "hmm_route", "hmm_route_static", "hmm_forward", "hmm_backward",
-    "hmm_backward_dx", "hmm_backward_dw", "hmm_status",
+    "hmm_backward_dx", "hmm_backward_dw", "hmm_forward_shared", "hmm_backward_shared",
+    "hmm_status",
     "hmm_error_string", "Context", "moe_ffn", "library_path", "load_library",
     "hmm_profile_read", "hmm_phase_name", "hmm_set_trace",
     "HMM_OPT_VALIDATE", "HMM_OPT_WAIT_BUDGET_NS", "HMM_OPT_INJECT_SKIP_READY", "HMM_OPT_PROFILE",
-    "HMM_OPT_BWD_DATA_SMS", "HMM_OPT_PAIR_WGRAD", "HMM_OPT_PAIR_ROWS",
+    "HMM_OPT_PAIR_ROWS",
     "HMM_DTYPE_BF16", "HMM_DTYPE_F32", "HMM_STATUS_EXPERT_ID", "HMM_STATUS_TIMEOUT",
 ]
 
@@ -56,8 +57,6 @@ HMM_OPT_VALIDATE = _C["HMM_OPT_VALIDATE"]
 HMM_OPT_WAIT_BUDGET_NS = _C["HMM_OPT_WAIT_BUDGET_NS"]
 HMM_OPT_INJECT_SKIP_READY = _C["HMM_OPT_INJECT_SKIP_READY"]
 HMM_OPT_PROFILE = _C["HMM_OPT_PROFILE"]
-HMM_OPT_BWD_DATA_SMS = _C["HMM_OPT_BWD_DATA_SMS"]
-HMM_OPT_PAIR_WGRAD = _C["HMM_OPT_PAIR_WGRAD"]
 HMM_OPT_PAIR_ROWS = _C["HMM_OPT_PAIR_ROWS"]
 HMM_DTYPE_BF16 = _C["HMM_DTYPE_BF16"]
 HMM_DTYPE_F32 = _C["HMM_DTYPE_F32"]
@@ -68,7 +67,7 @@ HMM_STATUS_TIMEOUT = _C["HMM_STATUS_TIMEOUT"]
 class HmmShape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int64), ("I", ctypes.c_int64),
                 ("E", ctypes.c_int64), ("K", ctypes.c_int64),
-                ("weights_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("weights_dtype", ctypes.c_int32), ("shared", ctypes.c_int32)]
 
 
 class HmmError(RuntimeError):
@@ -109,6 +108,9 @@ def load_library():
             "hmm_forward": [vp, sp, vp, vp, vp, vp, vp, vp, vp, sz, vp, sz, vp],
             "hmm_backward": [vp, sp, vp, vp, vp, vp, vp, sz, vp, vp, vp, vp, vp, sz, vp],
             "hmm_backward_dx": [vp, sp, vp, vp, vp, vp, vp, sz, vp, vp, vp, sz, vp],
+            "hmm_forward_shared": [vp, sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, sz, vp],
+            "hmm_backward_shared": [vp, sp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp, vp, vp,
+                                    vp, vp, sz, vp],
             "hmm_backward_dw": [vp, sp, vp, sz, vp, vp, vp, sz, vp],
             "hmm_status": [vp, vp, ctypes.POINTER(i32)],
             "hmm_profile_read": [vp, i32, ctypes.POINTER(ctypes.c_double),
@@ -153,8 +155,8 @@ def _check(rc: int, where: str):
         raise HmmError(rc, where)
 
 
-def make_shape(T, H, I, E, K, weights_dtype=HMM_DTYPE_BF16) -> HmmShape:
-    return HmmShape(int(T), int(H), int(I), int(E), int(K), int(weights_dtype), 0)
+def make_shape(T, H, I, E, K, weights_dtype=HMM_DTYPE_BF16, shared=0) -> HmmShape:
+    return HmmShape(int(T), int(H), int(I), int(E), int(K), int(weights_dtype), int(shared))
 
 
 def hmm_error_string(code: int) -> str:
@@ -216,6 +218,30 @@ def hmm_backward(ctx, shape, dy, topk_weights, up_proj_weight, down_proj_weight,
                                      _ptr(d_down_proj_weight), _ptr(d_topk_weights),
                                      _ptr(workspace), _nbytes(workspace), _stream(stream))
     _check(rc, "hmm_backward")
+
+
+def hmm_forward_shared(ctx, shape, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight,
+                       shared_up_proj_weight, shared_down_proj_weight, y, saved, workspace,
+                       stream=None):
+    rc = load_library().hmm_forward_shared(
+        ctx, ctypes.byref(shape), _ptr(x), _ptr(topk_ids), _ptr(topk_weights),
+        _ptr(up_proj_weight), _ptr(down_proj_weight), _ptr(shared_up_proj_weight),
+        _ptr(shared_down_proj_weight), _ptr(y), _ptr(saved), _nbytes(saved), _ptr(workspace),
+        _nbytes(workspace), _stream(stream))
+    _check(rc, "hmm_forward_shared")
+
+
+def hmm_backward_shared(ctx, shape, dy, topk_weights, up_proj_weight, down_proj_weight,
+                        shared_up_proj_weight, shared_down_proj_weight, saved, dx,
+                        d_up_proj_weight, d_down_proj_weight, d_shared_up_proj_weight,
+                        d_shared_down_proj_weight, d_topk_weights, workspace, stream=None):
+    rc = load_library().hmm_backward_shared(
+        ctx, ctypes.byref(shape), _ptr(dy), _ptr(topk_weights), _ptr(up_proj_weight),
+        _ptr(down_proj_weight), _ptr(shared_up_proj_weight), _ptr(shared_down_proj_weight),
+        _ptr(saved), _nbytes(saved), _ptr(dx), _ptr(d_up_proj_weight), _ptr(d_down_proj_weight),
+        _ptr(d_shared_up_proj_weight), _ptr(d_shared_down_proj_weight), _ptr(d_topk_weights),
+        _ptr(workspace), _nbytes(workspace), _stream(stream))
+    _check(rc, "hmm_backward_shared")
 
 
 def hmm_backward_dx(ctx, shape, dy, topk_weights, up_proj_weight, down_proj_weight, saved, dx,
@@ -310,7 +336,8 @@ class Context:
         hmm_set_option(self.handle, option, value)
 
     @staticmethod
-    def shape_of(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight) -> HmmShape:
+    def shape_of(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight,
+                 shared_up_proj_weight=None, shared_down_proj_weight=None) -> HmmShape:
         if x.dim() != 2 or topk_ids.dim() != 2 or up_proj_weight.dim() != 3:
             raise ValueError("x [T,H], topk_ids [T,K], up_proj_weight [E,H,2I] expected")
         T, H = x.shape
@@ -329,23 +356,43 @@ class Context:
             raise TypeError("topk_ids must be int32")
         if topk_weights.dtype not in _WDTYPES:
             raise TypeError("topk_weights must be bfloat16 or float32")
-        for t in (x, topk_ids, topk_weights, up_proj_weight, down_proj_weight):
-            if not t.is_cuda or not t.is_contiguous():
+        shared = shared_up_proj_weight is not None or shared_down_proj_weight is not None
+        if shared:
+            if shared_up_proj_weight is None or shared_down_proj_weight is None:
+                raise ValueError("the shared expert needs both shared weights")
+            if tuple(shared_up_proj_weight.shape) != (H, 2 * I) or \
+                    tuple(shared_down_proj_weight.shape) != (I, H):
+                raise ValueError(f"shared weights must be {(H, 2 * I)} and {(I, H)}")
+            if shared_up_proj_weight.dtype != torch.bfloat16 or \
+                    shared_down_proj_weight.dtype != torch.bfloat16:
+                raise TypeError("shared weights must be bfloat16")
+        for t in (x, topk_ids, topk_weights, up_proj_weight, down_proj_weight,
+                  shared_up_proj_weight, shared_down_proj_weight):
+            if t is not None and (not t.is_cuda or not t.is_contiguous()):
                 raise ValueError("all arguments must be contiguous CUDA tensors")
-        return make_shape(T, H, I, E, topk_ids.shape[1], _WDTYPES[topk_weights.dtype])
+        return make_shape(T, H, I, E, topk_ids.shape[1], _WDTYPES[topk_weights.dtype],
+                          1 if shared else 0)
 
-    def forward(self, x, topk_ids, topk_weights, W1, W2, training: bool, stream=None):
-        shape = self.shape_of(x, topk_ids, topk_weights, W1, W2)
+    def forward(self, x, topk_ids, topk_weights, W1, W2, training: bool, stream=None,
+                Ws1=None, Ws2=None):
+        shape = self.shape_of(x, topk_ids, topk_weights, W1, W2, Ws1, Ws2)
         fwd, sv, _ = hmm_workspace_size(shape, training)
         y = torch.empty_like(x)
         ws = _u8(fwd, x.device)
         saved = _u8(sv, x.device) if training else None
-        hmm_forward(self.handle, shape, x, topk_ids, topk_weights, W1, W2, y, saved, ws, stream)
+        if shape.shared:
+            hmm_forward_shared(self.handle, shape, x, topk_ids, topk_weights, W1, W2, Ws1, Ws2, y,
+                               saved, ws, stream)
+        else:
+            hmm_forward(self.handle, shape, x, topk_ids, topk_weights, W1, W2, y, saved, ws,
+                        stream)
         return y, saved
 
     def backward(self, dy, x, topk_ids, topk_weights, W1, W2, saved, need=(True, True, True, True),
-                 stream=None):
-        shape = self.shape_of(x, topk_ids, topk_weights, W1, W2)
+                 stream=None, Ws1=None, Ws2=None, need_shared=(True, True)):
+        """(dx, dW1, dW2, d_topk_weights) and, with the shared expert, (dWs1, dWs2)
+        appended; `need` / `need_shared` skip outputs."""
+        shape = self.shape_of(x, topk_ids, topk_weights, W1, W2, Ws1, Ws2)
         _, _, bwd = hmm_workspace_size(shape, True)
         dy = dy.contiguous()
         if dy.dtype != torch.bfloat16 or tuple(dy.shape) != tuple(x.shape):
@@ -355,9 +402,15 @@ class Context:
         dW2 = torch.empty_like(W2) if need[2] else None
         dw = torch.empty_like(topk_weights) if need[3] else None
         ws = _u8(bwd, x.device)
-        hmm_backward(self.handle, shape, dy, topk_weights, W1, W2, saved, dx, dW1, dW2, dw, ws,
-                     stream)
-        return dx, dW1, dW2, dw
+        if not shape.shared:
+            hmm_backward(self.handle, shape, dy, topk_weights, W1, W2, saved, dx, dW1, dW2, dw,
+                         ws, stream)
+            return dx, dW1, dW2, dw
+        dWs1 = torch.empty_like(Ws1) if need_shared[0] else None
+        dWs2 = torch.empty_like(Ws2) if need_shared[1] else None
+        hmm_backward_shared(self.handle, shape, dy, topk_weights, W1, W2, Ws1, Ws2, saved, dx,
+                            dW1, dW2, dWs1, dWs2, dw, ws, stream)
+        return dx, dW1, dW2, dw, dWs1, dWs2
 
 
 class _MoEFFN(torch.autograd.Function):
@@ -378,14 +431,41 @@ class _MoEFFN(torch.autograd.Function):
         return dx, None, dw, dW1, dW2
 
 
-def moe_ffn(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight):
+class _MoEFFNShared(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, topk_ids, topk_weights, W1, W2, Ws1, Ws2):
+        c = Context.for_device(x.device)
+        y, saved = c.forward(x, topk_ids, topk_weights, W1, W2, training=True, Ws1=Ws1, Ws2=Ws2)
+        ctx.save_for_backward(x, topk_ids, topk_weights, W1, W2, Ws1, Ws2, saved)
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        x, topk_ids, topk_weights, W1, W2, Ws1, Ws2, saved = ctx.saved_tensors
+        n = ctx.needs_input_grad
+        c = Context.for_device(x.device)
+        dx, dW1, dW2, dw, dWs1, dWs2 = c.backward(dy, x, topk_ids, topk_weights, W1, W2, saved,
+                                                  (n[0], n[3], n[4], n[2]), Ws1=Ws1, Ws2=Ws2,
+                                                  need_shared=(n[5], n[6]))
+        return dx, None, dw, dW1, dW2, dWs1, dWs2
+
+
+def moe_ffn(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight, *,
+            shared_up_proj_weight=None, shared_down_proj_weight=None):
     """y[T,H] = sum_k topk_weights[t,k] * FFN_{topk_ids[t,k]}(x[t]) with SwiGLU
-    experts (gate = first I columns of up_proj's 2I outputs).  Differentiable
-    in x, topk_weights and both weight tensors; topk_ids is not."""
-    if not (torch.is_grad_enabled() and any(
-            t.requires_grad for t in (x, topk_weights, up_proj_weight, down_proj_weight))):
+    experts (gate = first I columns of up_proj's 2I outputs), plus FFN_s(x[t])
+    of the optional shared expert (keyword-only weights [H, 2I] and [I, H]).
+    Differentiable in x, topk_weights and every weight tensor; topk_ids is
+    not."""
+    shared = (shared_up_proj_weight, shared_down_proj_weight)
+    has_shared = shared[0] is not None or shared[1] is not None
+    tensors = (x, topk_weights, up_proj_weight, down_proj_weight) + (shared if has_shared else ())
+    if not (torch.is_grad_enabled() and any(t.requires_grad for t in tensors)):
         c = Context.for_device(x.device)
         y, _ = c.forward(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight,
-                         training=False)
+                         training=False, Ws1=shared[0], Ws2=shared[1])
         return y
+    if has_shared:
+        return _MoEFFNShared.apply(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight,
+                                   *shared)
     return _MoEFFN.apply(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight)

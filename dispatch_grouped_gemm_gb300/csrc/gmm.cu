@@ -1,33 +1,47 @@
 // gmm.cu -- persistent grouped GEMM on sm_103a (TMA -> tcgen05.mma -> TMEM)
-// with a per-expert tile scheduler and fused epilogues.
+// with a per-expert tile scheduler and fused epilogues: the row-mode GEMMs of
+// the fused MoE-FFN.
 //
-// The GEMMs of the fused MoE-FFN [HyperMegaMoE §2.1 GMM1/up_proj ->
-// SwiGLU -> GMM2/down_proj; §2.2 act_grad, SwiGLUGrad, input-grad GMM,
-// W2Grad, W1Grad] all run through one kernel template:
+// [HyperMegaMoE §2.1 GMM1/up_proj -> SwiGLU -> GMM2/down_proj; §2.2 act_grad
+// with SwiGLUGrad, input-grad GMM]:
 //
-//   rows mode   out[rows of e] = A[rows of e] . B[e]       (A: permuted
-//               activations, K-major; B: expert weights, MN- or K-major)
-//   wgrad mode  out[e] = A[rows of e]^T . B[rows of e]     (contraction over
-//               the expert's padded rows; A, B: activations, MN-major)
+//   out[rows of e] = A[rows of e] . B[e]
 //
-// One launch holds up to four problems.  Tiles are handed out through a global
-// atomic ticket in "schedule steps": step j holds, for every problem p, the
-// tiles of expert j - lag_p.  A consumer problem runs a few experts behind its
-// producer and waits on a ready counter (per M-tile, or per expert for the
-// weight gradients) that the producer's epilogues release [HyperMegaMoE §2.1:
-// tasks split by token/expert tile, event counts release downstream tasks, no
-// global barrier; §2.2 / §5.2: W2Grad interleaved with the act_grad branch,
-// W1Grad overlapped with the input gradient].  Interleaving experts mixes
-// memory-bound and tensor-bound tiles in flight.  Every producer tile has a
-// smaller ticket than its consumers, so it was already taken by a running CTA
-// when a consumer spins: the wait cannot deadlock (and is bounded anyway).
+// A holds the expert's routed rows in the padded row space (128-row tiles
+// never span two experts): x_perm / dy_perm, written by the dispatch kernels,
+// or a / dH, written by the GMM1 / act_grad epilogues.  B is the expert's
+// weight slab, MN-major (forward) or K-major (backward).  (Gathering the A
+// rows by token with TMA gather4 loads instead of a separate permute was
+// measured about 3.5x slower per tile: 32 requests per K block.)  The weight
+// gradients run in gmm_pair.cu.
+//
+// One launch holds up to four problems: a producer and a consumer problem for
+// the routed experts [0, E) and, with the optional shared expert
+// [HyperMegaMoE §6.1], the same pair for the shared expert, which is expert
+// E of the padded row space (every token, routing weight 1) with its own
+// weight slabs.  Tiles are handed out through a global atomic ticket in
+// "schedule steps": step j holds, for every problem p, the tiles of expert
+// j - lag_p (if it lies in p's expert range).  The consumer problems run
+// behind every producer tile and wait on per-M-tile ready counters that the
+// producer's
+// epilogues release [HyperMegaMoE §2.1: tasks split by token/expert tile,
+// event counts release downstream tasks, no global barrier].  Every producer
+// tile has a smaller ticket than its consumers, so it was already taken by a
+// running CTA when a consumer spins: the wait cannot deadlock (and is bounded
+// anyway).
 //
 // CTA = 7 warps: warp 6 schedules tiles (tickets, decoding, dependency waits,
-// about one tile ahead), warp 0 issues TMA loads (one thread), warp 1
-// allocates TMEM and issues tcgen05.mma (one thread), warps 2..5 drain the
-// accumulators (each owns the 32 TMEM lanes of its warp id mod 4).  Two 128x256 fp32
-// accumulators in TMEM (512 columns) let the epilogue of one tile overlap the
-// MMAs of the next; a 4-stage ring of 48 KB smem stages feeds the MMAs.
+// about one tile ahead), warp 0 issues TMA loads, warp 1 allocates TMEM and
+// issues tcgen05.mma (one thread), warps 2..5 drain the accumulators (each
+// owns the 32 TMEM lanes of its warp id mod 4).  Two 128x256 fp32 accumulators
+// in TMEM (512 columns) let the epilogue of one tile overlap the MMAs of the
+// next; 192 KB of shared-memory stages feed the MMAs.
+//
+// PAIR = true: clusters of two CTAs compute 256x256 tiles (two 128-row M
+// tiles of one expert) with 2-SM MMAs (tcgen05.mma.cta_group::2): each CTA
+// stages its own 128 rows of A and 128 of the 256 columns of B and drains its
+// own 128x256 accumulator.  Only the even CTA schedules; it writes each tile
+// record into both CTAs' rings.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -39,15 +53,14 @@ namespace hmm {
 
 enum Epi : int { EPI_SWIGLU = 0, EPI_STORE = 1, EPI_DSWIGLU = 2 };
 
-template <int EPI_, bool WGRAD_, bool B_MN_>
+// EPI: epilogue; B_MN: B operand MN-major (else K-major).  A is K-major.
+template <int EPI_, bool B_MN_>
 struct Cfg {
   static constexpr int EPI = EPI_;
-  static constexpr bool WGRAD = WGRAD_;
-  static constexpr bool A_MN = WGRAD_;  // activations transposed in the wgrad mode
   static constexpr bool B_MN = B_MN_;
-  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, 0, B_MN ? 1 : 0);
   // 2-SM MMA of a CTA pair: M = 256 rows (128 per CTA), the same N
-  static constexpr uint32_t IDESC2 = idesc_bf16_f32(2 * BM, BN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+  static constexpr uint32_t IDESC2 = idesc_bf16_f32(2 * BM, BN, 0, B_MN ? 1 : 0);
 };
 
 constexpr int STAGES = 4;
@@ -63,60 +76,51 @@ constexpr int MAX_STAGES = PAIR_STAGES;
 static_assert(PAIR_STAGES * PAIR_STAGE_BYTES <= STAGES * STAGE_BYTES, "pair stages");
 constexpr int TI_DEPTH = 3;
 // Warp roles: 0 TMA producer, 1 MMA issuer, 2..5 epilogue (one per TMEM lane
-// quarter), 6 tile scheduler.  (Eight epilogue warps, two per quarter on
-// alternate column chunks, were measured slower: more scattered epilogue
-// traffic in flight slows the TMA operand feed of the same SM.)
+// quarter), 6 tile scheduler.  (Eight epilogue warps, two per quarter, were
+// measured slower: every SM sub-partition then runs two epilogue warps beside
+// the single-thread MMA and TMA loops.)
 constexpr int EPI_WARPS = 4;
 constexpr int CH_SPLIT = EPI_WARPS / 4;  // warps sharing a lane quarter
 constexpr int SCHED_WARP = 2 + EPI_WARPS;
-constexpr int NUM_THREADS = 32 * (SCHED_WARP + 1);  // 11 warps
+constexpr int NUM_THREADS = 32 * (SCHED_WARP + 1);  // 7 warps
+constexpr int MAX_PROB = 4;
+constexpr int MAX_STEPS = 2 * MAX_E + 8;
 // alignment slack + stages + epilogue buffers + barriers, tile-info ring and
 // schedule prefix table
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_WARPS * XBUF_BYTES + 512 +
-                           4 * (3 * MAX_E + 8 + 1) + 256;
+                           4 * (MAX_STEPS + 1) + 256;
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 constexpr uint32_t TMEM_COLS = 2 * BN;
 
 struct Prob {
-  int K;        // rows mode: contraction length
+  int K;        // contraction length
   int N;        // valid output columns (SwiGLU / SwiGLU grad: I)
-  int M;        // wgrad: output rows per expert
   int n_tiles;  // tiles along N
-  int m_tiles;  // wgrad: tiles along M
   int half;     // SwiGLU: I (offset of the up half in the 2I operand/outputs)
   void* out;
   int64_t ld_out;
-  int64_t out_estride;  // wgrad: elements between experts' outputs
   void* out2;
   int64_t ld_out2;
   void* out3;
   int64_t ld_out3;
   void* out4;           // SwiGLU grad: low bf16 half of dH (same layout as out)
   void* out5;           // SwiGLU grad: low bf16 half of w*a (same layout as out2)
-  int split;            // wgrad: 0 none, 1 A operand given as hi+lo, 2 B operand hi+lo
-  int wgrad;            // 1: contraction over the expert's rows (tile count fixed per expert)
+  int out_f32;          // STORE: fp32 outputs (else bf16)
   int lag;              // the tiles of expert e are issued at schedule step e + lag
-  int group;            // CTA group whose ticket queue holds this problem's tiles
+  int e_lo, e_hi;       // experts of this problem; B holds experts e_lo .. e_hi - 1
   const void* aux;
   int64_t ld_aux;
   const float* rowscale;
   int* signal_m;        // per-M-tile counters released after a tile's stores
-  int* signal_e;        // per-expert counters released after a tile's stores
   const int* wait_m;    // per-M-tile counter acquired before a tile's loads
-  const int* wait_e;    // per-expert counter acquired before a tile's loads
-  int wait_unit;        // target: wait_unit (per M-tile) or wait_unit * M-tiles of e
+  int wait_unit;        // per-M-tile target
 };
-
-constexpr int MAX_PROB = 4;
-constexpr int MAX_STEPS = 3 * MAX_E + 8;
 
 struct Params {
   Prob p[MAX_PROB];
   int nprob;
-  int pair;             // rows mode on CTA pairs: a tile is two M tiles of one expert
-  int steps[2];         // per CTA group: E + largest lag of its problems
-  int group_split;      // CTAs [0, group_split) serve group 0, the rest group 1
-                        // (0: one group)
+  int pair;             // CTA pairs: a tile is two M tiles of one expert
+  int steps;            // E + largest lag
   const int32_t* poff;
   const int32_t* counts;
   int E;
@@ -128,16 +132,15 @@ struct Params {
 };
 
 struct Maps {
-  CUtensorMap m[MAX_PROB][3];  // A, B, and the low half of a split operand
+  CUtensorMap m[MAX_PROB][2];  // A, B
 };
 
 struct TileInfo {
   int prob;   // -1: no more tiles
   int e;
-  int m0;     // rows mode: first padded row; wgrad: first output row
+  int m0;     // first padded row (of the pair)
   int n0;     // first output column
-  int kb;     // K blocks (0: empty wgrad tile -> zeros)
-  int krow0;  // wgrad: first padded row of the expert
+  int kb;     // K blocks
   int ph;     // pair tile whose second M tile lies past the expert (odd M-tile count)
 };
 
@@ -158,25 +161,22 @@ __device__ __forceinline__ int mtiles_of(const Params& P, int e) {
 }
 
 __device__ __forceinline__ int tiles_of(const Params& P, const Prob& pr, int e) {
-  if (e < 0 || e >= P.E) return 0;
-  if (pr.wgrad) return pr.m_tiles * pr.n_tiles;
+  if (e < pr.e_lo || e >= pr.e_hi) return 0;
   const int nm = mtiles_of(P, e);
   return (P.pair ? (nm + 1) / 2 : nm) * pr.n_tiles;
 }
 
-// Prefix sums of the tile counts of group g's schedule steps (one warp, into
-// smem).
-__device__ void build_schedule(const Params& P, int g, int* pref) {
+// Prefix sums of the tile counts of the schedule steps (one warp, into smem).
+__device__ void build_schedule(const Params& P, int* pref) {
   const int lane = threadIdx.x & 31;
-  const int steps = P.steps[g];
+  const int steps = P.steps;
   int carry = 0;
   if (lane == 0) pref[0] = 0;
   for (int base = 0; base < steps; base += 32) {
     const int j = base + lane;
     int v = 0;
     if (j < steps)
-      for (int q = 0; q < P.nprob; ++q)
-        if (P.p[q].group == g) v += tiles_of(P, P.p[q], j - P.p[q].lag);
+      for (int q = 0; q < P.nprob; ++q) v += tiles_of(P, P.p[q], j - P.p[q].lag);
     int inc = v;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -189,11 +189,9 @@ __device__ void build_schedule(const Params& P, int g, int* pref) {
   __syncwarp();
 }
 
-// Ticket t of group g -> (problem, expert, local tile index).  Returns false
-// past the end.
-__device__ bool locate_tile(const Params& P, int g, const int* pref, int t, int& prob, int& e,
-                            int& r) {
-  const int steps = P.steps[g];
+// Ticket t -> (problem, expert, local tile index).  Returns false past the end.
+__device__ bool locate_tile(const Params& P, const int* pref, int t, int& prob, int& e, int& r) {
+  const int steps = P.steps;
   if (t >= pref[steps]) return false;
   int lo = 0, hi = steps - 1;  // largest step j with pref[j] <= t
   while (lo < hi) {
@@ -205,7 +203,6 @@ __device__ bool locate_tile(const Params& P, int g, const int* pref, int t, int&
   }
   r = t - pref[lo];
   for (int q = 0; q < P.nprob; ++q) {
-    if (P.p[q].group != g) continue;
     const int eq = lo - P.p[q].lag;
     const int c = tiles_of(P, P.p[q], eq);
     if (r < c) {
@@ -221,128 +218,75 @@ __device__ bool locate_tile(const Params& P, int g, const int* pref, int t, int&
 template <class C>
 __device__ void decode_tile(const Params& P, const Prob& pr, int e, int r, TileInfo& ti) {
   ti.e = e;
-  if constexpr (C::WGRAD) {
-    ti.m0 = (r / pr.n_tiles) * BM;
-    ti.n0 = (r % pr.n_tiles) * BN;
-    ti.krow0 = P.poff[e];
-    // rows past counts[e] are zero padding: skip whole zero K blocks
-    ti.kb = (P.counts[e] + BK - 1) / BK * (pr.split ? 2 : 1);
-  } else {
-    const int nm = mtiles_of(P, e);
-    const int nu = P.pair ? (nm + 1) / 2 : nm;  // M tiles or M-tile pairs
-    const int nb = r / nu;  // M innermost: a weight tile is reused from L2
-    const int mu = r - nb * nu;
-    ti.m0 = P.poff[e] + mu * BM * (P.pair ? 2 : 1);
-    ti.ph = P.pair && 2 * mu + 1 >= nm;
-    ti.n0 = nb * (C::EPI == EPI_SWIGLU ? BN / 2 : BN);
-    ti.krow0 = 0;
-    ti.kb = (pr.K + BK - 1) / BK;
-  }
+  const int nm = mtiles_of(P, e);
+  const int nu = P.pair ? (nm + 1) / 2 : nm;  // M tiles or M-tile pairs
+  const int nb = r / nu;  // M innermost: a weight tile is reused from L2
+  const int mu = r - nb * nu;
+  ti.m0 = P.poff[e] + mu * BM * (P.pair ? 2 : 1);
+  ti.ph = P.pair && 2 * mu + 1 >= nm;
+  ti.n0 = nb * (C::EPI == EPI_SWIGLU ? BN / 2 : BN);
+  ti.kb = (pr.K + BK - 1) / BK;
 }
 
 // ----------------------------------------------------------------- producer
-// Loads the operand boxes of K block kb of a tile into one smem stage.  Every
-// box starts at an inner coordinate that is a multiple of 8 elements (16 bytes).
-template <class C>
-__device__ __forceinline__ void stage_boxes(const Prob& pr, const TileInfo& ti, int kb,
-                                            const CUtensorMap* tA, const CUtensorMap* tB,
-                                            const CUtensorMap* tS, uint8_t* sA, uint8_t* sB,
-                                            uint64_t* bar) {
-  auto ld2 = [&](void* dst, const CUtensorMap* m, int c0, int c1) {
-    tma_load_2d(dst, m, bar, c0, c1);
-  };
-  auto ld3 = [&](void* dst, const CUtensorMap* m, int c0, int c1, int c2) {
-    tma_load_3d(dst, m, bar, c0, c1, c2);
-  };
-
-  if constexpr (C::WGRAD) {
-    // with a split operand the K loop runs twice over the expert's rows:
-    // first against the high bf16 half, then against the low half
-    const int nk = pr.split ? ti.kb / 2 : ti.kb;
-    const bool lo = kb >= nk;
-    const int k = ti.krow0 + (lo ? kb - nk : kb) * BK;
-    const CUtensorMap* a = (pr.split == 1 && lo) ? tS : tA;
-    const CUtensorMap* b = (pr.split == 2 && lo) ? tS : tB;
-    ld2(sA, a, ti.m0, k);
-    ld2(sA + 8192, a, ti.m0 + 64, k);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) ld2(sB + j * 8192, b, ti.n0 + 64 * j, k);
+// K block kb of a tile into one smem stage (one thread).  Every box starts at
+// an inner coordinate that is a multiple of 8 elements (16 bytes).
+//   PAIR: this CTA's share (its 128 rows of A unless load_a is false, its 128
+//   columns of B), counted on the even CTA's full barrier (shared::cluster
+//   address bar_cl; the even CTA arms it for both).
+template <class C, bool PAIR>
+__device__ __forceinline__ void load_stage(const Prob& pr, const TileInfo& ti, int kb,
+                                           const CUtensorMap* tA, const CUtensorMap* tB,
+                                           uint8_t* sA, uint8_t* sB, uint64_t* bar,
+                                           uint32_t bar_cl, uint32_t rank, bool load_a) {
+  const int k = kb * BK;
+  const int eb = ti.e - pr.e_lo;  // expert index inside this problem's weight slabs
+  if constexpr (PAIR) {
+    if (rank == 0) mbar_arrive_expect_tx(bar, (ti.ph ? 1 : 2) * A_BYTES + 2 * PAIR_B_BYTES);
+    if (load_a) tma_load_2d_pair(sA, tA, bar_cl, k, ti.m0 + BM * static_cast<int>(rank));
+    if constexpr (C::B_MN) {
+      int c;
+      if constexpr (C::EPI == EPI_SWIGLU)
+        c = (rank == 0 ? 0 : pr.half) + ti.n0;  // gate columns | up columns
+      else
+        c = ti.n0 + (BN / 2) * static_cast<int>(rank);
+      tma_load_3d_pair(sB, tB, bar_cl, c, k, eb);
+      tma_load_3d_pair(sB + 8192, tB, bar_cl, c + 64, k, eb);
+    } else {
+      tma_load_3d_pair(sB, tB, bar_cl, k, ti.n0 + (BN / 2) * static_cast<int>(rank), eb);
+    }
   } else {
-    (void)tS;
-    const int k = kb * BK;
-    ld2(sA, tA, k, ti.m0);
+    mbar_arrive_expect_tx(bar, STAGE_BYTES);
+    tma_load_2d(sA, tA, bar, k, ti.m0);
     if constexpr (C::B_MN) {
       if constexpr (C::EPI == EPI_SWIGLU) {
-        ld3(sB, tB, ti.n0, k, ti.e);
-        ld3(sB + 8192, tB, ti.n0 + 64, k, ti.e);
-        ld3(sB + 16384, tB, pr.half + ti.n0, k, ti.e);
-        ld3(sB + 24576, tB, pr.half + ti.n0 + 64, k, ti.e);
+        tma_load_3d(sB, tB, bar, ti.n0, k, eb);
+        tma_load_3d(sB + 8192, tB, bar, ti.n0 + 64, k, eb);
+        tma_load_3d(sB + 16384, tB, bar, pr.half + ti.n0, k, eb);
+        tma_load_3d(sB + 24576, tB, bar, pr.half + ti.n0 + 64, k, eb);
       } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) ld3(sB + j * 8192, tB, ti.n0 + 64 * j, k, ti.e);
+        for (int j = 0; j < 4; ++j) tma_load_3d(sB + j * 8192, tB, bar, ti.n0 + 64 * j, k, eb);
       }
     } else {
-      ld3(sB, tB, k, ti.n0, ti.e);
+      tma_load_3d(sB, tB, bar, k, ti.n0, eb);
     }
   }
 }
 
-// CTA pair: this CTA's share of K block kb (its 128 rows of A unless it is
-// the empty half of the pair; its 128 columns of B) into its own smem, counted
-// on the even CTA's full barrier (bar: shared::cluster address).
-template <class C>
-__device__ __forceinline__ void stage_boxes_pair(const Prob& pr, const TileInfo& ti, int kb,
-                                                 const CUtensorMap* tA, const CUtensorMap* tB,
-                                                 uint8_t* sA, uint8_t* sB, uint32_t bar,
-                                                 uint32_t rank) {
-  static_assert(!C::WGRAD, "CTA pairs serve the rows-mode GEMMs");
-  const int k = kb * BK;
-  if (rank == 0 || !ti.ph) tma_load_2d_pair(sA, tA, bar, k, ti.m0 + BM * static_cast<int>(rank));
-  if constexpr (C::B_MN) {
-    int c;
-    if constexpr (C::EPI == EPI_SWIGLU)
-      c = (rank == 0 ? 0 : pr.half) + ti.n0;  // gate columns | up columns
-    else
-      c = ti.n0 + (BN / 2) * static_cast<int>(rank);
-    tma_load_3d_pair(sB, tB, bar, c, k, ti.e);
-    tma_load_3d_pair(sB + 8192, tB, bar, c + 64, k, ti.e);
-  } else {
-    tma_load_3d_pair(sB, tB, bar, k, ti.n0 + (BN / 2) * static_cast<int>(rank), ti.e);
-  }
-}
-
-template <class C>
-__device__ __forceinline__ void load_stage(const Prob& pr, const TileInfo& ti, int kb,
-                                           const CUtensorMap* tA, const CUtensorMap* tB,
-                                           const CUtensorMap* tS, uint8_t* sA, uint8_t* sB,
-                                           uint64_t* bar) {
-  stage_boxes<C>(pr, ti, kb, tA, tB, tS, sA, sB, bar);
-}
-
 // ---------------------------------------------------------------------- MMA
-template <class C>
+template <class C, bool PAIR>
 __device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t a_base, uint32_t b_base,
                                           bool first) {
 #pragma unroll
   for (int kk = 0; kk < BK / 16; ++kk) {
-    const uint64_t ad = C::A_MN ? smem_desc(a_base + kk * 2048, 8192, 1024, LAYOUT_SW128)
-                                : smem_desc(a_base + kk * 32, 16, 1024, LAYOUT_SW128);
+    const uint64_t ad = smem_desc(a_base + kk * 32, 16, 1024, LAYOUT_SW128);
     const uint64_t bd = C::B_MN ? smem_desc(b_base + kk * 2048, 8192, 1024, LAYOUT_SW128)
                                 : smem_desc(b_base + kk * 32, 16, 1024, LAYOUT_SW128);
-    umma_bf16(d_tmem, ad, bd, C::IDESC, (first && kk == 0) ? 0u : 1u);
-  }
-}
-
-template <class C>
-__device__ __forceinline__ void mma_stage_pair(uint32_t d_tmem, uint32_t a_base, uint32_t b_base,
-                                               bool first) {
-#pragma unroll
-  for (int kk = 0; kk < BK / 16; ++kk) {
-    const uint64_t ad = C::A_MN ? smem_desc(a_base + kk * 2048, 8192, 1024, LAYOUT_SW128)
-                                : smem_desc(a_base + kk * 32, 16, 1024, LAYOUT_SW128);
-    const uint64_t bd = C::B_MN ? smem_desc(b_base + kk * 2048, 8192, 1024, LAYOUT_SW128)
-                                : smem_desc(b_base + kk * 32, 16, 1024, LAYOUT_SW128);
-    umma_bf16_pair(d_tmem, ad, bd, C::IDESC2, (first && kk == 0) ? 0u : 1u);
+    if constexpr (PAIR)
+      umma_bf16_pair(d_tmem, ad, bd, C::IDESC2, (first && kk == 0) ? 0u : 1u);
+    else
+      umma_bf16(d_tmem, ad, bd, C::IDESC, (first && kk == 0) ? 0u : 1u);
   }
 }
 
@@ -414,7 +358,6 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
     }
   } else if constexpr (C::EPI == EPI_STORE) {
     __nv_bfloat16* base = static_cast<__nv_bfloat16*>(pr.out);
-    if constexpr (C::WGRAD) base += static_cast<int64_t>(ti.e) * pr.out_estride;
 #pragma unroll 1
     for (int c = ch; c < BN / 32; c += CH_SPLIT) {
       const int col = ti.n0 + c * 32;
@@ -428,7 +371,9 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int64_t row = rl + 8 * k;
-          if (!C::WGRAD || row < pr.M)
+          if (pr.out_f32)
+            store_f32x8(static_cast<float*>(pr.out) + row * pr.ld_out + col + cg, v[k]);
+          else
             *reinterpret_cast<uint4*>(base + row * pr.ld_out + col + cg) = pack_bf16x8(v[k]);
         }
       }
@@ -528,19 +473,6 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
   }
 }
 
-template <class C>
-__device__ __forceinline__ void epilogue_zero(const Prob& pr, const TileInfo& ti, int row_in_tile,
-                                              int ch) {
-  // wgrad tile of an expert with no rows: the gradient is exactly zero
-  const int64_t row = ti.m0 + row_in_tile;
-  if (row >= pr.M) return;
-  __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(pr.out) +
-                        static_cast<int64_t>(ti.e) * pr.out_estride + row * pr.ld_out;
-  const uint4 z = make_uint4(0, 0, 0, 0);
-  for (int c = ch; c < BN / 32; c += CH_SPLIT)
-    for (int col = ti.n0 + c * 32; col < min(ti.n0 + c * 32 + 32, pr.N); col += 8)
-      *reinterpret_cast<uint4*>(orow + col) = z;
-}
 
 // Bounded wait that ignores the abort flag (used only to drain in-flight
 // copies / MMAs before the CTA exits).
@@ -558,15 +490,23 @@ __device__ __noinline__ void pause_ns(uint64_t ns) {
 }
 
 // ------------------------------------------------------------------- kernel
-#define HMM_BY_PROB(q, F, ...)       \
-  switch (q) {                       \
-    case 0: F<C0>(__VA_ARGS__); break; \
-    case 1: F<C1>(__VA_ARGS__); break; \
-    case 2: F<C2>(__VA_ARGS__); break; \
-    default: F<C3>(__VA_ARGS__); break; \
+// Problems 0 and 2 share configuration C0 (producers: GMM1, act_grad),
+// problems 1 and 3 C1 (consumers: GMM2, input-grad); 2 and 3 are the shared
+// expert's.
+#define HMM_BY_PROB(q, F, ...)   \
+  if (((q) & 1) == 0) {          \
+    F<C0>(__VA_ARGS__);          \
+  } else {                       \
+    F<C1>(__VA_ARGS__);          \
+  }
+#define HMM_BY_PROB_P(q, F, ...)  \
+  if (((q) & 1) == 0) {           \
+    F<C0, PAIR>(__VA_ARGS__);     \
+  } else {                        \
+    F<C1, PAIR>(__VA_ARGS__);     \
   }
 
-template <bool PAIR, class C0, class C1, class C2, class C3>
+template <bool PAIR, class C0, class C1>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gmm_kernel(const __grid_constant__ Params P, const __grid_constant__ Maps maps) {
   constexpr int NST = PAIR ? PAIR_STAGES : STAGES;
@@ -637,7 +577,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_arrive_cluster(mapa_shared(smem_u32(&ti_empty[slot]), 0));
   };
 
-  const int group = (P.group_split > 0 && static_cast<int>(blockIdx.x) >= P.group_split) ? 1 : 0;
   if (warp == SCHED_WARP) {
     // --------------------------------------------------------- tile scheduler
     // Fetches tickets, decodes them and waits for each tile's dependencies
@@ -647,42 +586,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // reuse of the weights.)  Lane 0 does the bookkeeping.  In a pair only
     // the even CTA schedules; it writes each tile into both CTAs' rings.
     if (!PAIR || leader) {
-      build_schedule(P, group, s_pref);
+      build_schedule(P, s_pref);
       int ti_slot = 0;
       uint32_t ti_phase = 0;
       int lt = 0;  // tiles of this CTA so far (trace index)
       int t = 0;
-      if (lane == 0) t = atomicAdd(P.ticket + group, 1);
+      if (lane == 0) t = atomicAdd(P.ticket, 1);
       for (;;) {
         TileInfo ti;
         ti.prob = -1;
-        ti.e = ti.m0 = ti.n0 = ti.kb = ti.krow0 = ti.ph = 0;
+        ti.e = ti.m0 = ti.n0 = ti.kb = ti.ph = 0;
         bool ok = true;
         if (lane == 0) {
           int q = 0, e = 0, r = 0;
-          if (locate_tile(P, group, s_pref, t, q, e, r)) {
+          if (locate_tile(P, s_pref, t, q, e, r)) {
             ti.prob = q;
             HMM_BY_PROB(q, decode_tile, P, P.p[q], e, r, ti);
-            t = atomicAdd(P.ticket + group, 1);  // next ticket, early
+            t = atomicAdd(P.ticket, 1);  // next ticket, early
             const Prob& pr = P.p[q];
             if (pr.wait_m) {
               ok = counter_wait(&pr.wait_m[ti.m0 / BM], pr.wait_unit, wc);
               if (ok && PAIR && !ti.ph)
                 ok = counter_wait(&pr.wait_m[ti.m0 / BM + 1], pr.wait_unit, wc);
-            } else if (pr.wait_e) {
-              ok = counter_wait(&pr.wait_e[ti.e], pr.wait_unit * mtiles_of(P, ti.e), wc);
             }
           }
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         // every lane leaves the loop with lane 0 (end marker below)
         ti.prob = __shfl_sync(0xffffffffu, ti.prob, 0);
-        ti.e = __shfl_sync(0xffffffffu, ti.e, 0);
-        ti.m0 = __shfl_sync(0xffffffffu, ti.m0, 0);
-        ti.n0 = __shfl_sync(0xffffffffu, ti.n0, 0);
-        ti.kb = __shfl_sync(0xffffffffu, ti.kb, 0);
-        ti.krow0 = __shfl_sync(0xffffffffu, ti.krow0, 0);
-        ti.ph = __shfl_sync(0xffffffffu, ti.ph, 0);
         bool got = false;
         if (lane == 0) got = mbar_wait<PAIR>(&ti_empty[ti_slot], ti_phase ^ 1u, wc);
         if (!__shfl_sync(0xffffffffu, got, 0)) break;
@@ -722,7 +653,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int q = 0; q < P.nprob; ++q) {
         tma_prefetch_desc(&maps.m[q][0]);
         tma_prefetch_desc(&maps.m[q][1]);
-        if (P.p[q].split) tma_prefetch_desc(&maps.m[q][2]);
       }
       uint32_t stage = 0, sphase = 0;
       int ti_slot = 0;
@@ -745,10 +675,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const Prob& pr = P.p[ti.prob];
         // the scheduler acquired this tile's ready counter (gpu scope) before
         // publishing it; order that with the async-proxy loads below
-        if (pr.wait_m || pr.wait_e) fence_proxy_async_global();
+        if (pr.wait_m) fence_proxy_async_global();
         const CUtensorMap* mp = maps.m[ti.prob];
         uint64_t* rec = (!PAIR || leader) ? trace_rec(P, lt) : nullptr;
         ++lt;
+        // the odd CTA's half of the last pair of an expert with an odd number
+        // of M tiles has no rows of A
+        const bool load_a = !PAIR || leader || !ti.ph;
         for (int kb = 0; kb < ti.kb; ++kb) {
           if (!mbar_wait(&empty[stage], sphase ^ 1u, wc)) {
             ok = false;
@@ -756,18 +689,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           if (rec && kb == 0) rec[2] = globaltimer_ns();
           uint8_t* sA = stages + stage * SBYTES;
-          if constexpr (PAIR) {
-            uint8_t* sB = sA + A_BYTES;
-            if (leader)
-              mbar_arrive_expect_tx(&full[stage], (ti.ph ? 1 : 2) * A_BYTES + 2 * PAIR_B_BYTES);
-            const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
-            HMM_BY_PROB(ti.prob, stage_boxes_pair, pr, ti, kb, &mp[0], &mp[1], sA, sB, bar, rank);
-          } else {
-            uint8_t* sB = sA + A_BYTES;
-            mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-            HMM_BY_PROB(ti.prob, load_stage, pr, ti, kb, &mp[0], &mp[1], &mp[2], sA, sB,
-                        &full[stage]);
-          }
+          const uint32_t full_cl = PAIR ? mapa_shared(smem_u32(&full[stage]), 0) : 0u;
+          HMM_BY_PROB_P(ti.prob, load_stage, pr, ti, kb, &mp[0], &mp[1], sA, sA + A_BYTES,
+                        &full[stage], full_cl, rank, load_a);
           ++issued;
           if (++stage == NST) {
             stage = 0;
@@ -805,7 +729,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (ti.prob < 0) break;
         uint64_t* rec = trace_rec(P, lt++);
-        if (ti.kb == 0) continue;
         if (!mbar_wait<PAIR>(&tempty[acc], acc_phase ^ 1u, wc)) break;
         tc_fence_after();
         if (rec) rec[4] = globaltimer_ns();
@@ -819,13 +742,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t a_base = smem_u32(stages + stage * SBYTES);
           const uint32_t b_base = a_base + A_BYTES;
-          if constexpr (PAIR) {
-            HMM_BY_PROB(ti.prob, mma_stage_pair, d_tmem, a_base, b_base, kb == 0);
+          HMM_BY_PROB_P(ti.prob, mma_stage, d_tmem, a_base, b_base, kb == 0);
+          if constexpr (PAIR)
             umma_commit_pair(&empty[stage], 0x3);
-          } else {
-            HMM_BY_PROB(ti.prob, mma_stage, d_tmem, a_base, b_base, kb == 0);
+          else
             umma_commit(&empty[stage]);
-          }
           if (++stage == NST) {
             stage = 0;
             sphase ^= 1u;
@@ -851,7 +772,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------- epilogue
     const int q = warp & 3;
     const int ch = (warp - 2) / 4;  // which warp of the lane quarter
-    const int row_in_tile = q * 32 + lane;
     float* xbuf = xbufs + (warp - 2) * (XBUF_BYTES / 4);
     const uint32_t tempty_cl[2] = {PAIR ? mapa_shared(smem_u32(&tempty[0]), 0) : 0u,
                                    PAIR ? mapa_shared(smem_u32(&tempty[1]), 0) : 0u};
@@ -877,10 +797,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // one warp of the (even) CTA reports
       uint64_t* rec = (warp == 2 && lane == 0 && leader) ? trace_rec(P, lt) : nullptr;
       ++lt;
-      if (ti.kb == 0) {
-        HMM_BY_PROB(ti.prob, epilogue_zero, pr, ti, row_in_tile, ch);
-        continue;
-      }
       if (lane == 0) got = mbar_wait(&tfull[acc], acc_phase, wc);
       __syncwarp();
       got = __shfl_sync(0xffffffffu, got, 0);
@@ -904,13 +820,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_arrive_cluster(tempty_cl[acc]);
       }
       if (rec) rec[7] = globaltimer_ns();
-      if (real && (pr.signal_m || pr.signal_e)) {
+      if (real && pr.signal_m) {
         fence_proxy_async_global();
         __syncwarp();
-        if (lane == 0) {
-          if (pr.signal_m) red_release_add(&pr.signal_m[ti.m0 / BM], 1);
-          if (pr.signal_e) red_release_add(&pr.signal_e[ti.e], 1);
-        }
+        if (lane == 0) red_release_add(&pr.signal_m[ti.m0 / BM], 1);
       }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
@@ -966,38 +879,27 @@ int map_w(const GemmEnv& env, CUtensorMap* m, const void* base, int64_t E, int64
   return encode(env, m, base, 3, dims, str, box);
 }
 
-template <bool PAIR, class C0, class C1, class C2, class C3>
+template <bool PAIR, class C0, class C1>
 int launch(const GemmEnv& env, Params& P, const Maps& maps, int64_t max_tiles, int kind) {
   if (max_tiles <= 0 || P.nprob == 0) return HMM_OK;
   if (env.trace && env.trace_which == kind) {
     P.trace = env.trace;
     P.trace_cap = env.trace_cap;
   }
-  auto kern = gmm_kernel<PAIR, C0, C1, C2, C3>;
+  auto kern = gmm_kernel<PAIR, C0, C1>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
       cudaSuccess)
     return HMM_ERR_CUDA;
-  int max_lag[2] = {-1, -1};
-  for (int q = 0; q < P.nprob; ++q)
-    max_lag[P.p[q].group] = std::max(max_lag[P.p[q].group], P.p[q].lag);
-  for (int g = 0; g < 2; ++g) {
-    P.steps[g] = max_lag[g] < 0 ? 0 : P.E + max_lag[g];
-    if (P.steps[g] > MAX_STEPS) return HMM_ERR_SHAPE;
-  }
-  int grid = static_cast<int>(std::min<int64_t>(env.num_sms, max_tiles));
-  if (max_lag[1] < 0) P.group_split = 0;
-  if (P.group_split > 0) {
-    // both groups need CTAs: the grid is every SM, the split inside it
-    grid = env.num_sms;
-    P.group_split = std::min(std::max(P.group_split, 1), grid - 1);
-  }
+  int max_lag = 0;
+  for (int q = 0; q < P.nprob; ++q) max_lag = std::max(max_lag, P.p[q].lag);
+  P.steps = P.E + max_lag;
+  if (P.steps > MAX_STEPS) return HMM_ERR_SHAPE;
   P.status = env.status;
   P.budget_ns = env.budget_ns;
   P.pair = PAIR ? 1 : 0;
   if constexpr (PAIR) {
     // clusters of two CTAs, as many as can be resident at once (the tile
     // dependencies inside the launch need every CTA running)
-    if (P.group_split > 0) return HMM_ERR_ARG;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -1018,6 +920,7 @@ int launch(const GemmEnv& env, Params& P, const Maps& maps, int64_t max_tiles, i
     cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
     return cudaLaunchKernelEx(&cfg, kern, P, maps) == cudaSuccess ? HMM_OK : HMM_ERR_CUDA;
   } else {
+    const int grid = static_cast<int>(std::min<int64_t>(env.num_sms, max_tiles));
     kern<<<grid, NUM_THREADS, SMEM_BYTES, env.stream>>>(P, maps);
     return cudaGetLastError() == cudaSuccess ? HMM_OK : HMM_ERR_CUDA;
   }
@@ -1025,16 +928,32 @@ int launch(const GemmEnv& env, Params& P, const Maps& maps, int64_t max_tiles, i
 
 }  // namespace
 
-using CfgGmm1 = Cfg<EPI_SWIGLU, false, true>;
-using CfgGmm2 = Cfg<EPI_STORE, false, true>;
-using CfgActGrad = Cfg<EPI_DSWIGLU, false, false>;
-using CfgInGrad = Cfg<EPI_STORE, false, false>;
-using CfgW2Grad = Cfg<EPI_STORE, true, true>;
-using CfgW1Grad = Cfg<EPI_STORE, true, true>;
+using CfgGmm1 = Cfg<EPI_SWIGLU, true>;     // A = x_perm, B = W1 (MN-major)
+using CfgGmm2 = Cfg<EPI_STORE, true>;      // A = a, B = W2 (MN-major)
+using CfgActGrad = Cfg<EPI_DSWIGLU, false>; // A = dy_perm, B = W2 viewed K-major
+using CfgInGrad = Cfg<EPI_STORE, false>;   // A = dH, B = W1 viewed K-major
+
+namespace {
+
+// Problems 2 and 3 (the shared expert, expert E of the padded rows) copy
+// problems 0 and 1 with their own weight maps.
+void add_shared(Params& P, Maps& maps, int E, const CUtensorMap& B0, const CUtensorMap& B1) {
+  for (int q = 0; q < 2; ++q) {
+    P.p[2 + q] = P.p[q];
+    P.p[2 + q].e_lo = E;
+    P.p[2 + q].e_hi = E + 1;
+    maps.m[2 + q][0] = maps.m[q][0];
+  }
+  maps.m[2][1] = B0;
+  maps.m[3][1] = B1;
+  P.nprob = 4;
+}
+
+}  // namespace
 
 int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
-                         const void* x_perm, const void* W1, const void* W2, void* a, float* h32,
-                         void* o, bool skip_ready_release) {
+                         const void* x_perm, const void* W1, const void* W2, const void* Ws1,
+                         const void* Ws2, void* a, float* h32, void* o, bool skip_ready_release) {
   const int64_t H = p.H, I = p.I, E = p.E, R = p.R;
   Maps maps;
   int rc = HMM_OK;
@@ -1042,14 +961,17 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
   rc |= map_w(env, &maps.m[0][1], W1, E, H, 2 * I, 64);  // W1 [E, H, 2I]: MN-major B
   rc |= map_act(env, &maps.m[1][0], a, R, I, BM);        // a [R, I], K = I
   rc |= map_w(env, &maps.m[1][1], W2, E, I, H, 64);      // W2 [E, I, H]: MN-major B
+  CUtensorMap s0, s1;
+  if (p.shared) {
+    rc |= map_w(env, &s0, Ws1, 1, H, 2 * I, 64);  // shared expert's [H, 2I], [I, H]
+    rc |= map_w(env, &s1, Ws2, 1, I, H, 64);
+  }
   if (rc != HMM_OK) return HMM_ERR_CUDA;
-  maps.m[0][2] = maps.m[0][0];
-  maps.m[1][2] = maps.m[1][0];
   Params P{};
   P.nprob = 2;
   P.poff = m.poff;
   P.counts = m.counts;
-  P.E = static_cast<int>(E);
+  P.E = static_cast<int>(p.Ex);
   P.ticket = c.tickets + 0;
   Prob& g1 = P.p[0];
   g1.K = static_cast<int>(H);
@@ -1060,6 +982,8 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
   g1.ld_out = I;
   g1.out2 = h32;
   g1.ld_out2 = 2 * I;
+  g1.e_lo = 0;
+  g1.e_hi = static_cast<int>(E);
   g1.signal_m = skip_ready_release ? nullptr : c.ready;
   Prob& g2 = P.p[1];
   g2.K = static_cast<int>(I);
@@ -1067,53 +991,47 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
   g2.n_tiles = static_cast<int>((H + BN - 1) / BN);
   g2.out = o;
   g2.ld_out = H;
+  g2.out_f32 = p.shared ? 1 : 0;  // fp32 rows for the y combine with the shared expert
+  g2.e_lo = 0;
+  g2.e_hi = static_cast<int>(E);
   // GMM2 after every GMM1 tile has been handed out: its ready waits then only
   // meet the last wave of GMM1 tiles
-  g2.lag = static_cast<int>(E);
+  g2.lag = static_cast<int>(p.Ex);
   g2.wait_m = c.ready;
   g2.wait_unit = EPI_WARPS * g1.n_tiles;  // every epilogue warp of every GMM1 tile of the M tile
+  if (p.shared) add_shared(P, maps, static_cast<int>(E), s0, s1);
   const int64_t max_tiles = p.max_mtiles * (g1.n_tiles + g2.n_tiles);
-  if (env.pair_rows)
-    return launch<true, CfgGmm1, CfgGmm2, CfgGmm2, CfgGmm2>(env, P, maps, max_tiles, 0);
-  return launch<false, CfgGmm1, CfgGmm2, CfgGmm2, CfgGmm2>(env, P, maps, max_tiles, 0);
+  if (env.pair_rows) return launch<true, CfgGmm1, CfgGmm2>(env, P, maps, max_tiles, 0);
+  return launch<false, CfgGmm1, CfgGmm2>(env, P, maps, max_tiles, 0);
 }
 
-int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
-                          const void* x_perm, const void* dy_perm, const float* wperm,
-                          const float* h32, const void* W1, const void* W2, void* dH,
-                          void* dH_lo, void* wa, void* wa_lo, float* dwp, void* dx_perm,
-                          void* dW1, void* dW2, int part) {
+int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
+                           const void* dy_perm, const float* wperm, const float* h32,
+                           const void* W1, const void* W2, const void* Ws1, const void* Ws2,
+                           void* dH, void* dH_lo, void* wa, void* wa_lo, float* dwp,
+                           void* dx_perm) {
   const int64_t H = p.H, I = p.I, E = p.E, R = p.R;
   Maps maps;
   int rc = HMM_OK;
-  // data gradients on CTA pairs: each CTA loads 128 of the 256 B rows
-  const bool pair = env.pair_rows && env.bwd_data_sms <= 0;
-  const uint32_t b_rows = pair ? BN / 2 : BN;
-  if (part == 1) {  // (part 2 needs neither W1 nor W2)
-    // act_grad: G = dy_perm . W2^T   (B = W2 [E, I, H] read K-major, N = I)
-    rc |= map_act(env, &maps.m[0][0], dy_perm, R, H, BM);
-    rc |= map_w(env, &maps.m[0][1], W2, E, I, H, b_rows);
-    // input-grad: dX_perm = dH . W1^T (B = W1 [E, H, 2I] read K-major, N = H)
-    rc |= map_act(env, &maps.m[1][0], dH, R, 2 * I, BM);
-    rc |= map_w(env, &maps.m[1][1], W1, E, H, 2 * I, b_rows);
-    maps.m[0][2] = maps.m[0][0];
-    maps.m[1][2] = maps.m[1][0];
+  // on CTA pairs each CTA loads 128 of the 256 B rows
+  const uint32_t b_rows = env.pair_rows ? BN / 2 : BN;
+  // act_grad: G = dy_perm . W2^T   (B = W2 [E, I, H] read K-major, N = I)
+  rc |= map_act(env, &maps.m[0][0], dy_perm, R, H, BM);
+  rc |= map_w(env, &maps.m[0][1], W2, E, I, H, b_rows);
+  // input-grad: dX_perm = dH . W1^T (B = W1 [E, H, 2I] read K-major, N = H)
+  rc |= map_act(env, &maps.m[1][0], dH, R, 2 * I, BM);
+  rc |= map_w(env, &maps.m[1][1], W1, E, H, 2 * I, b_rows);
+  CUtensorMap s0, s1;
+  if (p.shared) {
+    rc |= map_w(env, &s0, Ws2, 1, I, H, b_rows);
+    rc |= map_w(env, &s1, Ws1, 1, H, 2 * I, b_rows);
   }
-  // W2Grad: dW2[e] = (wa_hi + wa_lo)^T . dy_perm    [I, rows] x [rows, H]
-  rc |= map_act(env, &maps.m[2][0], wa, R, I, 64);
-  rc |= map_act(env, &maps.m[2][1], dy_perm, R, H, 64);
-  rc |= map_act(env, &maps.m[2][2], wa_lo, R, I, 64);
-  // W1Grad: dW1[e] = x_perm^T . (dH_hi + dH_lo)     [H, rows] x [rows, 2I]
-  rc |= map_act(env, &maps.m[3][0], x_perm, R, H, 64);
-  rc |= map_act(env, &maps.m[3][1], dH, R, 2 * I, 64);
-  rc |= map_act(env, &maps.m[3][2], dH_lo, R, 2 * I, 64);
   if (rc != HMM_OK) return HMM_ERR_CUDA;
-  const CUtensorMap map_w2[3] = {maps.m[2][0], maps.m[2][1], maps.m[2][2]};
-  const CUtensorMap map_w1[3] = {maps.m[3][0], maps.m[3][1], maps.m[3][2]};
   Params P{};
+  P.nprob = 2;
   P.poff = m.poff;
   P.counts = m.counts;
-  P.E = static_cast<int>(E);
+  P.E = static_cast<int>(p.Ex);
   P.ticket = c.tickets + 1;
   Prob& ag = P.p[0];
   ag.K = static_cast<int>(H);
@@ -1132,86 +1050,26 @@ int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtr
   ag.aux = h32;
   ag.ld_aux = 2 * I;
   ag.rowscale = wperm;
+  ag.e_lo = 0;
+  ag.e_hi = static_cast<int>(E);
   ag.signal_m = c.ready;
-  ag.signal_e = c.eready;
   Prob& ig = P.p[1];
   ig.K = static_cast<int>(2 * I);
   ig.N = static_cast<int>(H);
   ig.n_tiles = static_cast<int>((H + BN - 1) / BN);
   ig.out = dx_perm;
   ig.ld_out = H;
+  ig.out_f32 = p.shared ? 1 : 0;  // fp32 rows for the dX combine with the shared expert
+  ig.e_lo = 0;
+  ig.e_hi = static_cast<int>(E);
   ig.wait_m = c.ready;
   ig.wait_unit = EPI_WARPS * ag.n_tiles;
-  Prob w2{}, w1{};
-  w2.M = static_cast<int>(I);
-  w2.N = static_cast<int>(H);
-  w2.m_tiles = static_cast<int>((I + BM - 1) / BM);
-  w2.n_tiles = static_cast<int>((H + BN - 1) / BN);
-  w2.out = dW2;
-  w2.ld_out = H;
-  w2.out_estride = I * H;
-  w2.split = 1;
-  w1.M = static_cast<int>(H);
-  w1.N = static_cast<int>(2 * I);
-  w1.m_tiles = static_cast<int>((H + BM - 1) / BM);
-  w1.n_tiles = static_cast<int>((2 * I + BN - 1) / BN);
-  w1.out = dW1;
-  w1.ld_out = 2 * I;
-  w1.out_estride = H * 2 * I;
-  w1.split = 2;
-  for (Prob* w : {&w2, &w1}) {
-    w->wgrad = 1;
-    w->wait_e = c.eready;
-    w->wait_unit = EPI_WARPS * ag.n_tiles;  // every act_grad tile of every M tile of the expert
-  }
-  ig.lag = static_cast<int>(E);  // input-grad after every act_grad tile is handed out
+  ig.lag = static_cast<int>(p.Ex);  // input-grad after every act_grad tile is handed out
+  if (p.shared) add_shared(P, maps, static_cast<int>(E), s0, s1);
   const int64_t data_tiles = p.max_mtiles * (ag.n_tiles + ig.n_tiles);
-  const int64_t w_tiles = (dW2 ? E * w2.m_tiles * w2.n_tiles : 0) +
-                          (dW1 ? E * w1.m_tiles * w1.n_tiles : 0);
-  const int nw = (dW2 ? 1 : 0) + (dW1 ? 1 : 0);
-  if (!dW2) w2.m_tiles = 0;  // fixed problem slots: W2Grad, then W1Grad
-  if (!dW1) w1.m_tiles = 0;
-  auto add_wgrad = [&](Params& Q, int first, int group) {
-    Q.p[first] = w2;
-    Q.p[first].group = group;
-    Q.p[first + 1] = w1;
-    Q.p[first + 1].group = group;
-    for (int j = 0; j < 3; ++j) {
-      maps.m[first][j] = map_w2[j];
-      maps.m[first + 1][j] = map_w1[j];
-    }
-    Q.nprob = first + 2;
-  };
-  if (env.bwd_data_sms > 0 && nw > 0) {
-    // Two CTA groups in one launch: env.bwd_data_sms SMs run act_grad and
-    // input-grad, the others the weight gradients, trailing act_grad expert by
-    // expert.  (All of it is part 1.)
-    if (part != 1) return HMM_OK;
-    add_wgrad(P, 2, 1);
-    P.group_split = env.bwd_data_sms;
-    return launch<false, CfgActGrad, CfgInGrad, CfgW2Grad, CfgW1Grad>(env, P, maps,
-                                                                     data_tiles + w_tiles, 1);
-  }
-  // Default: two launches.  The data gradients first; then the weight
-  // gradients, whose per-expert waits are already satisfied: on CTA pairs
-  // (2-SM MMAs) unless disabled, else on single CTAs.
-  P.nprob = 2;
-  if (part == 1)
-    return pair ? launch<true, CfgActGrad, CfgInGrad, CfgInGrad, CfgInGrad>(env, P, maps,
-                                                                            data_tiles, 1)
-                : launch<false, CfgActGrad, CfgInGrad, CfgInGrad, CfgInGrad>(env, P, maps,
-                                                                             data_tiles, 1);
-  if (nw == 0) return HMM_OK;
-  if (env.pair_wgrad)
-    return launch_wgrad_pair(env, p, m, x_perm, dy_perm, dH, dH_lo, wa, wa_lo, dW1, dW2);
-  Params W{};
-  W.poff = m.poff;
-  W.counts = m.counts;
-  W.E = static_cast<int>(E);
-  W.ticket = c.tickets + 3;
-  add_wgrad(W, 0, 0);
-  for (int q = 0; q < W.nprob; ++q) W.p[q].wait_e = nullptr;  // act_grad has completed
-  return launch<false, CfgW2Grad, CfgW1Grad, CfgW1Grad, CfgW1Grad>(env, W, maps, w_tiles, 2);
+  if (env.pair_rows)
+    return launch<true, CfgActGrad, CfgInGrad>(env, P, maps, data_tiles, 1);
+  return launch<false, CfgActGrad, CfgInGrad>(env, P, maps, data_tiles, 1);
 }
 
 }  // namespace hmm

@@ -3,6 +3,8 @@
 // [HyperMegaMoE §2.2 W2Grad, W1Grad]
 //   dW2[e] = (wa_hi + wa_lo)^T . dy_perm      [I, rows of e] x [rows of e, H]
 //   dW1[e] = x_perm^T . (dH_hi + dH_lo)       [H, rows of e] x [rows of e, 2I]
+// for the routed experts and, with the optional shared expert [HyperMegaMoE
+// §6.1], for the shared expert (expert E of the padded rows, every token).
 // (the rounded operand is read as a bf16 hi + lo pair: every 64-row K step
 // stages A, B and the low half of the split operand together and issues two
 // MMAs on them, so the unsplit operand is loaded once).
@@ -44,6 +46,7 @@ constexpr uint32_t P_TMEM_COLS = 512;
 constexpr uint32_t IDESC_PAIR = idesc_bf16_f32(256, 256, 1, 1);  // both MN-major
 
 struct PairProb {
+  int e_lo, n_e; // experts e_lo .. e_lo + n_e - 1 of the padded rows
   int M, N;      // output [M, N] per expert
   int mpairs;    // 256-row tile pairs along M
   int n_tiles;   // 256-column tiles along N
@@ -54,7 +57,7 @@ struct PairProb {
 };
 
 struct PairParams {
-  PairProb p[2];
+  PairProb p[4];
   int nprob;
   const int32_t* poff;
   const int32_t* counts;
@@ -66,7 +69,7 @@ struct PairParams {
 };
 
 struct PairMaps {
-  CUtensorMap m[2][3];  // A, B, low half of the split operand
+  CUtensorMap m[4][3];  // A, B, low half of the split operand
 };
 
 struct PairTile {
@@ -74,7 +77,7 @@ struct PairTile {
 };
 
 __device__ __forceinline__ int pair_tiles(const PairParams& P, int q) {
-  return P.E * P.p[q].mpairs * P.p[q].n_tiles;
+  return P.p[q].n_e * P.p[q].mpairs * P.p[q].n_tiles;
 }
 
 __device__ __forceinline__ void pair_decode(const PairParams& P, int u, PairTile& t) {
@@ -86,8 +89,9 @@ __device__ __forceinline__ void pair_decode(const PairParams& P, int u, PairTile
   const PairProb& pr = P.p[q];
   const int per = pr.mpairs * pr.n_tiles;
   t.prob = q;
-  t.e = u / per;
-  const int r = u - t.e * per;
+  const int le = u / per;  // expert index inside the problem
+  t.e = pr.e_lo + le;
+  const int r = u - le * per;
   t.m0 = (r / pr.n_tiles) * 256;
   t.n0 = (r % pr.n_tiles) * 256;
   t.krow0 = P.poff[t.e];
@@ -298,7 +302,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       uint64_t* rec = (warp == 2 && lane == 0) ? pair_rec(P, leader, lt) : nullptr;
       ++lt;
       const int64_t row = t.m0 + 128 * static_cast<int>(rank) + row_in_half;
-      __nv_bfloat16* orow = pr.out + static_cast<int64_t>(t.e) * pr.out_estride + row * pr.ld_out;
+      __nv_bfloat16* orow =
+          pr.out + static_cast<int64_t>(t.e - pr.e_lo) * pr.out_estride + row * pr.ld_out;
       if (t.kb == 0) {
         // an expert with no rows: its weight gradient is exactly zero
         if (row < pr.M)
@@ -315,7 +320,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + acc * 256;
       // this lane's rows after the transposition: rl + 8k
       const int64_t rl = t.m0 + 128 * static_cast<int>(rank) + q4 * 32 + (lane >> 2);
-      __nv_bfloat16* obase = pr.out + static_cast<int64_t>(t.e) * pr.out_estride;
+      __nv_bfloat16* obase = pr.out + static_cast<int64_t>(t.e - pr.e_lo) * pr.out_estride;
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         const int col = t.n0 + c * 32;
@@ -371,9 +376,9 @@ int encode2d(const GemmEnv& env, CUtensorMap* m, const void* base, int64_t rows,
 
 int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, const void* x_perm,
                       const void* dy_perm, const void* dH, const void* dH_lo, const void* wa,
-                      const void* wa_lo, void* dW1, void* dW2) {
+                      const void* wa_lo, void* dW1, void* dW2, void* dWs1, void* dWs2) {
   const int64_t H = p.H, I = p.I, E = p.E, R = p.R;
-  if (!dW1 && !dW2) return HMM_OK;
+  if (!dW1 && !dW2 && !dWs1 && !dWs2) return HMM_OK;
   PairMaps maps;
   PairParams P{};
   P.poff = m.poff;
@@ -387,38 +392,48 @@ int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, const void*
   }
   int rc = HMM_OK;
   int q = 0;
-  if (dW2) {
+  // dW2 of experts [e_lo, e_lo + n_e): (wa_hi + wa_lo)^T . dy_perm
+  auto add_w2 = [&](void* out, int e_lo, int n_e) {
     rc |= encode2d(env, &maps.m[q][0], wa, R, I);
     rc |= encode2d(env, &maps.m[q][1], dy_perm, R, H);
     rc |= encode2d(env, &maps.m[q][2], wa_lo, R, I);
     PairProb& w = P.p[q++];
+    w.e_lo = e_lo;
+    w.n_e = n_e;
     w.M = static_cast<int>(I);
     w.N = static_cast<int>(H);
     w.mpairs = static_cast<int>((I + 255) / 256);
     w.n_tiles = static_cast<int>((H + 255) / 256);
     w.split = 1;
-    w.out = static_cast<__nv_bfloat16*>(dW2);
+    w.out = static_cast<__nv_bfloat16*>(out);
     w.ld_out = H;
     w.out_estride = I * H;
-  }
-  if (dW1) {
+  };
+  // dW1 of experts [e_lo, e_lo + n_e): x_perm^T . (dH_hi + dH_lo)
+  auto add_w1 = [&](void* out, int e_lo, int n_e) {
     rc |= encode2d(env, &maps.m[q][0], x_perm, R, H);
     rc |= encode2d(env, &maps.m[q][1], dH, R, 2 * I);
     rc |= encode2d(env, &maps.m[q][2], dH_lo, R, 2 * I);
     PairProb& w = P.p[q++];
+    w.e_lo = e_lo;
+    w.n_e = n_e;
     w.M = static_cast<int>(H);
     w.N = static_cast<int>(2 * I);
     w.mpairs = static_cast<int>((H + 255) / 256);
     w.n_tiles = static_cast<int>((2 * I + 255) / 256);
     w.split = 2;
-    w.out = static_cast<__nv_bfloat16*>(dW1);
+    w.out = static_cast<__nv_bfloat16*>(out);
     w.ld_out = 2 * I;
     w.out_estride = H * 2 * I;
-  }
+  };
+  if (dW2) add_w2(dW2, 0, static_cast<int>(E));
+  if (dW1) add_w1(dW1, 0, static_cast<int>(E));
+  if (p.shared && dWs2) add_w2(dWs2, static_cast<int>(E), 1);
+  if (p.shared && dWs1) add_w1(dWs1, static_cast<int>(E), 1);
   if (rc != HMM_OK) return HMM_ERR_CUDA;
   P.nprob = q;
   int64_t total = 0;
-  for (int i = 0; i < q; ++i) total += E * P.p[i].mpairs * P.p[i].n_tiles;
+  for (int i = 0; i < q; ++i) total += int64_t(P.p[i].n_e) * P.p[i].mpairs * P.p[i].n_tiles;
   if (total <= 0) return HMM_OK;
   if (cudaFuncSetAttribute(wgrad_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            P_SMEM) != cudaSuccess)

@@ -14,6 +14,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <utility>
 #include <vector>
 
 #include "hmm_internal.h"
@@ -47,8 +48,6 @@ struct hmm_ctx {
   uint64_t budget_ns = 2000000000ull;
   int inject_skip_ready = 0;
   int profile = 0;
-  int bwd_data_sms = 0;
-  int pair_wgrad = 1;
   int pair_rows = 2;  // 0 off, 1 on, 2 automatic
   uint64_t* trace = nullptr;
   size_t trace_bytes = 0;
@@ -112,9 +111,14 @@ int make_plan(const hmm_shape* s, bool training, Plan* p) {
   p->E = s->E;
   p->K = s->K;
   p->TK = s->T * s->K;
+  p->shared = s->shared;
+  p->Ex = p->E + p->shared;
   p->training = training;
   const int64_t TK = p->TK;
-  int64_t R = TK == 0 ? 0 : TK + std::min<int64_t>(p->E, TK) * (BM - 1);
+  // padded rows: the routed slots and the shared expert's T rows, each
+  // expert's segment rounded up to BM
+  const int64_t rows = TK == 0 ? 0 : TK + p->shared * p->T;
+  int64_t R = rows == 0 ? 0 : rows + std::min<int64_t>(p->Ex, rows) * (BM - 1);
   R = (R + BM - 1) / BM * BM;
   p->R = R;
   p->max_mtiles = R / BM;
@@ -123,9 +127,9 @@ int make_plan(const hmm_shape* s, bool training, Plan* p) {
   p->dwp_ld = p->nt_dswiglu;  // one d_w partial per act_grad N tile and row
   const size_t A = 256;
   size_t o = 0;
-  p->off_counts = o;    o = align_up(o + 4 * p->E, A);
-  p->off_offsets = o;   o = align_up(o + 4 * (p->E + 1), A);
-  p->off_poff = o;      o = align_up(o + 4 * (p->E + 1), A);
+  p->off_counts = o;    o = align_up(o + 4 * p->Ex, A);
+  p->off_offsets = o;   o = align_up(o + 4 * (p->Ex + 1), A);
+  p->off_poff = o;      o = align_up(o + 4 * (p->Ex + 1), A);
   p->off_slot2prow = o; o = align_up(o + 4 * TK, A);
   p->off_prow2slot = o; o = align_up(o + 4 * R, A);
   p->meta_bytes = o;
@@ -134,13 +138,15 @@ int make_plan(const hmm_shape* s, bool training, Plan* p) {
   p->off_tickets = o;
   p->off_ready = o + 4 * NUM_TICKETS;  // tickets, ready, eready contiguous (zeroed together)
   p->off_eready = p->off_ready + 4 * p->max_mtiles;
-  p->ctrl_zero_count = NUM_TICKETS + p->max_mtiles + p->E;
-  o = align_up(p->off_eready + 4 * p->E, A);
+  p->ctrl_zero_count = NUM_TICKETS + p->max_mtiles + p->Ex;
+  o = align_up(p->off_eready + 4 * p->Ex, A);
   p->ctrl_bytes = o;
   const size_t xperm = align_up(static_cast<size_t>(R) * p->H * 2, A);
   const size_t hbytes = align_up(static_cast<size_t>(R) * 2 * p->I * 4, A);
   const size_t abytes = align_up(static_cast<size_t>(R) * p->I * 2, A);
-  const size_t obytes = align_up(static_cast<size_t>(R) * p->H * 2, A);
+  // o: fp32 with the shared expert (its unweighted term in the y combine),
+  // else bf16
+  const size_t obytes = align_up(static_cast<size_t>(R) * p->H * (p->shared ? 4 : 2), A);
   if (training) {
     p->sv_meta = 0;
     p->sv_xperm = p->meta_bytes;
@@ -167,7 +173,8 @@ int make_plan(const hmm_shape* s, bool training, Plan* p) {
   p->bw_dhlo = o;    o = align_up(o + static_cast<size_t>(R) * 2 * p->I * 2, A);
   p->bw_wa = o;      o = align_up(o + static_cast<size_t>(R) * p->I * 2, A);
   p->bw_walo = o;    o = align_up(o + static_cast<size_t>(R) * p->I * 2, A);
-  p->bw_dxperm = o;  o = align_up(o + static_cast<size_t>(R) * p->H * 2, A);
+  // dX_perm: fp32 with the shared expert (see the dX combine), else bf16
+  p->bw_dxperm = o;  o = align_up(o + static_cast<size_t>(R) * p->H * (p->shared ? 4 : 2), A);
   p->bw_dwp = o;     o = align_up(o + static_cast<size_t>(R) * p->dwp_ld * 4, A);
   p->bwd_ws_bytes = o;
   return HMM_OK;
@@ -204,15 +211,16 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int check_shape(const hmm_shape* s) {
   if (!s) return HMM_ERR_ARG;
-  if (s->reserved != 0) return HMM_ERR_ARG;
+  if (s->shared != 0 && s->shared != 1) return HMM_ERR_ARG;
   if (s->weights_dtype != HMM_DTYPE_BF16 && s->weights_dtype != HMM_DTYPE_F32)
     return HMM_ERR_DTYPE;
   if (s->T < 0 || s->H <= 0 || s->I <= 0 || s->E <= 0 || s->K <= 0) return HMM_ERR_SHAPE;
-  if (s->E > MAX_E || s->K > 32) return HMM_ERR_SHAPE;
+  // the shared expert is one more expert and, in the dispatch, one more slot
+  if (s->E + s->shared > MAX_E || s->K + s->shared > 32) return HMM_ERR_SHAPE;
   if (s->H > (1 << 20) || s->I > (1 << 20) || s->T > (int64_t(1) << 31)) return HMM_ERR_SHAPE;
   if (s->H % 8 != 0 || s->I % 8 != 0) return HMM_ERR_LAYOUT;
-  const int64_t TK = s->T * s->K;
-  const int64_t R = TK + std::min<int64_t>(s->E, TK) * (BM - 1) + BM;
+  const int64_t TK = s->T * (s->K + s->shared);
+  const int64_t R = TK + std::min<int64_t>(s->E + s->shared, TK) * (BM - 1) + BM;
   if (R >= (int64_t(1) << 31) - 1) return HMM_ERR_SHAPE;
   return HMM_OK;
 }
@@ -233,8 +241,6 @@ GemmEnv env_of(hmm_ctx* ctx, const Plan& p, cudaStream_t st) {
   GemmEnv e;
   e.encode = ctx->encode;
   e.num_sms = ctx->num_sms;
-  e.bwd_data_sms = ctx->bwd_data_sms;
-  e.pair_wgrad = ctx->pair_wgrad;
   // pairs pay off when most experts have two or more 128-row tiles
   e.pair_rows = ctx->pair_rows == 2 ? (p.TK >= 2 * BM * p.E ? 1 : 0) : ctx->pair_rows;
   e.trace = ctx->trace;
@@ -344,16 +350,9 @@ int hmm_set_option(hmm_ctx* ctx, int option, int64_t value) {
     case HMM_OPT_PROFILE:
       ctx->profile = value != 0;
       return HMM_OK;
-    case HMM_OPT_PAIR_WGRAD:
-      ctx->pair_wgrad = value != 0;
-      return HMM_OK;
     case HMM_OPT_PAIR_ROWS:
       if (value < 0 || value > 2) return HMM_ERR_ARG;
       ctx->pair_rows = static_cast<int>(value);
-      return HMM_OK;
-    case HMM_OPT_BWD_DATA_SMS:
-      if (value < 0 || value >= ctx->num_sms) return HMM_ERR_ARG;
-      ctx->bwd_data_sms = static_cast<int>(value);
       return HMM_OK;
     default:
       return HMM_ERR_ARG;
@@ -376,6 +375,8 @@ int hmm_route(hmm_ctx* ctx, const hmm_shape* shape, const int32_t* topk_ids, int
               int32_t* offsets, int32_t* slot2row, int32_t* row2slot, void* workspace,
               size_t workspace_bytes, void* stream) {
   if (!ctx) return HMM_ERR_ARG;
+  // routing of the routed experts only: a shape with the shared expert is refused
+  if (shape && shape->shared != 0) return HMM_ERR_ARG;
   int rc = check_shape(shape);
   if (rc != HMM_OK) return rc;
   Plan p;
@@ -399,10 +400,15 @@ int hmm_route(hmm_ctx* ctx, const hmm_shape* shape, const int32_t* topk_ids, int
   return HMM_OK;
 }
 
-int hmm_forward(hmm_ctx* ctx, const hmm_shape* shape, const void* x, const int32_t* topk_ids,
-                const void* topk_weights, const void* up_proj_weight,
-                const void* down_proj_weight, void* y, void* saved, size_t saved_bytes,
-                void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+// hmm_forward and hmm_forward_shared (Ws1, Ws2: the shared expert's weights,
+// exactly when shape->shared).
+int forward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* x, const int32_t* topk_ids,
+                 const void* topk_weights, const void* up_proj_weight,
+                 const void* down_proj_weight, const void* Ws1, const void* Ws2, void* y,
+                 void* saved, size_t saved_bytes, void* workspace, size_t workspace_bytes,
+                 void* stream) {
   if (!ctx) return HMM_ERR_ARG;
   int rc = check_shape(shape);
   if (rc != HMM_OK) return rc;
@@ -410,13 +416,13 @@ int hmm_forward(hmm_ctx* ctx, const hmm_shape* shape, const void* x, const int32
   Plan p;
   make_plan(shape, training, &p);
   if (p.TK > 0 && (!x || !topk_ids || !topk_weights || !up_proj_weight || !down_proj_weight ||
-                   !y || !workspace))
+                   !y || !workspace || (p.shared && (!Ws1 || !Ws2))))
     return HMM_ERR_ARG;
   if (p.TK == 0) return HMM_OK;
   for (const void* ptr : {x, static_cast<const void*>(topk_ids), topk_weights, up_proj_weight,
                           down_proj_weight, static_cast<const void*>(y),
-                          static_cast<const void*>(workspace)})
-    if (!aligned16(ptr)) return HMM_ERR_LAYOUT;
+                          static_cast<const void*>(workspace), Ws1, Ws2})
+    if (ptr && !aligned16(ptr)) return HMM_ERR_LAYOUT;
   if (training && !aligned16(saved)) return HMM_ERR_LAYOUT;
   if (workspace_bytes < p.fwd_ws_bytes) return HMM_ERR_CAPACITY;
   if (training && saved_bytes < p.saved_bytes) return HMM_ERR_CAPACITY;
@@ -451,11 +457,34 @@ int hmm_forward(hmm_ctx* ctx, const hmm_shape* shape, const void* x, const int32
   {
     PhaseScope ps(ctx, PH_GEMM_FWD, st);
     rc = launch_forward_gemms(env_of(ctx, p, st), p, m, c, x_perm, up_proj_weight, down_proj_weight,
-                              a, h32, o, inject);
+                              Ws1, Ws2, a, h32, o, inject);
   }
   if (rc != HMM_OK) return rc;
   PhaseScope ps(ctx, PH_COMBINE_Y, st);
   return cuda_rc(launch_combine_y(p, o, topk_weights, shape->weights_dtype, m, y, st));
+}
+
+}  // namespace
+
+int hmm_forward(hmm_ctx* ctx, const hmm_shape* shape, const void* x, const int32_t* topk_ids,
+                const void* topk_weights, const void* up_proj_weight,
+                const void* down_proj_weight, void* y, void* saved, size_t saved_bytes,
+                void* workspace, size_t workspace_bytes, void* stream) {
+  if (shape && shape->shared != 0) return HMM_ERR_ARG;  // hmm_forward_shared
+  return forward_impl(ctx, shape, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight,
+                      nullptr, nullptr, y, saved, saved_bytes, workspace, workspace_bytes, stream);
+}
+
+int hmm_forward_shared(hmm_ctx* ctx, const hmm_shape* shape, const void* x,
+                       const int32_t* topk_ids, const void* topk_weights,
+                       const void* up_proj_weight, const void* down_proj_weight,
+                       const void* shared_up_proj_weight, const void* shared_down_proj_weight,
+                       void* y, void* saved, size_t saved_bytes, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (!shape || shape->shared != 1) return HMM_ERR_ARG;
+  return forward_impl(ctx, shape, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight,
+                      shared_up_proj_weight, shared_down_proj_weight, y, saved, saved_bytes,
+                      workspace, workspace_bytes, stream);
 }
 
 namespace {
@@ -467,13 +496,17 @@ enum BackwardMode { BWD_FULL = 0, BWD_DX = 1, BWD_DW = 2 };
 // bf16 hi + lo) in the workspace; BWD_DW runs only the weight gradients from
 // them.
 int backward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const void* topk_weights,
-                  const void* up_proj_weight, const void* down_proj_weight, const void* saved,
-                  size_t saved_bytes, void* dx, void* d_up_proj_weight, void* d_down_proj_weight,
+                  const void* up_proj_weight, const void* down_proj_weight, const void* Ws1,
+                  const void* Ws2, const void* saved, size_t saved_bytes, void* dx,
+                  void* d_up_proj_weight, void* d_down_proj_weight, void* dWs1, void* dWs2,
                   void* d_topk_weights, void* workspace, size_t workspace_bytes, void* stream,
                   BackwardMode mode) {
   if (!ctx) return HMM_ERR_ARG;
   int rc = check_shape(shape);
   if (rc != HMM_OK) return rc;
+  // the split entry points serve layers without a shared expert
+  if (mode != BWD_FULL && shape->shared) return HMM_ERR_ARG;
+  if (!shape->shared) dWs1 = dWs2 = nullptr;
   if (mode == BWD_DX) d_up_proj_weight = d_down_proj_weight = nullptr;
   if (mode == BWD_DW) dx = d_topk_weights = nullptr;
   Plan p;
@@ -483,24 +516,27 @@ int backward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const vo
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (p.TK == 0) {
     // no token: every weight gradient is exactly zero
-    if (d_up_proj_weight) {
-      if (!aligned16(d_up_proj_weight)) return HMM_ERR_LAYOUT;
-      rc = cuda_rc(cudaMemsetAsync(d_up_proj_weight, 0, 2 * p.E * p.H * 2 * p.I, st));
+    const size_t up = size_t(2) * p.H * 2 * p.I, down = size_t(2) * p.I * p.H;
+    for (auto [ptr, bytes] : {std::pair<void*, size_t>{d_up_proj_weight, p.E * up},
+                              std::pair<void*, size_t>{d_down_proj_weight, p.E * down},
+                              std::pair<void*, size_t>{dWs1, up},
+                              std::pair<void*, size_t>{dWs2, down}}) {
+      if (!ptr) continue;
+      if (!aligned16(ptr)) return HMM_ERR_LAYOUT;
+      rc = cuda_rc(cudaMemsetAsync(ptr, 0, bytes, st));
       if (rc != HMM_OK) return rc;
-    }
-    if (d_down_proj_weight) {
-      if (!aligned16(d_down_proj_weight)) return HMM_ERR_LAYOUT;
-      rc = cuda_rc(cudaMemsetAsync(d_down_proj_weight, 0, 2 * p.E * p.I * p.H, st));
     }
     return rc;
   }
   if (!saved || !workspace) return HMM_ERR_ARG;
   if (mode != BWD_DW && (!dy || !topk_weights || !up_proj_weight || !down_proj_weight))
     return HMM_ERR_ARG;
-  for (const void* ptr : {dy, topk_weights, up_proj_weight, down_proj_weight, saved,
+  if (p.shared && (!Ws1 || !Ws2)) return HMM_ERR_ARG;
+  for (const void* ptr : {dy, topk_weights, up_proj_weight, down_proj_weight, Ws1, Ws2, saved,
                           static_cast<const void*>(workspace), static_cast<const void*>(dx),
                           static_cast<const void*>(d_up_proj_weight),
                           static_cast<const void*>(d_down_proj_weight),
+                          static_cast<const void*>(dWs1), static_cast<const void*>(dWs2),
                           static_cast<const void*>(d_topk_weights)})
     if (ptr && !aligned16(ptr)) return HMM_ERR_LAYOUT;
   if (saved_bytes < p.saved_bytes) return HMM_ERR_CAPACITY;
@@ -519,19 +555,16 @@ int backward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const vo
   void* wa_lo = ws + p.bw_walo;
   void* dx_perm = ws + p.bw_dxperm;
   float* dwp = reinterpret_cast<float*>(ws + p.bw_dwp);
-  GemmEnv env = env_of(ctx, p, st);
-  // the deferred weight gradients read what a two-launch data phase left
-  if (mode == BWD_DW) env.bwd_data_sms = 0;
-  auto gemms = [&](int part) {
-    return launch_backward_gemms(env, p, m, c, x_perm, dy_perm, wperm, h32, up_proj_weight,
-                                 down_proj_weight, dH, dH_lo, wa, wa_lo, dwp, dx_perm,
-                                 d_up_proj_weight, d_down_proj_weight, part);
+  const GemmEnv env = env_of(ctx, p, st);
+  auto weight_gemms = [&]() {
+    return launch_wgrad_pair(env, p, m, x_perm, dy_perm, dH, dH_lo, wa, wa_lo, d_up_proj_weight,
+                             d_down_proj_weight, dWs1, dWs2);
   };
-  const bool weights = (d_up_proj_weight || d_down_proj_weight) && env.bwd_data_sms == 0;
+  const bool weights = d_up_proj_weight || d_down_proj_weight || dWs1 || dWs2;
   if (mode == BWD_DW) {
     if (!weights) return HMM_OK;
     PhaseScope ps(ctx, PH_GEMM_BWD_WEIGHT, st);
-    return gemms(2);
+    return weight_gemms();
   }
 
   {
@@ -542,7 +575,8 @@ int backward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const vo
   if (rc != HMM_OK) return rc;
   {
     PhaseScope ps(ctx, PH_GEMM_BWD_DATA, st);
-    rc = gemms(1);
+    rc = launch_data_grad_gemms(env, p, m, c, dy_perm, wperm, h32, up_proj_weight,
+                                down_proj_weight, Ws1, Ws2, dH, dH_lo, wa, wa_lo, dwp, dx_perm);
   }
   if (rc != HMM_OK) return rc;
   // dx and d_topk_weights need only part 1: combine them on the side stream
@@ -564,7 +598,7 @@ int backward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const vo
   int r2 = rc;
   if (rc == HMM_OK && weights) {
     PhaseScope ps(ctx, PH_GEMM_BWD_WEIGHT, st);
-    r2 = gemms(2);
+    r2 = weight_gemms();
   }
   if (combine) {
     const int rw = cuda_rc(cudaStreamWaitEvent(st, ctx->join, 0));
@@ -580,26 +614,44 @@ int hmm_backward(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const voi
                  const void* up_proj_weight, const void* down_proj_weight, const void* saved,
                  size_t saved_bytes, void* dx, void* d_up_proj_weight, void* d_down_proj_weight,
                  void* d_topk_weights, void* workspace, size_t workspace_bytes, void* stream) {
-  return backward_impl(ctx, shape, dy, topk_weights, up_proj_weight, down_proj_weight, saved,
-                       saved_bytes, dx, d_up_proj_weight, d_down_proj_weight, d_topk_weights,
-                       workspace, workspace_bytes, stream, BWD_FULL);
+  if (shape && shape->shared != 0) return HMM_ERR_ARG;  // hmm_backward_shared
+  return backward_impl(ctx, shape, dy, topk_weights, up_proj_weight, down_proj_weight, nullptr,
+                       nullptr, saved, saved_bytes, dx, d_up_proj_weight, d_down_proj_weight,
+                       nullptr, nullptr, d_topk_weights, workspace, workspace_bytes, stream,
+                       BWD_FULL);
+}
+
+int hmm_backward_shared(hmm_ctx* ctx, const hmm_shape* shape, const void* dy,
+                        const void* topk_weights, const void* up_proj_weight,
+                        const void* down_proj_weight, const void* shared_up_proj_weight,
+                        const void* shared_down_proj_weight, const void* saved,
+                        size_t saved_bytes, void* dx, void* d_up_proj_weight,
+                        void* d_down_proj_weight, void* d_shared_up_proj_weight,
+                        void* d_shared_down_proj_weight, void* d_topk_weights, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  if (!shape || shape->shared != 1) return HMM_ERR_ARG;
+  return backward_impl(ctx, shape, dy, topk_weights, up_proj_weight, down_proj_weight,
+                       shared_up_proj_weight, shared_down_proj_weight, saved, saved_bytes, dx,
+                       d_up_proj_weight, d_down_proj_weight, d_shared_up_proj_weight,
+                       d_shared_down_proj_weight, d_topk_weights, workspace, workspace_bytes,
+                       stream, BWD_FULL);
 }
 
 int hmm_backward_dx(hmm_ctx* ctx, const hmm_shape* shape, const void* dy,
                     const void* topk_weights, const void* up_proj_weight,
                     const void* down_proj_weight, const void* saved, size_t saved_bytes, void* dx,
                     void* d_topk_weights, void* workspace, size_t workspace_bytes, void* stream) {
-  return backward_impl(ctx, shape, dy, topk_weights, up_proj_weight, down_proj_weight, saved,
-                       saved_bytes, dx, nullptr, nullptr, d_topk_weights, workspace,
-                       workspace_bytes, stream, BWD_DX);
+  return backward_impl(ctx, shape, dy, topk_weights, up_proj_weight, down_proj_weight, nullptr,
+                       nullptr, saved, saved_bytes, dx, nullptr, nullptr, nullptr, nullptr,
+                       d_topk_weights, workspace, workspace_bytes, stream, BWD_DX);
 }
 
 int hmm_backward_dw(hmm_ctx* ctx, const hmm_shape* shape, const void* saved, size_t saved_bytes,
                     void* d_up_proj_weight, void* d_down_proj_weight, void* workspace,
                     size_t workspace_bytes, void* stream) {
-  return backward_impl(ctx, shape, nullptr, nullptr, nullptr, nullptr, saved, saved_bytes,
-                       nullptr, d_up_proj_weight, d_down_proj_weight, nullptr, workspace,
-                       workspace_bytes, stream, BWD_DW);
+  return backward_impl(ctx, shape, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, saved,
+                       saved_bytes, nullptr, d_up_proj_weight, d_down_proj_weight, nullptr,
+                       nullptr, nullptr, workspace, workspace_bytes, stream, BWD_DW);
 }
 
 int hmm_status(hmm_ctx* ctx, void* stream, int* device_error) {

@@ -42,6 +42,8 @@ struct CtrlPtrs {
 
 struct Plan {
   int64_t T, H, I, E, K, TK;
+  int64_t shared;       // 1: the optional shared expert is expert E of the padded rows
+  int64_t Ex;           // E + shared: experts of the padded row space
   int64_t R;            // capacity of the padded row space
   int64_t max_mtiles;   // R / BM
   int64_t nchunks;      // routing warp-chunks
@@ -96,8 +98,6 @@ struct GemmEnv {
   uint64_t* trace;   // tile timeline buffer of the traced launch (null: off)
   int trace_cap;     // records per CTA
   int trace_which;   // which GEMM launch kind is traced
-  int bwd_data_sms;  // SMs for the data-gradient group of the backward (0: automatic)
-  int pair_wgrad;    // weight gradients on CTA pairs (2-SM MMA)
   int pair_rows;     // forward and data-gradient GEMMs on CTA pairs (2-SM MMA)
   unsigned* status;
   uint64_t budget_ns;
@@ -105,25 +105,24 @@ struct GemmEnv {
 };
 
 // forward GMM1(+SwiGLU) and GMM2 in one persistent launch with per-M-tile
-// ready counters.  h32 may be null (inference).
+// ready counters, for the routed experts and (p.shared) the shared expert
+// (Ws1 [H, 2I], Ws2 [I, H]).  h32 may be null (inference).
 int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
-                         const void* x_perm, const void* W1, const void* W2, void* a, float* h32,
-                         void* o, bool skip_ready_release);
-// backward GEMMs.  part 1: act_grad (+SwiGLU grad, d_w partials; dH and w*a
-// written as bf16 hi + lo) and input-grad (per-M-tile release) in one
-// persistent launch.  part 2: W2Grad and W1Grad (reading the hi + lo halves),
-// which need nothing from input-grad.  With env.bwd_data_sms > 0 all four run
-// in part 1 (two CTA groups, the weight gradients trailing act_grad per
-// expert) and part 2 does nothing.  dW1 / dW2 may be null.
-int launch_backward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
-                          const void* x_perm, const void* dy_perm, const float* wperm,
-                          const float* h32, const void* W1, const void* W2, void* dH,
-                          void* dH_lo, void* wa, void* wa_lo, float* dwp, void* dx_perm,
-                          void* dW1, void* dW2, int part);
-
-// weight-gradient GEMMs on CTA pairs (tcgen05 cta_group::2), 256 x 256 tiles
+                         const void* x_perm, const void* W1, const void* W2, const void* Ws1,
+                         const void* Ws2, void* a, float* h32, void* o, bool skip_ready_release);
+// backward data gradients in one persistent launch: act_grad (+SwiGLU grad,
+// d_w partials; dH and w*a written as bf16 hi + lo) and input-grad (released
+// per M tile), routed and shared experts.
+int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
+                           const void* dy_perm, const float* wperm, const float* h32,
+                           const void* W1, const void* W2, const void* Ws1, const void* Ws2,
+                           void* dH, void* dH_lo, void* wa, void* wa_lo, float* dwp,
+                           void* dx_perm);
+// weight gradients on CTA pairs (tcgen05 cta_group::2), 256 x 256 tiles:
+// dW1 / dW2 of the routed experts and dWs1 / dWs2 of the shared expert (any
+// may be null).
 int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, const void* x_perm,
                       const void* dy_perm, const void* dH, const void* dH_lo, const void* wa,
-                      const void* wa_lo, void* dW1, void* dW2);
+                      const void* wa_lo, void* dW1, void* dW2, void* dWs1, void* dWs2);
 
 }  // namespace hmm

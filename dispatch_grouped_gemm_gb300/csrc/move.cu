@@ -57,12 +57,14 @@ constexpr int UNROLL = 4;
 
 }  // namespace
 
-// Dispatch: token t's row of src goes to the padded rows of its K slots; the
+// Dispatch: token t's row of src goes to the padded rows of its K slots and,
+// with the shared expert (E < Ex), to the shared expert's row poff[E] + t; the
 // warps past T zero the padding rows of each expert (so every padded row of
 // the GEMM operands is defined).  Optionally also scatters the routing weight
-// of every slot to its padded row (wperm, 0 on padding rows).
+// of every slot to its padded row (wperm: 1 on the shared rows, 0 on padding
+// rows).
 __global__ void __launch_bounds__(MOVE_THREADS) dispatch_rows_kernel(
-    const uint4* __restrict__ src, int64_t T, int64_t K, int64_t H8, MetaPtrs m, int E,
+    const uint4* __restrict__ src, int64_t T, int64_t K, int64_t H8, MetaPtrs m, int E, int Ex,
     uint4* __restrict__ dst, const void* w, int w_dtype, float* wperm, int32_t* zero_ptr,
     int64_t zero_count) {
   const int lane = threadIdx.x & 31;
@@ -76,6 +78,12 @@ __global__ void __launch_bounds__(MOVE_THREADS) dispatch_rows_kernel(
     int32_t prow_l = -1;
     if (lane < K) prow_l = m.slot2prow[g * K + lane];
     if (wperm && lane < K && prow_l >= 0) wperm[prow_l] = ld_weight(w, g * K + lane, w_dtype);
+    // the shared expert's row of this token, handled as slot K
+    if (E < Ex && lane == K) {
+      prow_l = m.poff[E] + static_cast<int32_t>(g);
+      if (wperm) wperm[prow_l] = 1.0f;
+    }
+    const int64_t KS = K + (E < Ex ? 1 : 0);
     const uint4* s = src + g * H8;
     for (int64_t c0 = lane; c0 < H8; c0 += 32 * UNROLL) {
       uint4 v[UNROLL];
@@ -84,7 +92,7 @@ __global__ void __launch_bounds__(MOVE_THREADS) dispatch_rows_kernel(
         const int64_t c = c0 + 32 * u;
         if (c < H8) v[u] = s[c];
       }
-      for (int k = 0; k < K; ++k) {
+      for (int k = 0; k < KS; ++k) {
         const int32_t prow = __shfl_sync(0xffffffffu, prow_l, k);
         if (prow < 0) continue;
         uint4* d = dst + static_cast<int64_t>(prow) * H8;
@@ -98,7 +106,7 @@ __global__ void __launch_bounds__(MOVE_THREADS) dispatch_rows_kernel(
   } else {
     const int64_t q = g - T;
     const int64_t e = q / BM;
-    if (e >= E) return;
+    if (e >= Ex) return;
     const int32_t row = m.poff[e] + m.counts[e] + static_cast<int32_t>(q % BM);
     if (row >= m.poff[e + 1]) return;
     if (wperm && lane == 0) wperm[row] = 0.0f;
@@ -108,16 +116,37 @@ __global__ void __launch_bounds__(MOVE_THREADS) dispatch_rows_kernel(
   }
 }
 
-// Combine: out[t] = sum_k scale_k * rows[slot2prow[t*K+k]], fp32 in k order,
-// one bf16 rounding.  scale_k = topk_weights[t,k] (forward) or 1 (dX).
+// Eight consecutive values (8-column group c) of row `row` of a bf16 or fp32
+// row array with H8 groups per row, accumulated as acc += s * values.
+template <bool F32>
+__device__ __forceinline__ void acc_group(float (&acc)[8], const void* rows, int64_t row,
+                                          int64_t c, int64_t H8, float s) {
+  if constexpr (F32) {
+    const float4* r = static_cast<const float4*>(rows) + (row * H8 + c) * 2;
+    const float4 a = r[0], b = r[1];
+    acc[0] = fmaf(s, a.x, acc[0]); acc[1] = fmaf(s, a.y, acc[1]);
+    acc[2] = fmaf(s, a.z, acc[2]); acc[3] = fmaf(s, a.w, acc[3]);
+    acc[4] = fmaf(s, b.x, acc[4]); acc[5] = fmaf(s, b.y, acc[5]);
+    acc[6] = fmaf(s, b.z, acc[6]); acc[7] = fmaf(s, b.w, acc[7]);
+  } else {
+    acc8(acc, static_cast<const uint4*>(rows)[row * H8 + c], s);
+  }
+}
+
+// Combine: out[t] = sum_k scale_k * rows[slot2prow[t*K+k]] (+ rows[*shared_row0
+// + t], the shared expert's row, unit weight, when shared_row0 is given),
+// fp32 in k order then the shared term, one bf16 rounding.  scale_k =
+// topk_weights[t,k] (forward) or 1 (dX).  F32: the rows are fp32 (o and dX
+// with the shared expert, whose unweighted term would otherwise carry a bf16
+// rounding several times larger than the routed terms').
 // With dwp != null (backward) lane k also writes
 //   d_topk_weights[t,k] = sum over the act_grad N tiles of the per-row
 //   partial dot products <G_s, a_s> (fixed order).
-template <bool WEIGHTED>
+template <bool WEIGHTED, bool F32>
 __global__ void __launch_bounds__(MOVE_THREADS) combine_rows_kernel(
-    const uint4* __restrict__ rows, const void* w, int w_dtype, int64_t T, int64_t K, int64_t H8,
-    const int32_t* __restrict__ slot2prow, uint4* __restrict__ out, const float* dwp,
-    int64_t dwp_ld, void* dw) {
+    const void* __restrict__ rows, const void* w, int w_dtype, int64_t T, int64_t K, int64_t H8,
+    const int32_t* __restrict__ slot2prow, const int32_t* shared_row0, uint4* __restrict__ out,
+    const float* dwp, int64_t dwp_ld, void* dw) {
   const int lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * MOVE_WARPS + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -134,6 +163,7 @@ __global__ void __launch_bounds__(MOVE_THREADS) combine_rows_kernel(
     st_weight(dw, t * K + lane, w_dtype, d);
   }
   if (!out) return;
+  const int64_t srow = shared_row0 ? *shared_row0 + t : -1;
   for (int64_t c0 = lane; c0 < H8; c0 += 32 * UNROLL) {
     float acc[UNROLL][8];
 #pragma unroll
@@ -144,17 +174,17 @@ __global__ void __launch_bounds__(MOVE_THREADS) combine_rows_kernel(
       const int32_t prow = __shfl_sync(0xffffffffu, prow_l, k);
       const float s = __shfl_sync(0xffffffffu, w_l, k);
       if (prow < 0) continue;
-      const uint4* r = rows + static_cast<int64_t>(prow) * H8;
-      uint4 v[UNROLL];
 #pragma unroll
       for (int u = 0; u < UNROLL; ++u) {
         const int64_t c = c0 + 32 * u;
-        if (c < H8) v[u] = r[c];
+        if (c < H8) acc_group<F32>(acc[u], rows, prow, c, H8, s);
       }
+    }
+    if (srow >= 0) {
 #pragma unroll
       for (int u = 0; u < UNROLL; ++u) {
         const int64_t c = c0 + 32 * u;
-        if (c < H8) acc8(acc[u], v[u], s);
+        if (c < H8) acc_group<F32>(acc[u], rows, srow, c, H8, 1.0f);
       }
     }
 #pragma unroll
@@ -171,39 +201,42 @@ static int move_grid(int64_t warps) {
 
 cudaError_t launch_dispatch_x(const Plan& p, const void* x, MetaPtrs m, void* x_perm,
                               cudaStream_t st) {
-  const int64_t warps = p.T + p.E * BM;
+  const int64_t warps = p.T + p.Ex * BM;
   dispatch_rows_kernel<<<move_grid(warps), MOVE_THREADS, 0, st>>>(
       static_cast<const uint4*>(x), p.T, p.K, p.H / 8, m, static_cast<int>(p.E),
-      static_cast<uint4*>(x_perm), nullptr, 0, nullptr, nullptr, 0);
+      static_cast<int>(p.Ex), static_cast<uint4*>(x_perm), nullptr, 0, nullptr, nullptr, 0);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dispatch_dy(const Plan& p, const void* dy, const void* w, int w_dtype,
                                MetaPtrs m, CtrlPtrs c, void* dy_perm, float* wperm,
                                cudaStream_t st) {
-  const int64_t warps = p.T + p.E * BM;
+  const int64_t warps = p.T + p.Ex * BM;
   // also zero the backward launch counters (tickets, per-M-tile and
   // per-expert ready counters are contiguous in the control block)
   const int64_t nzero = p.ctrl_zero_count;
   dispatch_rows_kernel<<<move_grid(warps), MOVE_THREADS, 0, st>>>(
       static_cast<const uint4*>(dy), p.T, p.K, p.H / 8, m, static_cast<int>(p.E),
-      static_cast<uint4*>(dy_perm), w, w_dtype, wperm, c.tickets, nzero);
+      static_cast<int>(p.Ex), static_cast<uint4*>(dy_perm), w, w_dtype, wperm, c.tickets, nzero);
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine_y(const Plan& p, const void* o, const void* w, int w_dtype, MetaPtrs m,
                              void* y, cudaStream_t st) {
-  combine_rows_kernel<true><<<move_grid(p.T), MOVE_THREADS, 0, st>>>(
-      static_cast<const uint4*>(o), w, w_dtype, p.T, p.K, p.H / 8, m.slot2prow,
-      static_cast<uint4*>(y), nullptr, 0, nullptr);
+  auto kern = p.shared ? combine_rows_kernel<true, true> : combine_rows_kernel<true, false>;
+  kern<<<move_grid(p.T), MOVE_THREADS, 0, st>>>(
+      o, w, w_dtype, p.T, p.K, p.H / 8, m.slot2prow,
+      p.shared ? m.poff + p.E : nullptr, static_cast<uint4*>(y), nullptr, 0, nullptr);
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine_dx(const Plan& p, const void* dx_perm, const float* dwp, MetaPtrs m,
                               void* dx, void* dw, int w_dtype, cudaStream_t st) {
-  combine_rows_kernel<false><<<move_grid(p.T), MOVE_THREADS, 0, st>>>(
-      static_cast<const uint4*>(dx_perm), nullptr, w_dtype, p.T, p.K, p.H / 8, m.slot2prow,
-      static_cast<uint4*>(dx), dw ? dwp : nullptr, p.dwp_ld, dw);
+  auto kern = p.shared ? combine_rows_kernel<false, true> : combine_rows_kernel<false, false>;
+  kern<<<move_grid(p.T), MOVE_THREADS, 0, st>>>(
+      dx_perm, nullptr, w_dtype, p.T, p.K, p.H / 8, m.slot2prow,
+      p.shared ? m.poff + p.E : nullptr, static_cast<uint4*>(dx), dw ? dwp : nullptr, p.dwp_ld,
+      dw);
   return cudaGetLastError();
 }
 

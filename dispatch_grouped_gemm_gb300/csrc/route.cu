@@ -89,14 +89,17 @@ __device__ int32_t block_exclusive_scan(int32_t v, int32_t* warp_tot, int32_t* t
   return r;
 }
 
-__global__ void __launch_bounds__(1024) route_scan_kernel(int E, int64_t nchunks, MetaPtrs m,
+// Ex = E + shared experts; the shared expert (e == E, when present) owns all
+// T tokens, in token order, after the routed experts.
+__global__ void __launch_bounds__(1024) route_scan_kernel(int E, int Ex, int32_t T,
+                                                          int64_t nchunks, MetaPtrs m,
                                                           CtrlPtrs c, int64_t zero_count) {
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t tot_cnt, tot_pad;
   const int e = threadIdx.x;
   // counts of expert e over the chunks, loaded eight chunks at a time
   constexpr int CB = 8;
-  int32_t cnt = 0;
+  int32_t cnt = (e >= E && e < Ex) ? T : 0;
   if (e < E) {
     for (int64_t ch0 = 0; ch0 < nchunks; ch0 += CB) {
       int32_t v[CB];
@@ -110,13 +113,13 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int64_t nchunks
   const int32_t padded = (cnt + BM - 1) / BM * BM;
   const int32_t off = block_exclusive_scan(cnt, warp_tot, &tot_cnt);
   const int32_t poff = block_exclusive_scan(padded, warp_tot, &tot_pad);
-  if (e < E) {
+  if (e < Ex) {
     m.counts[e] = cnt;
     m.offsets[e] = off;
     m.poff[e] = poff;
     // chunk counts -> first row of each chunk's slots of e
     int32_t run = off;
-    for (int64_t ch0 = 0; ch0 < nchunks; ch0 += CB) {
+    for (int64_t ch0 = 0; e < E && ch0 < nchunks; ch0 += CB) {
       int32_t v[CB];
 #pragma unroll
       for (int j = 0; j < CB; ++j)
@@ -130,8 +133,8 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int64_t nchunks
     for (int32_t r = poff + cnt; r < poff + padded; ++r) m.prow2slot[r] = -1;
   }
   if (e == 0) {
-    m.offsets[E] = tot_cnt;
-    m.poff[E] = tot_pad;
+    m.offsets[Ex] = tot_cnt;
+    m.poff[Ex] = tot_pad;
   }
   // tickets, per-M-tile and per-expert ready counters of this call
   for (int64_t i = e; i < zero_count; i += blockDim.x) c.tickets[i] = 0;
@@ -193,7 +196,8 @@ cudaError_t launch_route(const Plan& p, const int32_t* ids, MetaPtrs m, CtrlPtrs
     route_count_kernel<<<blocks, RWARPS * 32, smem, st>>>(ids, p.TK, E, p.nchunks, c.chunk_base,
                                                           status);
   }
-  route_scan_kernel<<<1, 1024, 0, st>>>(E, p.nchunks, m, c, p.ctrl_zero_count);
+  route_scan_kernel<<<1, 1024, 0, st>>>(E, static_cast<int>(p.Ex), static_cast<int32_t>(p.T),
+                                        p.nchunks, m, c, p.ctrl_zero_count);
   if (p.nchunks > 0) {
     route_rank_kernel<<<blocks, RWARPS * 32, smem, st>>>(ids, p.TK, E, p.nchunks, m,
                                                          c.chunk_base, slot2row, row2slot);

@@ -52,7 +52,8 @@ extern "C" int hmm_route_static(const hmm_shape* shape, const int32_t* topk_ids,
                                 int32_t* offsets, int32_t* slot2row, int32_t* row2slot,
                                 void* stream) {
   using namespace hmm;
-  if (!shape || shape->reserved != 0) return HMM_ERR_ARG;
+  // routing of the routed experts only: a shape with the shared expert is refused
+  if (!shape || shape->shared != 0) return HMM_ERR_ARG;
   if (shape->weights_dtype != HMM_DTYPE_BF16 && shape->weights_dtype != HMM_DTYPE_F32)
     return HMM_ERR_DTYPE;
   if (shape->T < 0 || shape->H <= 0 || shape->I <= 0 || shape->E <= 0 || shape->K <= 0 ||

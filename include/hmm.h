@@ -90,7 +90,10 @@ typedef struct hmm_shape {
   int64_t E;             /* experts, >= 1 */
   int64_t K;             /* experts per token, >= 1 */
   int32_t weights_dtype; /* HMM_DTYPE_BF16 or HMM_DTYPE_F32 for topk_weights */
-  int32_t reserved;      /* must be 0 */
+  int32_t shared;        /* 1: one shared expert [HyperMegaMoE §6.1], used through
+                            hmm_forward_shared / hmm_backward_shared (the sizes of
+                            hmm_workspace_size include it); 0: none.  With 1,
+                            E + 1 <= 1024 and K <= 31. */
 } hmm_shape;
 
 /* Create a context bound to CUDA device `device` (must be sm_103).  Allocates
@@ -117,16 +120,7 @@ int hmm_destroy(hmm_ctx* ctx);
  *                         recorded on the call's stream (read them with
  *                         hmm_profile_read).  Default 0. */
 #define HMM_OPT_PROFILE 4
-/*   HMM_OPT_BWD_DATA_SMS  0 (default): the backward GEMMs run as phases of one
- *                         queue (act_grad, input-grad, then the weight
- *                         gradients).  n > 0: n SMs run the data-gradient
- *                         GEMMs while the others run the weight-gradient
- *                         GEMMs concurrently, trailing act_grad per expert. */
-#define HMM_OPT_BWD_DATA_SMS 5
-/*   HMM_OPT_PAIR_WGRAD    1 (default): the weight-gradient GEMMs run on CTA
- *                         pairs with 2-SM MMAs (256 x 256 tiles); 0: on single
- *                         CTAs (128 x 256 tiles). */
-#define HMM_OPT_PAIR_WGRAD 6
+/*   (option ids 5 and 6 are not used) */
 /*   HMM_OPT_PAIR_ROWS     2 (default): automatic; the forward GEMMs and the
  *                         data-gradient GEMMs run on CTA pairs with 2-SM MMAs
  *                         (two 128-row tiles of one expert per 256 x 256 tile)
@@ -139,8 +133,7 @@ int hmm_set_option(hmm_ctx* ctx, int option, int64_t value);
 /* Launch phases timed under HMM_OPT_PROFILE (index = phase id):
  *   0 route (3 kernels)  1 dispatch_x  2 gemm_fwd (GMM1+SwiGLU, GMM2)
  *   3 combine_y          4 dispatch_dy
- *   5 gemm_bwd_data (act_grad + SwiGLU grad, input-grad; with
- *     HMM_OPT_BWD_DATA_SMS > 0 also W2Grad, W1Grad)
+ *   5 gemm_bwd_data (act_grad + SwiGLU grad, input-grad)
  *   6 gemm_bwd_weight (W2Grad, W1Grad)
  *   7 combine_dx (+ d_topk_weights; on a second stream, beside phase 6)  */
 #define HMM_NUM_PHASES 8
@@ -239,6 +232,39 @@ int hmm_backward(hmm_ctx* ctx, const hmm_shape* shape, const void* dy,
                  size_t saved_bytes, void* dx, void* d_up_proj_weight,
                  void* d_down_proj_weight, void* d_topk_weights,
                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Optional shared expert [HyperMegaMoE §6.1: shared-expert weights whose GMM1,
+ * SwiGLU and GMM2 are scheduled with the routed experts' pipeline and whose
+ * output is merged at Combine; the interface gains the shared weights only
+ * when the feature is used].  shape->shared must be 1 (hmm_forward and
+ * hmm_backward refuse such a shape, these refuse shared == 0).
+ *   y[t] = sum_k topk_weights[t,k] FFN_{topk_ids[t,k]}(x[t]) + FFN_s(x[t])
+ * (reading: every token, unit weight, no gate), FFN_s the expert FFN on
+ *   shared_up_proj_weight   bf16 [H, 2I]  (gate | up, like one routed expert)
+ *   shared_down_proj_weight bf16 [I, H]
+ * The shared expert runs as one more expert of the same launches (its rows
+ * are the T tokens in order).  The backward adds its part of dx and writes
+ * d_shared_up_proj_weight [H, 2I] and d_shared_down_proj_weight [I, H]
+ * (either may be NULL); d_topk_weights is unchanged by it.  Arguments,
+ * layouts and errors otherwise as for hmm_forward / hmm_backward; sizes come
+ * from hmm_workspace_size with the same shape.  The split entry points
+ * hmm_backward_dx / hmm_backward_dw refuse shared == 1. */
+int hmm_forward_shared(hmm_ctx* ctx, const hmm_shape* shape, const void* x,
+                       const int32_t* topk_ids, const void* topk_weights,
+                       const void* up_proj_weight, const void* down_proj_weight,
+                       const void* shared_up_proj_weight,
+                       const void* shared_down_proj_weight, void* y, void* saved,
+                       size_t saved_bytes, void* workspace,
+                       size_t workspace_bytes, void* stream);
+int hmm_backward_shared(hmm_ctx* ctx, const hmm_shape* shape, const void* dy,
+                        const void* topk_weights, const void* up_proj_weight,
+                        const void* down_proj_weight,
+                        const void* shared_up_proj_weight,
+                        const void* shared_down_proj_weight, const void* saved,
+                        size_t saved_bytes, void* dx, void* d_up_proj_weight,
+                        void* d_down_proj_weight, void* d_shared_up_proj_weight,
+                        void* d_shared_down_proj_weight, void* d_topk_weights,
+                        void* workspace, size_t workspace_bytes, void* stream);
 
 /* The backward split into its data and weight halves, for schedulers that
  * defer the weight gradients [EP overlap issue §2.3 (W/D split, deferred W
