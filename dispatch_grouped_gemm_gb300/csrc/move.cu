@@ -85,7 +85,9 @@ __global__ void __launch_bounds__(MOVE_THREADS) dispatch_rows_kernel(
     }
     const int64_t KS = K + (E < Ex ? 1 : 0);
     const uint4* s = src + g * H8;
-    for (int64_t c0 = lane; c0 < H8; c0 += 32 * UNROLL) {
+    // every lane runs every iteration (the shuffles below read other lanes'
+    // slots); only the loads and stores are guarded
+    for (int64_t c0 = lane; c0 - lane < H8; c0 += 32 * UNROLL) {
       uint4 v[UNROLL];
 #pragma unroll
       for (int u = 0; u < UNROLL; ++u) {
@@ -164,7 +166,9 @@ __global__ void __launch_bounds__(MOVE_THREADS) combine_rows_kernel(
   }
   if (!out) return;
   const int64_t srow = shared_row0 ? *shared_row0 + t : -1;
-  for (int64_t c0 = lane; c0 < H8; c0 += 32 * UNROLL) {
+  // every lane runs every iteration (the shuffles below read other lanes'
+  // slots); only the loads and stores are guarded
+  for (int64_t c0 = lane; c0 - lane < H8; c0 += 32 * UNROLL) {
     float acc[UNROLL][8];
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u)
