@@ -136,10 +136,9 @@ int make_plan(const hmm_shape* s, bool training, Plan* p) {
   o = 0;
   p->off_chunk_base = o; o = align_up(o + 4 * p->nchunks * p->E, A);
   p->off_tickets = o;
-  p->off_ready = o + 4 * NUM_TICKETS;  // tickets, ready, eready contiguous (zeroed together)
-  p->off_eready = p->off_ready + 4 * p->max_mtiles;
-  p->ctrl_zero_count = NUM_TICKETS + p->max_mtiles + p->Ex;
-  o = align_up(p->off_eready + 4 * p->Ex, A);
+  p->off_ready = o + 4 * NUM_TICKETS;  // tickets and ready counters contiguous (zeroed together)
+  p->ctrl_zero_count = NUM_TICKETS + p->max_mtiles;
+  o = align_up(p->off_ready + 4 * p->max_mtiles, A);
   p->ctrl_bytes = o;
   const size_t xperm = align_up(static_cast<size_t>(R) * p->H * 2, A);
   const size_t hbytes = align_up(static_cast<size_t>(R) * 2 * p->I * 4, A);
@@ -197,7 +196,6 @@ CtrlPtrs ctrl_at(const Plan& p, void* base) {
   c.chunk_base = reinterpret_cast<int32_t*>(b + p.off_chunk_base);
   c.tickets = reinterpret_cast<int32_t*>(b + p.off_tickets);
   c.ready = reinterpret_cast<int32_t*>(b + p.off_ready);
-  c.eready = reinterpret_cast<int32_t*>(b + p.off_eready);
   return c;
 }
 

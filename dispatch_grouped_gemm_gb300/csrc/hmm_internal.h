@@ -37,7 +37,6 @@ struct CtrlPtrs {
   int32_t* chunk_base;  // [nchunks * E]
   int32_t* tickets;     // [NUM_TICKETS]      } contiguous: zeroed together
   int32_t* ready;       // [max_mtiles]       } at the start of every call
-  int32_t* eready;      // [E]                }
 };
 
 struct Plan {
@@ -54,7 +53,7 @@ struct Plan {
   size_t meta_bytes;
   size_t off_counts, off_offsets, off_poff, off_slot2prow, off_prow2slot;  // inside meta
   size_t ctrl_bytes;
-  size_t off_chunk_base, off_tickets, off_ready, off_eready;               // inside ctrl
+  size_t off_chunk_base, off_tickets, off_ready;                           // inside ctrl
   int64_t ctrl_zero_count;  // int32 counters from off_tickets that each call zeroes
   // forward: saved = [meta | x_perm | h]      (training)
   //          workspace = [ctrl | a | o]       (training)

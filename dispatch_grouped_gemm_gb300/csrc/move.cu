@@ -216,8 +216,8 @@ cudaError_t launch_dispatch_dy(const Plan& p, const void* dy, const void* w, int
                                MetaPtrs m, CtrlPtrs c, void* dy_perm, float* wperm,
                                cudaStream_t st) {
   const int64_t warps = p.T + p.Ex * BM;
-  // also zero the backward launch counters (tickets, per-M-tile and
-  // per-expert ready counters are contiguous in the control block)
+  // also zero the backward launch counters (tickets and per-M-tile ready
+  // counters are contiguous in the control block)
   const int64_t nzero = p.ctrl_zero_count;
   dispatch_rows_kernel<<<move_grid(warps), MOVE_THREADS, 0, st>>>(
       static_cast<const uint4*>(dy), p.T, p.K, p.H / 8, m, static_cast<int>(p.E),
