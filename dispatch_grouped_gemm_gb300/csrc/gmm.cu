@@ -574,7 +574,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (!PAIR || leader)
       mbar_arrive(&ti_empty[slot]);
     else
-      mbar_arrive_cluster(mapa_shared(smem_u32(&ti_empty[slot]), 0));
+      mbar_arrive_peer(mapa_shared(smem_u32(&ti_empty[slot]), 0));
   };
 
   if (warp == SCHED_WARP) {
@@ -817,7 +817,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!PAIR || leader)
           mbar_arrive(&tempty[acc]);
         else
-          mbar_arrive_cluster(tempty_cl[acc]);
+          mbar_arrive_peer(tempty_cl[acc]);
       }
       if (rec) rec[7] = globaltimer_ns();
       if (real && pr.signal_m) {

@@ -344,7 +344,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         if (leader)
           mbar_arrive(&tempty[acc]);
         else
-          mbar_arrive_cluster(tempty_cl[acc]);
+          mbar_arrive_peer(tempty_cl[acc]);
       }
       if (rec) rec[7] = globaltimer_ns();
       acc ^= 1u;

@@ -261,6 +261,16 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
+// Arrive on the peer CTA's mbarrier with CTA-scope release: for signals that
+// publish no memory to the peer (a drained TMEM accumulator, ordered by the
+// tcgen05 fences; a tile-info slot this thread has finished reading).  A
+// cluster-scope release would first wait until every global store this
+// thread issued is performed at cluster scope, i.e. for the L2's
+// acknowledgements of a whole epilogue's output.
+__device__ __forceinline__ void mbar_arrive_peer(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
 // TMA load into this CTA's smem whose completion is counted on an mbarrier that
 // may live in the peer CTA of the pair (cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m, uint32_t bar_cl,
