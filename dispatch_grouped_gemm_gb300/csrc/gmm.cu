@@ -100,7 +100,7 @@ struct Prob {
   void* out;
   int64_t ld_out;
   void* out2;
-  int64_t ld_out2;
+  int64_t ld_out2;      // SwiGLU: column blocks of the blocked pre-activations
   void* out3;
   int64_t ld_out3;
   void* out4;           // SwiGLU grad: low bf16 half of dH (same layout as out)
@@ -108,8 +108,8 @@ struct Prob {
   int out_f32;          // STORE: fp32 outputs (else bf16)
   int lag;              // the tiles of expert e are issued at schedule step e + lag
   int e_lo, e_hi;       // experts of this problem; B holds experts e_lo .. e_hi - 1
-  const void* aux;
-  int64_t ld_aux;
+  const void* aux;      // SwiGLU grad: the blocked fp32 pre-activations
+  int64_t ld_aux;       // their column blocks per row block
   const float* rowscale;
   int* signal_m;        // per-M-tile counters released after a tile's stores
   const int* wait_m;    // per-M-tile counter acquired before a tile's loads
@@ -311,6 +311,17 @@ __device__ __forceinline__ void store_bf16x8_split(__nv_bfloat16* hi, __nv_bfloa
   *reinterpret_cast<uint4*>(lo) = pack_bf16x8(l);
 }
 
+// The fp32 pre-activations saved for the backward are stored in 32 x 32
+// blocks: block (row / 32, col / 32) of the gate half followed by the same
+// block of the up half, 8 KB contiguous, blocks ordered by row block, then
+// column block (ncb = ceil(I / 32) per row block).  The forward epilogue
+// writes, and the SwiGLU-grad epilogue reads, exactly these blocks (a 32-row
+// TMEM lane quarter times a 32-column chunk), so both move 8 KB runs instead
+// of 128-byte pieces of rows 2I floats apart.
+__device__ __forceinline__ int64_t hblock_offset(int64_t row, int col, int64_t ncb) {
+  return (((row >> 5) * ncb + (col >> 5)) << 11) + ((row & 31) << 5) + (col & 31);
+}
+
 __device__ __forceinline__ void store_f32x8(float* dst, const float* v) {
   reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
   reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
@@ -349,9 +360,9 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
           *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(pr.out) + row * pr.ld_out + col +
                                     cg) = pack_bf16x8(av);
           if (pr.out2) {
-            float* h_row = static_cast<float*>(pr.out2) + row * pr.ld_out2;
-            store_f32x8(h_row + col + cg, gv[k]);
-            store_f32x8(h_row + pr.half + col + cg, uv[k]);
+            float* hp = static_cast<float*>(pr.out2) + hblock_offset(row, col + cg, pr.ld_out2);
+            store_f32x8(hp, gv[k]);
+            store_f32x8(hp + 1024, uv[k]);
           }
         }
       }
@@ -400,9 +411,8 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const float4* p =
-            reinterpret_cast<const float4*>(hb + (rl + 8 * k) * pr.ld_aux + col + cg);
-        const float4* pu =
-            reinterpret_cast<const float4*>(hb + (rl + 8 * k) * pr.ld_aux + pr.half + col + cg);
+            reinterpret_cast<const float4*>(hb + hblock_offset(rl + 8 * k, col + cg, pr.ld_aux));
+        const float4* pu = p + 256;  // the up block follows the gate block
         const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
         gn[k][0] = ok ? __ldg(p) : z;
         gn[k][1] = ok ? __ldg(p + 1) : z;
@@ -981,7 +991,7 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
   g1.out = a;
   g1.ld_out = I;
   g1.out2 = h32;
-  g1.ld_out2 = 2 * I;
+  g1.ld_out2 = (I + 31) / 32;  // column blocks of the blocked layout
   g1.e_lo = 0;
   g1.e_hi = static_cast<int>(E);
   g1.signal_m = skip_ready_release ? nullptr : c.ready;
@@ -1048,7 +1058,7 @@ int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPt
   ag.out4 = dH_lo;
   ag.out5 = wa_lo;
   ag.aux = h32;
-  ag.ld_aux = 2 * I;
+  ag.ld_aux = (I + 31) / 32;
   ag.rowscale = wperm;
   ag.e_lo = 0;
   ag.e_hi = static_cast<int>(E);

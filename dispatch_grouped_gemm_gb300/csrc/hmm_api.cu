@@ -141,7 +141,8 @@ int make_plan(const hmm_shape* s, bool training, Plan* p) {
   o = align_up(p->off_ready + 4 * p->max_mtiles, A);
   p->ctrl_bytes = o;
   const size_t xperm = align_up(static_cast<size_t>(R) * p->H * 2, A);
-  const size_t hbytes = align_up(static_cast<size_t>(R) * 2 * p->I * 4, A);
+  // fp32 pre-activations in 32 x 32 blocks (gate and up), columns padded to 32
+  const size_t hbytes = align_up(static_cast<size_t>(R) * 2 * ((p->I + 31) / 32 * 32) * 4, A);
   const size_t abytes = align_up(static_cast<size_t>(R) * p->I * 2, A);
   // o: fp32 with the shared expert (its unweighted term in the y combine),
   // else bf16
