@@ -231,9 +231,12 @@ __device__ void decode_tile(const Params& P, const Prob& pr, int e, int r, TileI
 // ----------------------------------------------------------------- producer
 // K block kb of a tile into one smem stage (one thread).  Every box starts at
 // an inner coordinate that is a multiple of 8 elements (16 bytes).
-//   PAIR: this CTA's share (its 128 rows of A unless load_a is false, its 128
-//   columns of B), counted on the even CTA's full barrier (shared::cluster
-//   address bar_cl; the even CTA arms it for both).
+//   PAIR: this CTA's share (its 128 rows of A, its 128 columns of B), counted
+//   on the even CTA's full barrier (shared::cluster address bar_cl; the even
+//   CTA arms it for both).  Without rows of A (load_a false: the empty half of
+//   an expert's last pair) the A box starts at row -BM, entirely outside the
+//   tensor: the copy fills the stage with zeros and reads no memory, so that
+//   half's MMAs run on zeros instead of a stale stage.
 template <class C, bool PAIR>
 __device__ __forceinline__ void load_stage(const Prob& pr, const TileInfo& ti, int kb,
                                            const CUtensorMap* tA, const CUtensorMap* tB,
@@ -242,8 +245,8 @@ __device__ __forceinline__ void load_stage(const Prob& pr, const TileInfo& ti, i
   const int k = kb * BK;
   const int eb = ti.e - pr.e_lo;  // expert index inside this problem's weight slabs
   if constexpr (PAIR) {
-    if (rank == 0) mbar_arrive_expect_tx(bar, (ti.ph ? 1 : 2) * A_BYTES + 2 * PAIR_B_BYTES);
-    if (load_a) tma_load_2d_pair(sA, tA, bar_cl, k, ti.m0 + BM * static_cast<int>(rank));
+    if (rank == 0) mbar_arrive_expect_tx(bar, 2 * A_BYTES + 2 * PAIR_B_BYTES);
+    tma_load_2d_pair(sA, tA, bar_cl, k, load_a ? ti.m0 + BM * static_cast<int>(rank) : -BM);
     if constexpr (C::B_MN) {
       int c;
       if constexpr (C::EPI == EPI_SWIGLU)

@@ -53,7 +53,8 @@ __device__ __forceinline__ uint4 pack8(const float (&acc)[8]) {
 
 constexpr int MOVE_THREADS = 256;
 constexpr int MOVE_WARPS = MOVE_THREADS / 32;
-constexpr int UNROLL = 4;
+constexpr int UNROLL = 4;           // combine: 16-byte groups per lane per pass (x K rows)
+constexpr int DISPATCH_UNROLL = 8;  // dispatch: a whole 2048-wide row per pass
 
 }  // namespace
 
@@ -87,10 +88,10 @@ __global__ void __launch_bounds__(MOVE_THREADS) dispatch_rows_kernel(
     const uint4* s = src + g * H8;
     // every lane runs every iteration (the shuffles below read other lanes'
     // slots); only the loads and stores are guarded
-    for (int64_t c0 = lane; c0 - lane < H8; c0 += 32 * UNROLL) {
-      uint4 v[UNROLL];
+    for (int64_t c0 = lane; c0 - lane < H8; c0 += 32 * DISPATCH_UNROLL) {
+      uint4 v[DISPATCH_UNROLL];
 #pragma unroll
-      for (int u = 0; u < UNROLL; ++u) {
+      for (int u = 0; u < DISPATCH_UNROLL; ++u) {
         const int64_t c = c0 + 32 * u;
         if (c < H8) v[u] = s[c];
       }
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(MOVE_THREADS) dispatch_rows_kernel(
         if (prow < 0) continue;
         uint4* d = dst + static_cast<int64_t>(prow) * H8;
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
+        for (int u = 0; u < DISPATCH_UNROLL; ++u) {
           const int64_t c = c0 + 32 * u;
           if (c < H8) d[c] = v[u];
         }
