@@ -103,8 +103,9 @@ struct Prob {
   int64_t ld_out2;      // SwiGLU: column blocks of the blocked pre-activations
   void* out3;
   int64_t ld_out3;
-  void* out4;           // SwiGLU grad: low bf16 half of dH (same layout as out)
-  void* out5;           // SwiGLU grad: low bf16 half of w*a (same layout as out2)
+  void* out4;           // SwiGLU grad: e5m2 low part of dH (ld_lo4 bytes per row)
+  void* out5;           // SwiGLU grad: e5m2 low part of w*a (ld_lo5 bytes per row)
+  int64_t ld_lo4, ld_lo5;
   int out_f32;          // STORE: fp32 outputs (else bf16)
   int lag;              // the tiles of expert e are issued at schedule step e + lag
   int e_lo, e_hi;       // experts of this problem; B holds experts e_lo .. e_hi - 1
@@ -300,9 +301,11 @@ __device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t a_base, uint
 __device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 __device__ __forceinline__ float silu_f(float g) { return g * sigmoid_f(g); }
 
-// v = hi + lo with hi = bf16(v), lo = bf16(v - hi): the pair carries about
-// 16 significant bits, enough for the weight-gradient GEMMs that consume it.
-__device__ __forceinline__ void store_bf16x8_split(__nv_bfloat16* hi, __nv_bfloat16* lo,
+// v ~ hi + lo with hi = bf16(v) and lo = e5m2(v - hi): the weight-gradient
+// GEMMs take hi in a bf16 MMA and lo, at most 2^-9 |v| and needed only to a
+// few bits, in an fp8 MMA against an fp8 copy of the other operand (e5m2
+// keeps lo's small magnitudes in range).
+__device__ __forceinline__ void store_bf16x8_split(__nv_bfloat16* hi, uint8_t* lo,
                                                    const float* v) {
   float h[8], l[8];
 #pragma unroll
@@ -311,7 +314,7 @@ __device__ __forceinline__ void store_bf16x8_split(__nv_bfloat16* hi, __nv_bfloa
     l[j] = v[j] - h[j];
   }
   *reinterpret_cast<uint4*>(hi) = pack_bf16x8(h);
-  *reinterpret_cast<uint4*>(lo) = pack_bf16x8(l);
+  *reinterpret_cast<uint2*>(lo) = pack_fp8x8<true>(l);
 }
 
 // The fp32 pre-activations saved for the backward are stored in 32 x 32
@@ -397,10 +400,10 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
     // fp32 pre-activations g, u and the slot's routing weight w:
     //   a = silu(g) u,  dA = w G,
     //   dgate = dA u s (1 + g (1 - s)),  dup = dA g s     (s = sigmoid(g))
-    // writes dH = [dgate | dup] (bf16 hi + lo), wa = w a (bf16 hi + lo, the
-    // W2Grad operand) and the partial d_w = sum_j G_j a_j of this column
-    // block (fp32).  The pre-activations of the next chunk are loaded while
-    // the current one is computed.
+    // writes dH = [dgate | dup] and wa = w a (the W2Grad operand), each as
+    // a bf16 high part and an e5m2 low part, and the partial
+    // d_w = sum_j G_j a_j of this column block (fp32).  The pre-activations
+    // of the next chunk are loaded while the current one is computed.
     const float* hb = static_cast<const float*>(pr.aux);
     float w[4], dwp[4];
 #pragma unroll
@@ -460,11 +463,11 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
             wa[j] = w[k] * a;
           }
           __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(pr.out) + row * pr.ld_out + col + cg;
-          __nv_bfloat16* dl = static_cast<__nv_bfloat16*>(pr.out4) + row * pr.ld_out + col + cg;
+          uint8_t* dl = static_cast<uint8_t*>(pr.out4) + row * pr.ld_lo4 + col + cg;
           store_bf16x8_split(dh, dl, dg);
           store_bf16x8_split(dh + pr.half, dl + pr.half, du);
           store_bf16x8_split(static_cast<__nv_bfloat16*>(pr.out2) + row * pr.ld_out2 + col + cg,
-                             static_cast<__nv_bfloat16*>(pr.out5) + row * pr.ld_out2 + col + cg,
+                             static_cast<uint8_t*>(pr.out5) + row * pr.ld_lo5 + col + cg,
                              wa);
         }
       }
@@ -1059,7 +1062,9 @@ int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPt
   static_assert(CH_SPLIT == 1, "the d_w partial buffer holds one entry per act_grad N tile");
   ag.ld_out3 = p.dwp_ld;
   ag.out4 = dH_lo;
+  ag.ld_lo4 = p.ld8_2i;
   ag.out5 = wa_lo;
+  ag.ld_lo5 = p.ld8_i;
   ag.aux = h32;
   ag.ld_aux = (I + 31) / 32;
   ag.rowscale = wperm;

@@ -1,19 +1,21 @@
 // gmm_pair.cu -- the weight-gradient GEMMs on CTA pairs (tcgen05 cta_group::2).
 //
 // [HyperMegaMoE §2.2 W2Grad, W1Grad]
-//   dW2[e] = (wa_hi + wa_lo)^T . dy_perm      [I, rows of e] x [rows of e, H]
-//   dW1[e] = x_perm^T . (dH_hi + dH_lo)       [H, rows of e] x [rows of e, 2I]
+//   dW2[e] = wa_hi^T . dy_perm + wa_lo^T . dy8      [I, rows of e] x [rows of e, H]
+//   dW1[e] = x_perm^T . dH_hi + x8^T . dH_lo        [H, rows of e] x [rows of e, 2I]
 // for the routed experts and, with the optional shared expert [HyperMegaMoE
 // §6.1], for the shared expert (expert E of the padded rows, every token).
-// (the rounded operand is read as a bf16 hi + lo pair: every 64-row K step
-// stages A, B and the low half of the split operand together and issues two
-// MMAs on them, so the unsplit operand is loaded once).
+// The rounded operand comes as a bf16 high part and an e5m2 low part (the
+// rest, at most 2^-9 of the value); the low part meets an fp8 copy of the
+// other operand (x8 e4m3, dy8 e5m2) in an fp8 MMA at twice the bf16 rate,
+// accumulating into the same fp32 TMEM tile.  Every 64-row K step stages the
+// bf16 A and B and the two fp8 operands together (48 KB per CTA) and issues
+// four bf16 and two fp8 MMAs.
 //
 // Two CTAs of a cluster compute one 256 x 256 output tile with 2-SM MMAs:
 // each CTA loads its 128 rows of A and its 128 of the 256 columns of B, and
-// each accumulates its 128 rows x 256 columns in its own TMEM.  Per SM that is
-// 48 KB of operands per 64-deep K step (two MMAs) instead of 96 KB for 1-SM
-// 128 x 256 tiles that reload the unsplit operand for the low half.
+// each accumulates its 128 rows x 256 columns in its own TMEM (the fp8 MMAs
+// add into the same accumulator).
 //
 // Roles per CTA: warp 0 issues TMA (both CTAs, one thread), warp 1 issues the
 // MMAs (even CTA only), warps 2..5 drain TMEM (both CTAs).  The even CTA's
@@ -34,23 +36,27 @@ namespace hmm {
 namespace {
 
 constexpr int PSTAGES = 4;
-constexpr int PA_BYTES = 128 * 64 * 2;  // this CTA's 128 rows of A, 64 deep
-constexpr int PB_BYTES = 128 * 64 * 2;  // this CTA's 128 columns of B, 64 deep
-constexpr int PX_BYTES = 128 * 64 * 2;  // the low half of the split one of them
-constexpr int PSTAGE = PA_BYTES + PB_BYTES + PX_BYTES;
+constexpr int PA_BYTES = 128 * 64 * 2;  // this CTA's 128 rows of A, 64 deep (bf16)
+constexpr int PB_BYTES = 128 * 64 * 2;  // this CTA's 128 columns of B, 64 deep (bf16)
+constexpr int PL_BYTES = 128 * 64;      // the low part of the split one of them (e5m2)
+constexpr int PO_BYTES = 128 * 64;      // the fp8 copy of the other one
+constexpr int PSTAGE = PA_BYTES + PB_BYTES + PL_BYTES + PO_BYTES;
 constexpr int P_THREADS = 192;
 constexpr int P_EPI_WARPS = 4;
 constexpr int P_SMEM = 1024 + PSTAGES * PSTAGE + P_EPI_WARPS * XBUF_BYTES + 512;
 static_assert(P_SMEM <= 232448, "shared memory per CTA");
 constexpr uint32_t P_TMEM_COLS = 512;
 constexpr uint32_t IDESC_PAIR = idesc_bf16_f32(256, 256, 1, 1);  // both MN-major
+// fp8 MMAs on the low part: W1Grad x8 (e4m3) . dH_lo (e5m2); W2Grad wa_lo (e5m2) . dy8 (e5m2)
+constexpr uint32_t IDESC_LO_B = idesc_f8_f32(256, 256, F8_E4M3, F8_E5M2, 1, 1);
+constexpr uint32_t IDESC_LO_A = idesc_f8_f32(256, 256, F8_E5M2, F8_E5M2, 1, 1);
 
 struct PairProb {
   int e_lo, n_e; // experts e_lo .. e_lo + n_e - 1 of the padded rows
   int M, N;      // output [M, N] per expert
   int mpairs;    // 256-row tile pairs along M
   int n_tiles;   // 256-column tiles along N
-  int split;     // 1: A given as hi + lo, 2: B given as hi + lo
+  int split;     // the operand given as bf16 high + e5m2 low parts: 1 A, 2 B
   __nv_bfloat16* out;
   int64_t ld_out;
   int64_t out_estride;
@@ -69,7 +75,7 @@ struct PairParams {
 };
 
 struct PairMaps {
-  CUtensorMap m[4][3];  // A, B, low half of the split operand
+  CUtensorMap m[4][4];  // A, B (bf16), low part of the split one, fp8 copy of the other
 };
 
 struct PairTile {
@@ -173,7 +179,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     if (lane == 0) {
       // ------------------------------------------------------- TMA producer
       for (int q = 0; q < P.nprob; ++q)
-        for (int j = 0; j < 3; ++j) tma_prefetch_desc(&maps.m[q][j]);
+        for (int j = 0; j < 4; ++j) tma_prefetch_desc(&maps.m[q][j]);
       uint32_t stage = 0, sphase = 0;
       uint32_t issued = 0;
       bool ok = true;
@@ -203,16 +209,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
           const int k = t.krow0 + kb * 64;
           uint8_t* sA = stages + stage * PSTAGE;
           uint8_t* sB = sA + PA_BYTES;
-          uint8_t* sX = sB + PB_BYTES;
-          const int xc = pr.split == 1 ? ma : nbc;  // the low half's columns
+          uint8_t* sL = sB + PB_BYTES;
+          uint8_t* sO = sL + PL_BYTES;
+          // the low part sits on the split side, the fp8 copy on the other
+          const int lc = pr.split == 1 ? ma : nbc;
+          const int oc = pr.split == 1 ? nbc : ma;
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * PSTAGE);
           const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
           tma_load_2d_pair(sA, &mp[0], bar, ma, k);
           tma_load_2d_pair(sA + 8192, &mp[0], bar, ma + 64, k);
           tma_load_2d_pair(sB, &mp[1], bar, nbc, k);
           tma_load_2d_pair(sB + 8192, &mp[1], bar, nbc + 64, k);
-          tma_load_2d_pair(sX, &mp[2], bar, xc, k);
-          tma_load_2d_pair(sX + 8192, &mp[2], bar, xc + 64, k);
+          tma_load_2d_pair(sL, &mp[2], bar, lc, k);  // 128 fp8 columns in one box
+          tma_load_2d_pair(sO, &mp[3], bar, oc, k);
           ++issued;
           if (++stage == PSTAGES) {
             stage = 0;
@@ -256,19 +265,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
           tc_fence_after();
           const uint32_t a_base = smem_u32(stages + stage * PSTAGE);
           const uint32_t b_base = a_base + PA_BYTES;
-          const uint32_t x_base = b_base + PB_BYTES;
-          // second MMA of each K=16 step: the low half against the other operand
-          const uint32_t a2_base = split == 1 ? x_base : a_base;
-          const uint32_t b2_base = split == 1 ? b_base : x_base;
+          const uint32_t l_base = b_base + PB_BYTES;
+          const uint32_t o_base = l_base + PL_BYTES;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            // MN-major halves: two 64-wide chunks 8 KB apart, 8-row groups 1 KB
+            // MN-major bf16: two 64-wide chunks 8 KB apart, 8-row groups 1 KB
             const uint64_t ad = smem_desc(a_base + kk * 2048, 8192, 1024, LAYOUT_SW128);
             const uint64_t bd = smem_desc(b_base + kk * 2048, 8192, 1024, LAYOUT_SW128);
             umma_bf16_pair(d_tmem, ad, bd, IDESC_PAIR, (kb == 0 && kk == 0) ? 0u : 1u);
-            const uint64_t ad2 = smem_desc(a2_base + kk * 2048, 8192, 1024, LAYOUT_SW128);
-            const uint64_t bd2 = smem_desc(b2_base + kk * 2048, 8192, 1024, LAYOUT_SW128);
-            umma_bf16_pair(d_tmem, ad2, bd2, IDESC_PAIR, 1u);
+          }
+          // the low part against the fp8 copy: MN-major fp8, one 128-wide
+          // chunk, 8-row groups 1 KB, 32 rows of K per MMA
+          const uint32_t a2_base = split == 1 ? l_base : o_base;
+          const uint32_t b2_base = split == 1 ? o_base : l_base;
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const uint64_t ad = smem_desc(a2_base + kk * 4096, 8192, 1024, LAYOUT_SW128);
+            const uint64_t bd = smem_desc(b2_base + kk * 4096, 8192, 1024, LAYOUT_SW128);
+            umma_f8_pair(d_tmem, ad, bd, split == 1 ? IDESC_LO_A : IDESC_LO_B, 1u);
           }
           umma_commit_pair(&empty[stage], 0x3);
           if (++stage == PSTAGES) {
@@ -361,6 +375,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   }
 }
 
+// fp8 rows (ld bytes apart): boxes of 128 columns x 64 rows
+int encode2d_u8(const GemmEnv& env, CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
+                int64_t ld) {
+  const cuuint64_t gd[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t gs[1] = {static_cast<cuuint64_t>(ld)};
+  const cuuint32_t bx[2] = {128, 64};
+  const cuuint32_t es[2] = {1, 1};
+  CUresult r = env.encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gd, gs,
+                          bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? HMM_OK : HMM_ERR_CUDA;
+}
+
 int encode2d(const GemmEnv& env, CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
   const cuuint64_t gd[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t gs[1] = {static_cast<cuuint64_t>(cols) * 2};
@@ -375,8 +402,9 @@ int encode2d(const GemmEnv& env, CUtensorMap* m, const void* base, int64_t rows,
 }  // namespace
 
 int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, const void* x_perm,
-                      const void* dy_perm, const void* dH, const void* dH_lo, const void* wa,
-                      const void* wa_lo, void* dW1, void* dW2, void* dWs1, void* dWs2) {
+                      const void* x8, const void* dy_perm, const void* dy8, const void* dH,
+                      const void* dH_lo8, const void* wa, const void* wa_lo8, void* dW1,
+                      void* dW2, void* dWs1, void* dWs2) {
   const int64_t H = p.H, I = p.I, E = p.E, R = p.R;
   if (!dW1 && !dW2 && !dWs1 && !dWs2) return HMM_OK;
   PairMaps maps;
@@ -392,11 +420,12 @@ int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, const void*
   }
   int rc = HMM_OK;
   int q = 0;
-  // dW2 of experts [e_lo, e_lo + n_e): (wa_hi + wa_lo)^T . dy_perm
+  // dW2 of experts [e_lo, e_lo + n_e): wa_hi^T . dy_perm + wa_lo^T . dy8
   auto add_w2 = [&](void* out, int e_lo, int n_e) {
     rc |= encode2d(env, &maps.m[q][0], wa, R, I);
     rc |= encode2d(env, &maps.m[q][1], dy_perm, R, H);
-    rc |= encode2d(env, &maps.m[q][2], wa_lo, R, I);
+    rc |= encode2d_u8(env, &maps.m[q][2], wa_lo8, R, I, p.ld8_i);
+    rc |= encode2d_u8(env, &maps.m[q][3], dy8, R, H, p.ld8_h);
     PairProb& w = P.p[q++];
     w.e_lo = e_lo;
     w.n_e = n_e;
@@ -409,11 +438,12 @@ int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, const void*
     w.ld_out = H;
     w.out_estride = I * H;
   };
-  // dW1 of experts [e_lo, e_lo + n_e): x_perm^T . (dH_hi + dH_lo)
+  // dW1 of experts [e_lo, e_lo + n_e): x_perm^T . dH_hi + x8^T . dH_lo
   auto add_w1 = [&](void* out, int e_lo, int n_e) {
     rc |= encode2d(env, &maps.m[q][0], x_perm, R, H);
     rc |= encode2d(env, &maps.m[q][1], dH, R, 2 * I);
-    rc |= encode2d(env, &maps.m[q][2], dH_lo, R, 2 * I);
+    rc |= encode2d_u8(env, &maps.m[q][2], dH_lo8, R, 2 * I, p.ld8_2i);
+    rc |= encode2d_u8(env, &maps.m[q][3], x8, R, H, p.ld8_h);
     PairProb& w = P.p[q++];
     w.e_lo = e_lo;
     w.n_e = n_e;

@@ -125,6 +125,9 @@ int make_plan(const hmm_shape* s, bool training, Plan* p) {
   p->nchunks = (TK + RCHUNK - 1) / RCHUNK;
   p->nt_dswiglu = (p->I + BN - 1) / BN;
   p->dwp_ld = p->nt_dswiglu;  // one d_w partial per act_grad N tile and row
+  p->ld8_h = (p->H + 15) / 16 * 16;
+  p->ld8_2i = (2 * p->I + 15) / 16 * 16;
+  p->ld8_i = (p->I + 15) / 16 * 16;
   const size_t A = 256;
   size_t o = 0;
   p->off_counts = o;    o = align_up(o + 4 * p->Ex, A);
@@ -150,7 +153,8 @@ int make_plan(const hmm_shape* s, bool training, Plan* p) {
   if (training) {
     p->sv_meta = 0;
     p->sv_xperm = p->meta_bytes;
-    p->sv_h = p->sv_xperm + xperm;
+    p->sv_x8 = p->sv_xperm + xperm;
+    p->sv_h = p->sv_x8 + align_up(static_cast<size_t>(R) * p->ld8_h, A);
     p->saved_bytes = p->sv_h + hbytes;
     p->fw_ctrl = 0;
     p->fw_a = p->ctrl_bytes;
@@ -168,11 +172,12 @@ int make_plan(const hmm_shape* s, bool training, Plan* p) {
   o = 0;
   p->bw_ctrl = o;    o = align_up(o + p->ctrl_bytes, A);
   p->bw_dyperm = o;  o = align_up(o + static_cast<size_t>(R) * p->H * 2, A);
+  p->bw_dy8 = o;     o = align_up(o + static_cast<size_t>(R) * p->ld8_h, A);
   p->bw_wperm = o;   o = align_up(o + static_cast<size_t>(R) * 4, A);
   p->bw_dh = o;      o = align_up(o + static_cast<size_t>(R) * 2 * p->I * 2, A);
-  p->bw_dhlo = o;    o = align_up(o + static_cast<size_t>(R) * 2 * p->I * 2, A);
+  p->bw_dhlo = o;    o = align_up(o + static_cast<size_t>(R) * p->ld8_2i, A);
   p->bw_wa = o;      o = align_up(o + static_cast<size_t>(R) * p->I * 2, A);
-  p->bw_walo = o;    o = align_up(o + static_cast<size_t>(R) * p->I * 2, A);
+  p->bw_walo = o;    o = align_up(o + static_cast<size_t>(R) * p->ld8_i, A);
   // dX_perm: fp32 with the shared expert (see the dX combine), else bf16
   p->bw_dxperm = o;  o = align_up(o + static_cast<size_t>(R) * p->H * (p->shared ? 4 : 2), A);
   p->bw_dwp = o;     o = align_up(o + static_cast<size_t>(R) * p->dwp_ld * 4, A);
@@ -433,6 +438,7 @@ int forward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* x, const int3
   CtrlPtrs c = ctrl_at(p, ws + p.fw_ctrl);
   MetaPtrs m = meta_at(p, training ? sv + p.sv_meta : ws + p.fw_meta);
   void* x_perm = training ? sv + p.sv_xperm : ws + p.fw_xperm;
+  void* x8 = training ? sv + p.sv_x8 : nullptr;
   float* h32 = training ? reinterpret_cast<float*>(sv + p.sv_h) : nullptr;
   void* a = ws + p.fw_a;
   void* o = ws + p.fw_o;
@@ -448,7 +454,7 @@ int forward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* x, const int3
   }
   {
     PhaseScope ps(ctx, PH_DISPATCH_X, st);
-    rc = cuda_rc(launch_dispatch_x(p, x, m, x_perm, st));
+    rc = cuda_rc(launch_dispatch_x(p, x, m, x_perm, x8, st));
   }
   if (rc != HMM_OK) return rc;
   const bool inject = ctx->inject_skip_ready != 0;
@@ -491,9 +497,10 @@ namespace {
 enum BackwardMode { BWD_FULL = 0, BWD_DX = 1, BWD_DW = 2 };
 
 // hmm_backward, hmm_backward_dx and hmm_backward_dw.  BWD_DX runs everything
-// but the weight gradients and leaves their operands (dy_perm, dH and w*a as
-// bf16 hi + lo) in the workspace; BWD_DW runs only the weight gradients from
-// them.
+// but the weight gradients and leaves their operands (dy_perm and its fp8
+// copy, dH and w*a as bf16 high + e5m2 low parts) in the workspace; BWD_DW
+// runs only the weight gradients from them and the saved x_perm (and its fp8
+// copy).
 int backward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const void* topk_weights,
                   const void* up_proj_weight, const void* down_proj_weight, const void* Ws1,
                   const void* Ws2, const void* saved, size_t saved_bytes, void* dx,
@@ -544,9 +551,11 @@ int backward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const vo
   uint8_t* sv = const_cast<uint8_t*>(static_cast<const uint8_t*>(saved));
   MetaPtrs m = meta_at(p, sv + p.sv_meta);
   const void* x_perm = sv + p.sv_xperm;
+  const void* x8 = sv + p.sv_x8;
   const float* h32 = reinterpret_cast<const float*>(sv + p.sv_h);
   CtrlPtrs c = ctrl_at(p, ws + p.bw_ctrl);
   void* dy_perm = ws + p.bw_dyperm;
+  void* dy8 = ws + p.bw_dy8;
   float* wperm = reinterpret_cast<float*>(ws + p.bw_wperm);
   void* dH = ws + p.bw_dh;
   void* dH_lo = ws + p.bw_dhlo;
@@ -556,8 +565,8 @@ int backward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const vo
   float* dwp = reinterpret_cast<float*>(ws + p.bw_dwp);
   const GemmEnv env = env_of(ctx, p, st);
   auto weight_gemms = [&]() {
-    return launch_wgrad_pair(env, p, m, x_perm, dy_perm, dH, dH_lo, wa, wa_lo, d_up_proj_weight,
-                             d_down_proj_weight, dWs1, dWs2);
+    return launch_wgrad_pair(env, p, m, x_perm, x8, dy_perm, dy8, dH, dH_lo, wa, wa_lo,
+                             d_up_proj_weight, d_down_proj_weight, dWs1, dWs2);
   };
   const bool weights = d_up_proj_weight || d_down_proj_weight || dWs1 || dWs2;
   if (mode == BWD_DW) {
@@ -569,7 +578,8 @@ int backward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const vo
   {
     PhaseScope ps(ctx, PH_DISPATCH_DY, st);
     rc = cuda_rc(
-        launch_dispatch_dy(p, dy, topk_weights, shape->weights_dtype, m, c, dy_perm, wperm, st));
+        launch_dispatch_dy(p, dy, topk_weights, shape->weights_dtype, m, c, dy_perm, dy8, wperm,
+                           st));
   }
   if (rc != HMM_OK) return rc;
   {

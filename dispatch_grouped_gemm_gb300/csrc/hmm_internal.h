@@ -48,6 +48,9 @@ struct Plan {
   int64_t nchunks;      // routing warp-chunks
   int64_t nt_dswiglu;   // N tiles of the act_grad GEMM
   int64_t dwp_ld;       // per-row d_w partials (one per act_grad N tile)
+  // row strides (bytes) of the fp8 arrays of the weight-gradient low halves,
+  // padded to 16 bytes for TMA: H columns (x_perm8, dy_perm8), 2I (dH_lo8), I (wa_lo8)
+  int64_t ld8_h, ld8_2i, ld8_i;
   bool training;
   // byte offsets inside the buffers
   size_t meta_bytes;
@@ -55,16 +58,16 @@ struct Plan {
   size_t ctrl_bytes;
   size_t off_chunk_base, off_tickets, off_ready;                           // inside ctrl
   int64_t ctrl_zero_count;  // int32 counters from off_tickets that each call zeroes
-  // forward: saved = [meta | x_perm | h]      (training)
+  // forward: saved = [meta | x_perm | x_perm8 | h]   (training)
   //          workspace = [ctrl | a | o]       (training)
   //          workspace = [ctrl | meta | x_perm | a | o]   (inference)
   size_t saved_bytes, fwd_ws_bytes;
-  size_t sv_meta, sv_xperm, sv_h;
+  size_t sv_meta, sv_xperm, sv_x8, sv_h;
   size_t fw_ctrl, fw_meta, fw_xperm, fw_a, fw_o;
   // backward workspace =
-  //   [ctrl | dy_perm | wperm | dH | dH_lo | wa | wa_lo | dX_perm | dwp]
+  //   [ctrl | dy_perm | dy_perm8 | wperm | dH | dH_lo8 | wa | wa_lo8 | dX_perm | dwp]
   size_t bwd_ws_bytes;
-  size_t bw_ctrl, bw_dyperm, bw_wperm, bw_dh, bw_dhlo, bw_wa, bw_walo, bw_dxperm, bw_dwp;
+  size_t bw_ctrl, bw_dyperm, bw_dy8, bw_wperm, bw_dh, bw_dhlo, bw_wa, bw_walo, bw_dxperm, bw_dwp;
 };
 
 int make_plan(const hmm_shape* s, bool training, Plan* p);
@@ -76,12 +79,14 @@ CtrlPtrs ctrl_at(const Plan& p, void* base);
 cudaError_t launch_route(const Plan& p, const int32_t* ids, MetaPtrs m, CtrlPtrs c,
                          int32_t* slot2row, int32_t* row2slot, unsigned* status,
                          cudaStream_t st);
-cudaError_t launch_dispatch_x(const Plan& p, const void* x, MetaPtrs m, void* x_perm,
+// x8 (training, else null): also x_perm as e4m3 (ld8_h bytes per row)
+cudaError_t launch_dispatch_x(const Plan& p, const void* x, MetaPtrs m, void* x_perm, void* x8,
                               cudaStream_t st);
 cudaError_t launch_combine_y(const Plan& p, const void* o, const void* w, int w_dtype, MetaPtrs m,
                              void* y, cudaStream_t st);
+// also dy_perm as e5m2 (dy8, ld8_h bytes per row)
 cudaError_t launch_dispatch_dy(const Plan& p, const void* dy, const void* w, int w_dtype,
-                               MetaPtrs m, CtrlPtrs c, void* dy_perm, float* wperm,
+                               MetaPtrs m, CtrlPtrs c, void* dy_perm, void* dy8, float* wperm,
                                cudaStream_t st);
 cudaError_t launch_combine_dx(const Plan& p, const void* dx_perm, const float* dwp, MetaPtrs m,
                               void* dx, void* dw, int w_dtype, cudaStream_t st);
@@ -110,8 +115,8 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
                          const void* x_perm, const void* W1, const void* W2, const void* Ws1,
                          const void* Ws2, void* a, float* h32, void* o, bool skip_ready_release);
 // backward data gradients in one persistent launch: act_grad (+SwiGLU grad,
-// d_w partials; dH and w*a written as bf16 hi + lo) and input-grad (released
-// per M tile), routed and shared experts.
+// d_w partials; dH and w*a written as a bf16 high part plus an e5m2 low part)
+// and input-grad (released per M tile), routed and shared experts.
 int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
                            const void* dy_perm, const float* wperm, const float* h32,
                            const void* W1, const void* W2, const void* Ws1, const void* Ws2,
@@ -119,9 +124,11 @@ int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPt
                            void* dx_perm);
 // weight gradients on CTA pairs (tcgen05 cta_group::2), 256 x 256 tiles:
 // dW1 / dW2 of the routed experts and dWs1 / dWs2 of the shared expert (any
-// may be null).
+// may be null).  The low parts (dH_lo8, wa_lo8: e5m2) meet fp8 copies of the
+// other operand (x8: e4m3, dy8: e5m2) in a second, fp8 MMA.
 int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, const void* x_perm,
-                      const void* dy_perm, const void* dH, const void* dH_lo, const void* wa,
-                      const void* wa_lo, void* dW1, void* dW2, void* dWs1, void* dWs2);
+                      const void* x8, const void* dy_perm, const void* dy8, const void* dH,
+                      const void* dH_lo8, const void* wa, const void* wa_lo8, void* dW1,
+                      void* dW2, void* dWs1, void* dWs2);
 
 }  // namespace hmm

@@ -12,6 +12,7 @@
 #include <cuda_bf16.h>
 
 #include "hmm_internal.h"
+#include "ptx.cuh"
 
 namespace hmm {
 
@@ -40,6 +41,19 @@ __device__ __forceinline__ void acc8(float (&acc)[8], const uint4& v, float s) {
   }
 }
 
+// Eight bf16 values to eight fp8 values (e5m2 or e4m3, saturating).
+template <bool E5M2>
+__device__ __forceinline__ uint2 bf16x8_to_fp8(const uint4& v) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  float f[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    f[2 * j] = __uint_as_float(u[j] << 16);
+    f[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
+  }
+  return pack_fp8x8<E5M2>(f);
+}
+
 __device__ __forceinline__ uint4 pack8(const float (&acc)[8]) {
   uint4 r;
   uint32_t* u = reinterpret_cast<uint32_t*>(&r);
@@ -63,11 +77,14 @@ constexpr int DISPATCH_UNROLL = 8;  // dispatch: a whole 2048-wide row per pass
 // warps past T zero the padding rows of each expert (so every padded row of
 // the GEMM operands is defined).  Optionally also scatters the routing weight
 // of every slot to its padded row (wperm: 1 on the shared rows, 0 on padding
-// rows).
+// rows), and writes an fp8 copy of every row (dst8, ld8 8-byte groups per
+// row; E5M2: e5m2, else e4m3), the weight-gradient GEMMs' operand for the
+// low parts of their split operand.
+template <bool E5M2>
 __global__ void __launch_bounds__(MOVE_THREADS) dispatch_rows_kernel(
     const uint4* __restrict__ src, int64_t T, int64_t K, int64_t H8, MetaPtrs m, int E, int Ex,
-    uint4* __restrict__ dst, const void* w, int w_dtype, float* wperm, int32_t* zero_ptr,
-    int64_t zero_count) {
+    uint4* __restrict__ dst, uint2* __restrict__ dst8, int64_t ld8, const void* w, int w_dtype,
+    float* wperm, int32_t* zero_ptr, int64_t zero_count) {
   const int lane = threadIdx.x & 31;
   const int64_t g = static_cast<int64_t>(blockIdx.x) * MOVE_WARPS + (threadIdx.x >> 5);
   if (zero_ptr) {
@@ -104,6 +121,14 @@ __global__ void __launch_bounds__(MOVE_THREADS) dispatch_rows_kernel(
           const int64_t c = c0 + 32 * u;
           if (c < H8) d[c] = v[u];
         }
+        if (dst8) {
+          uint2* d8 = dst8 + static_cast<int64_t>(prow) * ld8;
+#pragma unroll
+          for (int u = 0; u < DISPATCH_UNROLL; ++u) {
+            const int64_t c = c0 + 32 * u;
+            if (c < H8) d8[c] = bf16x8_to_fp8<E5M2>(v[u]);
+          }
+        }
       }
     }
   } else {
@@ -116,6 +141,10 @@ __global__ void __launch_bounds__(MOVE_THREADS) dispatch_rows_kernel(
     uint4* d = dst + static_cast<int64_t>(row) * H8;
     const uint4 z = make_uint4(0, 0, 0, 0);
     for (int64_t c = lane; c < H8; c += 32) d[c] = z;
+    if (dst8) {
+      uint2* d8 = dst8 + static_cast<int64_t>(row) * ld8;
+      for (int64_t c = lane; c < H8; c += 32) d8[c] = make_uint2(0, 0);
+    }
   }
 }
 
@@ -204,25 +233,27 @@ static int move_grid(int64_t warps) {
   return static_cast<int>((warps + MOVE_WARPS - 1) / MOVE_WARPS);
 }
 
-cudaError_t launch_dispatch_x(const Plan& p, const void* x, MetaPtrs m, void* x_perm,
+cudaError_t launch_dispatch_x(const Plan& p, const void* x, MetaPtrs m, void* x_perm, void* x8,
                               cudaStream_t st) {
   const int64_t warps = p.T + p.Ex * BM;
-  dispatch_rows_kernel<<<move_grid(warps), MOVE_THREADS, 0, st>>>(
+  dispatch_rows_kernel<false><<<move_grid(warps), MOVE_THREADS, 0, st>>>(
       static_cast<const uint4*>(x), p.T, p.K, p.H / 8, m, static_cast<int>(p.E),
-      static_cast<int>(p.Ex), static_cast<uint4*>(x_perm), nullptr, 0, nullptr, nullptr, 0);
+      static_cast<int>(p.Ex), static_cast<uint4*>(x_perm), static_cast<uint2*>(x8), p.ld8_h / 8,
+      nullptr, 0, nullptr, nullptr, 0);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dispatch_dy(const Plan& p, const void* dy, const void* w, int w_dtype,
-                               MetaPtrs m, CtrlPtrs c, void* dy_perm, float* wperm,
+                               MetaPtrs m, CtrlPtrs c, void* dy_perm, void* dy8, float* wperm,
                                cudaStream_t st) {
   const int64_t warps = p.T + p.Ex * BM;
   // also zero the backward launch counters (tickets and per-M-tile ready
   // counters are contiguous in the control block)
   const int64_t nzero = p.ctrl_zero_count;
-  dispatch_rows_kernel<<<move_grid(warps), MOVE_THREADS, 0, st>>>(
+  dispatch_rows_kernel<true><<<move_grid(warps), MOVE_THREADS, 0, st>>>(
       static_cast<const uint4*>(dy), p.T, p.K, p.H / 8, m, static_cast<int>(p.E),
-      static_cast<int>(p.Ex), static_cast<uint4*>(dy_perm), w, w_dtype, wperm, c.tickets, nzero);
+      static_cast<int>(p.Ex), static_cast<uint4*>(dy_perm), static_cast<uint2*>(dy8),
+      p.ld8_h / 8, w, w_dtype, wperm, c.tickets, nzero);
   return cudaGetLastError();
 }
 

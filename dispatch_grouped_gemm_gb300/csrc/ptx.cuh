@@ -315,6 +315,15 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, 
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The same with 8-bit operands (kind::f8f6f4: K = 32 per instruction).
+__device__ __forceinline__ void umma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrive on the mbarrier at the same offset in every CTA of `mask` once the
 // pair MMAs issued so far are done.
 __device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t mask) {
@@ -353,6 +362,43 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
          | (static_cast<uint32_t>(b_mn) << 16)      // B major
          | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// Instruction descriptor of tcgen05.mma kind::f8f6f4 with 8-bit operands
+// (format codes F8_E4M3, F8_E5M2) -> fp32.
+constexpr int F8_E4M3 = 0;
+constexpr int F8_E5M2 = 1;
+__host__ __device__ constexpr uint32_t idesc_f8_f32(int M, int N, int a_fmt, int b_fmt, int a_mn,
+                                                    int b_mn) {
+  return (1u << 4)                                  // D format: f32
+         | (static_cast<uint32_t>(a_fmt) << 7)      // A format
+         | (static_cast<uint32_t>(b_fmt) << 10)     // B format
+         | (static_cast<uint32_t>(a_mn) << 15)      // A major
+         | (static_cast<uint32_t>(b_mn) << 16)      // B major
+         | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// Two floats to two fp8 values (round to nearest even, saturating to the
+// largest finite value), lo in the low byte.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t cvt_e5m2x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Eight floats to eight fp8 values (E5M2: e5m2, else e4m3), element 0 in byte 0.
+template <bool E5M2>
+__device__ __forceinline__ uint2 pack_fp8x8(const float* v) {
+  uint32_t q[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    q[j] = E5M2 ? cvt_e5m2x2(v[2 * j], v[2 * j + 1]) : cvt_e4m3x2(v[2 * j], v[2 * j + 1]);
+  return make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
 }
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }

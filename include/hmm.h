@@ -273,8 +273,8 @@ int hmm_backward_shared(hmm_ctx* ctx, const hmm_shape* shape, const void* dy,
  * hmm_backward_dx: what hmm_backward does without the weight gradients
  *   (dispatch dY, act_grad + SwiGLU grad, input-grad, combine dX and
  *   d_topk_weights; dx or d_topk_weights may be NULL).  It leaves in
- *   `workspace` the operands of the weight gradients: dY permuted, dH and
- *   w*a (bf16 hi + lo halves).
+ *   `workspace` the operands of the weight gradients: dY permuted (bf16 and
+ *   an fp8 copy), dH and w*a (bf16 high parts and fp8 low parts).
  * hmm_backward_dw: d_up_proj_weight and d_down_proj_weight (either may be
  *   NULL) from those operands and `saved`.  Call it on the same stream, after
  *   the hmm_backward_dx of the same shape, `saved` and `workspace`; nothing
