@@ -374,12 +374,15 @@ def run_ours(args, dist: Dist):
     # per-phase algorithmic work and roofline of the dominant kernel
     TK = T * K
     F = 2.0 * TK * H * I  # one "unit": 2*TK*H*I flops
+    # dispatch: x (dy) read once, K bf16 rows written, and in training an fp8
+    # copy of each row (the weight-gradient GEMMs' operand for the low parts)
+    fp8_rows = 0.0 if fwd_only else TK * H * 1.0
     algo = {
         "route": ("hbm", 3 * TK * 4.0),
-        "dispatch_x": ("hbm", (T * H + TK * H) * 2.0),
+        "dispatch_x": ("hbm", (T * H + TK * H) * 2.0 + fp8_rows),
         "gemm_fwd": ("tensor", 3 * F),
         "combine_y": ("hbm", (TK * H + T * H) * 2.0 + TK * 2.0),
-        "dispatch_dy": ("hbm", (T * H + TK * H) * 2.0),
+        "dispatch_dy": ("hbm", (T * H + TK * H) * 2.0 + fp8_rows),
         "gemm_bwd_data": ("tensor", 3 * F),    # act_grad F + input-grad 2F
         "gemm_bwd_weight": ("tensor", 3 * F),  # W1Grad 2F + W2Grad F
         "combine_dx": ("hbm", (TK * H + T * H) * 2.0),
