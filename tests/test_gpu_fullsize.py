@@ -90,8 +90,13 @@ def test_backward_full_size(run):
         ids_s = np.zeros((t_idx.size, 1), np.int32)
         rW1, rW2 = oracle.weight_grad(0, prob.x[t_idx], ids_s, w_s, prob.expert_W1(e)[None],
                                       prob.expert_W2(e)[None], prob.dy[t_idx])
-        gu.check(f"d_up_proj_weight[{e}]", gu.f64(dW1[e]), rW1)
-        gu.check(f"d_down_proj_weight[{e}]", gu.f64(dW2[e]), rW2)
+        # the weight-gradient GEMMs add the e5m2 low part of their rounded
+        # operand; with the bf16 part alone the worst element of these
+        # experts lands near 3x the bound, with it the bf16 rounding of dW
+        # itself dominates (a CPU rounding model puts both near 0.2-0.3)
+        r1 = gu.check(f"d_up_proj_weight[{e}]", gu.f64(dW1[e]), rW1)
+        r2 = gu.check(f"d_down_proj_weight[{e}]", gu.f64(dW2[e]), rW2)
+        assert max(r1, r2) < 0.6, (e, r1, r2)
     assert run.status() == (0, 0)
 
 
