@@ -39,6 +39,28 @@ __device__ __forceinline__ void xpose(float* buf, int lane, const uint32_t (&r)[
   __syncwarp();
 }
 
+// The same two halves for an accumulator whose TMEM lanes are output columns
+// and whose TMEM columns are output rows (the row-mode GEMMs keep the weights
+// on the MMA's M side): thread t writes its 32 values, rows 0..31 of column t,
+// down column t of the buffer (conflict-free: row i of the 32 threads spans
+// all banks), so the buffer holds the block row-major ...
+__device__ __forceinline__ void xwrite_t(float* buf, int lane, const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) buf[i * XS + lane] = __uint_as_float(r[i]);
+}
+// ... and, after a __syncwarp (or a barrier with the writing warp), lane l
+// reads the eight columns 8*(l & 3) .. +7 of the rows (l >> 2) + 8k.
+__device__ __forceinline__ void xread(const float* buf, int lane, float (&o)[4][8]) {
+  const float* s = buf + (lane >> 2) * XS + (lane & 3) * 8;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float4 a = *reinterpret_cast<const float4*>(s + k * 8 * XS);
+    const float4 b = *reinterpret_cast<const float4*>(s + k * 8 * XS + 4);
+    o[k][0] = a.x; o[k][1] = a.y; o[k][2] = a.z; o[k][3] = a.w;
+    o[k][4] = b.x; o[k][5] = b.y; o[k][6] = b.z; o[k][7] = b.w;
+  }
+}
+
 __device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
   uint4 u;
   u.x = pack_bf16(v[0], v[1]);

@@ -5,15 +5,19 @@
 // [HyperMegaMoE §2.1 GMM1/up_proj -> SwiGLU -> GMM2/down_proj; §2.2 act_grad
 // with SwiGLUGrad, input-grad GMM]:
 //
-//   out[rows of e] = A[rows of e] . B[e]
+//   out[rows of e] = T[rows of e] . W[e]
 //
-// A holds the expert's routed rows in the padded row space (128-row tiles
-// never span two experts): x_perm / dy_perm, written by the dispatch kernels,
-// or a / dH, written by the GMM1 / act_grad epilogues.  B is the expert's
-// weight slab, MN-major (forward) or K-major (backward).  (Gathering the A
-// rows by token with TMA gather4 loads instead of a separate permute was
-// measured about 3.5x slower per tile: 32 requests per K block.)  The weight
-// gradients run in gmm_pair.cu.
+// T holds the expert's routed token rows in the padded row space (x_perm /
+// dy_perm, written by the dispatch kernels, or a / dH, written by the GMM1 /
+// act_grad epilogues); W is the expert's weight slab.  The MMA computes the
+// transposed product, out^T = W^T . T^T: the weight columns sit on M (128 per
+// CTA, the TMEM lanes) and the token rows on N (up to 256 per tile, the
+// accumulator columns).  A tile's token block is cut at a multiple of 64 rows
+// past the expert's last row, so an expert of 384 rows costs 256 + 128 rows of
+// MMA work instead of four 128-row tiles.  (Gathering the token rows with TMA
+// gather4 loads instead of a separate permute was measured about 3.5x slower
+// per tile: 32 requests per K block.)  The weight gradients run in
+// gmm_pair.cu.
 //
 // One launch holds up to four problems: a producer and a consumer problem for
 // the routed experts [0, E) and, with the optional shared expert
@@ -22,26 +26,26 @@
 // weight slabs.  Tiles are handed out through a global atomic ticket in
 // "schedule steps": step j holds, for every problem p, the tiles of expert
 // j - lag_p (if it lies in p's expert range).  The consumer problems run
-// behind every producer tile and wait on per-M-tile ready counters that the
-// producer's
-// epilogues release [HyperMegaMoE §2.1: tasks split by token/expert tile,
-// event counts release downstream tasks, no global barrier].  Every producer
-// tile has a smaller ticket than its consumers, so it was already taken by a
-// running CTA when a consumer spins: the wait cannot deadlock (and is bounded
-// anyway).
+// behind every producer tile and wait on per-token-block ready counters that
+// the producer's epilogues release [HyperMegaMoE §2.1: tasks split by
+// token/expert tile, event counts release downstream tasks, no global
+// barrier].  Every producer tile has a smaller ticket than its consumers, so
+// it was already taken by a running CTA when a consumer spins: the wait
+// cannot deadlock (and is bounded anyway).
 //
 // CTA = 7 warps: warp 6 schedules tiles (tickets, decoding, dependency waits,
 // about one tile ahead), warp 0 issues TMA loads, warp 1 allocates TMEM and
 // issues tcgen05.mma (one thread), warps 2..5 drain the accumulators (each
-// owns the 32 TMEM lanes of its warp id mod 4).  Two 128x256 fp32 accumulators
-// in TMEM (512 columns) let the epilogue of one tile overlap the MMAs of the
-// next; 192 KB of shared-memory stages feed the MMAs.
+// owns the 32 TMEM lanes, i.e. weight columns, of its warp id mod 4).  Two
+// 128 x 256 fp32 accumulators in TMEM (512 columns) let the epilogue of one
+// tile overlap the MMAs of the next; 192 KB of shared-memory stages feed the
+// MMAs.
 //
-// PAIR = true: clusters of two CTAs compute 256x256 tiles (two 128-row M
-// tiles of one expert) with 2-SM MMAs (tcgen05.mma.cta_group::2): each CTA
-// stages its own 128 rows of A and 128 of the 256 columns of B and drains its
-// own 128x256 accumulator.  Only the even CTA schedules; it writes each tile
-// record into both CTAs' rings.
+// PAIR = true: clusters of two CTAs compute tiles of 256 weight columns with
+// 2-SM MMAs (tcgen05.mma.cta_group::2): each CTA stages its own 128 weight
+// columns and half of the token rows and drains its own 128 x N accumulator.
+// Only the even CTA schedules; it writes each tile record into both CTAs'
+// rings.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -53,25 +57,36 @@ namespace hmm {
 
 enum Epi : int { EPI_SWIGLU = 0, EPI_STORE = 1, EPI_DSWIGLU = 2 };
 
-// EPI: epilogue; B_MN: B operand MN-major (else K-major).  A is K-major.
-template <int EPI_, bool B_MN_>
+// Weight columns per CTA (the TMEM lanes), token rows per tile at most (the
+// accumulator columns) and the granularity of a token block's end.
+constexpr int BW = 128;
+constexpr int NT = 256;
+constexpr int TROWS = 64;  // also the weight-gradient GEMMs' K block: rows they read are written
+
+// EPI: epilogue; W_MN: weights MN-major (forward), else K-major (data
+// gradients).  Token rows are K-major.  IDESC / IDESC2: instruction
+// descriptors (1 CTA: M = 128; CTA pair: M = 256) without N, which each tile
+// sets to its token rows.
+template <int EPI_, bool W_MN_>
 struct Cfg {
   static constexpr int EPI = EPI_;
-  static constexpr bool B_MN = B_MN_;
-  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, 0, B_MN ? 1 : 0);
-  // 2-SM MMA of a CTA pair: M = 256 rows (128 per CTA), the same N
-  static constexpr uint32_t IDESC2 = idesc_bf16_f32(2 * BM, BN, 0, B_MN ? 1 : 0);
+  static constexpr bool W_MN = W_MN_;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BW, 0, W_MN ? 1 : 0, 0);
+  static constexpr uint32_t IDESC2 = idesc_bf16_f32(2 * BW, 0, W_MN ? 1 : 0, 0);
+  // output columns (SwiGLU: I columns, gate and up) of one CTA's 128 lanes
+  static constexpr int WCOLS = EPI == EPI_SWIGLU ? BW / 2 : BW;
 };
+__host__ __device__ constexpr uint32_t idesc_n(int n) { return static_cast<uint32_t>(n >> 3) << 17; }
 
 constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-// CTA pairs: each CTA stages its 128 rows of A and 128 of the 256 columns of
-// B, 32 KB per K block, in six stages (the same 192 KB)
+constexpr int W_BYTES = BW * BK * 2;  // 16 KB: 128 weight columns, 64 deep
+constexpr int T_BYTES = NT * BK * 2;  // 32 KB: 256 token rows, 64 deep
+constexpr int STAGE_BYTES = W_BYTES + T_BYTES;
+// CTA pairs: each CTA stages its 128 weight columns and up to 128 of the
+// token rows, 32 KB per K block, in six stages (the same 192 KB)
 constexpr int PAIR_STAGES = 6;
-constexpr int PAIR_B_BYTES = (BN / 2) * BK * 2;  // 16 KB
-constexpr int PAIR_STAGE_BYTES = A_BYTES + PAIR_B_BYTES;
+constexpr int PAIR_T_BYTES = (NT / 2) * BK * 2;  // 16 KB
+constexpr int PAIR_STAGE_BYTES = W_BYTES + PAIR_T_BYTES;
 constexpr int MAX_STAGES = PAIR_STAGES;
 static_assert(PAIR_STAGES * PAIR_STAGE_BYTES <= STAGES * STAGE_BYTES, "pair stages");
 constexpr int TI_DEPTH = 3;
@@ -80,7 +95,6 @@ constexpr int TI_DEPTH = 3;
 // measured slower: every SM sub-partition then runs two epilogue warps beside
 // the single-thread MMA and TMA loops.)
 constexpr int EPI_WARPS = 4;
-constexpr int CH_SPLIT = EPI_WARPS / 4;  // warps sharing a lane quarter
 constexpr int SCHED_WARP = 2 + EPI_WARPS;
 constexpr int NUM_THREADS = 32 * (SCHED_WARP + 1);  // 7 warps
 constexpr int MAX_PROB = 4;
@@ -90,12 +104,12 @@ constexpr int MAX_STEPS = 2 * MAX_E + 8;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_WARPS * XBUF_BYTES + 512 +
                            4 * (MAX_STEPS + 1) + 256;
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
-constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr uint32_t TMEM_COLS = 2 * NT;
 
 struct Prob {
   int K;        // contraction length
   int N;        // valid output columns (SwiGLU / SwiGLU grad: I)
-  int n_tiles;  // tiles along N
+  int n_tiles;  // weight tiles along N (a CTA pair's tile spans both CTAs' columns)
   int half;     // SwiGLU: I (offset of the up half in the 2I operand/outputs)
   void* out;
   int64_t ld_out;
@@ -108,19 +122,19 @@ struct Prob {
   int64_t ld_lo4, ld_lo5;
   int out_f32;          // STORE: fp32 outputs (else bf16)
   int lag;              // the tiles of expert e are issued at schedule step e + lag
-  int e_lo, e_hi;       // experts of this problem; B holds experts e_lo .. e_hi - 1
+  int e_lo, e_hi;       // experts of this problem; W holds experts e_lo .. e_hi - 1
   const void* aux;      // SwiGLU grad: the blocked fp32 pre-activations
   int64_t ld_aux;       // their column blocks per row block
   const float* rowscale;
-  int* signal_m;        // per-M-tile counters released after a tile's stores
-  const int* wait_m;    // per-M-tile counter acquired before a tile's loads
-  int wait_unit;        // per-M-tile target
+  int* signal_m;        // per-token-block counters (index row0 / 64) released after a tile
+  const int* wait_m;    // per-token-block counter acquired before a tile's loads
+  int wait_unit;        // per-token-block target
 };
 
 struct Params {
   Prob p[MAX_PROB];
   int nprob;
-  int pair;             // CTA pairs: a tile is two M tiles of one expert
+  int pair;             // CTA pairs: a tile spans 256 weight columns
   int steps;            // E + largest lag
   const int32_t* poff;
   const int32_t* counts;
@@ -133,16 +147,16 @@ struct Params {
 };
 
 struct Maps {
-  CUtensorMap m[MAX_PROB][2];  // A, B
+  CUtensorMap m[MAX_PROB][2];  // token rows, weights
 };
 
 struct TileInfo {
   int prob;   // -1: no more tiles
   int e;
-  int m0;     // first padded row (of the pair)
-  int n0;     // first output column
+  int row0;   // first padded row of the token block (a multiple of 64)
+  int nrow;   // token rows of the block: 64 .. 256, a multiple of 64
+  int w0;     // first output column of the tile (of the even CTA in a pair)
   int kb;     // K blocks
-  int ph;     // pair tile whose second M tile lies past the expert (odd M-tile count)
 };
 
 // ------------------------------------------------------------------ tracing
@@ -157,14 +171,15 @@ __device__ __forceinline__ uint32_t sm_id() {
 }
 
 // ----------------------------------------------------------------- scheduler
-__device__ __forceinline__ int mtiles_of(const Params& P, int e) {
-  return (P.poff[e + 1] - P.poff[e]) / BM;
+// Token blocks of expert e: 256 rows each, the last one ending at the first
+// multiple of 64 rows at or past the expert's last row.
+__device__ __forceinline__ int nblocks_of(const Params& P, int e) {
+  return (P.counts[e] + NT - 1) / NT;
 }
 
 __device__ __forceinline__ int tiles_of(const Params& P, const Prob& pr, int e) {
   if (e < pr.e_lo || e >= pr.e_hi) return 0;
-  const int nm = mtiles_of(P, e);
-  return (P.pair ? (nm + 1) / 2 : nm) * pr.n_tiles;
+  return nblocks_of(P, e) * pr.n_tiles;
 }
 
 // Prefix sums of the tile counts of the schedule steps (one warp, into smem).
@@ -219,78 +234,75 @@ __device__ bool locate_tile(const Params& P, const int* pref, int t, int& prob, 
 template <class C>
 __device__ void decode_tile(const Params& P, const Prob& pr, int e, int r, TileInfo& ti) {
   ti.e = e;
-  const int nm = mtiles_of(P, e);
-  const int nu = P.pair ? (nm + 1) / 2 : nm;  // M tiles or M-tile pairs
-  const int nb = r / nu;  // M innermost: a weight tile is reused from L2
-  const int mu = r - nb * nu;
-  ti.m0 = P.poff[e] + mu * BM * (P.pair ? 2 : 1);
-  ti.ph = P.pair && 2 * mu + 1 >= nm;
-  ti.n0 = nb * (C::EPI == EPI_SWIGLU ? BN / 2 : BN);
+  const int nb = nblocks_of(P, e);
+  const int wt = r / nb;  // token blocks innermost: a weight tile is reused from L2
+  const int b = r - wt * nb;
+  const int rows = (P.counts[e] + TROWS - 1) / TROWS * TROWS;
+  ti.row0 = P.poff[e] + NT * b;
+  ti.nrow = min(NT, rows - NT * b);
+  ti.w0 = wt * C::WCOLS * (P.pair ? 2 : 1);
   ti.kb = (pr.K + BK - 1) / BK;
 }
 
 // ----------------------------------------------------------------- producer
-// K block kb of a tile into one smem stage (one thread).  Every box starts at
-// an inner coordinate that is a multiple of 8 elements (16 bytes).
-//   PAIR: this CTA's share (its 128 rows of A, its 128 columns of B), counted
-//   on the even CTA's full barrier (shared::cluster address bar_cl; the even
-//   CTA arms it for both).  Without rows of A (load_a false: the empty half of
-//   an expert's last pair) the A box starts at row -BM, entirely outside the
-//   tensor: the copy fills the stage with zeros and reads no memory, so that
-//   half's MMAs run on zeros instead of a stale stage.
+// K block kb of a tile into one smem stage (one thread): this CTA's 128 weight
+// columns (sW) and the tile's token rows (sT).  Every box starts at an inner
+// coordinate that is a multiple of 8 elements (16 bytes).
+//   PAIR: this CTA's share (its weight columns, its half of the token rows),
+//   counted on the even CTA's full barrier (shared::cluster address bar_cl;
+//   the even CTA arms it for both).  A 128-row token box always lands whole;
+//   the MMA reads the rows it needs.  (64-row boxes sized to each tile cut the
+//   bytes of tiles under 256 rows but made both launches slower: the
+//   pipeline is bound by the latency of a stage's loads, not their bytes.)
 template <class C, bool PAIR>
 __device__ __forceinline__ void load_stage(const Prob& pr, const TileInfo& ti, int kb,
-                                           const CUtensorMap* tA, const CUtensorMap* tB,
-                                           uint8_t* sA, uint8_t* sB, uint64_t* bar,
-                                           uint32_t bar_cl, uint32_t rank, bool load_a) {
+                                           const CUtensorMap* tT, const CUtensorMap* tW,
+                                           uint8_t* sW, uint8_t* sT, uint64_t* bar,
+                                           uint32_t bar_cl, uint32_t rank) {
   const int k = kb * BK;
   const int eb = ti.e - pr.e_lo;  // expert index inside this problem's weight slabs
+  const int wc = ti.w0 + C::WCOLS * static_cast<int>(rank);  // this CTA's first column
   if constexpr (PAIR) {
-    if (rank == 0) mbar_arrive_expect_tx(bar, 2 * A_BYTES + 2 * PAIR_B_BYTES);
-    tma_load_2d_pair(sA, tA, bar_cl, k, load_a ? ti.m0 + BM * static_cast<int>(rank) : -BM);
-    if constexpr (C::B_MN) {
-      int c;
-      if constexpr (C::EPI == EPI_SWIGLU)
-        c = (rank == 0 ? 0 : pr.half) + ti.n0;  // gate columns | up columns
-      else
-        c = ti.n0 + (BN / 2) * static_cast<int>(rank);
-      tma_load_3d_pair(sB, tB, bar_cl, c, k, eb);
-      tma_load_3d_pair(sB + 8192, tB, bar_cl, c + 64, k, eb);
+    if (rank == 0) mbar_arrive_expect_tx(bar, 2 * (W_BYTES + PAIR_T_BYTES));
+    if constexpr (C::W_MN) {
+      // SwiGLU: 64 gate columns, then the same 64 up columns
+      const int c2 = C::EPI == EPI_SWIGLU ? pr.half + wc : wc + 64;
+      tma_load_3d_pair(sW, tW, bar_cl, wc, k, eb);
+      tma_load_3d_pair(sW + 8192, tW, bar_cl, c2, k, eb);
     } else {
-      tma_load_3d_pair(sB, tB, bar_cl, k, ti.n0 + (BN / 2) * static_cast<int>(rank), eb);
+      tma_load_3d_pair(sW, tW, bar_cl, k, wc, eb);
     }
+    tma_load_2d_pair(sT, tT, bar_cl, k, ti.row0 + (ti.nrow / 2) * static_cast<int>(rank));
   } else {
-    mbar_arrive_expect_tx(bar, STAGE_BYTES);
-    tma_load_2d(sA, tA, bar, k, ti.m0);
-    if constexpr (C::B_MN) {
-      if constexpr (C::EPI == EPI_SWIGLU) {
-        tma_load_3d(sB, tB, bar, ti.n0, k, eb);
-        tma_load_3d(sB + 8192, tB, bar, ti.n0 + 64, k, eb);
-        tma_load_3d(sB + 16384, tB, bar, pr.half + ti.n0, k, eb);
-        tma_load_3d(sB + 24576, tB, bar, pr.half + ti.n0 + 64, k, eb);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) tma_load_3d(sB + j * 8192, tB, bar, ti.n0 + 64 * j, k, eb);
-      }
+    const bool two = ti.nrow > NT / 2;
+    mbar_arrive_expect_tx(bar, W_BYTES + (two ? 2 : 1) * PAIR_T_BYTES);
+    if constexpr (C::W_MN) {
+      const int c2 = C::EPI == EPI_SWIGLU ? pr.half + wc : wc + 64;
+      tma_load_3d(sW, tW, bar, wc, k, eb);
+      tma_load_3d(sW + 8192, tW, bar, c2, k, eb);
     } else {
-      tma_load_3d(sB, tB, bar, k, ti.n0, eb);
+      tma_load_3d(sW, tW, bar, k, wc, eb);
     }
+    tma_load_2d(sT, tT, bar, k, ti.row0);
+    if (two) tma_load_2d(sT + PAIR_T_BYTES, tT, bar, k, ti.row0 + NT / 2);
   }
 }
 
 // ---------------------------------------------------------------------- MMA
+// Weights: MN-major (two 64-column chunks 8 KB apart, 8-row groups 1 KB,
+// 2 KB per 16-deep step) or K-major; token rows K-major.
 template <class C, bool PAIR>
-__device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t a_base, uint32_t b_base,
-                                          bool first) {
+__device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t w_base, uint32_t t_base,
+                                          uint32_t idesc, bool first) {
 #pragma unroll
   for (int kk = 0; kk < BK / 16; ++kk) {
-    const uint64_t ad = smem_desc(a_base + kk * 32, 16, 1024, LAYOUT_SW128);
-    const uint64_t bd = C::B_MN ? smem_desc(b_base + kk * 2048, 8192, 1024, LAYOUT_SW128)
-                                : smem_desc(b_base + kk * 32, 16, 1024, LAYOUT_SW128);
+    const uint64_t ad = C::W_MN ? smem_desc(w_base + kk * 2048, 8192, 1024, LAYOUT_SW128)
+                                : smem_desc(w_base + kk * 32, 16, 1024, LAYOUT_SW128);
+    const uint64_t bd = smem_desc(t_base + kk * 32, 16, 1024, LAYOUT_SW128);
     if constexpr (PAIR)
-      umma_bf16_pair(d_tmem, ad, bd, C::IDESC2, (first && kk == 0) ? 0u : 1u);
+      umma_bf16_pair(d_tmem, ad, bd, idesc, (first && kk == 0) ? 0u : 1u);
     else
-      umma_bf16(d_tmem, ad, bd, C::IDESC, (first && kk == 0) ? 0u : 1u);
+      umma_bf16(d_tmem, ad, bd, idesc, (first && kk == 0) ? 0u : 1u);
   }
 }
 
@@ -333,162 +345,226 @@ __device__ __forceinline__ void store_f32x8(float* dst, const float* v) {
   reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
 
-// Drains the accumulator of one tile.  taddr addresses this warp's TMEM lane
-// quarter, whose rows are r0 .. r0 + 31 of the output (r0 = m0 + 32 * quarter);
-// ch: which warp of the lane quarter (column chunks ch, ch + CH_SPLIT, ...).
-// Column chunks are skipped per lane with plain conditionals, never an early
-// continue: the next chunk's TMEM load is a warp-wide instruction.
+// State an epilogue warp carries from tile to tile.  The SwiGLU epilogue
+// pairs the gate lane quarter g (0, 1) with the up quarter g + 2: both stage
+// their transposed 32 x 32 block in shared memory and each then reads both
+// blocks for half of the rows; xfull / xfree (two arrivals each) order the
+// exchange, one phase per chunk.
+struct EpiState {
+  int q;            // TMEM lane quarter of this warp
+  int lane;
+  float* xbufs;     // the four quarters' transposition buffers
+  uint64_t* xfull;  // [2], per gate quarter
+  uint64_t* xfree;  // [2]
+  uint32_t nchunk;  // chunks exchanged so far (SwiGLU)
+};
+
+// lane 0 waits (bounded) on bar's phase `parity`; every lane gets the result
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int lane,
+                                          const WaitCtl& wc) {
+  bool ok = false;
+  if (lane == 0) ok = mbar_wait(bar, parity, wc);
+  __syncwarp();
+  return __shfl_sync(0xffffffffu, ok, 0);
+}
+
+// Drains the accumulator of one tile: TMEM lanes of quarter q are the output
+// columns c0 .. c0 + 31 (c0 = first column of this CTA + 32 q; SwiGLU: the I
+// columns of the gate / up quarter pair), TMEM columns 32 j .. 32 j + 31 the
+// token rows row0 + 32 j .. of chunk j.  Each chunk goes through the
+// transposition buffer, after which lane l holds columns 8 (l & 3) .. + 7 of
+// the rows (l >> 2) + 8 k.  Column chunks are skipped per lane with plain
+// conditionals, never an early exit: the next chunk's TMEM load is a
+// warp-wide instruction.  ok turns false when a bounded wait gave up.
 template <class C>
 __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti, uint32_t taddr,
-                                              int64_t r0, int lane, int ch, float* xbuf) {
-  const int cg = (lane & 3) * 8;        // this lane's first column within a 32-column chunk
-  const int64_t rl = r0 + (lane >> 2);  // this lane's rows: rl + 8k
+                                              uint32_t rank, EpiState& es, const WaitCtl& wc,
+                                              bool& ok) {
+  const int cta_col0 = ti.w0 + C::WCOLS * static_cast<int>(rank);
+  const int lane = es.lane;
+  const int q = es.q;
+  const int cg = (lane & 3) * 8;  // this lane's first column within a 32-column block
+  const int nch = ti.nrow / 32;
+  float* own = es.xbufs + q * (XBUF_BYTES / 4);
   if constexpr (C::EPI == EPI_SWIGLU) {
-    // cols [0,128): gate of n0..n0+127, [128,256): up of the same columns
+    // a = silu(gate) * up of I columns c .. c + 7; training also saves the
+    // fp32 pre-activations (blocked layout)
+    const int gq = q & 1;
+    const float* gbuf = es.xbufs + gq * (XBUF_BYTES / 4);
+    const float* ubuf = es.xbufs + (gq + 2) * (XBUF_BYTES / 4);
+    const int kh = q < 2 ? 0 : 2;  // gate quarter: rows k = 0, 1 of a chunk; up quarter: 2, 3
+    const int c = cta_col0 + 32 * gq + cg;
 #pragma unroll 1
-    for (int c = ch; c < 4; c += CH_SPLIT) {
-      const int col = ti.n0 + c * 32;
-      if (col >= pr.N) break;
-      uint32_t g[32], u[32];
-      tmem_ld32(taddr + c * 32, g);
-      tmem_ld32(taddr + 128 + c * 32, u);
+    for (int j = 0; j < nch; ++j) {
+      uint32_t r[32];
+      tmem_ld32(taddr + j * 32, r);
       tmem_ld_wait();
-      float gv[4][8], uv[4][8];
-      xpose(xbuf, lane, g, gv);
-      xpose(xbuf, lane, u, uv);
-      if (col + cg < pr.N) {
+      const uint32_t ph = es.nchunk & 1u;
+      // the partner has read the previous chunk out of this buffer
+      if (!warp_wait(&es.xfree[gq], ph ^ 1u, lane, wc)) {
+        ok = false;
+        return;
+      }
+      xwrite_t(own, lane, r);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&es.xfull[gq]);
+      if (!warp_wait(&es.xfull[gq], ph, lane, wc)) {
+        ok = false;
+        return;
+      }
+      const float* gs = gbuf + (lane >> 2) * XS + cg;
+      const float* us = ubuf + (lane >> 2) * XS + cg;
+      float gv[2][8], uv[2][8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int64_t row = rl + 8 * k;
+      for (int kk = 0; kk < 2; ++kk) {
+        const int o = (kh + kk) * 8 * XS;
+        const float4 g0 = *reinterpret_cast<const float4*>(gs + o);
+        const float4 g1 = *reinterpret_cast<const float4*>(gs + o + 4);
+        const float4 u0 = *reinterpret_cast<const float4*>(us + o);
+        const float4 u1 = *reinterpret_cast<const float4*>(us + o + 4);
+        gv[kk][0] = g0.x; gv[kk][1] = g0.y; gv[kk][2] = g0.z; gv[kk][3] = g0.w;
+        gv[kk][4] = g1.x; gv[kk][5] = g1.y; gv[kk][6] = g1.z; gv[kk][7] = g1.w;
+        uv[kk][0] = u0.x; uv[kk][1] = u0.y; uv[kk][2] = u0.z; uv[kk][3] = u0.w;
+        uv[kk][4] = u1.x; uv[kk][5] = u1.y; uv[kk][6] = u1.z; uv[kk][7] = u1.w;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&es.xfree[gq]);
+      ++es.nchunk;
+      if (c < pr.N) {
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const int64_t row = ti.row0 + 32 * j + (lane >> 2) + 8 * (kh + kk);
           float av[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) av[j] = silu_f(gv[k][j]) * uv[k][j];
-          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(pr.out) + row * pr.ld_out + col +
-                                    cg) = pack_bf16x8(av);
+          for (int i = 0; i < 8; ++i) av[i] = silu_f(gv[kk][i]) * uv[kk][i];
+          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(pr.out) + row * pr.ld_out + c) =
+              pack_bf16x8(av);
           if (pr.out2) {
-            float* hp = static_cast<float*>(pr.out2) + hblock_offset(row, col + cg, pr.ld_out2);
-            store_f32x8(hp, gv[k]);
-            store_f32x8(hp + 1024, uv[k]);
+            float* hp = static_cast<float*>(pr.out2) + hblock_offset(row, c, pr.ld_out2);
+            store_f32x8(hp, gv[kk]);
+            store_f32x8(hp + 1024, uv[kk]);
           }
         }
       }
     }
   } else if constexpr (C::EPI == EPI_STORE) {
-    __nv_bfloat16* base = static_cast<__nv_bfloat16*>(pr.out);
+    const int c = cta_col0 + 32 * q + cg;
 #pragma unroll 1
-    for (int c = ch; c < BN / 32; c += CH_SPLIT) {
-      const int col = ti.n0 + c * 32;
-      if (col >= pr.N) break;
+    for (int j = 0; j < nch; ++j) {
       uint32_t r[32];
-      tmem_ld32(taddr + c * 32, r);
+      tmem_ld32(taddr + j * 32, r);
       tmem_ld_wait();
       float v[4][8];
-      xpose(xbuf, lane, r, v);
-      if (col + cg < pr.N) {
+      xwrite_t(own, lane, r);
+      __syncwarp();
+      xread(own, lane, v);
+      __syncwarp();
+      if (c < pr.N) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const int64_t row = rl + 8 * k;
+          const int64_t row = ti.row0 + 32 * j + (lane >> 2) + 8 * k;
           if (pr.out_f32)
-            store_f32x8(static_cast<float*>(pr.out) + row * pr.ld_out + col + cg, v[k]);
+            store_f32x8(static_cast<float*>(pr.out) + row * pr.ld_out + c, v[k]);
           else
-            *reinterpret_cast<uint4*>(base + row * pr.ld_out + col + cg) = pack_bf16x8(v[k]);
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(pr.out) + row * pr.ld_out + c) =
+                pack_bf16x8(v[k]);
         }
       }
     }
   } else {  // EPI_DSWIGLU
-    // acc = G = dy_perm . W2^T for columns n0..n0+255 of I.  With the saved
-    // fp32 pre-activations g, u and the slot's routing weight w:
+    // acc = G^T, G = dy_perm . W2^T for I columns c0 .. c0 + 31.  With the
+    // saved fp32 pre-activations g, u and the slot's routing weight w:
     //   a = silu(g) u,  dA = w G,
     //   dgate = dA u s (1 + g (1 - s)),  dup = dA g s     (s = sigmoid(g))
     // writes dH = [dgate | dup] and wa = w a (the W2Grad operand), each as
     // a bf16 high part and an e5m2 low part, and the partial
-    // d_w = sum_j G_j a_j of this column block (fp32).  The pre-activations
-    // of the next chunk are loaded while the current one is computed.
+    // d_w = sum_j G_j a_j over these 32 columns (fp32).  The pre-activations
+    // and routing weights of the next chunk are loaded while the current one
+    // is computed.
     const float* hb = static_cast<const float*>(pr.aux);
-    float w[4], dwp[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      w[k] = pr.rowscale[rl + 8 * k];
-      dwp[k] = 0.0f;
-    }
+    const int c0 = cta_col0 + 32 * q;
+    const int c = c0 + cg;
+    const bool colok = c < pr.N;
     float4 gn[4][2], un[4][2];
-    auto load_h = [&](int col) {
-      const bool ok = col + cg < pr.N;
+    float wn[4];
+    auto load_h = [&](int j) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float4* p =
-            reinterpret_cast<const float4*>(hb + hblock_offset(rl + 8 * k, col + cg, pr.ld_aux));
+        const int64_t row = ti.row0 + 32 * j + (lane >> 2) + 8 * k;
+        const float4* p = reinterpret_cast<const float4*>(hb + hblock_offset(row, c, pr.ld_aux));
         const float4* pu = p + 256;  // the up block follows the gate block
         const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        gn[k][0] = ok ? __ldg(p) : z;
-        gn[k][1] = ok ? __ldg(p + 1) : z;
-        un[k][0] = ok ? __ldg(pu) : z;
-        un[k][1] = ok ? __ldg(pu + 1) : z;
+        gn[k][0] = colok ? __ldg(p) : z;
+        gn[k][1] = colok ? __ldg(p + 1) : z;
+        un[k][0] = colok ? __ldg(pu) : z;
+        un[k][1] = colok ? __ldg(pu + 1) : z;
+        wn[k] = __ldg(pr.rowscale + row);
       }
     };
-    if (ti.n0 + ch * 32 < pr.N) load_h(ti.n0 + ch * 32);
+    load_h(0);
 #pragma unroll 1
-    for (int c = ch; c < BN / 32; c += CH_SPLIT) {
-      const int col = ti.n0 + c * 32;
-      if (col >= pr.N) break;
-      float gv[4][8], uv[4][8];
+    for (int j = 0; j < nch; ++j) {
+      float gv[4][8], uv[4][8], w[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         gv[k][0] = gn[k][0].x; gv[k][1] = gn[k][0].y; gv[k][2] = gn[k][0].z; gv[k][3] = gn[k][0].w;
         gv[k][4] = gn[k][1].x; gv[k][5] = gn[k][1].y; gv[k][6] = gn[k][1].z; gv[k][7] = gn[k][1].w;
         uv[k][0] = un[k][0].x; uv[k][1] = un[k][0].y; uv[k][2] = un[k][0].z; uv[k][3] = un[k][0].w;
         uv[k][4] = un[k][1].x; uv[k][5] = un[k][1].y; uv[k][6] = un[k][1].z; uv[k][7] = un[k][1].w;
+        w[k] = wn[k];
       }
-      const int ncol = col + 32 * CH_SPLIT;
-      if (c + CH_SPLIT < BN / 32 && ncol < pr.N) load_h(ncol);
+      if (j + 1 < nch) load_h(j + 1);
       uint32_t r[32];
-      tmem_ld32(taddr + c * 32, r);
+      tmem_ld32(taddr + j * 32, r);
       tmem_ld_wait();
       float Gv[4][8];
-      xpose(xbuf, lane, r, Gv);
-      if (col + cg < pr.N) {
+      xwrite_t(own, lane, r);
+      __syncwarp();
+      xread(own, lane, Gv);
+      __syncwarp();
+      float dwp[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int64_t row = rl + 8 * k;
-          float dg[8], du[8], wa[8];
+      for (int k = 0; k < 4; ++k) {
+        const int64_t row = ti.row0 + 32 * j + (lane >> 2) + 8 * k;
+        float dg[8], du[8], wa[8];
+        dwp[k] = 0.0f;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float G = Gv[k][j], g = gv[k][j], u = uv[k][j];
-            const float sg = sigmoid_f(g);
-            const float a = g * sg * u;
-            dwp[k] = fmaf(G, a, dwp[k]);
-            const float dA = w[k] * G;
-            dg[j] = dA * u * sg * (1.0f + g * (1.0f - sg));
-            du[j] = dA * g * sg;
-            wa[j] = w[k] * a;
-          }
-          __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(pr.out) + row * pr.ld_out + col + cg;
-          uint8_t* dl = static_cast<uint8_t*>(pr.out4) + row * pr.ld_lo4 + col + cg;
+        for (int i = 0; i < 8; ++i) {
+          const float G = Gv[k][i], g = gv[k][i], u = uv[k][i];
+          const float sg = sigmoid_f(g);
+          const float a = g * sg * u;
+          dwp[k] = fmaf(G, a, dwp[k]);
+          const float dA = w[k] * G;
+          dg[i] = dA * u * sg * (1.0f + g * (1.0f - sg));
+          du[i] = dA * g * sg;
+          wa[i] = w[k] * a;
+        }
+        if (colok) {
+          __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(pr.out) + row * pr.ld_out + c;
+          uint8_t* dl = static_cast<uint8_t*>(pr.out4) + row * pr.ld_lo4 + c;
           store_bf16x8_split(dh, dl, dg);
           store_bf16x8_split(dh + pr.half, dl + pr.half, du);
-          store_bf16x8_split(static_cast<__nv_bfloat16*>(pr.out2) + row * pr.ld_out2 + col + cg,
-                             static_cast<uint8_t*>(pr.out5) + row * pr.ld_lo5 + col + cg,
-                             wa);
+          store_bf16x8_split(static_cast<__nv_bfloat16*>(pr.out2) + row * pr.ld_out2 + c,
+                             static_cast<uint8_t*>(pr.out5) + row * pr.ld_lo5 + c, wa);
+        }
+      }
+      // one partial per (row, 32-column block): the four lanes of a row add
+      // theirs in a fixed tree, the combine sums the blocks in order
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        dwp[k] += __shfl_xor_sync(0xffffffffu, dwp[k], 1);
+        dwp[k] += __shfl_xor_sync(0xffffffffu, dwp[k], 2);
+      }
+      if (cg == 0 && c0 < pr.N) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int64_t row = ti.row0 + 32 * j + (lane >> 2) + 8 * k;
+          static_cast<float*>(pr.out3)[row * pr.ld_out3 + c0 / 32] = dwp[k];
         }
       }
     }
-    // one partial per (row, column block, warp of the quarter): the four
-    // lanes of a row add theirs in a fixed tree, the combine sums the blocks
-    // in order
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      dwp[k] += __shfl_xor_sync(0xffffffffu, dwp[k], 1);
-      dwp[k] += __shfl_xor_sync(0xffffffffu, dwp[k], 2);
-    }
-    if (cg == 0) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        static_cast<float*>(pr.out3)[(rl + 8 * k) * pr.ld_out3 + (ti.n0 / BN) * CH_SPLIT + ch] =
-            dwp[k];
-    }
   }
 }
-
 
 // Bounded wait that ignores the abort flag (used only to drain in-flight
 // copies / MMAs before the CTA exits).
@@ -541,7 +617,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* ti_full = tempty + 2;
   uint64_t* ti_empty = ti_full + TI_DEPTH;  // in a pair: the even CTA's, both CTAs arrive
   uint64_t* mma_done = ti_empty + TI_DEPTH;
-  TileInfo* s_ti = reinterpret_cast<TileInfo*>(mma_done + 1);
+  uint64_t* xfull = mma_done + 1;           // [2] SwiGLU epilogue exchange
+  uint64_t* xfree = xfull + 2;              // [2]
+  TileInfo* s_ti = reinterpret_cast<TileInfo*>(xfree + 2);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_ti + TI_DEPTH);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int* s_pref = reinterpret_cast<int*>(s_tmem + 2);  // [steps + 1]
@@ -567,6 +645,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&ti_empty[i], PAIR ? 2 * (1 + EPI_WARPS) + 1 : 2 + EPI_WARPS);
     }
     mbar_init(mma_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&xfull[i], 2);
+      mbar_init(&xfree[i], 2);
+    }
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -598,8 +680,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Fetches tickets, decodes them and waits for each tile's dependencies
     // about one tile ahead of the TMA producer, so neither the ticket atomic
     // nor a ready-counter poll sits on the load path.  (A deeper lookahead
-    // spreads the M tiles that share a weight tile over time and costs L2
-    // reuse of the weights.)  Lane 0 does the bookkeeping.  In a pair only
+    // spreads the token blocks that share a weight tile over time and costs
+    // L2 reuse of the weights.)  Lane 0 does the bookkeeping.  In a pair only
     // the even CTA schedules; it writes each tile into both CTAs' rings.
     if (!PAIR || leader) {
       build_schedule(P, s_pref);
@@ -611,7 +693,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (;;) {
         TileInfo ti;
         ti.prob = -1;
-        ti.e = ti.m0 = ti.n0 = ti.kb = ti.ph = 0;
+        ti.e = ti.row0 = ti.nrow = ti.w0 = ti.kb = 0;
         bool ok = true;
         if (lane == 0) {
           int q = 0, e = 0, r = 0;
@@ -620,11 +702,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             HMM_BY_PROB(q, decode_tile, P, P.p[q], e, r, ti);
             t = atomicAdd(P.ticket, 1);  // next ticket, early
             const Prob& pr = P.p[q];
-            if (pr.wait_m) {
-              ok = counter_wait(&pr.wait_m[ti.m0 / BM], pr.wait_unit, wc);
-              if (ok && PAIR && !ti.ph)
-                ok = counter_wait(&pr.wait_m[ti.m0 / BM + 1], pr.wait_unit, wc);
-            }
+            if (pr.wait_m) ok = counter_wait(&pr.wait_m[ti.row0 / TROWS], pr.wait_unit, wc);
           }
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -695,19 +773,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const CUtensorMap* mp = maps.m[ti.prob];
         uint64_t* rec = (!PAIR || leader) ? trace_rec(P, lt) : nullptr;
         ++lt;
-        // the odd CTA's half of the last pair of an expert with an odd number
-        // of M tiles has no rows of A
-        const bool load_a = !PAIR || leader || !ti.ph;
         for (int kb = 0; kb < ti.kb; ++kb) {
           if (!mbar_wait(&empty[stage], sphase ^ 1u, wc)) {
             ok = false;
             break;
           }
           if (rec && kb == 0) rec[2] = globaltimer_ns();
-          uint8_t* sA = stages + stage * SBYTES;
+          uint8_t* sW = stages + stage * SBYTES;
           const uint32_t full_cl = PAIR ? mapa_shared(smem_u32(&full[stage]), 0) : 0u;
-          HMM_BY_PROB_P(ti.prob, load_stage, pr, ti, kb, &mp[0], &mp[1], sA, sA + A_BYTES,
-                        &full[stage], full_cl, rank, load_a);
+          HMM_BY_PROB_P(ti.prob, load_stage, pr, ti, kb, &mp[0], &mp[1], sW, sW + W_BYTES,
+                        &full[stage], full_cl, rank);
           ++issued;
           if (++stage == NST) {
             stage = 0;
@@ -748,7 +823,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!mbar_wait<PAIR>(&tempty[acc], acc_phase ^ 1u, wc)) break;
         tc_fence_after();
         if (rec) rec[4] = globaltimer_ns();
-        const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t d_tmem = tmem_base + acc * NT;
+        uint32_t idesc = idesc_n(ti.nrow);  // N = the tile's token rows
+        if (ti.prob & 1)
+          idesc |= PAIR ? C1::IDESC2 : C1::IDESC;
+        else
+          idesc |= PAIR ? C0::IDESC2 : C0::IDESC;
         bool ok = true;
         for (int kb = 0; kb < ti.kb; ++kb) {
           if (!mbar_wait(&full[stage], sphase, wc)) {
@@ -756,9 +836,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(stages + stage * SBYTES);
-          const uint32_t b_base = a_base + A_BYTES;
-          HMM_BY_PROB_P(ti.prob, mma_stage, d_tmem, a_base, b_base, kb == 0);
+          const uint32_t w_base = smem_u32(stages + stage * SBYTES);
+          const uint32_t t_base = w_base + W_BYTES;
+          HMM_BY_PROB_P(ti.prob, mma_stage, d_tmem, w_base, t_base, idesc, kb == 0);
           if constexpr (PAIR)
             umma_commit_pair(&empty[stage], 0x3);
           else
@@ -786,9 +866,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
     // ------------------------------------------------------------- epilogue
-    const int q = warp & 3;
-    const int ch = (warp - 2) / 4;  // which warp of the lane quarter
-    float* xbuf = xbufs + (warp - 2) * (XBUF_BYTES / 4);
+    EpiState es;
+    es.q = warp & 3;
+    es.lane = lane;
+    es.xbufs = xbufs;
+    es.xfull = xfull;
+    es.xfree = xfree;
+    es.nchunk = 0;
     const uint32_t tempty_cl[2] = {PAIR ? mapa_shared(smem_u32(&tempty[0]), 0) : 0u,
                                    PAIR ? mapa_shared(smem_u32(&tempty[1]), 0) : 0u};
     int ti_slot = 0;
@@ -819,14 +903,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!got) break;
       tc_fence_after();
       if (rec) rec[6] = globaltimer_ns();
-      // this CTA's 128 rows of a pair tile; the odd CTA's half of the last
-      // pair of an expert with an odd number of M tiles holds no rows
-      const bool real = !PAIR || leader || !ti.ph;
-      ti.m0 += PAIR ? BM * static_cast<int>(rank) : 0;
-      if (real) {
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-        HMM_BY_PROB(ti.prob, epilogue_tile, pr, ti, taddr, ti.m0 + q * 32, lane, ch, xbuf);
-      }
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(es.q * 32) << 16) + acc * NT;
+      bool eok = true;
+      HMM_BY_PROB(ti.prob, epilogue_tile, pr, ti, taddr, rank, es, wc, eok);
+      if (!eok) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -836,10 +916,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_arrive_peer(tempty_cl[acc]);
       }
       if (rec) rec[7] = globaltimer_ns();
-      if (real && pr.signal_m) {
+      if (pr.signal_m) {
         fence_proxy_async_global();
         __syncwarp();
-        if (lane == 0) red_release_add(&pr.signal_m[ti.m0 / BM], 1);
+        if (lane == 0) red_release_add(&pr.signal_m[ti.row0 / TROWS], 1);
       }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
@@ -944,15 +1024,18 @@ int launch(const GemmEnv& env, Params& P, const Maps& maps, int64_t max_tiles, i
 
 }  // namespace
 
-using CfgGmm1 = Cfg<EPI_SWIGLU, true>;     // A = x_perm, B = W1 (MN-major)
-using CfgGmm2 = Cfg<EPI_STORE, true>;      // A = a, B = W2 (MN-major)
-using CfgActGrad = Cfg<EPI_DSWIGLU, false>; // A = dy_perm, B = W2 viewed K-major
-using CfgInGrad = Cfg<EPI_STORE, false>;   // A = dH, B = W1 viewed K-major
+using CfgGmm1 = Cfg<EPI_SWIGLU, true>;     // tokens x_perm, weights W1 (MN-major)
+using CfgGmm2 = Cfg<EPI_STORE, true>;      // tokens a, weights W2 (MN-major)
+using CfgActGrad = Cfg<EPI_DSWIGLU, false>; // tokens dy_perm, weights W2 rows (K-major)
+using CfgInGrad = Cfg<EPI_STORE, false>;   // tokens dH, weights W1 rows (K-major)
 
 namespace {
 
 // Problems 2 and 3 (the shared expert, expert E of the padded rows) copy
 // problems 0 and 1 with their own weight maps.
+//   Tile counts and ready units: a tile spans WCOLS output columns per CTA;
+// every epilogue warp of every CTA of a producer tile releases the tile's
+// token block once.
 void add_shared(Params& P, Maps& maps, int E, const CUtensorMap& B0, const CUtensorMap& B1) {
   for (int q = 0; q < 2; ++q) {
     P.p[2 + q] = P.p[q];
@@ -973,10 +1056,10 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
   const int64_t H = p.H, I = p.I, E = p.E, R = p.R;
   Maps maps;
   int rc = HMM_OK;
-  rc |= map_act(env, &maps.m[0][0], x_perm, R, H, BM);   // x_perm [R, H], K = H
-  rc |= map_w(env, &maps.m[0][1], W1, E, H, 2 * I, 64);  // W1 [E, H, 2I]: MN-major B
-  rc |= map_act(env, &maps.m[1][0], a, R, I, BM);        // a [R, I], K = I
-  rc |= map_w(env, &maps.m[1][1], W2, E, I, H, 64);      // W2 [E, I, H]: MN-major B
+  rc |= map_act(env, &maps.m[0][0], x_perm, R, H, NT / 2);  // x_perm [R, H], K = H
+  rc |= map_w(env, &maps.m[0][1], W1, E, H, 2 * I, 64);     // W1 [E, H, 2I]: MN-major
+  rc |= map_act(env, &maps.m[1][0], a, R, I, NT / 2);       // a [R, I], K = I
+  rc |= map_w(env, &maps.m[1][1], W2, E, I, H, 64);         // W2 [E, I, H]: MN-major
   CUtensorMap s0, s1;
   if (p.shared) {
     rc |= map_w(env, &s0, Ws1, 1, H, 2 * I, 64);  // shared expert's [H, 2I], [I, H]
@@ -993,7 +1076,8 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
   g1.K = static_cast<int>(H);
   g1.N = static_cast<int>(I);
   g1.half = static_cast<int>(I);
-  g1.n_tiles = static_cast<int>((I + BN / 2 - 1) / (BN / 2));
+  const int ncta = env.pair_rows ? 2 : 1;
+  g1.n_tiles = static_cast<int>((I + CfgGmm1::WCOLS * ncta - 1) / (CfgGmm1::WCOLS * ncta));
   g1.out = a;
   g1.ld_out = I;
   g1.out2 = h32;
@@ -1004,7 +1088,7 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
   Prob& g2 = P.p[1];
   g2.K = static_cast<int>(I);
   g2.N = static_cast<int>(H);
-  g2.n_tiles = static_cast<int>((H + BN - 1) / BN);
+  g2.n_tiles = static_cast<int>((H + CfgGmm2::WCOLS * ncta - 1) / (CfgGmm2::WCOLS * ncta));
   g2.out = o;
   g2.ld_out = H;
   g2.out_f32 = p.shared ? 1 : 0;  // fp32 rows for the y combine with the shared expert
@@ -1014,9 +1098,9 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
   // meet the last wave of GMM1 tiles
   g2.lag = static_cast<int>(p.Ex);
   g2.wait_m = c.ready;
-  g2.wait_unit = EPI_WARPS * g1.n_tiles;  // every epilogue warp of every GMM1 tile of the M tile
+  g2.wait_unit = EPI_WARPS * ncta * g1.n_tiles;  // every GMM1 tile of the token block
   if (p.shared) add_shared(P, maps, static_cast<int>(E), s0, s1);
-  const int64_t max_tiles = p.max_mtiles * (g1.n_tiles + g2.n_tiles);
+  const int64_t max_tiles = (p.R / TROWS) * (g1.n_tiles + g2.n_tiles);
   if (env.pair_rows) return launch<true, CfgGmm1, CfgGmm2>(env, P, maps, max_tiles, 0);
   return launch<false, CfgGmm1, CfgGmm2>(env, P, maps, max_tiles, 0);
 }
@@ -1029,18 +1113,16 @@ int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPt
   const int64_t H = p.H, I = p.I, E = p.E, R = p.R;
   Maps maps;
   int rc = HMM_OK;
-  // on CTA pairs each CTA loads 128 of the 256 B rows
-  const uint32_t b_rows = env.pair_rows ? BN / 2 : BN;
-  // act_grad: G = dy_perm . W2^T   (B = W2 [E, I, H] read K-major, N = I)
-  rc |= map_act(env, &maps.m[0][0], dy_perm, R, H, BM);
-  rc |= map_w(env, &maps.m[0][1], W2, E, I, H, b_rows);
-  // input-grad: dX_perm = dH . W1^T (B = W1 [E, H, 2I] read K-major, N = H)
-  rc |= map_act(env, &maps.m[1][0], dH, R, 2 * I, BM);
-  rc |= map_w(env, &maps.m[1][1], W1, E, H, 2 * I, b_rows);
+  // act_grad: G = dy_perm . W2^T   (weights: 128 rows of W2 [E, I, H] per CTA, N = I)
+  rc |= map_act(env, &maps.m[0][0], dy_perm, R, H, NT / 2);
+  rc |= map_w(env, &maps.m[0][1], W2, E, I, H, BW);
+  // input-grad: dX_perm = dH . W1^T (weights: 128 rows of W1 [E, H, 2I] per CTA, N = H)
+  rc |= map_act(env, &maps.m[1][0], dH, R, 2 * I, NT / 2);
+  rc |= map_w(env, &maps.m[1][1], W1, E, H, 2 * I, BW);
   CUtensorMap s0, s1;
   if (p.shared) {
-    rc |= map_w(env, &s0, Ws2, 1, I, H, b_rows);
-    rc |= map_w(env, &s1, Ws1, 1, H, 2 * I, b_rows);
+    rc |= map_w(env, &s0, Ws2, 1, I, H, BW);
+    rc |= map_w(env, &s1, Ws1, 1, H, 2 * I, BW);
   }
   if (rc != HMM_OK) return HMM_ERR_CUDA;
   Params P{};
@@ -1053,14 +1135,14 @@ int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPt
   ag.K = static_cast<int>(H);
   ag.N = static_cast<int>(I);
   ag.half = static_cast<int>(I);
-  ag.n_tiles = static_cast<int>(p.nt_dswiglu);
+  const int ncta = env.pair_rows ? 2 : 1;
+  ag.n_tiles = static_cast<int>((I + CfgActGrad::WCOLS * ncta - 1) / (CfgActGrad::WCOLS * ncta));
   ag.out = dH;
   ag.ld_out = 2 * I;
   ag.out2 = wa;
   ag.ld_out2 = I;
   ag.out3 = dwp;
-  static_assert(CH_SPLIT == 1, "the d_w partial buffer holds one entry per act_grad N tile");
-  ag.ld_out3 = p.dwp_ld;
+  ag.ld_out3 = p.dwp_ld;  // one d_w partial per row and 32-column block of I
   ag.out4 = dH_lo;
   ag.ld_lo4 = p.ld8_2i;
   ag.out5 = wa_lo;
@@ -1074,17 +1156,17 @@ int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPt
   Prob& ig = P.p[1];
   ig.K = static_cast<int>(2 * I);
   ig.N = static_cast<int>(H);
-  ig.n_tiles = static_cast<int>((H + BN - 1) / BN);
+  ig.n_tiles = static_cast<int>((H + CfgInGrad::WCOLS * ncta - 1) / (CfgInGrad::WCOLS * ncta));
   ig.out = dx_perm;
   ig.ld_out = H;
   ig.out_f32 = p.shared ? 1 : 0;  // fp32 rows for the dX combine with the shared expert
   ig.e_lo = 0;
   ig.e_hi = static_cast<int>(E);
   ig.wait_m = c.ready;
-  ig.wait_unit = EPI_WARPS * ag.n_tiles;
+  ig.wait_unit = EPI_WARPS * ncta * ag.n_tiles;
   ig.lag = static_cast<int>(p.Ex);  // input-grad after every act_grad tile is handed out
   if (p.shared) add_shared(P, maps, static_cast<int>(E), s0, s1);
-  const int64_t data_tiles = p.max_mtiles * (ag.n_tiles + ig.n_tiles);
+  const int64_t data_tiles = (p.R / TROWS) * (ag.n_tiles + ig.n_tiles);
   if (env.pair_rows)
     return launch<true, CfgActGrad, CfgInGrad>(env, P, maps, data_tiles, 1);
   return launch<false, CfgActGrad, CfgInGrad>(env, P, maps, data_tiles, 1);

@@ -123,8 +123,7 @@ int make_plan(const hmm_shape* s, bool training, Plan* p) {
   p->R = R;
   p->max_mtiles = R / BM;
   p->nchunks = (TK + RCHUNK - 1) / RCHUNK;
-  p->nt_dswiglu = (p->I + BN - 1) / BN;
-  p->dwp_ld = p->nt_dswiglu;  // one d_w partial per act_grad N tile and row
+  p->dwp_ld = (p->I + 31) / 32;  // one d_w partial per row and 32-column block of I
   p->ld8_h = (p->H + 15) / 16 * 16;
   p->ld8_2i = (2 * p->I + 15) / 16 * 16;
   p->ld8_i = (p->I + 15) / 16 * 16;
@@ -140,8 +139,9 @@ int make_plan(const hmm_shape* s, bool training, Plan* p) {
   p->off_chunk_base = o; o = align_up(o + 4 * p->nchunks * p->E, A);
   p->off_tickets = o;
   p->off_ready = o + 4 * NUM_TICKETS;  // tickets and ready counters contiguous (zeroed together)
-  p->ctrl_zero_count = NUM_TICKETS + p->max_mtiles;
-  o = align_up(p->off_ready + 4 * p->max_mtiles, A);
+  // one ready counter per 64 padded rows (token blocks start on multiples of 64)
+  p->ctrl_zero_count = NUM_TICKETS + R / 64;
+  o = align_up(p->off_ready + 4 * (R / 64), A);
   p->ctrl_bytes = o;
   const size_t xperm = align_up(static_cast<size_t>(R) * p->H * 2, A);
   // fp32 pre-activations in 32 x 32 blocks (gate and up), columns padded to 32
@@ -245,7 +245,8 @@ GemmEnv env_of(hmm_ctx* ctx, const Plan& p, cudaStream_t st) {
   GemmEnv e;
   e.encode = ctx->encode;
   e.num_sms = ctx->num_sms;
-  // pairs pay off when most experts have two or more 128-row tiles
+  // pairs (half the tiles, half the token rows staged per SM) pay off when
+  // experts average a full 256-row token block
   e.pair_rows = ctx->pair_rows == 2 ? (p.TK >= 2 * BM * p.E ? 1 : 0) : ctx->pair_rows;
   e.trace = ctx->trace;
   e.trace_cap = ctx->trace ? static_cast<int>(ctx->trace_bytes / (64 * ctx->num_sms)) : 0;

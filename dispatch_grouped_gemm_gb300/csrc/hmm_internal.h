@@ -11,11 +11,10 @@
 
 namespace hmm {
 
-// Rows of one GEMM tile (tcgen05 M).  Every expert's rows start on a multiple
-// of BM in the permuted ("padded") layout, so an M-tile never spans experts;
-// padding rows are zero.
+// Every expert's rows start on a multiple of BM in the permuted ("padded")
+// layout, so no GEMM tile or K block spans two experts; padding rows are
+// zero (x_perm, dy_perm) or computed from zeros (a, h, dH, w*a).
 constexpr int BM = 128;
-constexpr int BN = 256;   // tcgen05 N per tile
 constexpr int BK = 64;    // K per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr int RCHUNK = 1024;  // slots per routing warp-chunk
 constexpr int RWARPS = 8;     // warps per routing block
@@ -36,7 +35,7 @@ struct MetaPtrs {
 struct CtrlPtrs {
   int32_t* chunk_base;  // [nchunks * E]
   int32_t* tickets;     // [NUM_TICKETS]      } contiguous: zeroed together
-  int32_t* ready;       // [max_mtiles]       } at the start of every call
+  int32_t* ready;       // [R / 64]           } at the start of every call
 };
 
 struct Plan {
@@ -46,8 +45,7 @@ struct Plan {
   int64_t R;            // capacity of the padded row space
   int64_t max_mtiles;   // R / BM
   int64_t nchunks;      // routing warp-chunks
-  int64_t nt_dswiglu;   // N tiles of the act_grad GEMM
-  int64_t dwp_ld;       // per-row d_w partials (one per act_grad N tile)
+  int64_t dwp_ld;       // per-row d_w partials (one per 32 columns of I)
   // row strides (bytes) of the fp8 arrays of the weight-gradient low halves,
   // padded to 16 bytes for TMA: H columns (x_perm8, dy_perm8), 2I (dH_lo8), I (wa_lo8)
   int64_t ld8_h, ld8_2i, ld8_i;
@@ -108,7 +106,7 @@ struct GemmEnv {
   cudaStream_t stream;
 };
 
-// forward GMM1(+SwiGLU) and GMM2 in one persistent launch with per-M-tile
+// forward GMM1(+SwiGLU) and GMM2 in one persistent launch with per-token-block
 // ready counters, for the routed experts and (p.shared) the shared expert
 // (Ws1 [H, 2I], Ws2 [I, H]).  h32 may be null (inference).
 int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
@@ -116,7 +114,7 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
                          const void* Ws2, void* a, float* h32, void* o, bool skip_ready_release);
 // backward data gradients in one persistent launch: act_grad (+SwiGLU grad,
 // d_w partials; dH and w*a written as a bf16 high part plus an e5m2 low part)
-// and input-grad (released per M tile), routed and shared experts.
+// and input-grad (released per token block), routed and shared experts.
 int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
                            const void* dy_perm, const float* wperm, const float* h32,
                            const void* W1, const void* W2, const void* Ws1, const void* Ws2,

@@ -247,7 +247,7 @@ cudaError_t launch_dispatch_dy(const Plan& p, const void* dy, const void* w, int
                                MetaPtrs m, CtrlPtrs c, void* dy_perm, void* dy8, float* wperm,
                                cudaStream_t st) {
   const int64_t warps = p.T + p.Ex * BM;
-  // also zero the backward launch counters (tickets and per-M-tile ready
+  // also zero the backward launch counters (tickets and per-token-block ready
   // counters are contiguous in the control block)
   const int64_t nzero = p.ctrl_zero_count;
   dispatch_rows_kernel<true><<<move_grid(warps), MOVE_THREADS, 0, st>>>(

@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int Ex, int32_t
     m.offsets[Ex] = tot_cnt;
     m.poff[Ex] = tot_pad;
   }
-  // tickets and per-M-tile ready counters of this call
+  // tickets and per-token-block ready counters of this call
   for (int64_t i = e; i < zero_count; i += blockDim.x) c.tickets[i] = 0;
 }
 

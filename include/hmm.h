@@ -123,10 +123,11 @@ int hmm_destroy(hmm_ctx* ctx);
 /*   (option ids 5 and 6 are not used) */
 /*   HMM_OPT_PAIR_ROWS     2 (default): automatic; the forward GEMMs and the
  *                         data-gradient GEMMs run on CTA pairs with 2-SM MMAs
- *                         (two 128-row tiles of one expert per 256 x 256 tile)
- *                         when the routed rows average at least two 128-row
- *                         tiles per expert (T * K >= 256 * E), else on single
- *                         CTAs.  1: always on CTA pairs; 0: never. */
+ *                         (256 weight columns per tile, 128 per CTA) when the
+ *                         routed rows average at least 256 per expert
+ *                         (T * K >= 256 * E), else on single CTAs (128 weight
+ *                         columns per tile).  1: always on CTA pairs; 0: never.
+ *                         Results do not depend on it. */
 #define HMM_OPT_PAIR_ROWS 7
 int hmm_set_option(hmm_ctx* ctx, int option, int64_t value);
 
