@@ -12,16 +12,19 @@
 // plus the padded layout the GEMMs use: expert e owns padded rows
 // [poff[e], poff[e+1]) with poff[e+1]-poff[e] = counts[e] rounded up to BM.
 //
-// Three launches: per-warp-chunk histograms -> one-block scan -> per-chunk
-// stable ranks (warp match_any groups equal ids inside each 32-slot step, so
-// the order inside a chunk follows s).  Each warp loads its whole chunk of
-// ids into registers before the first step, so the steps do not wait on
+// Three launches: per-chunk histograms -> one-block scan -> per-chunk stable
+// ranks.  A chunk (1024 slots) belongs to one block of 8 warps, 128 slots per
+// warp: warp match_any groups equal ids inside each 32-slot step, so the order
+// inside a warp follows s, and the warps' per-expert counts are prefix-summed
+// in shared memory, so the order across warps follows s too.  Each warp loads
+// its ids into registers before the first step, so the steps do not wait on
 // global loads one after another.
 #include "hmm_internal.h"
 
 namespace hmm {
 
-constexpr int RSTEPS = RCHUNK / 32;  // 32-slot steps per chunk
+constexpr int WSLOTS = RCHUNK / RWARPS;  // slots per warp of a chunk
+constexpr int RSTEPS = WSLOTS / 32;      // 32-slot steps per warp
 
 // ids of slots s0 + 32 j + lane, j < RSTEPS (-2 past s1: "no slot")
 __device__ __forceinline__ void load_chunk_ids(const int32_t* __restrict__ ids, int64_t s0,
@@ -38,29 +41,28 @@ __global__ void __launch_bounds__(RWARPS * 32) route_count_kernel(const int32_t*
                                                                   int64_t nchunks,
                                                                   int32_t* __restrict__ chunk_cnt,
                                                                   unsigned* status) {
-  extern __shared__ int32_t sh[];
+  extern __shared__ int32_t sh[];  // [E]: the chunk's histogram
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int32_t* cnt = sh + warp * E;
-  const int64_t chunk = static_cast<int64_t>(blockIdx.x) * RWARPS + warp;
-  if (chunk >= nchunks) return;
-  for (int e = lane; e < E; e += 32) cnt[e] = 0;
-  __syncwarp();
-  const int64_t s0 = chunk * RCHUNK;
-  const int64_t s1 = (s0 + RCHUNK < TK ? s0 + RCHUNK : TK);
+  const int64_t chunk = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
+  __syncthreads();
+  const int64_t c0 = chunk * RCHUNK;
+  const int64_t c1 = (c0 + RCHUNK < TK ? c0 + RCHUNK : TK);
+  const int64_t s0 = c0 + static_cast<int64_t>(warp) * WSLOTS;
   int v[RSTEPS];
-  load_chunk_ids(ids, s0, s1, lane, v);
+  load_chunk_ids(ids, s0, c1, lane, v);
   bool bad = false;
 #pragma unroll
   for (int j = 0; j < RSTEPS; ++j) {
     const int e = v[j];
     if (static_cast<unsigned>(e) < static_cast<unsigned>(E))
-      atomicAdd(&cnt[e], 1);
+      atomicAdd(&sh[e], 1);
     else if (e != -2)
       bad = true;
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(status, HMM_STATUS_EXPERT_ID);
-  __syncwarp();
-  for (int e = lane; e < E; e += 32) chunk_cnt[chunk * E + e] = cnt[e];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_cnt[chunk * E + e] = sh[e];
 }
 
 // Block-wide exclusive scan of one value per thread (blockDim.x == 1024).
@@ -143,27 +145,51 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int Ex, int32_t
 __global__ void __launch_bounds__(RWARPS * 32) route_rank_kernel(
     const int32_t* __restrict__ ids, int64_t TK, int E, int64_t nchunks, MetaPtrs m,
     const int32_t* __restrict__ chunk_base, int32_t* slot2row, int32_t* row2slot) {
-  extern __shared__ int32_t sh[];
+  extern __shared__ int32_t sh[];  // [RWARPS][E]: per-warp counts, then cursors
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int32_t* cnt = sh + warp * E;
-  const int64_t chunk = static_cast<int64_t>(blockIdx.x) * RWARPS + warp;
-  if (chunk >= nchunks) return;
-  // cursor of each expert: the padded row of its next slot in this chunk
-  for (int e = lane; e < E; e += 32)
-    cnt[e] = chunk_base[chunk * E + e] + (m.poff[e] - m.offsets[e]);
-  __syncwarp();
-  const int64_t s0 = chunk * RCHUNK;
-  const int64_t s1 = (s0 + RCHUNK < TK ? s0 + RCHUNK : TK);
+  const int64_t chunk = blockIdx.x;
+  const int64_t c0 = chunk * RCHUNK;
+  const int64_t c1 = (c0 + RCHUNK < TK ? c0 + RCHUNK : TK);
+  const int64_t s0 = c0 + static_cast<int64_t>(warp) * WSLOTS;
   int v[RSTEPS];
-  load_chunk_ids(ids, s0, s1, lane, v);
+  load_chunk_ids(ids, s0, c1, lane, v);
+  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  __syncwarp();
+  // 1. this warp's slots per expert (one lane per group of equal ids adds)
 #pragma unroll
   for (int j = 0; j < RSTEPS; ++j) {
-    if (s0 + 32 * j < s1) {  // warp-uniform
+    if (s0 + 32 * j < c1) {  // warp-uniform
+      const int e = v[j];
+      const bool ok = static_cast<unsigned>(e) < static_cast<unsigned>(E);
+      const int key = ok ? e : -1 - lane;  // invalid lanes never group
+      const unsigned peers = __match_any_sync(0xffffffffu, key);
+      if (ok && lane == 31 - __clz(peers)) cnt[e] += __popc(peers);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  // 2. cursor of warp w for expert e: the padded row of its first slot of e
+  //    = the chunk's first row of e + the slots of e in warps 0 .. w-1
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int32_t run = chunk_base[chunk * E + e] + (m.poff[e] - m.offsets[e]);
+#pragma unroll
+    for (int w = 0; w < RWARPS; ++w) {
+      const int32_t c = sh[w * E + e];
+      sh[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  // 3. stable ranks inside the warp, rows from the cursors
+#pragma unroll
+  for (int j = 0; j < RSTEPS; ++j) {
+    if (s0 + 32 * j < c1) {  // warp-uniform
       const int64_t s = s0 + 32 * j + lane;
-      const bool in = s < s1;
+      const bool in = s < c1;
       const int e = v[j];
       const bool ok = in && static_cast<unsigned>(e) < static_cast<unsigned>(E);
-      const int key = ok ? e : -1 - lane;  // invalid lanes never group
+      const int key = ok ? e : -1 - lane;
       const unsigned peers = __match_any_sync(0xffffffffu, key);
       int32_t prow = 0;
       if (ok) prow = cnt[e] + __popc(peers & ((1u << lane) - 1u));
@@ -190,11 +216,11 @@ cudaError_t launch_route(const Plan& p, const int32_t* ids, MetaPtrs m, CtrlPtrs
                          int32_t* slot2row, int32_t* row2slot, unsigned* status,
                          cudaStream_t st) {
   const int E = static_cast<int>(p.E);
-  const int blocks = static_cast<int>((p.nchunks + RWARPS - 1) / RWARPS);
+  const int blocks = static_cast<int>(p.nchunks);  // one block per chunk
   const size_t smem = sizeof(int32_t) * RWARPS * E;
   if (p.nchunks > 0) {
-    route_count_kernel<<<blocks, RWARPS * 32, smem, st>>>(ids, p.TK, E, p.nchunks, c.chunk_base,
-                                                          status);
+    route_count_kernel<<<blocks, RWARPS * 32, sizeof(int32_t) * E, st>>>(ids, p.TK, E, p.nchunks,
+                                                                       c.chunk_base, status);
   }
   route_scan_kernel<<<1, 1024, 0, st>>>(E, static_cast<int>(p.Ex), static_cast<int32_t>(p.T),
                                         p.nchunks, m, c, p.ctrl_zero_count);
