@@ -87,8 +87,17 @@ constexpr int STAGE_BYTES = W_BYTES + T_BYTES;
 constexpr int PAIR_STAGES = 6;
 constexpr int PAIR_T_BYTES = (NT / 2) * BK * 2;  // 16 KB
 constexpr int PAIR_STAGE_BYTES = W_BYTES + PAIR_T_BYTES;
-constexpr int MAX_STAGES = PAIR_STAGES;
+// Small token blocks (routings of a few rows per expert, e.g. decode): single
+// CTAs with blocks of at most 64 rows and eight 24 KB stages, so as many
+// weight bytes are in flight per SM as with 256-row blocks (the weights are
+// what such a launch streams).
+constexpr int SMALL_NT = 64;
+constexpr int SMALL_STAGES = 8;
+constexpr int SMALL_T_BYTES = SMALL_NT * BK * 2;  // 8 KB
+constexpr int SMALL_STAGE_BYTES = W_BYTES + SMALL_T_BYTES;
+constexpr int MAX_STAGES = SMALL_STAGES;
 static_assert(PAIR_STAGES * PAIR_STAGE_BYTES <= STAGES * STAGE_BYTES, "pair stages");
+static_assert(SMALL_STAGES * SMALL_STAGE_BYTES <= STAGES * STAGE_BYTES, "small stages");
 constexpr int TI_DEPTH = 3;
 // Warp roles: 0 TMA producer, 1 MMA issuer, 2..5 epilogue (one per TMEM lane
 // quarter), 6 tile scheduler.  (Eight epilogue warps, two per quarter, were
@@ -135,6 +144,7 @@ struct Params {
   Prob p[MAX_PROB];
   int nprob;
   int pair;             // CTA pairs: a tile spans 256 weight columns
+  int nt;               // token rows per block at most (256, or 64 in small mode)
   int steps;            // E + largest lag
   const int32_t* poff;
   const int32_t* counts;
@@ -174,7 +184,7 @@ __device__ __forceinline__ uint32_t sm_id() {
 // Token blocks of expert e: 256 rows each, the last one ending at the first
 // multiple of 64 rows at or past the expert's last row.
 __device__ __forceinline__ int nblocks_of(const Params& P, int e) {
-  return (P.counts[e] + NT - 1) / NT;
+  return (P.counts[e] + P.nt - 1) / P.nt;
 }
 
 __device__ __forceinline__ int tiles_of(const Params& P, const Prob& pr, int e) {
@@ -238,8 +248,8 @@ __device__ void decode_tile(const Params& P, const Prob& pr, int e, int r, TileI
   const int wt = r / nb;  // token blocks innermost: a weight tile is reused from L2
   const int b = r - wt * nb;
   const int rows = (P.counts[e] + TROWS - 1) / TROWS * TROWS;
-  ti.row0 = P.poff[e] + NT * b;
-  ti.nrow = min(NT, rows - NT * b);
+  ti.row0 = P.poff[e] + P.nt * b;
+  ti.nrow = min(P.nt, rows - P.nt * b);
   ti.w0 = wt * C::WCOLS * (P.pair ? 2 : 1);
   ti.kb = (pr.K + BK - 1) / BK;
 }
@@ -254,7 +264,7 @@ __device__ void decode_tile(const Params& P, const Prob& pr, int e, int r, TileI
 //   the MMA reads the rows it needs.  (64-row boxes sized to each tile cut the
 //   bytes of tiles under 256 rows but made both launches slower: the
 //   pipeline is bound by the latency of a stage's loads, not their bytes.)
-template <class C, bool PAIR>
+template <class C, bool PAIR, bool SMALL>
 __device__ __forceinline__ void load_stage(const Prob& pr, const TileInfo& ti, int kb,
                                            const CUtensorMap* tT, const CUtensorMap* tW,
                                            uint8_t* sW, uint8_t* sT, uint64_t* bar,
@@ -274,8 +284,9 @@ __device__ __forceinline__ void load_stage(const Prob& pr, const TileInfo& ti, i
     }
     tma_load_2d_pair(sT, tT, bar_cl, k, ti.row0 + (ti.nrow / 2) * static_cast<int>(rank));
   } else {
-    const bool two = ti.nrow > NT / 2;
-    mbar_arrive_expect_tx(bar, W_BYTES + (two ? 2 : 1) * PAIR_T_BYTES);
+    // small mode: one 64-row box; else one or two 128-row boxes
+    const bool two = !SMALL && ti.nrow > NT / 2;
+    mbar_arrive_expect_tx(bar, W_BYTES + (SMALL ? SMALL_T_BYTES : (two ? 2 : 1) * PAIR_T_BYTES));
     if constexpr (C::W_MN) {
       const int c2 = C::EPI == EPI_SWIGLU ? pr.half + wc : wc + 64;
       tma_load_3d(sW, tW, bar, wc, k, eb);
@@ -597,12 +608,19 @@ __device__ __noinline__ void pause_ns(uint64_t ns) {
   } else {                        \
     F<C1, PAIR>(__VA_ARGS__);     \
   }
+#define HMM_BY_PROB_PS(q, F, ...)     \
+  if (((q) & 1) == 0) {               \
+    F<C0, PAIR, SMALL>(__VA_ARGS__);  \
+  } else {                            \
+    F<C1, PAIR, SMALL>(__VA_ARGS__);  \
+  }
 
-template <bool PAIR, class C0, class C1>
+template <bool PAIR, bool SMALL, class C0, class C1>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gmm_kernel(const __grid_constant__ Params P, const __grid_constant__ Maps maps) {
-  constexpr int NST = PAIR ? PAIR_STAGES : STAGES;
-  constexpr int SBYTES = PAIR ? PAIR_STAGE_BYTES : STAGE_BYTES;
+  static_assert(!(PAIR && SMALL), "small token blocks run on single CTAs");
+  constexpr int NST = PAIR ? PAIR_STAGES : (SMALL ? SMALL_STAGES : STAGES);
+  constexpr int SBYTES = PAIR ? PAIR_STAGE_BYTES : (SMALL ? SMALL_STAGE_BYTES : STAGE_BYTES);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -781,8 +799,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (rec && kb == 0) rec[2] = globaltimer_ns();
           uint8_t* sW = stages + stage * SBYTES;
           const uint32_t full_cl = PAIR ? mapa_shared(smem_u32(&full[stage]), 0) : 0u;
-          HMM_BY_PROB_P(ti.prob, load_stage, pr, ti, kb, &mp[0], &mp[1], sW, sW + W_BYTES,
-                        &full[stage], full_cl, rank);
+          HMM_BY_PROB_PS(ti.prob, load_stage, pr, ti, kb, &mp[0], &mp[1], sW, sW + W_BYTES,
+                         &full[stage], full_cl, rank);
           ++issued;
           if (++stage == NST) {
             stage = 0;
@@ -975,14 +993,14 @@ int map_w(const GemmEnv& env, CUtensorMap* m, const void* base, int64_t E, int64
   return encode(env, m, base, 3, dims, str, box);
 }
 
-template <bool PAIR, class C0, class C1>
+template <bool PAIR, bool SMALL, class C0, class C1>
 int launch(const GemmEnv& env, Params& P, const Maps& maps, int64_t max_tiles, int kind) {
   if (max_tiles <= 0 || P.nprob == 0) return HMM_OK;
   if (env.trace && env.trace_which == kind) {
     P.trace = env.trace;
     P.trace_cap = env.trace_cap;
   }
-  auto kern = gmm_kernel<PAIR, C0, C1>;
+  auto kern = gmm_kernel<PAIR, SMALL, C0, C1>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
       cudaSuccess)
     return HMM_ERR_CUDA;
@@ -993,6 +1011,7 @@ int launch(const GemmEnv& env, Params& P, const Maps& maps, int64_t max_tiles, i
   P.status = env.status;
   P.budget_ns = env.budget_ns;
   P.pair = PAIR ? 1 : 0;
+  P.nt = SMALL ? SMALL_NT : NT;
   if constexpr (PAIR) {
     // clusters of two CTAs, as many as can be resident at once (the tile
     // dependencies inside the launch need every CTA running)
@@ -1056,9 +1075,10 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
   const int64_t H = p.H, I = p.I, E = p.E, R = p.R;
   Maps maps;
   int rc = HMM_OK;
-  rc |= map_act(env, &maps.m[0][0], x_perm, R, H, NT / 2);  // x_perm [R, H], K = H
-  rc |= map_w(env, &maps.m[0][1], W1, E, H, 2 * I, 64);     // W1 [E, H, 2I]: MN-major
-  rc |= map_act(env, &maps.m[1][0], a, R, I, NT / 2);       // a [R, I], K = I
+  const uint32_t tbox = env.small_rows ? SMALL_NT : NT / 2;     // token rows per box
+  rc |= map_act(env, &maps.m[0][0], x_perm, R, H, tbox);  // x_perm [R, H], K = H
+  rc |= map_w(env, &maps.m[0][1], W1, E, H, 2 * I, 64);   // W1 [E, H, 2I]: MN-major
+  rc |= map_act(env, &maps.m[1][0], a, R, I, tbox);       // a [R, I], K = I
   rc |= map_w(env, &maps.m[1][1], W2, E, I, H, 64);         // W2 [E, I, H]: MN-major
   CUtensorMap s0, s1;
   if (p.shared) {
@@ -1101,8 +1121,9 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
   g2.wait_unit = EPI_WARPS * ncta * g1.n_tiles;  // every GMM1 tile of the token block
   if (p.shared) add_shared(P, maps, static_cast<int>(E), s0, s1);
   const int64_t max_tiles = (p.R / TROWS) * (g1.n_tiles + g2.n_tiles);
-  if (env.pair_rows) return launch<true, CfgGmm1, CfgGmm2>(env, P, maps, max_tiles, 0);
-  return launch<false, CfgGmm1, CfgGmm2>(env, P, maps, max_tiles, 0);
+  if (env.pair_rows) return launch<true, false, CfgGmm1, CfgGmm2>(env, P, maps, max_tiles, 0);
+  if (env.small_rows) return launch<false, true, CfgGmm1, CfgGmm2>(env, P, maps, max_tiles, 0);
+  return launch<false, false, CfgGmm1, CfgGmm2>(env, P, maps, max_tiles, 0);
 }
 
 int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
@@ -1114,10 +1135,11 @@ int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPt
   Maps maps;
   int rc = HMM_OK;
   // act_grad: G = dy_perm . W2^T   (weights: 128 rows of W2 [E, I, H] per CTA, N = I)
-  rc |= map_act(env, &maps.m[0][0], dy_perm, R, H, NT / 2);
+  const uint32_t tbox = env.small_rows ? SMALL_NT : NT / 2;  // token rows per box
+  rc |= map_act(env, &maps.m[0][0], dy_perm, R, H, tbox);
   rc |= map_w(env, &maps.m[0][1], W2, E, I, H, BW);
   // input-grad: dX_perm = dH . W1^T (weights: 128 rows of W1 [E, H, 2I] per CTA, N = H)
-  rc |= map_act(env, &maps.m[1][0], dH, R, 2 * I, NT / 2);
+  rc |= map_act(env, &maps.m[1][0], dH, R, 2 * I, tbox);
   rc |= map_w(env, &maps.m[1][1], W1, E, H, 2 * I, BW);
   CUtensorMap s0, s1;
   if (p.shared) {
@@ -1168,8 +1190,10 @@ int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPt
   if (p.shared) add_shared(P, maps, static_cast<int>(E), s0, s1);
   const int64_t data_tiles = (p.R / TROWS) * (ag.n_tiles + ig.n_tiles);
   if (env.pair_rows)
-    return launch<true, CfgActGrad, CfgInGrad>(env, P, maps, data_tiles, 1);
-  return launch<false, CfgActGrad, CfgInGrad>(env, P, maps, data_tiles, 1);
+    return launch<true, false, CfgActGrad, CfgInGrad>(env, P, maps, data_tiles, 1);
+  if (env.small_rows)
+    return launch<false, true, CfgActGrad, CfgInGrad>(env, P, maps, data_tiles, 1);
+  return launch<false, false, CfgActGrad, CfgInGrad>(env, P, maps, data_tiles, 1);
 }
 
 }  // namespace hmm

@@ -48,7 +48,7 @@ struct hmm_ctx {
   uint64_t budget_ns = 2000000000ull;
   int inject_skip_ready = 0;
   int profile = 0;
-  int pair_rows = 2;  // 0 off, 1 on, 2 automatic
+  int pair_rows = 2;  // 0 single CTAs, 1 CTA pairs, 2 automatic, 3 single CTAs, small blocks
   uint64_t* trace = nullptr;
   size_t trace_bytes = 0;
   int trace_which = 0;
@@ -246,8 +246,12 @@ GemmEnv env_of(hmm_ctx* ctx, const Plan& p, cudaStream_t st) {
   e.encode = ctx->encode;
   e.num_sms = ctx->num_sms;
   // pairs (half the tiles, half the token rows staged per SM) pay off when
-  // experts average a full 256-row token block
-  e.pair_rows = ctx->pair_rows == 2 ? (p.TK >= 2 * BM * p.E ? 1 : 0) : ctx->pair_rows;
+  // experts average a full 256-row token block; below 64 rows per expert the
+  // launches stream weights, best with small token blocks and more stages
+  int mode = ctx->pair_rows;
+  if (mode == 2) mode = p.TK >= 2 * BM * p.E ? 1 : (p.TK < 64 * p.E ? 3 : 0);
+  e.pair_rows = mode == 1 ? 1 : 0;
+  e.small_rows = mode == 3 ? 1 : 0;
   e.trace = ctx->trace;
   e.trace_cap = ctx->trace ? static_cast<int>(ctx->trace_bytes / (64 * ctx->num_sms)) : 0;
   e.trace_which = ctx->trace_which;
@@ -356,7 +360,7 @@ int hmm_set_option(hmm_ctx* ctx, int option, int64_t value) {
       ctx->profile = value != 0;
       return HMM_OK;
     case HMM_OPT_PAIR_ROWS:
-      if (value < 0 || value > 2) return HMM_ERR_ARG;
+      if (value < 0 || value > 3) return HMM_ERR_ARG;
       ctx->pair_rows = static_cast<int>(value);
       return HMM_OK;
     default:

@@ -101,6 +101,7 @@ struct GemmEnv {
   int trace_cap;     // records per CTA
   int trace_which;   // which GEMM launch kind is traced
   int pair_rows;     // forward and data-gradient GEMMs on CTA pairs (2-SM MMA)
+  int small_rows;    // ... on single CTAs with token blocks of at most 64 rows
   unsigned* status;
   uint64_t budget_ns;
   cudaStream_t stream;

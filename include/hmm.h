@@ -121,13 +121,16 @@ int hmm_destroy(hmm_ctx* ctx);
  *                         hmm_profile_read).  Default 0. */
 #define HMM_OPT_PROFILE 4
 /*   (option ids 5 and 6 are not used) */
-/*   HMM_OPT_PAIR_ROWS     2 (default): automatic; the forward GEMMs and the
- *                         data-gradient GEMMs run on CTA pairs with 2-SM MMAs
- *                         (256 weight columns per tile, 128 per CTA) when the
- *                         routed rows average at least 256 per expert
- *                         (T * K >= 256 * E), else on single CTAs (128 weight
- *                         columns per tile).  1: always on CTA pairs; 0: never.
- *                         Results do not depend on it. */
+/*   HMM_OPT_PAIR_ROWS     tiling of the forward and data-gradient GEMMs:
+ *                         1: CTA pairs with 2-SM MMAs (256 weight columns per
+ *                         tile, 128 per CTA, token blocks of up to 256 rows);
+ *                         0: single CTAs (128 weight columns, blocks of up to
+ *                         256 rows); 3: single CTAs with blocks of up to 64
+ *                         rows and deeper pipelines (weight streaming);
+ *                         2 (default): automatic, 1 when the routed rows
+ *                         average at least 256 per expert (T * K >= 256 * E),
+ *                         3 below 64 per expert, else 0.  Results do not
+ *                         depend on it. */
 #define HMM_OPT_PAIR_ROWS 7
 int hmm_set_option(hmm_ctx* ctx, int option, int64_t value);
 

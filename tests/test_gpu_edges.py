@@ -22,7 +22,7 @@ def run():
     return gu.Runner()
 
 
-@pytest.fixture(params=[0, 1], ids=["cta", "pair"])
+@pytest.fixture(params=[0, 1, 3], ids=["cta", "pair", "small"])
 def rows_mode(run, request):
     hmm.hmm_set_option(run.ctx.handle, hmm.HMM_OPT_PAIR_ROWS, request.param)
     yield request.param

@@ -107,9 +107,10 @@ def _scenarios():
 SCEN = list(_scenarios())
 
 
-@pytest.fixture(params=[0, 1], ids=["cta", "pair"])
+@pytest.fixture(params=[0, 1, 3], ids=["cta", "pair", "small"])
 def rows_mode(run, request):
-    """Rows-mode GEMMs on single CTAs or on CTA pairs (2-SM MMAs)."""
+    """Rows-mode GEMMs on single CTAs, on CTA pairs (2-SM MMAs) or on single
+    CTAs with token blocks of at most 64 rows."""
     hmm.hmm_set_option(run.ctx.handle, hmm.HMM_OPT_PAIR_ROWS, request.param)
     yield request.param
     hmm.hmm_set_option(run.ctx.handle, hmm.HMM_OPT_PAIR_ROWS, 2)
