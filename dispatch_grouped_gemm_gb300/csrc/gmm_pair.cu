@@ -336,12 +336,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       const int64_t rl = t.m0 + 128 * static_cast<int>(rank) + q4 * 32 + (lane >> 2);
       __nv_bfloat16* obase = pr.out + static_cast<int64_t>(t.e - pr.e_lo) * pr.out_estride;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      // each chunk's TMEM load is issued before the previous chunk is
+      // transposed and stored, so its latency hides behind that work
+      const int nch = min(8, (pr.N - t.n0 + 31) / 32);  // chunks inside the output
+      uint32_t ra[32], rb[32];
+      if (nch > 0) {
+        tmem_ld32(taddr, ra);
+        tmem_ld_wait_for(ra);
+      }
+      auto drain = [&](const uint32_t (&r)[32], int c) {
         const int col = t.n0 + c * 32;
-        if (col >= pr.N) break;
-        uint32_t r[32];
-        tmem_ld32(taddr + c * 32, r);
-        tmem_ld_wait();
         float v[4][8];
         xpose(xbuf, lane, r, v);
         if (col + cg < pr.N) {
@@ -350,6 +354,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             if (rl + 8 * k < pr.M)
               *reinterpret_cast<uint4*>(obase + (rl + 8 * k) * pr.ld_out + col + cg) =
                   pack_bf16x8(v[k]);
+        }
+      };
+#pragma unroll
+      for (int c = 0; c < 8; c += 2) {
+        if (c < nch) {
+          if (c + 1 < nch) tmem_ld32(taddr + (c + 1) * 32, rb);
+          drain(ra, c);
+          if (c + 1 < nch) {
+            tmem_ld_wait_for(rb);
+            if (c + 2 < nch) tmem_ld32(taddr + (c + 2) * 32, ra);
+            drain(rb, c + 1);
+            if (c + 2 < nch) tmem_ld_wait_for(ra);
+          }
         }
       }
       tc_fence_before();
