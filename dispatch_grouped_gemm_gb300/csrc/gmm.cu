@@ -512,9 +512,22 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
         wn[k] = __ldg(pr.rowscale + row);
       }
     };
+    // the 8 KB block (gate, then up) of the chunk PF_H ahead into L2: two
+    // 128-byte lines per lane, no registers held (the loads of the next
+    // chunk are all the registers allow)
+    auto prefetch_h = [&](int j) {
+      const int64_t row = ti.row0 + 32 * j;
+      const char* blk = reinterpret_cast<const char*>(hb + hblock_offset(row, c0, pr.ld_aux));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(blk + lane * 128));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(blk + 4096 + lane * 128));
+    };
+    constexpr int PF_H = 2;
     load_h(0);
+    if (c0 < pr.N)
+      for (int j = 1; j < PF_H && j < nch; ++j) prefetch_h(j);
 #pragma unroll 1
     for (int j = 0; j < nch; ++j) {
+      if (j + PF_H < nch && c0 < pr.N) prefetch_h(j + PF_H);
       float gv[4][8], uv[4][8], w[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
