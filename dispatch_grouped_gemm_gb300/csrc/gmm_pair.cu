@@ -35,11 +35,15 @@ namespace hmm {
 
 namespace {
 
-constexpr int PSTAGES = 4;
-constexpr int PA_BYTES = 128 * 64 * 2;  // this CTA's 128 rows of A, 64 deep (bf16)
-constexpr int PB_BYTES = 128 * 64 * 2;  // this CTA's 128 columns of B, 64 deep (bf16)
-constexpr int PL_BYTES = 128 * 64;      // the low part of the split one of them (e5m2)
-constexpr int PO_BYTES = 128 * 64;      // the fp8 copy of the other one
+// Expert rows per K step (a multiple of 32) and stages (192 KB in all).  Eight
+// 24 KB stages of 32 rows made the launch 23 % slower than four of 64: more,
+// smaller copies and barrier round trips per byte.
+constexpr int PK = 64;
+constexpr int PSTAGES = 4 * 64 / PK;
+constexpr int PA_BYTES = 128 * PK * 2;  // this CTA's 128 rows of A, PK deep (bf16)
+constexpr int PB_BYTES = 128 * PK * 2;  // this CTA's 128 columns of B, PK deep (bf16)
+constexpr int PL_BYTES = 128 * PK;      // the low part of the split one of them (e5m2)
+constexpr int PO_BYTES = 128 * PK;      // the fp8 copy of the other one
 constexpr int PSTAGE = PA_BYTES + PB_BYTES + PL_BYTES + PO_BYTES;
 constexpr int P_THREADS = 192;
 constexpr int P_EPI_WARPS = 4;
@@ -102,7 +106,7 @@ __device__ __forceinline__ void pair_decode(const PairParams& P, int u, PairTile
   t.n0 = (r % pr.n_tiles) * 256;
   t.krow0 = P.poff[t.e];
   // rows past counts[e] are zero padding: skip whole zero K blocks
-  t.kb = (P.counts[t.e] + 63) / 64;
+  t.kb = (P.counts[t.e] + PK - 1) / PK;
 }
 
 // Timeline record of this CTA's lt-th tile (even CTA of the pair only).
@@ -206,7 +210,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             break;
           }
           if (rec && kb == 0) rec[2] = globaltimer_ns();
-          const int k = t.krow0 + kb * 64;
+          const int k = t.krow0 + kb * PK;
           uint8_t* sA = stages + stage * PSTAGE;
           uint8_t* sB = sA + PA_BYTES;
           uint8_t* sL = sB + PB_BYTES;
@@ -217,9 +221,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * PSTAGE);
           const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
           tma_load_2d_pair(sA, &mp[0], bar, ma, k);
-          tma_load_2d_pair(sA + 8192, &mp[0], bar, ma + 64, k);
+          tma_load_2d_pair(sA + PA_BYTES / 2, &mp[0], bar, ma + 64, k);
           tma_load_2d_pair(sB, &mp[1], bar, nbc, k);
-          tma_load_2d_pair(sB + 8192, &mp[1], bar, nbc + 64, k);
+          tma_load_2d_pair(sB + PB_BYTES / 2, &mp[1], bar, nbc + 64, k);
           tma_load_2d_pair(sL, &mp[2], bar, lc, k);  // 128 fp8 columns in one box
           tma_load_2d_pair(sO, &mp[3], bar, oc, k);
           ++issued;
@@ -268,10 +272,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
           const uint32_t l_base = b_base + PB_BYTES;
           const uint32_t o_base = l_base + PL_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // MN-major bf16: two 64-wide chunks 8 KB apart, 8-row groups 1 KB
-            const uint64_t ad = smem_desc(a_base + kk * 2048, 8192, 1024, LAYOUT_SW128);
-            const uint64_t bd = smem_desc(b_base + kk * 2048, 8192, 1024, LAYOUT_SW128);
+          for (int kk = 0; kk < PK / 16; ++kk) {
+            // MN-major bf16: two 64-wide chunks PA_BYTES / 2 apart, 8-row groups 1 KB
+            const uint64_t ad = smem_desc(a_base + kk * 2048, PA_BYTES / 2, 1024, LAYOUT_SW128);
+            const uint64_t bd = smem_desc(b_base + kk * 2048, PB_BYTES / 2, 1024, LAYOUT_SW128);
             umma_bf16_pair(d_tmem, ad, bd, IDESC_PAIR, (kb == 0 && kk == 0) ? 0u : 1u);
           }
           // the low part against the fp8 copy: MN-major fp8, one 128-wide
@@ -279,7 +283,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
           const uint32_t a2_base = split == 1 ? l_base : o_base;
           const uint32_t b2_base = split == 1 ? o_base : l_base;
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
+          for (int kk = 0; kk < PK / 32; ++kk) {
             const uint64_t ad = smem_desc(a2_base + kk * 4096, 8192, 1024, LAYOUT_SW128);
             const uint64_t bd = smem_desc(b2_base + kk * 4096, 8192, 1024, LAYOUT_SW128);
             umma_f8_pair(d_tmem, ad, bd, split == 1 ? IDESC_LO_A : IDESC_LO_B, 1u);
@@ -392,12 +396,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   }
 }
 
-// fp8 rows (ld bytes apart): boxes of 128 columns x 64 rows
+// fp8 rows (ld bytes apart): boxes of 128 columns x PK rows
 int encode2d_u8(const GemmEnv& env, CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
                 int64_t ld) {
   const cuuint64_t gd[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t gs[1] = {static_cast<cuuint64_t>(ld)};
-  const cuuint32_t bx[2] = {128, 64};
+  const cuuint32_t bx[2] = {128, PK};
   const cuuint32_t es[2] = {1, 1};
   CUresult r = env.encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gd, gs,
                           bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -408,7 +412,7 @@ int encode2d_u8(const GemmEnv& env, CUtensorMap* m, const void* base, int64_t ro
 int encode2d(const GemmEnv& env, CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
   const cuuint64_t gd[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t gs[1] = {static_cast<cuuint64_t>(cols) * 2};
-  const cuuint32_t bx[2] = {64, 64};
+  const cuuint32_t bx[2] = {64, PK};
   const cuuint32_t es[2] = {1, 1};
   CUresult r = env.encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gd, gs,
                           bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
