@@ -697,6 +697,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
+  // set-up done: from here on global memory (routing metadata, operands,
+  // counters) that the stream's previous kernel may still be writing
+  grid_dep_wait();
+  grid_dep_launch();
   const WaitCtl wc{s_abort, P.status, P.budget_ns};
   // in a pair the odd CTA's consumers release the even CTA's tile-info slots
   auto ti_release = [&](int slot) {
@@ -1045,12 +1049,16 @@ int launch(const GemmEnv& env, Params& P, const Maps& maps, int64_t max_tiles, i
     if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active <= 0)
       return HMM_ERR_CUDA;
     clusters = static_cast<int>(std::min<int64_t>(std::min(clusters, active), max_tiles));
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-    return cudaLaunchKernelEx(&cfg, kern, P, maps) == cudaSuccess ? HMM_OK : HMM_ERR_CUDA;
+    return launch_kernel(kern, 2 * clusters, NUM_THREADS, SMEM_BYTES, env.stream, env.pdl, 2, P,
+                         maps) == cudaSuccess
+               ? HMM_OK
+               : HMM_ERR_CUDA;
   } else {
     const int grid = static_cast<int>(std::min<int64_t>(env.num_sms, max_tiles));
-    kern<<<grid, NUM_THREADS, SMEM_BYTES, env.stream>>>(P, maps);
-    return cudaGetLastError() == cudaSuccess ? HMM_OK : HMM_ERR_CUDA;
+    return launch_kernel(kern, grid, NUM_THREADS, SMEM_BYTES, env.stream, env.pdl, 1, P, maps) ==
+                   cudaSuccess
+               ? HMM_OK
+               : HMM_ERR_CUDA;
   }
 }
 

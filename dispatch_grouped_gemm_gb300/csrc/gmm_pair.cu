@@ -172,6 +172,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
+  // set-up done: from here on global memory the stream's previous kernel may
+  // still be writing
+  grid_dep_wait();
+  grid_dep_launch();
   const WaitCtl wc{s_abort, P.status, P.budget_ns};
 
   int total = 0;
@@ -509,8 +513,11 @@ int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, const void*
       clusters = std::min(clusters, active);
   }
   clusters = static_cast<int>(std::min<int64_t>(clusters, total));
-  wgrad_pair_kernel<<<2 * clusters, P_THREADS, P_SMEM, env.stream>>>(P, maps);
-  return cudaGetLastError() == cudaSuccess ? HMM_OK : HMM_ERR_CUDA;
+  // (cluster shape from the kernel's __cluster_dims__)
+  return launch_kernel(wgrad_pair_kernel, 2 * clusters, P_THREADS, P_SMEM, env.stream, env.pdl, 1,
+                       P, maps) == cudaSuccess
+             ? HMM_OK
+             : HMM_ERR_CUDA;
 }
 
 }  // namespace hmm

@@ -26,6 +26,7 @@ struct PhaseInfo {
   int kernels;
 };
 constexpr PhaseInfo kPhases[HMM_NUM_PHASES] = {
+    // route launches 2 or 3 kernels (route_launches); 3 is the most
     {"route", 3},       {"dispatch_x", 1},    {"gemm_fwd", 1},        {"combine_y", 1},
     {"dispatch_dy", 1}, {"gemm_bwd_data", 1}, {"gemm_bwd_weight", 1}, {"combine_dx", 1}};
 enum Phase {
@@ -35,6 +36,7 @@ enum Phase {
 
 struct ProfRec {
   int phase;
+  int kernels;  // kernels the phase launched
   cudaEvent_t begin, end;
 };
 
@@ -49,6 +51,7 @@ struct hmm_ctx {
   int inject_skip_ready = 0;
   int profile = 0;
   int pair_rows = 2;  // 0 single CTAs, 1 CTA pairs, 2 automatic, 3 single CTAs, small blocks
+  int overlap = 1;    // programmatic dependent launches
   uint64_t* trace = nullptr;
   size_t trace_bytes = 0;
   int trace_which = 0;
@@ -81,8 +84,10 @@ struct PhaseScope {
   hmm_ctx* c;
   int phase;
   cudaStream_t st;
+  int kernels;
   cudaEvent_t begin = nullptr;
-  PhaseScope(hmm_ctx* ctx, int ph, cudaStream_t s) : c(ctx), phase(ph), st(s) {
+  PhaseScope(hmm_ctx* ctx, int ph, cudaStream_t s, int nkern = -1)
+      : c(ctx), phase(ph), st(s), kernels(nkern >= 0 ? nkern : kPhases[ph].kernels) {
     if (c->profile && (begin = take_event(c)) != nullptr) cudaEventRecord(begin, st);
   }
   ~PhaseScope() {
@@ -93,7 +98,7 @@ struct PhaseScope {
       return;
     }
     cudaEventRecord(end, st);
-    c->recs.push_back({phase, begin, end});
+    c->recs.push_back({phase, kernels, begin, end});
   }
 };
 
@@ -258,6 +263,7 @@ GemmEnv env_of(hmm_ctx* ctx, const Plan& p, cudaStream_t st) {
   e.status = ctx->status;
   e.budget_ns = ctx->budget_ns;
   e.stream = st;
+  e.pdl = ctx->overlap != 0;
   return e;
 }
 
@@ -363,6 +369,9 @@ int hmm_set_option(hmm_ctx* ctx, int option, int64_t value) {
       if (value < 0 || value > 3) return HMM_ERR_ARG;
       ctx->pair_rows = static_cast<int>(value);
       return HMM_OK;
+    case HMM_OPT_OVERLAP_LAUNCHES:
+      ctx->overlap = value != 0;
+      return HMM_OK;
     default:
       return HMM_ERR_ARG;
   }
@@ -399,7 +408,8 @@ int hmm_route(hmm_ctx* ctx, const hmm_shape* shape, const int32_t* topk_ids, int
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   CtrlPtrs c = ctrl_at(p, workspace);
   MetaPtrs m = meta_at(p, static_cast<uint8_t*>(workspace) + p.ctrl_bytes);
-  rc = cuda_rc(launch_route(p, topk_ids, m, c, slot2row, row2slot, ctx->status, st));
+  rc = cuda_rc(launch_route(p, topk_ids, m, c, slot2row, row2slot, ctx->status, st,
+                                  ctx->overlap != 0));
   if (rc != HMM_OK) return rc;
   rc = cuda_rc(cudaMemcpyAsync(counts, m.counts, 4 * p.E, cudaMemcpyDeviceToDevice, st));
   if (rc != HMM_OK) return rc;
@@ -449,8 +459,9 @@ int forward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* x, const int3
   void* o = ws + p.fw_o;
 
   {
-    PhaseScope ps(ctx, PH_ROUTE, st);
-    rc = cuda_rc(launch_route(p, topk_ids, m, c, nullptr, nullptr, ctx->status, st));
+    PhaseScope ps(ctx, PH_ROUTE, st, route_launches(p));
+    rc = cuda_rc(launch_route(p, topk_ids, m, c, nullptr, nullptr, ctx->status, st,
+                              ctx->overlap != 0));
   }
   if (rc != HMM_OK) return rc;
   if (ctx->validate) {
@@ -459,7 +470,7 @@ int forward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* x, const int3
   }
   {
     PhaseScope ps(ctx, PH_DISPATCH_X, st);
-    rc = cuda_rc(launch_dispatch_x(p, x, m, x_perm, x8, st));
+    rc = cuda_rc(launch_dispatch_x(p, x, m, x_perm, x8, st, ctx->overlap != 0));
   }
   if (rc != HMM_OK) return rc;
   const bool inject = ctx->inject_skip_ready != 0;
@@ -471,7 +482,8 @@ int forward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* x, const int3
   }
   if (rc != HMM_OK) return rc;
   PhaseScope ps(ctx, PH_COMBINE_Y, st);
-  return cuda_rc(launch_combine_y(p, o, topk_weights, shape->weights_dtype, m, y, st));
+  return cuda_rc(launch_combine_y(p, o, topk_weights, shape->weights_dtype, m, y, st,
+                                ctx->overlap != 0));
 }
 
 }  // namespace
@@ -584,7 +596,7 @@ int backward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const vo
     PhaseScope ps(ctx, PH_DISPATCH_DY, st);
     rc = cuda_rc(
         launch_dispatch_dy(p, dy, topk_weights, shape->weights_dtype, m, c, dy_perm, dy8, wperm,
-                           st));
+                           st, ctx->overlap != 0));
   }
   if (rc != HMM_OK) return rc;
   {
@@ -603,8 +615,9 @@ int backward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const vo
     if (rc != HMM_OK) return rc;
     {
       PhaseScope pc(ctx, PH_COMBINE_DX, ctx->side);
+      // (behind an event wait: launched in plain stream order)
       rc = cuda_rc(launch_combine_dx(p, dx_perm, dwp, m, dx, d_topk_weights,
-                                     shape->weights_dtype, ctx->side));
+                                     shape->weights_dtype, ctx->side, false));
     }
     const int rj = cuda_rc(cudaEventRecord(ctx->join, ctx->side));
     if (rc == HMM_OK) rc = rj;
@@ -697,7 +710,7 @@ int hmm_profile_read(hmm_ctx* ctx, int n, double* ms, int64_t* launches) {
         cudaEventElapsedTime(&t, r.begin, r.end) != cudaSuccess)
       rc = HMM_ERR_CUDA;
     acc[r.phase] += t;
-    cnt[r.phase] += kPhases[r.phase].kernels;
+    cnt[r.phase] += r.kernels;
     ctx->pool.push_back(r.begin);
     ctx->pool.push_back(r.end);
   }

@@ -72,22 +72,71 @@ int make_plan(const hmm_shape* s, bool training, Plan* p);
 MetaPtrs meta_at(const Plan& p, void* base);
 CtrlPtrs ctrl_at(const Plan& p, void* base);
 
+// ------------------------------------------- programmatic dependent launches
+// Every kernel of the library may be launched with programmatic stream
+// serialization (pdl): it is then scheduled while the previous kernel of its
+// stream drains, runs its set-up (barriers, TMEM) meanwhile, and calls
+// grid_dep_wait() before its first access to global memory; that returns once
+// the previous kernel has completed and its writes are visible, and is a
+// no-op in a kernel launched without the attribute.  grid_dep_launch(), called
+// by every CTA right after its wait, lets the stream's next kernel be
+// scheduled in turn.  Event records and waits between launches keep their
+// full ordering.
+#ifdef __CUDACC__
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
+
+// Launch `kern` on `st` (clusters of cluster_x CTAs when > 1; with pdl, with
+// programmatic stream serialization).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, bool pdl, unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = n ? attr : nullptr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ------------------------------------------------------------ kernel launchers
-// Each returns a cudaError_t of its launch.
+// Each returns a cudaError_t of its launch; pdl as for launch_kernel.
 cudaError_t launch_route(const Plan& p, const int32_t* ids, MetaPtrs m, CtrlPtrs c,
                          int32_t* slot2row, int32_t* row2slot, unsigned* status,
-                         cudaStream_t st);
+                         cudaStream_t st, bool pdl);
+int route_launches(const Plan& p);  // kernels launch_route launches for p
 // x8 (training, else null): also x_perm as e4m3 (ld8_h bytes per row)
 cudaError_t launch_dispatch_x(const Plan& p, const void* x, MetaPtrs m, void* x_perm, void* x8,
-                              cudaStream_t st);
+                              cudaStream_t st, bool pdl);
 cudaError_t launch_combine_y(const Plan& p, const void* o, const void* w, int w_dtype, MetaPtrs m,
-                             void* y, cudaStream_t st);
+                             void* y, cudaStream_t st, bool pdl);
 // also dy_perm as e5m2 (dy8, ld8_h bytes per row)
 cudaError_t launch_dispatch_dy(const Plan& p, const void* dy, const void* w, int w_dtype,
                                MetaPtrs m, CtrlPtrs c, void* dy_perm, void* dy8, float* wperm,
-                               cudaStream_t st);
+                               cudaStream_t st, bool pdl);
 cudaError_t launch_combine_dx(const Plan& p, const void* dx_perm, const float* dwp, MetaPtrs m,
-                              void* dx, void* dw, int w_dtype, cudaStream_t st);
+                              void* dx, void* dw, int w_dtype, cudaStream_t st, bool pdl);
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -105,6 +154,7 @@ struct GemmEnv {
   unsigned* status;
   uint64_t budget_ns;
   cudaStream_t stream;
+  bool pdl;          // programmatic dependent launches (launch_kernel)
 };
 
 // forward GMM1(+SwiGLU) and GMM2 in one persistent launch with per-token-block

@@ -87,6 +87,8 @@ __global__ void __launch_bounds__(MOVE_THREADS) dispatch_rows_kernel(
     float* wperm, int32_t* zero_ptr, int64_t zero_count) {
   const int lane = threadIdx.x & 31;
   const int64_t g = static_cast<int64_t>(blockIdx.x) * MOVE_WARPS + (threadIdx.x >> 5);
+  grid_dep_wait();
+  grid_dep_launch();
   if (zero_ptr) {
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * MOVE_THREADS + threadIdx.x;
          i < zero_count; i += static_cast<int64_t>(gridDim.x) * MOVE_THREADS)
@@ -181,6 +183,8 @@ __global__ void __launch_bounds__(MOVE_THREADS) combine_rows_kernel(
     const float* dwp, int64_t dwp_ld, void* dw) {
   const int lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * MOVE_WARPS + (threadIdx.x >> 5);
+  grid_dep_wait();
+  grid_dep_launch();
   if (t >= T) return;
   int32_t prow_l = -1;
   float w_l = 0.0f;
@@ -234,46 +238,46 @@ static int move_grid(int64_t warps) {
 }
 
 cudaError_t launch_dispatch_x(const Plan& p, const void* x, MetaPtrs m, void* x_perm, void* x8,
-                              cudaStream_t st) {
+                              cudaStream_t st, bool pdl) {
   const int64_t warps = p.T + p.Ex * BM;
-  dispatch_rows_kernel<false><<<move_grid(warps), MOVE_THREADS, 0, st>>>(
-      static_cast<const uint4*>(x), p.T, p.K, p.H / 8, m, static_cast<int>(p.E),
-      static_cast<int>(p.Ex), static_cast<uint4*>(x_perm), static_cast<uint2*>(x8), p.ld8_h / 8,
-      nullptr, 0, nullptr, nullptr, 0);
-  return cudaGetLastError();
+  return launch_kernel(dispatch_rows_kernel<false>, move_grid(warps), MOVE_THREADS, 0, st, pdl, 1,
+                       static_cast<const uint4*>(x), p.T, p.K, p.H / 8, m, static_cast<int>(p.E),
+                       static_cast<int>(p.Ex), static_cast<uint4*>(x_perm),
+                       static_cast<uint2*>(x8), p.ld8_h / 8, nullptr, 0, nullptr, nullptr,
+                       int64_t(0));
 }
 
 cudaError_t launch_dispatch_dy(const Plan& p, const void* dy, const void* w, int w_dtype,
                                MetaPtrs m, CtrlPtrs c, void* dy_perm, void* dy8, float* wperm,
-                               cudaStream_t st) {
+                               cudaStream_t st, bool pdl) {
   const int64_t warps = p.T + p.Ex * BM;
   // also zero the backward launch counters (tickets and per-token-block ready
   // counters are contiguous in the control block)
   const int64_t nzero = p.ctrl_zero_count;
-  dispatch_rows_kernel<true><<<move_grid(warps), MOVE_THREADS, 0, st>>>(
-      static_cast<const uint4*>(dy), p.T, p.K, p.H / 8, m, static_cast<int>(p.E),
-      static_cast<int>(p.Ex), static_cast<uint4*>(dy_perm), static_cast<uint2*>(dy8),
-      p.ld8_h / 8, w, w_dtype, wperm, c.tickets, nzero);
-  return cudaGetLastError();
+  return launch_kernel(dispatch_rows_kernel<true>, move_grid(warps), MOVE_THREADS, 0, st, pdl, 1,
+                       static_cast<const uint4*>(dy), p.T, p.K, p.H / 8, m, static_cast<int>(p.E),
+                       static_cast<int>(p.Ex), static_cast<uint4*>(dy_perm),
+                       static_cast<uint2*>(dy8), p.ld8_h / 8, w, w_dtype, wperm, c.tickets, nzero);
 }
 
 cudaError_t launch_combine_y(const Plan& p, const void* o, const void* w, int w_dtype, MetaPtrs m,
-                             void* y, cudaStream_t st) {
+                             void* y, cudaStream_t st, bool pdl) {
   auto kern = p.shared ? combine_rows_kernel<true, true> : combine_rows_kernel<true, false>;
-  kern<<<move_grid(p.T), MOVE_THREADS, 0, st>>>(
-      o, w, w_dtype, p.T, p.K, p.H / 8, m.slot2prow,
-      p.shared ? m.poff + p.E : nullptr, static_cast<uint4*>(y), nullptr, 0, nullptr);
-  return cudaGetLastError();
+  return launch_kernel(kern, move_grid(p.T), MOVE_THREADS, 0, st, pdl, 1, o, w, w_dtype, p.T, p.K,
+                       p.H / 8, static_cast<const int32_t*>(m.slot2prow),
+                       static_cast<const int32_t*>(p.shared ? m.poff + p.E : nullptr),
+                       static_cast<uint4*>(y), static_cast<const float*>(nullptr), int64_t(0),
+                       static_cast<void*>(nullptr));
 }
 
 cudaError_t launch_combine_dx(const Plan& p, const void* dx_perm, const float* dwp, MetaPtrs m,
-                              void* dx, void* dw, int w_dtype, cudaStream_t st) {
+                              void* dx, void* dw, int w_dtype, cudaStream_t st, bool pdl) {
   auto kern = p.shared ? combine_rows_kernel<false, true> : combine_rows_kernel<false, false>;
-  kern<<<move_grid(p.T), MOVE_THREADS, 0, st>>>(
-      dx_perm, nullptr, w_dtype, p.T, p.K, p.H / 8, m.slot2prow,
-      p.shared ? m.poff + p.E : nullptr, static_cast<uint4*>(dx), dw ? dwp : nullptr, p.dwp_ld,
-      dw);
-  return cudaGetLastError();
+  return launch_kernel(kern, move_grid(p.T), MOVE_THREADS, 0, st, pdl, 1, dx_perm,
+                       static_cast<const void*>(nullptr), w_dtype, p.T, p.K, p.H / 8,
+                       static_cast<const int32_t*>(m.slot2prow),
+                       static_cast<const int32_t*>(p.shared ? m.poff + p.E : nullptr),
+                       static_cast<uint4*>(dx), dw ? dwp : nullptr, p.dwp_ld, dw);
 }
 
 }  // namespace hmm

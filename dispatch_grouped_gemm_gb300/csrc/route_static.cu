@@ -79,11 +79,12 @@ extern "C" int hmm_route_static(const hmm_shape* shape, const int32_t* topk_ids,
   m.counts = counts;
   m.offsets = offsets;
   // Nothing here must start at zero: the count kernel writes every histogram
-  // entry it covers, the scan kernel writes the counters and the padded
-  // offsets, the rank kernel writes every slot.  Stale contents of a previous
-  // call are overwritten before they are read.
+  // entry it covers, the scan (its own kernel, or inside the rank kernel)
+  // writes the counters and the padded offsets, the rank kernel writes every
+  // slot.  Stale contents of a previous call are overwritten before they are
+  // read.
   return launch_route(p, topk_ids, m, c, slot2row, row2slot, status,
-                      static_cast<cudaStream_t>(stream)) == cudaSuccess
+                      static_cast<cudaStream_t>(stream), true) == cudaSuccess
              ? HMM_OK
              : HMM_ERR_CUDA;
 }

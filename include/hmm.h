@@ -132,10 +132,17 @@ int hmm_destroy(hmm_ctx* ctx);
  *                         3 below 64 per expert, else 0.  Results do not
  *                         depend on it. */
 #define HMM_OPT_PAIR_ROWS 7
+/*   HMM_OPT_OVERLAP_LAUNCHES  0/1: launch every kernel with programmatic
+ *                         stream serialization, so that it is scheduled and
+ *                         sets itself up while the previous kernel of the
+ *                         stream drains; it still reads nothing before that
+ *                         kernel has completed.  Default 1.  Results do not
+ *                         depend on it. */
+#define HMM_OPT_OVERLAP_LAUNCHES 8
 int hmm_set_option(hmm_ctx* ctx, int option, int64_t value);
 
 /* Launch phases timed under HMM_OPT_PROFILE (index = phase id):
- *   0 route (3 kernels)  1 dispatch_x  2 gemm_fwd (GMM1+SwiGLU, GMM2)
+ *   0 route (2 or 3 kernels)  1 dispatch_x  2 gemm_fwd (GMM1+SwiGLU, GMM2)
  *   3 combine_y          4 dispatch_dy
  *   5 gemm_bwd_data (act_grad + SwiGLU grad, input-grad)
  *   6 gemm_bwd_weight (W2Grad, W1Grad)

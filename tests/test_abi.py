@@ -80,6 +80,16 @@ def test_error_strings(lib):
     assert "unknown" in hmm.hmm_error_string(-99)
 
 
+def test_phase_names(lib):
+    """Phase ids name the launch phases in step order; bench.py keys its
+    per-kernel roofline on these names."""
+    names = [hmm.hmm_phase_name(i) for i in range(hmm._C["HMM_NUM_PHASES"])]
+    assert names == ["route", "dispatch_x", "gemm_fwd", "combine_y", "dispatch_dy",
+                     "gemm_bwd_data", "gemm_bwd_weight", "combine_dx"]
+    assert hmm.hmm_phase_name(-1) is None
+    assert hmm.hmm_phase_name(len(names)) is None
+
+
 def test_create_without_gpu_fails_cleanly(lib):
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():

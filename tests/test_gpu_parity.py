@@ -55,6 +55,11 @@ def _routing_cases():
     yield "empty_hot", ids, 40
     yield "one_slot", np.array([[3]], np.int32), 4
     yield "E1", np.zeros((100, 1), np.int32), 1
+    # the scan inside the rank blocks at its limit (64 chunks x 512 experts),
+    # and the separate scan launch past it (E > 512; 157 chunks x 256 experts)
+    yield "fused_scan_limit", r.integers(0, 512, size=(8192, 8)).astype(np.int32), 512
+    yield "scan_launch_wide_E", r.integers(0, 600, size=(3000, 6)).astype(np.int32), 600
+    yield "scan_launch_many_chunks", r.integers(0, 256, size=(20000, 8)).astype(np.int32), 256
 
 
 @pytest.mark.parametrize("case", list(_routing_cases()), ids=lambda c: c[0])
@@ -170,6 +175,27 @@ def test_repeated_calls_bit_identical(run, rows_mode):
     for a, b in zip(outs[0], outs[2]):
         assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
                            b.view(torch.int16) if b.dtype == torch.bfloat16 else b)
+
+
+def test_overlapped_launches_bit_identical(run):
+    """Programmatic dependent launches change when kernels are scheduled,
+    never what they compute: forward and backward with and without them agree
+    bit for bit."""
+    p = dict(SCEN)["multi_tile"]
+    d = gu.upload(p)
+    outs = []
+    try:
+        for overlap in (0, 1):
+            hmm.hmm_set_option(run.ctx.handle, hmm.HMM_OPT_OVERLAP_LAUNCHES, overlap)
+            y, saved = run.forward(d)
+            outs.append([y.clone()] + [t.clone() for t in run.backward(d, saved)])
+        torch.cuda.synchronize()
+    finally:
+        hmm.hmm_set_option(run.ctx.handle, hmm.HMM_OPT_OVERLAP_LAUNCHES, 1)
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b)
+    assert run.status() == (0, 0)
 
 
 def test_out_of_range_expert_id_reported(run):
