@@ -80,6 +80,7 @@ struct PairParams {
 
 struct PairMaps {
   CUtensorMap m[4][4];  // A, B (bf16), low part of the split one, fp8 copy of the other
+  CUtensorMap out[4];   // the output [experts][M][N] (bf16), stored in 32 x 32 boxes
 };
 
 struct PairTile {
@@ -188,6 +189,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       // ------------------------------------------------------- TMA producer
       for (int q = 0; q < P.nprob; ++q)
         for (int j = 0; j < 4; ++j) tma_prefetch_desc(&maps.m[q][j]);
+      for (int q = 0; q < P.nprob; ++q) tma_prefetch_desc(&maps.out[q]);
       uint32_t stage = 0, sphase = 0;
       uint32_t issued = 0;
       bool ok = true;
@@ -311,8 +313,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     // ------------------------------------------------------------- epilogue
     const int q4 = warp & 3;
     const int row_in_half = q4 * 32 + lane;
-    float* xbuf = xbufs + (warp - 2) * (XBUF_BYTES / 4);
-    const int cg = (lane & 3) * 8;  // this lane's columns within a 32-column chunk
+    // two 2 KB staging buffers of 32 rows x 32 bf16 columns, 64-byte swizzled
+    // (16-byte unit u of row r at u ^ ((r >> 1) & 3)), one per chunk in turn
+    uint8_t* obuf = reinterpret_cast<uint8_t*>(xbufs + (warp - 2) * (XBUF_BYTES / 4));
+    uint32_t ck = 0;  // chunks this warp has stored
     uint32_t acc = 0, acc_phase = 0;
     const uint32_t tempty_cl[2] = {mapa_shared(smem_u32(&tempty[0]), 0),
                                    mapa_shared(smem_u32(&tempty[1]), 0)};
@@ -340,12 +344,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       tc_fence_after();
       if (rec) rec[6] = globaltimer_ns();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + acc * 256;
-      // this lane's rows after the transposition: rl + 8k
-      const int64_t rl = t.m0 + 128 * static_cast<int>(rank) + q4 * 32 + (lane >> 2);
-      __nv_bfloat16* obase = pr.out + static_cast<int64_t>(t.e - pr.e_lo) * pr.out_estride;
-#pragma unroll 1
+      // rows of this warp's chunks (the store leaves out rows past M and
+      // columns past N)
+      const int row0 = t.m0 + 128 * static_cast<int>(rank) + q4 * 32;
+      const CUtensorMap* omap = &maps.out[t.prob];
       // each chunk's TMEM load is issued before the previous chunk is
-      // transposed and stored, so its latency hides behind that work
+      // converted and stored, so its latency hides behind that work
       const int nch = min(8, (pr.N - t.n0 + 31) / 32);  // chunks inside the output
       uint32_t ra[32], rb[32];
       if (nch > 0) {
@@ -353,16 +357,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         tmem_ld_wait_for(ra);
       }
       auto drain = [&](const uint32_t (&r)[32], int c) {
-        const int col = t.n0 + c * 32;
-        float v[4][8];
-        xpose(xbuf, lane, r, v);
-        if (col + cg < pr.N) {
+        uint8_t* sb = obuf + (ck & 1u) * 2048;
+        if (lane == 0) bulk_wait_group_read<1>();  // chunk ck - 2's store has read sb
+        __syncwarp();
+        // lane = row: its 32 columns as four 16-byte units
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if (rl + 8 * k < pr.M)
-              *reinterpret_cast<uint4*>(obase + (rl + 8 * k) * pr.ld_out + col + cg) =
-                  pack_bf16x8(v[k]);
+        for (int u = 0; u < 4; ++u) {
+          float f[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(r[8 * u + i]);
+          *reinterpret_cast<uint4*>(sb + lane * 64 + 16 * (u ^ ((lane >> 1) & 3))) =
+              pack_bf16x8(f);
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(omap, sb, t.n0 + 32 * c, row0, t.e - pr.e_lo);
+          bulk_commit_group();
+        }
+        ++ck;
       };
 #pragma unroll
       for (int c = 0; c < 8; c += 2) {
@@ -389,6 +402,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (lane == 0) bulk_wait_group<0>();  // every store has landed
   }
 
   tc_fence_before();
@@ -410,6 +424,22 @@ int encode2d_u8(const GemmEnv& env, CUtensorMap* m, const void* base, int64_t ro
   CUresult r = env.encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gd, gs,
                           bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? HMM_OK : HMM_ERR_CUDA;
+}
+
+// the bf16 outputs [experts][rows][cols] (rows * cols per expert, cols per
+// row): boxes of 32 columns x 32 rows of one expert, 64-byte swizzled
+int encode_out(const GemmEnv& env, CUtensorMap* m, void* base, int64_t experts, int64_t rows,
+               int64_t cols) {
+  const cuuint64_t gd[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                            static_cast<cuuint64_t>(experts)};
+  const cuuint64_t gs[2] = {static_cast<cuuint64_t>(cols) * 2,
+                            static_cast<cuuint64_t>(rows * cols) * 2};
+  const cuuint32_t bx[3] = {32, 32, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = env.encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, gd, gs, bx, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? HMM_OK : HMM_ERR_CUDA;
 }
 
@@ -451,6 +481,7 @@ int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, const void*
     rc |= encode2d(env, &maps.m[q][1], dy_perm, R, H);
     rc |= encode2d_u8(env, &maps.m[q][2], wa_lo8, R, I, p.ld8_i);
     rc |= encode2d_u8(env, &maps.m[q][3], dy8, R, H, p.ld8_h);
+    rc |= encode_out(env, &maps.out[q], out, n_e, I, H);
     PairProb& w = P.p[q++];
     w.e_lo = e_lo;
     w.n_e = n_e;
@@ -469,6 +500,7 @@ int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, const void*
     rc |= encode2d(env, &maps.m[q][1], dH, R, 2 * I);
     rc |= encode2d_u8(env, &maps.m[q][2], dH_lo8, R, 2 * I, p.ld8_2i);
     rc |= encode2d_u8(env, &maps.m[q][3], x8, R, H, p.ld8_h);
+    rc |= encode_out(env, &maps.out[q], out, n_e, H, 2 * I);
     PairProb& w = P.p[q++];
     w.e_lo = e_lo;
     w.n_e = n_e;

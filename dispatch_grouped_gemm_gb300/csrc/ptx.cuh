@@ -88,6 +88,12 @@ __device__ __forceinline__ void raise_timeout(const WaitCtl& w) {
   atomicOr(w.status, HMM_STATUS_TIMEOUT);
 }
 
+// A wait reads the global status word (another CTA's timeout) only after it
+// has lasted this long: a global load under a GEMM's memory traffic takes
+// about a microsecond, and a phase that completes meanwhile would be seen that
+// much later.
+constexpr uint64_t STATUS_POLL_AFTER_NS = 20000;
+
 // Slow path of a bounded wait: true when the barrier phase completed, false
 // after the budget ran out, the CTA aborted, or another CTA reported a timeout.
 // CL: cluster-scope acquire (see mbar_try_wait_cl).
@@ -98,12 +104,14 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
     if (mbar_try_wait_s<CL>(bar, parity)) return true;
     if ((it & 31u) == 0) {
       if (*w.abort) return false;
-      if (*reinterpret_cast<volatile unsigned*>(w.status) & HMM_STATUS_TIMEOUT) {
-        *w.abort = 1;
+      const uint64_t dt = globaltimer_ns() - t0;
+      if (dt > w.budget_ns) {
+        raise_timeout(w);
         return false;
       }
-      if (globaltimer_ns() - t0 > w.budget_ns) {
-        raise_timeout(w);
+      if (dt > STATUS_POLL_AFTER_NS &&
+          (*reinterpret_cast<volatile unsigned*>(w.status) & HMM_STATUS_TIMEOUT)) {
+        *w.abort = 1;
         return false;
       }
     }
@@ -152,7 +160,36 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Order this thread's generic-proxy shared-memory writes before async-proxy
+// (TMA) reads of the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------- TMA
+// Store the box at src to the tensor at {c0, c1, c2}; parts outside the
+// tensor's bounds are not written.  One entry of this thread's bulk group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until at most N of this thread's bulk groups are incomplete.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
