@@ -698,9 +698,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
   // set-up done: from here on global memory (routing metadata, operands,
-  // counters) that the stream's previous kernel may still be writing
+  // counters) that the stream's previous kernel may still be writing.  (The
+  // next kernel is let in only when this CTA's producer has issued its last
+  // tile: its CTAs would otherwise wait beside this launch for all of it.)
   grid_dep_wait();
-  grid_dep_launch();
   const WaitCtl wc{s_abort, P.status, P.budget_ns};
   // in a pair the odd CTA's consumers release the even CTA's tile-info slots
   auto ti_release = [&](int slot) {
@@ -836,6 +837,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           pause_ns(200000);  // the even CTA counts our bytes; give the copies time to land
         }
       }
+      grid_dep_launch();  // this CTA is in its last tile
     }
   } else if (warp == 1) {
     if (lane == 0 && (!PAIR || leader)) {

@@ -174,9 +174,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
   // set-up done: from here on global memory the stream's previous kernel may
-  // still be writing
+  // still be writing.  (The next kernel is let in only when this CTA's
+  // producer has issued its last tile.)
   grid_dep_wait();
-  grid_dep_launch();
   const WaitCtl wc{s_abort, P.status, P.budget_ns};
 
   int total = 0;
@@ -249,6 +249,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
           pair_pause_ns(200000);  // the even CTA counts our bytes; give copies time to land
         }
       }
+      grid_dep_launch();  // this CTA is in its last tile
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {

@@ -78,10 +78,12 @@ CtrlPtrs ctrl_at(const Plan& p, void* base);
 // stream drains, runs its set-up (barriers, TMEM) meanwhile, and calls
 // grid_dep_wait() before its first access to global memory; that returns once
 // the previous kernel has completed and its writes are visible, and is a
-// no-op in a kernel launched without the attribute.  grid_dep_launch(), called
-// by every CTA right after its wait, lets the stream's next kernel be
-// scheduled in turn.  Event records and waits between launches keep their
-// full ordering.
+// no-op in a kernel launched without the attribute.  grid_dep_launch() lets
+// the stream's next kernel be scheduled once every CTA has called it (or
+// exited): the short kernels call it right after their wait, the persistent
+// GEMMs when a CTA has issued the loads of its last tile, so that the next
+// kernel's CTAs wait beside the GEMM's tail only.  Event records and waits
+// between launches keep their full ordering.
 #ifdef __CUDACC__
 __device__ __forceinline__ void grid_dep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
