@@ -44,36 +44,40 @@ def build(force: bool = False) -> str:
         return _LIB_PATH
 
 
+def _configure(lib):
+    """Declare the C entry points' signatures on a loaded library."""
+    i64, vp = ctypes.c_int64, ctypes.c_void_p
+    lib.oracle_route.restype = i64
+    lib.oracle_route.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp]
+    lib.oracle_forward.restype = i64
+    lib.oracle_forward.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int,
+                                   vp, vp, vp, vp, vp, vp]
+    lib.oracle_backward_tokens.restype = i64
+    lib.oracle_backward_tokens.argtypes = [i64, i64, i64, i64, i64,
+                                           ctypes.c_int, vp, vp, vp, vp,
+                                           vp, vp, vp, vp]
+    lib.oracle_weight_grad.restype = i64
+    lib.oracle_weight_grad.argtypes = [i64, i64, i64, i64, i64,
+                                       ctypes.c_int, i64, vp, vp, vp, vp,
+                                       vp, vp, vp, vp]
+    lib.oracle_expert_ffn.restype = None
+    lib.oracle_expert_ffn.argtypes = [i64, i64, ctypes.c_int, vp, i64, vp,
+                                      i64, vp, i64, vp, vp, vp]
+    lib.oracle_shared_forward.restype = None
+    lib.oracle_shared_forward.argtypes = [i64, i64, i64, ctypes.c_int, vp, vp, vp, vp]
+    lib.oracle_shared_backward.restype = None
+    lib.oracle_shared_backward.argtypes = [i64, i64, i64, ctypes.c_int, vp, vp, vp, vp,
+                                           vp, vp, vp]
+    lib.oracle_num_threads.restype = ctypes.c_int
+    lib.oracle_num_threads.argtypes = []
+    return lib
+
+
 def _load():
     global _lib
     if _lib is None:
         build()
-        lib = ctypes.CDLL(_LIB_PATH)
-        i64, vp = ctypes.c_int64, ctypes.c_void_p
-        lib.oracle_route.restype = i64
-        lib.oracle_route.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp]
-        lib.oracle_forward.restype = i64
-        lib.oracle_forward.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int,
-                                       vp, vp, vp, vp, vp, vp]
-        lib.oracle_backward_tokens.restype = i64
-        lib.oracle_backward_tokens.argtypes = [i64, i64, i64, i64, i64,
-                                               ctypes.c_int, vp, vp, vp, vp,
-                                               vp, vp, vp, vp]
-        lib.oracle_weight_grad.restype = i64
-        lib.oracle_weight_grad.argtypes = [i64, i64, i64, i64, i64,
-                                           ctypes.c_int, i64, vp, vp, vp, vp,
-                                           vp, vp, vp, vp]
-        lib.oracle_expert_ffn.restype = None
-        lib.oracle_expert_ffn.argtypes = [i64, i64, ctypes.c_int, vp, i64, vp,
-                                          i64, vp, i64, vp, vp, vp]
-        lib.oracle_shared_forward.restype = None
-        lib.oracle_shared_forward.argtypes = [i64, i64, i64, ctypes.c_int, vp, vp, vp, vp]
-        lib.oracle_shared_backward.restype = None
-        lib.oracle_shared_backward.argtypes = [i64, i64, i64, ctypes.c_int, vp, vp, vp, vp,
-                                               vp, vp, vp]
-        lib.oracle_num_threads.restype = ctypes.c_int
-        lib.oracle_num_threads.argtypes = []
-        _lib = lib
+        _lib = _configure(ctypes.CDLL(_LIB_PATH))
     return _lib
 
 
