@@ -53,6 +53,12 @@ MUTANTS = [
     ("permutation not stable inside an expert",
      "slot2row[s] = offsets[e] + seen[e];",
      "slot2row[s] = offsets[e] + (counts[e] - 1 - seen[e]);"),
+    ("shared expert's dx from the gate half only",
+     "acc += DH[t * 2 * I + j] * ld(Ws1, i * 2 * I + j, dt);",
+     "acc += (j < I ? DH[t * 2 * I + j] : 0.0) * ld(Ws1, i * 2 * I + j, dt);"),
+    ("shared expert's dWs2 with a transposed output",
+     "dWs2[j * H + c] += aj * ld(dy, t * H + c, dt);",
+     "dWs2[c * I + j] += aj * ld(dy, t * H + c, dt);"),
 ]
 
 
@@ -70,6 +76,11 @@ def _pin_checks():
         ("finite differences, repeats", lambda: pins.test_backward_finite_differences(False)),
         ("E=1 K=1 torch autograd", pins.test_backward_E1_K1_torch_autograd),
         ("d_topk_weights linear response", pins.test_backward_dw_is_exact_linear_response),
+        ("shared expert: torch forward", pins.test_shared_forward_is_a_dense_swiglu_ffn_torch),
+        ("shared expert: torch autograd", pins.test_shared_backward_matches_torch_autograd),
+        ("shared expert: finite differences", pins.test_shared_backward_finite_differences),
+        ("shared expert = unit-weight routed expert",
+         pins.test_shared_expert_equals_a_routed_expert_with_unit_weight),
     ]
 
 
