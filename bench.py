@@ -51,8 +51,10 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-sample", type=int, default=1024,
                     help="tokens of the oracle's CPU-baseline sample")
-    ap.add_argument("--ref-sample", type=int, default=48,
-                    help="tokens per step of the reference (oracle) arm")
+    ap.add_argument("--ref-sample", type=int, default=0,
+                    help="tokens per step of the reference arm (0: sized from the first warm-up "
+                         "step so that the whole run takes about --ref-seconds)")
+    ap.add_argument("--ref-seconds", type=float, default=150.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--workload", choices=["prefill_fwd_bwd", "skewed_fwd", "decode_fwd"],
@@ -236,7 +238,20 @@ def run_reference(args, dist: Dist):
     W1, W2 = prob.W1, prob.W2
     rng = np.random.default_rng(1)
     n = args.ref_sample
-    for _ in range(args.warmup):
+    warm = args.warmup
+    if n <= 0:
+        # one warm-up step on 16 tokens sets the sample so that the remaining
+        # warm-up and the timed steps take about --ref-seconds, between 16 and
+        # 48 tokens a step (a step's cost per token falls as the sample grows:
+        # every expert it touches writes full-size weight gradients)
+        n0 = 16
+        t0 = time.perf_counter()
+        cpu_step(prob, W1, W2, np.sort(rng.choice(prob.shape.T, n0, replace=False)))
+        per_token = (time.perf_counter() - t0) / n0
+        left = max(1, args.steps + args.warmup - 1)
+        n = int(min(48, max(16, args.ref_seconds / (left * per_token))))
+        warm = max(0, args.warmup - 1)
+    for _ in range(warm):
         cpu_step(prob, W1, W2, np.sort(rng.choice(prob.shape.T, n, replace=False)))
     times = []
     for _ in range(args.steps):
