@@ -248,8 +248,13 @@ __device__ void decode_tile(const Params& P, const Prob& pr, int e, int r, TileI
   const int wt = r / nb;  // token blocks innermost: a weight tile is reused from L2
   const int b = r - wt * nb;
   const int rows = (P.counts[e] + TROWS - 1) / TROWS * TROWS;
-  ti.row0 = P.poff[e] + P.nt * b;
-  ti.nrow = min(P.nt, rows - P.nt * b);
+  // the expert's rows in nb blocks of equal size (a multiple of 64, the last
+  // one shorter): 384 rows as 192 + 192, not 256 + 128.  A tile's MMAs take
+  // about as long for any block size, its SwiGLU-grad epilogue in proportion
+  // to the rows, so even blocks keep that epilogue under the MMAs.
+  const int nt = (rows / nb + TROWS - 1) / TROWS * TROWS;
+  ti.row0 = P.poff[e] + nt * b;
+  ti.nrow = min(nt, rows - nt * b);
   ti.w0 = wt * C::WCOLS * (P.pair ? 2 : 1);
   ti.kb = (pr.K + BK - 1) / BK;
 }
