@@ -468,10 +468,14 @@ def run_ours(args, dist: Dist):
             t1 = torch.cuda.Event(enable_timing=True)
 
             def copy_in(i):
+                # inputs of step i into buffer set b, once step i - nb no longer
+                # reads them and its outputs (the set's output buffers) have been
+                # read back: the compute stream then waits on ev_in alone
                 b = i % nb
                 with torch.cuda.stream(s_in):
                     if i >= nb:
                         s_in.wait_event(ev_done[b])
+                        s_in.wait_event(ev_out[b])
                     for d, h in zip(ins[b], (hx, hids, hw, hdy)):
                         d.copy_(h, non_blocking=True)
                     ev_in[b].record(s_in)
@@ -483,8 +487,6 @@ def run_ours(args, dist: Dist):
             for i in range(n):
                 b = i % nb
                 stream.wait_event(ev_in[b])
-                if i >= nb:
-                    stream.wait_event(ev_out[b])
                 step(*ins[b], *outs[b])
                 ev_done[b].record(stream)
                 with torch.cuda.stream(s_out):
