@@ -17,6 +17,14 @@ with host inputs copied in and results copied out inside the timed region
 are new host copies and its weights and activations exceed L2).
 `--impl reference` times the CPU oracle (the baseline arm) on a bounded
 token sample of the same workload.
+
+The default line also carries three sub-results measured in the same run
+(each its own timed loop, L2 flushed before every call, clocks sampled):
+`skewed_fwd` (T=16384 H=7168 I=2048 E=32 K=8, Zipf routing, inference
+forward), `decode_fwd` (T=128 H=7168 I=2048 E=256 K=8, weight streaming) and
+`skewed_bwd` (the prefill shape with Zipf routing, fwd+bwd: the hot-expert
+case of the weight-gradient schedule).  Their weights are drawn on the device
+from a seeded generator (same distributions as the seeded host inputs).
 """
 from __future__ import annotations
 
@@ -41,6 +49,7 @@ WORKLOAD = dict(T=4096, H=2048, I=1408, E=64, K=6)
 WORKLOAD_NAME = "prefill-shaped MoE-FFN fwd+bwd: T=4096 H=2048 I=1408 E=64 K=6"
 METRIC = "MoE-FFN tokens/s (fused fwd+bwd step)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FUSED_COMBINE = None  # --fused-combine
 
 
 def parse():
@@ -57,7 +66,12 @@ def parse():
     ap.add_argument("--ref-seconds", type=float, default=150.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--workload", choices=["prefill_fwd_bwd", "skewed_fwd", "decode_fwd"],
+    ap.add_argument("--fused-combine", type=int, choices=[0, 1], default=None,
+                    help="HMM_OPT_FUSED_COMBINE for every workload (default: the library's)")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="skip the skewed / decode / skewed-backward sub-results")
+    ap.add_argument("--workload", choices=["prefill_fwd_bwd", "skewed_fwd", "decode_fwd",
+                                           "skewed_bwd"],
                     default="prefill_fwd_bwd",
                     help="prefill_fwd_bwd is the benchmark line; the forward-only modes "
                          "measure the skewed and decode workloads")
@@ -68,6 +82,8 @@ def parse():
         WORKLOAD.update(T=16384, H=7168, I=2048, E=32, K=8)
     elif a.workload == "decode_fwd":
         WORKLOAD.update(T=128, H=7168, I=2048, E=256, K=8)
+    if a.workload != "prefill_fwd_bwd":
+        a.no_sub = True
     if a.shape:
         T, H, I, E, K = (int(v) for v in a.shape.split(","))
         WORKLOAD.update(T=T, H=H, I=I, E=E, K=K)
@@ -274,119 +290,11 @@ def run_reference(args, dist: Dist):
 
 
 # -------------------------------------------------------------------- GPU arm
-def run_ours(args, dist: Dist):
-    import torch
-
-    import dispatch_grouped_gemm_gb300 as hmm
-    import moe_inputs as mi
-
-    dev = torch.device("cuda", dist.local_rank)
-    torch.cuda.set_device(dev)
-    T, H, I, E, K = (WORKLOAD[k] for k in ("T", "H", "I", "E", "K"))
-    fwd_only = args.workload != "prefill_fwd_bwd"
-    if args.shape:
-        prob = mi.make_shape(T, H, I, E, K, seed=1004)
-    elif args.workload == "skewed_fwd":
-        prob = mi.make("skewed")
-    elif args.workload == "decode_fwd":
-        prob = mi.make("decode")
-    else:
-        prob = mi.make("backward")
-
-    def bf16(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
-
-    x = bf16(prob.x).to(dev)
-    ids = torch.from_numpy(prob.topk_ids).to(dev)
-    w = bf16(prob.topk_weights).to(dev)
-    dy = bf16(prob.dy).to(dev)
-    W1 = torch.empty((E, H, 2 * I), dtype=torch.bfloat16, device=dev)
-    W2 = torch.empty((E, I, H), dtype=torch.bfloat16, device=dev)
-    from concurrent.futures import ThreadPoolExecutor
-    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
-        for e, w1, w2 in ex.map(lambda e: (e, prob.expert_W1(e), prob.expert_W2(e)), range(E)):
-            W1[e].copy_(bf16(w1))
-            W2[e].copy_(bf16(w2))
-
-    ctx = hmm.Context.for_device(dev)
-    shape = hmm.Context.shape_of(x, ids, w, W1, W2)
-    fws, svb, bws = hmm.hmm_workspace_size(shape, not fwd_only)
-    y = torch.empty_like(x)
-    saved = torch.empty(svb, dtype=torch.uint8, device=dev) if not fwd_only else None
-    fwork = torch.empty(fws, dtype=torch.uint8, device=dev)
-    bwork = torch.empty(bws, dtype=torch.uint8, device=dev) if not fwd_only else None
-    dx = torch.empty_like(x)
-    dW1 = torch.empty_like(W1) if not fwd_only else None
-    dW2 = torch.empty_like(W2) if not fwd_only else None
-    dw = torch.empty_like(w)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def step(xx=x, ii=ids, ww=w, dd=dy, yy=y, dxx=dx, dww=dw):
-        hmm.hmm_forward(ctx.handle, shape, xx, ii, ww, W1, W2, yy, saved, fwork, stream)
-        if not fwd_only:
-            hmm.hmm_backward(ctx.handle, shape, dd, ww, W1, W2, saved, dxx, dW1, dW2, dww, bwork,
-                             stream)
-
-    # first call (module load, tensor maps, attribute setup) vs steady state
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_host = time.perf_counter()
-    e0.record(stream)
-    step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    first_call_ms = e0.elapsed_time(e1)
-    first_call_host_ms = 1e3 * (time.perf_counter() - t_host)
-    for _ in range(max(args.warmup, 3)):
-        step()
-    rc, bits = hmm.hmm_status(ctx.handle)
-    if rc != 0:
-        raise RuntimeError(f"device status after warm-up: {rc} bits={bits}")
-
-    # ---------------------------------------------------------- timed region
-    # Only the per-step events: the per-phase events of HMM_OPT_PROFILE sit
-    # between the kernels of a step and cost about 3 % of it, so the phases
-    # are timed in a second pass of the same steps (below).
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    sampler = ClockSampler(dev.index)
-    sampler.start()
-    time.sleep(0.3)
-    dist.barrier()
-    torch.cuda.synchronize()
-    for s, e in ev:
-        flush.zero_()
-        s.record(stream)
-        step()
-        e.record(stream)
-    torch.cuda.synchronize()
-    dist.barrier()
-    clocks = sampler.stop()
-    step_ms = sum(s.elapsed_time(e) for s, e in ev) / args.steps
-    step_ms_max = dist.max(step_ms)
-
-    # ------------------------------------------- instrumented pass (phases)
-    # The same steps again with CUDA events around every launch phase, on the
-    # stream each phase runs on: per-kernel durations for the roofline.
-    n_prof = min(args.steps, 100)
-    ctx.set_option(hmm.HMM_OPT_PROFILE, 1)
-    hmm.hmm_profile_read(ctx.handle)  # reset
-    torch.cuda.synchronize()
-    for _ in range(n_prof):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    prof = hmm.hmm_profile_read(ctx.handle)
-    ctx.set_option(hmm.HMM_OPT_PROFILE, 0)
-    value = dist.world * T / (step_ms_max / 1e3)
-    rc, bits = hmm.hmm_status(ctx.handle)
-    if rc != 0:
-        raise RuntimeError(f"device status after timed region: {rc} bits={bits}")
-
-    # per-phase algorithmic work and roofline of the dominant kernel
+def algo_work(T, H, I, E, K, fwd_only, touched=None):
+    """Algorithmic work of every launch phase: ("tensor", flops) or ("hbm",
+    bytes).  One unit F = 2*T*K*H*I flops; each GEMM launch does 3F."""
     TK = T * K
-    F = 2.0 * TK * H * I  # one "unit": 2*TK*H*I flops
+    F = 2.0 * TK * H * I
     # dispatch: x (dy) read once, K bf16 rows written, and in training an fp8
     # copy of each row (the weight-gradient GEMMs' operand for the low parts)
     fp8_rows = 0.0 if fwd_only else TK * H * 1.0
@@ -400,37 +308,294 @@ def run_ours(args, dist: Dist):
         "gemm_bwd_weight": ("tensor", 3 * F),  # W1Grad 2F + W2Grad F
         "combine_dx": ("hbm", (TK * H + T * H) * 2.0),
     }
-    if args.workload == "decode_fwd":
-        touched = int(np.unique(prob.topk_ids).size)
-        algo["gemm_fwd"] = ("hbm", touched * (H * 2 * I + I * H) * 2.0 + (T * K) * (H + I) * 4.0)
-    peaks, peak_src = load_peaks()
+    if touched is not None:
+        # weight streaming: the bytes of every routed expert's weights plus
+        # the token rows in and out (fp32-equivalent bound)
+        algo["gemm_fwd"] = ("hbm", touched * (H * 2 * I + I * H) * 2.0 + TK * (H + I) * 4.0)
+    return algo
+
+
+def peak_for(bound, region_ms, peaks):
+    """Denominator of a roofline fraction: the measured HBM copy rate for
+    bandwidth-bound launches; for tensor launches the burst bf16 figure when
+    the timed region is short (under 2 s, as the default driver run is), the
+    sustained one (a seconds-long loop under the power cap) otherwise."""
+    if bound != "tensor":
+        return peaks["hbm_gbs"], "hbm_gbs"
+    if region_ms < 2000.0:
+        return peaks["bf16_tflops"], "bf16_tflops"
+    return peaks["bf16_tflops_sustained"], "bf16_tflops_sustained"
+
+
+def phase_table(prof, n_prof, step_ms, algo, peaks, region_ms):
     phases = {}
     for name, (ms, launches) in prof.items():
         if launches == 0:
             continue
         per_ms = ms / n_prof
         bound, work = algo[name]
+        peak, _ = peak_for(bound, region_ms, peaks)
         if bound == "tensor":
             ach = work / (per_ms / 1e3) / 1e12
-            peak = peaks["bf16_tflops_sustained"]
             unit = "TFLOP/s"
         else:
             ach = work / (per_ms / 1e3) / 1e9
-            peak = peaks["hbm_gbs"]
             unit = "GB/s"
         # share of the step time (combine_dx overlaps gemm_bwd_weight)
-        phases[name] = {"ms": per_ms, "share": per_ms / step_ms,
-                        "bound": bound, "achieved": ach, "unit": unit, "frac": ach / peak,
-                        "launches": launches}
+        ph = {"ms": per_ms, "share": per_ms / step_ms, "bound": bound, "achieved": ach,
+              "unit": unit, "frac": ach / peak, "launches": launches}
+        if bound == "tensor":
+            ph["frac_burst"] = ach / peaks["bf16_tflops"]
+            ph["frac_sustained"] = ach / peaks["bf16_tflops_sustained"]
+        phases[name] = ph
+    return phases
+
+
+def bf16_dev(bits, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def device_weights(E, H, I, seed, dev):
+    """Expert weights drawn on the device from a seeded generator:
+    up_proj ~ N(0, 1/H), down_proj ~ N(0, 1/I), drawn in fp32 and rounded to
+    bf16 once (the distributions of the seeded host inputs, without drawing
+    tens of GB on the host)."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    W1 = torch.empty((E, H, 2 * I), dtype=torch.bfloat16, device=dev)
+    W2 = torch.empty((E, I, H), dtype=torch.bfloat16, device=dev)
+    for e in range(E):
+        W1[e].copy_(torch.randn((H, 2 * I), generator=g, device=dev).mul_(1.0 / np.sqrt(H)))
+        W2[e].copy_(torch.randn((I, H), generator=g, device=dev).mul_(1.0 / np.sqrt(I)))
+    return W1, W2
+
+
+class Workload:
+    """Device buffers of one workload and its step (forward, or forward +
+    backward) through the library's C ABI."""
+
+    def __init__(self, hmm, prob, W1, W2, fwd_only, dev, stream):
+        import torch
+        s = prob.shape
+        self.hmm, self.prob, self.fwd_only, self.stream = hmm, prob, fwd_only, stream
+        self.T, self.H, self.I, self.E, self.K = s.T, s.H, s.I, s.E, s.K
+        self.x = bf16_dev(prob.x, dev)
+        self.ids = torch.from_numpy(prob.topk_ids).to(dev)
+        self.w = bf16_dev(prob.topk_weights, dev)
+        self.dy = None if fwd_only else bf16_dev(prob.dy, dev)
+        self.W1, self.W2 = W1, W2
+        self.ctx = hmm.Context.for_device(dev)
+        if FUSED_COMBINE is not None:
+            self.ctx.set_option(hmm.HMM_OPT_FUSED_COMBINE, FUSED_COMBINE)
+        self.shape = hmm.Context.shape_of(self.x, self.ids, self.w, W1, W2)
+        fws, svb, bws = hmm.hmm_workspace_size(self.shape, not fwd_only)
+        self.y = torch.empty_like(self.x)
+        self.saved = None if fwd_only else torch.empty(svb, dtype=torch.uint8, device=dev)
+        self.fwork = torch.empty(fws, dtype=torch.uint8, device=dev)
+        self.bwork = None if fwd_only else torch.empty(bws, dtype=torch.uint8, device=dev)
+        self.dx = torch.empty_like(self.x)
+        self.dW1 = None if fwd_only else torch.empty_like(W1)
+        self.dW2 = None if fwd_only else torch.empty_like(W2)
+        self.dw = torch.empty_like(self.w)
+
+    def step(self, xx=None, ii=None, ww=None, dd=None, yy=None, dxx=None, dww=None):
+        hmm = self.hmm
+        xx = self.x if xx is None else xx
+        ii = self.ids if ii is None else ii
+        ww = self.w if ww is None else ww
+        hmm.hmm_forward(self.ctx.handle, self.shape, xx, ii, ww, self.W1, self.W2,
+                        self.y if yy is None else yy, self.saved, self.fwork, self.stream)
+        if not self.fwd_only:
+            hmm.hmm_backward(self.ctx.handle, self.shape, self.dy if dd is None else dd, ww,
+                             self.W1, self.W2, self.saved, self.dx if dxx is None else dxx,
+                             self.dW1, self.dW2, self.dw if dww is None else dww, self.bwork,
+                             self.stream)
+
+    def check_status(self, when):
+        rc, bits = self.hmm.hmm_status(self.ctx.handle)
+        if rc != 0:
+            raise RuntimeError(f"device status {when}: {rc} bits={bits}")
+
+    def timed(self, n, flush, dist):
+        """n steps, each bracketed by CUDA events on the launching stream,
+        the L2 flushed (256 MiB written) before each; clocks sampled."""
+        import torch
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        sampler = ClockSampler(self.x.device.index)
+        sampler.start()
+        time.sleep(0.3)
+        dist.barrier()
+        torch.cuda.synchronize()
+        for s0, e0 in ev:
+            flush.zero_()
+            s0.record(self.stream)
+            self.step()
+            e0.record(self.stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+        clocks = sampler.stop()
+        return sum(s0.elapsed_time(e0) for s0, e0 in ev) / n, clocks
+
+    def phases(self, n, flush):
+        """The same steps again with CUDA events around every launch phase,
+        on the stream each phase runs on (HMM_OPT_PROFILE): per-kernel
+        durations for the roofline.  Those events sit between the kernels of
+        a step and cost about 3 % of it, hence a pass of its own."""
+        import torch
+        hmm = self.hmm
+        self.ctx.set_option(hmm.HMM_OPT_PROFILE, 1)
+        hmm.hmm_profile_read(self.ctx.handle)  # reset
+        torch.cuda.synchronize()
+        for _ in range(n):
+            flush.zero_()
+            self.step()
+        torch.cuda.synchronize()
+        prof = hmm.hmm_profile_read(self.ctx.handle)
+        self.ctx.set_option(hmm.HMM_OPT_PROFILE, 0)
+        return prof
+
+
+# Sub-results of the default line: workload, moe_inputs config, forward only,
+# timed steps (a timed region of at least about half a second for the clock
+# samples).
+SUB = {
+    "skewed_fwd": ("skewed", True, 64),
+    "decode_fwd": ("decode", True, 150),
+    "skewed_bwd": ("skewed_bwd", False, 400),
+}
+
+
+def run_sub(name, hmm, mi, dev, stream, flush, dist, peaks, uniform_phases=None):
+    import torch
+    cfg, fwd_only, n = SUB[name]
+    prob = mi.make(cfg)
+    s = prob.shape
+    W1, W2 = device_weights(s.E, s.H, s.I, mi.CONFIGS[cfg]["seed"], dev)
+    wl = Workload(hmm, prob, W1, W2, fwd_only, dev, stream)
+    for _ in range(3):
+        wl.step()
+    wl.check_status(f"after the {name} warm-up")
+    ms, clocks = wl.timed(n, flush, dist)
+    ms = dist.max(ms)
+    prof = wl.phases(min(n, 100), flush)
+    wl.check_status(f"after the {name} timed region")
+    counts = np.bincount(prob.topk_ids.reshape(-1), minlength=s.E)
+    touched = int((counts > 0).sum())
+    algo = algo_work(s.T, s.H, s.I, s.E, s.K, fwd_only,
+                     touched if name == "decode_fwd" else None)
+    phases = phase_table(prof, min(n, 100), ms, algo, peaks, n * ms)
+    F = 2.0 * s.T * s.K * s.H * s.I
+    flops = (3 if fwd_only else 9) * F
+    gemm_ms = sum(phases[k]["ms"] for k in ("gemm_fwd", "gemm_bwd_data", "gemm_bwd_weight")
+                  if k in phases)
+    out = {"workload": f"{cfg}: T={s.T} H={s.H} I={s.I} E={s.E} K={s.K}, {prob.routing} routing"
+                       + (", inference forward" if fwd_only else ", fwd+bwd"),
+           "steps": n, "warmup": 3, "ms_per_step": ms,
+           "tokens_per_s": dist.world * s.T / (ms / 1e3),
+           "expert_rows": {"max": int(counts.max()), "empty": int((counts == 0).sum()),
+                           "touched": touched},
+           "l2": "256 MiB flush before each step", "clocks": clocks, "phases": phases}
+    if name == "decode_fwd":
+        g = phases["gemm_fwd"]
+        out["weight_stream"] = {"GB/s": g["achieved"], "frac_hbm": g["frac"],
+                                "bytes": algo["gemm_fwd"][1]}
+    else:
+        out["grouped_gemm_tflops"] = flops / (gemm_ms / 1e3) / 1e12 if gemm_ms else None
+        out["grouped_gemm_frac_burst"] = out["grouped_gemm_tflops"] / peaks["bf16_tflops"]
+    if name == "skewed_bwd" and uniform_phases and "gemm_bwd_weight" in uniform_phases:
+        # the same algorithmic weight-gradient work as the uniform step (every
+        # slot contributes to one expert's dW): the time ratio measures the
+        # schedule's balance under a hot expert
+        out["wgrad_ms_vs_uniform"] = (phases["gemm_bwd_weight"]["ms"]
+                                      / uniform_phases["gemm_bwd_weight"]["ms"])
+    del wl, W1, W2
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, dist: Dist):
+    import torch
+
+    import dispatch_grouped_gemm_gb300 as hmm
+    import moe_inputs as mi
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    T, H, I, E, K = (WORKLOAD[k] for k in ("T", "H", "I", "E", "K"))
+    fwd_only = args.workload in ("skewed_fwd", "decode_fwd")
+    if args.shape:
+        prob = mi.make_shape(T, H, I, E, K, seed=1004)
+    elif args.workload == "skewed_fwd":
+        prob = mi.make("skewed")
+    elif args.workload == "decode_fwd":
+        prob = mi.make("decode")
+    elif args.workload == "skewed_bwd":
+        prob = mi.make("skewed_bwd")
+    else:
+        prob = mi.make("backward")
+
+    if args.workload in ("skewed_fwd", "decode_fwd"):
+        W1, W2 = device_weights(E, H, I, prob.seed, dev)
+    else:
+        W1 = torch.empty((E, H, 2 * I), dtype=torch.bfloat16, device=dev)
+        W2 = torch.empty((E, I, H), dtype=torch.bfloat16, device=dev)
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+            for e, w1, w2 in ex.map(lambda e: (e, prob.expert_W1(e), prob.expert_W2(e)),
+                                    range(E)):
+                W1[e].copy_(bf16_dev(w1, dev))
+                W2[e].copy_(bf16_dev(w2, dev))
+
+    stream = torch.cuda.current_stream()
+    wl = Workload(hmm, prob, W1, W2, fwd_only, dev, stream)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    # first call (module load, tensor maps, attribute setup) vs steady state
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host = time.perf_counter()
+    e0.record(stream)
+    wl.step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    first_call_ms = e0.elapsed_time(e1)
+    first_call_host_ms = 1e3 * (time.perf_counter() - t_host)
+    for _ in range(max(args.warmup, 3)):
+        wl.step()
+    wl.check_status("after warm-up")
+
+    # ---------------------------------------------------------- timed region
+    # only the per-step events (the per-phase ones come in a second pass)
+    step_ms, clocks = wl.timed(args.steps, flush, dist)
+    step_ms_max = dist.max(step_ms)
+    region_ms = args.steps * step_ms_max
+
+    # ------------------------------------------- instrumented pass (phases)
+    n_prof = min(args.steps, 100)
+    prof = wl.phases(n_prof, flush)
+    value = dist.world * T / (step_ms_max / 1e3)
+    wl.check_status("after the timed region")
+
+    # per-phase algorithmic work and roofline of the dominant kernel
+    F = 2.0 * T * K * H * I  # one "unit": 2*TK*H*I flops
+    touched = int(np.unique(prob.topk_ids).size) if args.workload == "decode_fwd" else None
+    algo = algo_work(T, H, I, E, K, fwd_only, touched)
+    peaks, peak_src = load_peaks()
+    phases = phase_table(prof, n_prof, step_ms, algo, peaks, region_ms)
     dom = max(phases, key=lambda k: phases[k]["ms"])
     dp = phases[dom]
-    roofline = {"kernel": dom, "bound": dp["bound"], "achieved": dp["achieved"],
-                "peak": peaks["bf16_tflops_sustained"] if dp["bound"] == "tensor"
-                else peaks["hbm_gbs"],
-                "unit": dp["unit"], "frac": dp["frac"], "traffic": None if args.shape else load_traffic(dom, args.workload),
-                "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if dp['bound'] == 'tensor' else 'hbm_gbs'})"}
+    peak, peak_key = peak_for(dp["bound"], region_ms, peaks)
+    roofline = {"kernel": dom, "bound": dp["bound"], "achieved": dp["achieved"], "peak": peak,
+                "unit": dp["unit"], "frac": dp["frac"],
+                "traffic": None if args.shape else load_traffic(dom, args.workload),
+                "peak_source": f"{peak_src} ({peak_key}: timed region {region_ms:.0f} ms)"}
 
-    fwd_ms = sum(phases[k]["ms"] for k in ("route", "dispatch_x", "gemm_fwd", "combine_y"))
+    # (no combine_y phase when the combine runs in the GMM2 epilogue)
+    fwd_ms = sum(phases[k]["ms"] for k in ("route", "dispatch_x", "gemm_fwd", "combine_y")
+                 if k in phases)
     # combine_dx runs beside gemm_bwd_weight on a second stream
     bwd_ms = sum(phases[k]["ms"] for k in ("dispatch_dy", "gemm_bwd_data", "gemm_bwd_weight")
                  if k in phases)
@@ -441,10 +606,11 @@ def run_ours(args, dist: Dist):
     # ------------------------------------------------------------------ e2e
     e2e = None
     if not args.no_e2e and not fwd_only:
-        hx = bf16(prob.x).pin_memory()
-        hids = torch.from_numpy(prob.topk_ids).pin_memory()
-        hw = bf16(prob.topk_weights).pin_memory()
-        hdy = bf16(prob.dy).pin_memory()
+        x, ids, w, dy, y, dx, dw = wl.x, wl.ids, wl.w, wl.dy, wl.y, wl.dx, wl.dw
+        hx = x.cpu().pin_memory()
+        hids = ids.cpu().pin_memory()
+        hw = w.cpu().pin_memory()
+        hdy = dy.cpu().pin_memory()
         oy = torch.empty_like(hx).pin_memory()
         odx = torch.empty_like(hx).pin_memory()
         odw = torch.empty_like(hw).pin_memory()
@@ -487,7 +653,7 @@ def run_ours(args, dist: Dist):
             for i in range(n):
                 b = i % nb
                 stream.wait_event(ev_in[b])
-                step(*ins[b], *outs[b])
+                wl.step(*ins[b], *outs[b])
                 ev_done[b].record(stream)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(ev_done[b])
@@ -533,8 +699,17 @@ def run_ours(args, dist: Dist):
     if fwd_only:
         out["metric"] = "MoE-FFN tokens/s (fused forward, inference)"
         out["config"]["workload"] = f"{args.workload}: T={T} H={H} I={I} E={E} K={K}"
+    elif args.workload == "skewed_bwd":
+        out["config"]["workload"] = f"skewed_bwd: T={T} H={H} I={I} E={E} K={K}, Zipf routing"
     if args.shape:
         out["config"]["workload"] = f"profiling case T={T} H={H} I={I} E={E} K={K}"
+    if not args.no_sub:
+        # the other workloads of the acceptance list, each in its own timed loop
+        del wl
+        torch.cuda.empty_cache()
+        for name in SUB:
+            out[name] = run_sub(name, hmm, mi, dev, stream, flush, dist, peaks,
+                                uniform_phases=phases)
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and not fwd_only:
         out["cpu_baseline"] = cpu_baseline(prob, args.cpu_sample)
     if dist.rank == 0:
@@ -542,7 +717,9 @@ def run_ours(args, dist: Dist):
 
 
 def main():
+    global FUSED_COMBINE
     args = parse()
+    FUSED_COMBINE = args.fused_combine
     dist = Dist(args.gpus)
     try:
         if args.impl == "reference":

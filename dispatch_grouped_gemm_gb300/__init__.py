@@ -28,7 +28,7 @@ __all__ = [
     "hmm_error_string", "Context", "moe_ffn", "library_path", "load_library",
     "hmm_profile_read", "hmm_phase_name", "hmm_set_trace",
     "HMM_OPT_VALIDATE", "HMM_OPT_WAIT_BUDGET_NS", "HMM_OPT_INJECT_SKIP_READY", "HMM_OPT_PROFILE",
-    "HMM_OPT_PAIR_ROWS", "HMM_OPT_OVERLAP_LAUNCHES",
+    "HMM_OPT_PAIR_ROWS", "HMM_OPT_OVERLAP_LAUNCHES", "HMM_OPT_FUSED_COMBINE",
     "HMM_DTYPE_BF16", "HMM_DTYPE_F32", "HMM_STATUS_EXPERT_ID", "HMM_STATUS_TIMEOUT",
 ]
 
@@ -59,6 +59,7 @@ HMM_OPT_INJECT_SKIP_READY = _C["HMM_OPT_INJECT_SKIP_READY"]
 HMM_OPT_PROFILE = _C["HMM_OPT_PROFILE"]
 HMM_OPT_PAIR_ROWS = _C["HMM_OPT_PAIR_ROWS"]
 HMM_OPT_OVERLAP_LAUNCHES = _C["HMM_OPT_OVERLAP_LAUNCHES"]
+HMM_OPT_FUSED_COMBINE = _C["HMM_OPT_FUSED_COMBINE"]
 HMM_DTYPE_BF16 = _C["HMM_DTYPE_BF16"]
 HMM_DTYPE_F32 = _C["HMM_DTYPE_F32"]
 HMM_STATUS_EXPERT_ID = _C["HMM_STATUS_EXPERT_ID"]

@@ -18,7 +18,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 SOURCES = ["hmm_api.cu", "route.cu", "move.cu", "gmm.cu", "gmm_pair.cu", "route_static.cu"]
-HEADERS = ["hmm_internal.h", "ptx.cuh"]
+HEADERS = ["hmm_internal.h", "ptx.cuh", "epilogue.cuh"]
 LIB = os.path.join(HERE, "libhmm.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

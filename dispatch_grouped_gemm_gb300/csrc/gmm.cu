@@ -138,6 +138,14 @@ struct Prob {
   int* signal_m;        // per-token-block counters (index row0 / 64) released after a tile
   const int* wait_m;    // per-token-block counter acquired before a tile's loads
   int wait_unit;        // per-token-block target
+  // the combine folded into this (GMM2) epilogue; cmb == null: a separate kernel
+  int* cmb;                   // [T][cmb_nseg] rows counted per (token, 32-column segment)
+  const int32_t* slot2prow;   // [T * K]
+  const int32_t* prow2slot;   // [R]
+  const int32_t* cmb_poff;    // padded offsets (the shared expert's rows start at [cmb_E])
+  const void* cmb_w;          // topk_weights [T, K], bf16 or fp32 (cmb_w_f32)
+  void* cmb_y;                // y [T, N] bf16
+  int cmb_w_f32, cmb_K, cmb_KS, cmb_T, cmb_nseg, cmb_E;
 };
 
 struct Params {
@@ -595,19 +603,92 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
   }
 }
 
-// Bounded wait that ignores the abort flag (used only to drain in-flight
-// copies / MMAs before the CTA exits).
-__device__ __noinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0; it < (1u << 28); ++it) {
-    if (mbar_try_wait(bar, parity)) return;
-    if ((it & 31u) == 31u && globaltimer_ns() - t0 > budget_ns) return;
+// ------------------------------------------------------------ fused combine
+// The combine folded into the GMM2 epilogue [HyperMegaMoE §6.2: unpermute and
+// top-k weighted merge inside the fused operator; MoE overlap explainer §6:
+// a token is published once all of its branches have arrived].  After a warp
+// has stored its 32 columns (segment c0 / 32) of o for the token block of a
+// tile, it counts each routed row on its token's counter of that segment;
+// the lane whose count completes the token's KS rows (K, plus the shared
+// expert's row) owns the token's segment, and the warp then sums those rows
+// and writes y.  The sum is the separate combine's, operation for operation:
+// fp32 fmaf over k = 0 .. K-1 in order with the routing weight (slots with an
+// invalid id skipped), then the shared row with weight 1, one bf16 rounding.
+template <bool F32>
+__device__ __forceinline__ void cmb_acc(float (&acc)[8], const void* o, int64_t row, int64_t ld,
+                                        int col, float s) {
+  if constexpr (F32) {
+    const float4* r = reinterpret_cast<const float4*>(static_cast<const float*>(o) + row * ld + col);
+    const float4 a = __ldcg(r), b = __ldcg(r + 1);
+    acc[0] = fmaf(s, a.x, acc[0]); acc[1] = fmaf(s, a.y, acc[1]);
+    acc[2] = fmaf(s, a.z, acc[2]); acc[3] = fmaf(s, a.w, acc[3]);
+    acc[4] = fmaf(s, b.x, acc[4]); acc[5] = fmaf(s, b.y, acc[5]);
+    acc[6] = fmaf(s, b.z, acc[6]); acc[7] = fmaf(s, b.w, acc[7]);
+  } else {
+    const uint4 v = __ldcg(reinterpret_cast<const uint4*>(
+        static_cast<const __nv_bfloat16*>(o) + row * ld + col));
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc[2 * j] = fmaf(s, bf16_lo(u[j]), acc[2 * j]);
+      acc[2 * j + 1] = fmaf(s, bf16_hi(u[j]), acc[2 * j + 1]);
+    }
   }
 }
 
-__device__ __noinline__ void pause_ns(uint64_t ns) {
-  const uint64_t t0 = globaltimer_ns();
-  while (globaltimer_ns() - t0 < ns) __nanosleep(1000);
+template <bool F32>
+__device__ __noinline__ void combine_tile(const Prob& pr, const TileInfo& ti, int c0, int lane) {
+  if (c0 >= pr.N) return;
+  const int seg = c0 >> 5;
+  const bool shared = ti.e == pr.cmb_E;
+  const int64_t srow0 = shared ? pr.cmb_poff[pr.cmb_E] : 0;
+  // this warp's stores of o are visible at gpu scope before its counts
+  __threadfence();
+  __syncwarp();
+#pragma unroll 1
+  for (int j = 0; j < ti.nrow; j += 32) {
+    const int64_t prow = ti.row0 + j + lane;
+    int t = -1;
+    if (shared) {
+      if (prow - srow0 < pr.cmb_T) t = static_cast<int>(prow - srow0);
+    } else {
+      const int32_t sl = pr.prow2slot[prow];
+      if (sl >= 0) t = sl / pr.cmb_K;
+    }
+    bool fin = false;
+    if (t >= 0)
+      fin = atomicAdd(&pr.cmb[static_cast<int64_t>(t) * pr.cmb_nseg + seg], 1) == pr.cmb_KS - 1;
+    const unsigned fmask = __ballot_sync(0xffffffffu, fin);
+    if (fmask == 0) continue;
+    __threadfence();  // the other rows of the completed segments, written by other warps
+    const int nfin = __popc(fmask);
+    const int g = lane >> 2;                // eight tokens per pass,
+    const int col = c0 + 8 * (lane & 3);    // four lanes of eight columns each
+#pragma unroll 1
+    for (int base = 0; base < nfin; base += 8) {
+      const int idx = base + g;
+      const int src = idx < nfin ? static_cast<int>(__fns(fmask, 0, idx + 1)) : 0;
+      const int tt = __shfl_sync(0xffffffffu, t, src);
+      if (idx < nfin && col < pr.N) {
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int k = 0; k < pr.cmb_K; ++k) {
+          const int64_t sk = static_cast<int64_t>(tt) * pr.cmb_K + k;
+          const int32_t pk = pr.slot2prow[sk];
+          const float w = pr.cmb_w_f32
+                              ? static_cast<const float*>(pr.cmb_w)[sk]
+                              : bf16_lo(static_cast<const uint16_t*>(pr.cmb_w)[sk]);
+          if (pk < 0) continue;
+          cmb_acc<F32>(acc, pr.out, pk, pr.ld_out, col, w);
+        }
+        if (pr.cmb_KS > pr.cmb_K)
+          cmb_acc<F32>(acc, pr.out, pr.cmb_poff[pr.cmb_E] + tt, pr.ld_out, col, 1.0f);
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(pr.cmb_y) +
+                                  static_cast<int64_t>(tt) * pr.N + col) = pack_bf16x8(acc);
+      }
+    }
+  }
 }
 
 // ------------------------------------------------------------------- kernel
@@ -658,7 +739,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   TileInfo* s_ti = reinterpret_cast<TileInfo*>(xfree + 2);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_ti + TI_DEPTH);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
-  int* s_pref = reinterpret_cast<int*>(s_tmem + 2);  // [steps + 1]
+  uint32_t* s_issued = s_tmem + 2;  // K blocks this CTA's producer issued
+  uint32_t* s_peer = s_tmem + 3;    // [2] even CTA of a pair: the odd CTA's count, abort flag
+  int* s_pref = reinterpret_cast<int*>(s_tmem + 6);  // [steps + 1]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -686,6 +769,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&xfree[i], 2);
     }
     *s_abort = 0;
+    *s_issued = 0;
+    s_peer[0] = s_peer[1] = 0;
     fence_mbar_init();
   }
   if constexpr (PAIR) cluster_sync_all();  // barriers initialised before any remote arrive
@@ -833,15 +918,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (rec && ok) rec[3] = globaltimer_ns();
         if (!ok) break;
       }
-      if (!ok) {
-        // wait (bounded) for the copies still in flight before leaving
-        if (!PAIR || leader) {
-          for (uint32_t s = 0; s < NST; ++s)
-            if (issued > s) drain_wait(&full[s], ((issued - 1 - s) / NST) & 1u, P.budget_ns);
-        } else {
-          pause_ns(200000);  // the even CTA counts our bytes; give the copies time to land
-        }
-      }
+      // wait (bounded) for the copies still in flight before leaving (CTA
+      // pairs: both CTAs' copies, at teardown, see pair_teardown)
+      if (!PAIR && !ok)
+        for (uint32_t s = 0; s < NST; ++s)
+          if (issued > s) drain_wait(&full[s], ((issued - 1 - s) / NST) & 1u, P.budget_ns);
+      *s_issued = issued;
       grid_dep_launch();  // this CTA is in its last tile
     }
   } else if (warp == 1) {
@@ -963,6 +1045,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         if (lane == 0) red_release_add(&pr.signal_m[ti.row0 / TROWS], 1);
       }
+      if (pr.cmb) {
+        // after the accumulator's release: this overlaps the next tile's MMAs
+        const int c0 = ti.w0 + C1::WCOLS * static_cast<int>(rank) + 32 * es.q;
+        if (pr.out_f32)
+          combine_tile<true>(pr, ti, c0, lane);
+        else
+          combine_tile<false>(pr, ti, c0, lane);
+      }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -970,7 +1060,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if constexpr (PAIR) cluster_sync_all();  // no peer access to our smem or TMEM after this
+  // no copy of either CTA in flight, no peer access to our smem or TMEM after this
+  if constexpr (PAIR)
+    pair_teardown<NST>(leader, *s_issued, *s_abort, s_peer, full, W_BYTES + PAIR_T_BYTES,
+                       P.budget_ns);
   if (warp == 1) {
     tc_fence_after();
     if constexpr (PAIR)
@@ -1099,7 +1192,8 @@ void add_shared(Params& P, Maps& maps, int E, const CUtensorMap& B0, const CUten
 
 int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
                          const void* x_perm, const void* W1, const void* W2, const void* Ws1,
-                         const void* Ws2, void* a, float* h32, void* o, bool skip_ready_release) {
+                         const void* Ws2, void* a, float* h32, void* o, bool skip_ready_release,
+                         int* cmb, const void* w, int w_dtype, void* fused_y) {
   const int64_t H = p.H, I = p.I, E = p.E, R = p.R;
   Maps maps;
   int rc = HMM_OK;
@@ -1147,6 +1241,20 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
   g2.lag = static_cast<int>(p.Ex);
   g2.wait_m = c.ready;
   g2.wait_unit = EPI_WARPS * ncta * g1.n_tiles;  // every GMM1 tile of the token block
+  if (fused_y) {
+    g2.cmb = cmb;
+    g2.slot2prow = m.slot2prow;
+    g2.prow2slot = m.prow2slot;
+    g2.cmb_poff = m.poff;
+    g2.cmb_w = w;
+    g2.cmb_y = fused_y;
+    g2.cmb_w_f32 = w_dtype == HMM_DTYPE_F32 ? 1 : 0;
+    g2.cmb_K = static_cast<int>(p.K);
+    g2.cmb_KS = static_cast<int>(p.K + p.shared);
+    g2.cmb_T = static_cast<int>(p.T);
+    g2.cmb_nseg = static_cast<int>(p.cmb_nseg);
+    g2.cmb_E = static_cast<int>(E);
+  }
   if (p.shared) add_shared(P, maps, static_cast<int>(E), s0, s1);
   const int64_t max_tiles = (p.R / TROWS) * (g1.n_tiles + g2.n_tiles);
   if (env.pair_rows) return launch<true, false, CfgGmm1, CfgGmm2>(env, P, maps, max_tiles, 0);
@@ -1158,7 +1266,7 @@ int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPt
                            const void* dy_perm, const float* wperm, const float* h32,
                            const void* W1, const void* W2, const void* Ws1, const void* Ws2,
                            void* dH, void* dH_lo, void* wa, void* wa_lo, float* dwp,
-                           void* dx_perm) {
+                           void* dx_perm, bool skip_ready_release) {
   const int64_t H = p.H, I = p.I, E = p.E, R = p.R;
   Maps maps;
   int rc = HMM_OK;
@@ -1202,7 +1310,7 @@ int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPt
   ag.rowscale = wperm;
   ag.e_lo = 0;
   ag.e_hi = static_cast<int>(E);
-  ag.signal_m = c.ready;
+  ag.signal_m = skip_ready_release ? nullptr : c.ready;
   Prob& ig = P.p[1];
   ig.K = static_cast<int>(2 * I);
   ig.N = static_cast<int>(H);

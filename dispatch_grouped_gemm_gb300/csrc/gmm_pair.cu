@@ -18,12 +18,21 @@
 // add into the same accumulator).
 //
 // Roles per CTA: warp 0 issues TMA (both CTAs, one thread), warp 1 issues the
-// MMAs (even CTA only), warps 2..5 drain TMEM (both CTAs).  The even CTA's
+// MMAs (even CTA only), warps 2..5 drain TMEM (both CTAs), warp 6 schedules
+// (even CTA only).  The even CTA's
 // full barriers count the bytes of both CTAs; the MMA commits arrive on the
 // empty / accumulator-full barriers of both CTAs; both CTAs' epilogues release
-// the even CTA's accumulator-empty barrier.  Tiles are assigned statically
-// (cluster c takes tiles c, c + #clusters, ...): these GEMMs depend on nothing
-// inside the launch.  Every wait is bounded.
+// the even CTA's accumulator-empty barrier.
+//
+// Schedule: a tile's cost is its expert's K blocks (rows / 64), so with a hot
+// expert a few tiles cost ten times the others.  Tiles are therefore handed
+// out longest first: the experts sorted by routed rows (descending, ties by
+// id; empty experts last), all tiles of one expert together, through a global
+// ticket.  The even CTA's scheduler warp takes the tickets (each one a tile
+// ahead of its use, so the atomic's latency stays off every other role) and
+// publishes the tiles in a shared-memory ring of both CTAs, up to
+// P_TI_DEPTH tiles ahead of the slowest reader.  The last cluster to finish
+// resets the ticket for the next launch.  Every wait is bounded.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -45,9 +54,14 @@ constexpr int PB_BYTES = 128 * PK * 2;  // this CTA's 128 columns of B, PK deep 
 constexpr int PL_BYTES = 128 * PK;      // the low part of the split one of them (e5m2)
 constexpr int PO_BYTES = 128 * PK;      // the fp8 copy of the other one
 constexpr int PSTAGE = PA_BYTES + PB_BYTES + PL_BYTES + PO_BYTES;
-constexpr int P_THREADS = 192;
 constexpr int P_EPI_WARPS = 4;
-constexpr int P_SMEM = 1024 + PSTAGES * PSTAGE + P_EPI_WARPS * XBUF_BYTES + 512;
+constexpr int P_SCHED_WARP = 2 + P_EPI_WARPS;
+constexpr int P_THREADS = 32 * (P_SCHED_WARP + 1);  // 7 warps
+constexpr int P_TI_DEPTH = 8;  // tile ring: the producer runs up to a few small tiles ahead
+// the routed rows of every expert, the sorted expert order and the tile
+// prefix over it (experts 0 .. MAX_E, the last one the optional shared expert)
+constexpr int P_ORD_BYTES = 4 * (MAX_E + 1) + 4 * (MAX_E + 1) + 4 * (MAX_E + 2);
+constexpr int P_SMEM = 1024 + PSTAGES * PSTAGE + P_EPI_WARPS * XBUF_BYTES + 1024 + P_ORD_BYTES;
 static_assert(P_SMEM <= 232448, "shared memory per CTA");
 constexpr uint32_t P_TMEM_COLS = 512;
 constexpr uint32_t IDESC_PAIR = idesc_bf16_f32(256, 256, 1, 1);  // both MN-major
@@ -71,7 +85,8 @@ struct PairParams {
   int nprob;
   const int32_t* poff;
   const int32_t* counts;
-  int E;
+  int Ex;           // experts of the padded rows (E, plus the shared expert)
+  int* ticket;      // [2] tile ticket and finished-cluster count, zero at launch
   unsigned* status;
   unsigned long long budget_ns;
   uint64_t* trace;  // per-tile timeline records of the even CTA (null: off)
@@ -83,50 +98,90 @@ struct PairMaps {
   CUtensorMap out[4];   // the output [experts][M][N] (bf16), stored in 32 x 32 boxes
 };
 
+// One tile of the ring (prob < 0: no more tiles).
 struct PairTile {
   int prob, e, m0, n0, kb, krow0;
 };
 
-__device__ __forceinline__ int pair_tiles(const PairParams& P, int q) {
-  return P.p[q].n_e * P.p[q].mpairs * P.p[q].n_tiles;
+// Tiles of expert x over all problems that include it.
+__device__ __forceinline__ int expert_tiles(const PairParams& P, int x) {
+  int n = 0;
+  for (int q = 0; q < P.nprob; ++q)
+    if (x >= P.p[q].e_lo && x < P.p[q].e_lo + P.p[q].n_e) n += P.p[q].mpairs * P.p[q].n_tiles;
+  return n;
 }
 
-__device__ __forceinline__ void pair_decode(const PairParams& P, int u, PairTile& t) {
+// Longest first: ord[i] = the expert of rank i (routed rows descending, ties
+// by id), pre[i] = tiles of the experts of rank < i.  One CTA's threads; cnt
+// is scratch for the routed rows.
+__device__ void build_order(const PairParams& P, int* cnt, int* ord, int* pre) {
+  const int Ex = P.Ex;
+  for (int x = threadIdx.x; x < Ex; x += blockDim.x) cnt[x] = P.counts[x];
+  __syncthreads();
+  for (int x = threadIdx.x; x < Ex; x += blockDim.x) {
+    const int cx = cnt[x];
+    int r = 0;
+    for (int y = 0; y < Ex; ++y) {
+      const int cy = cnt[y];
+      r += (cy > cx || (cy == cx && y < x)) ? 1 : 0;
+    }
+    ord[r] = x;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry = 0;
+    if (lane == 0) pre[0] = 0;
+    for (int base = 0; base < Ex; base += 32) {
+      const int i = base + lane;
+      int v = i < Ex ? expert_tiles(P, ord[i]) : 0;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d) v += n;
+      }
+      if (i < Ex) pre[i + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  __syncthreads();
+}
+
+// Ticket u (< pre[Ex]) -> tile.
+__device__ void pair_decode(const PairParams& P, const int* ord, const int* pre, int u,
+                            PairTile& t) {
+  int lo = 0, hi = P.Ex - 1;  // largest rank i with pre[i] <= u
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= u)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int x = ord[lo];
+  int r = u - pre[lo];
   int q = 0;
-  while (q + 1 < P.nprob && u >= pair_tiles(P, q)) {
-    u -= pair_tiles(P, q);
-    ++q;
+  for (; q < P.nprob; ++q) {
+    const PairProb& pr = P.p[q];
+    if (x < pr.e_lo || x >= pr.e_lo + pr.n_e) continue;
+    const int per = pr.mpairs * pr.n_tiles;
+    if (r < per) break;
+    r -= per;
   }
   const PairProb& pr = P.p[q];
-  const int per = pr.mpairs * pr.n_tiles;
   t.prob = q;
-  const int le = u / per;  // expert index inside the problem
-  t.e = pr.e_lo + le;
-  const int r = u - le * per;
+  t.e = x;
   t.m0 = (r / pr.n_tiles) * 256;
   t.n0 = (r % pr.n_tiles) * 256;
-  t.krow0 = P.poff[t.e];
+  t.krow0 = P.poff[x];
   // rows past counts[e] are zero padding: skip whole zero K blocks
-  t.kb = (P.counts[t.e] + PK - 1) / PK;
+  t.kb = (P.counts[x] + PK - 1) / PK;
 }
 
 // Timeline record of this CTA's lt-th tile (even CTA of the pair only).
 __device__ __forceinline__ uint64_t* pair_rec(const PairParams& P, bool leader, int lt) {
   if (!leader || P.trace == nullptr || lt >= P.trace_cap) return nullptr;
   return P.trace + (static_cast<int64_t>(blockIdx.x) * P.trace_cap + lt) * 8;
-}
-
-__device__ __noinline__ void pair_drain_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0; it < (1u << 28); ++it) {
-    if (mbar_try_wait(bar, parity)) return;
-    if ((it & 31u) == 31u && globaltimer_ns() - t0 > budget_ns) return;
-  }
-}
-
-__device__ __noinline__ void pair_pause_ns(uint64_t ns) {
-  const uint64_t t0 = globaltimer_ns();
-  while (globaltimer_ns() - t0 < ns) __nanosleep(1000);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
@@ -138,13 +193,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   float* xbufs = reinterpret_cast<float*>(smem + PSTAGES * PSTAGE);
   uint64_t* bars =
       reinterpret_cast<uint64_t*>(smem + PSTAGES * PSTAGE + P_EPI_WARPS * XBUF_BYTES);
-  uint64_t* full = bars;               // used in the even CTA
-  uint64_t* empty = bars + PSTAGES;    // both CTAs
-  uint64_t* tfull = empty + PSTAGES;   // both CTAs
-  uint64_t* tempty = tfull + 2;        // even CTA
-  uint64_t* mma_done = tempty + 2;     // even CTA
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* full = bars;                    // used in the even CTA
+  uint64_t* empty = bars + PSTAGES;         // both CTAs
+  uint64_t* tfull = empty + PSTAGES;        // both CTAs
+  uint64_t* tempty = tfull + 2;             // even CTA
+  uint64_t* mma_done = tempty + 2;          // even CTA
+  uint64_t* ti_full = mma_done + 1;         // [P_TI_DEPTH] both CTAs
+  uint64_t* ti_empty = ti_full + P_TI_DEPTH;  // [P_TI_DEPTH] even CTA: every reader arrives
+  PairTile* s_ti = reinterpret_cast<PairTile*>(ti_empty + P_TI_DEPTH);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_ti + P_TI_DEPTH);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  uint32_t* s_issued = s_tmem + 2;  // K blocks this CTA's producer issued
+  uint32_t* s_peer = s_tmem + 3;    // [2] even CTA: the odd CTA's count and abort flag
+  int* s_cnt = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + 1024);
+  int* s_ord = s_cnt + (MAX_E + 1);
+  int* s_pre = s_ord + (MAX_E + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -161,7 +224,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       mbar_init(&tempty[a], 8);  // 4 epilogue warps in each CTA of the pair
     }
     mbar_init(mma_done, 1);
+    for (int i = 0; i < P_TI_DEPTH; ++i) {
+      mbar_init(&ti_full[i], 1);
+      // readers: both CTAs' producers and epilogue warps, the even CTA's MMA
+      // issuer
+      mbar_init(&ti_empty[i], 3 + 2 * P_EPI_WARPS);
+    }
     *s_abort = 0;
+    *s_issued = 0;
+    s_peer[0] = s_peer[1] = 0;
     fence_mbar_init();
   }
   cluster_sync_all();  // the peer's barriers are initialised before any remote arrive
@@ -178,11 +249,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   // producer has issued its last tile.)
   grid_dep_wait();
   const WaitCtl wc{s_abort, P.status, P.budget_ns};
-
-  int total = 0;
-  for (int q = 0; q < P.nprob; ++q) total += pair_tiles(P, q);
-  const int first = static_cast<int>(cluster_id_x());
-  const int stride = static_cast<int>(ncluster_x());
+  if (leader) build_order(P, s_cnt, s_ord, s_pre);  // only the even CTA decodes tickets
+  // readers of the ring: the odd CTA's release the even CTA's slots
+  const auto ti_release = [&](int slot) {
+    if (leader)
+      mbar_arrive(&ti_empty[slot]);
+    else
+      mbar_arrive_peer(mapa_shared(smem_u32(&ti_empty[slot]), 0));
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -192,11 +266,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       for (int q = 0; q < P.nprob; ++q) tma_prefetch_desc(&maps.out[q]);
       uint32_t stage = 0, sphase = 0;
       uint32_t issued = 0;
+      int ti_slot = 0;
+      uint32_t ti_phase = 0;
       bool ok = true;
       int lt = 0;
-      for (int u = first; u < total && ok; u += stride) {
-        PairTile t;
-        pair_decode(P, u, t);
+      for (;;) {
+        const bool got = leader ? mbar_wait(&ti_full[ti_slot], ti_phase, wc)
+                                : mbar_wait<true>(&ti_full[ti_slot], ti_phase, wc);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        const PairTile t = s_ti[ti_slot];
+        ti_release(ti_slot);
+        if (++ti_slot == P_TI_DEPTH) {
+          ti_slot = 0;
+          ti_phase ^= 1u;
+        }
+        if (t.prob < 0) break;
         const PairProb& pr = P.p[t.prob];
         const CUtensorMap* mp = maps.m[t.prob];
         uint64_t* rec = pair_rec(P, leader, lt++);
@@ -239,28 +326,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
           }
         }
         if (rec && ok) rec[3] = globaltimer_ns();
+        if (!ok) break;
       }
-      if (!ok) {
-        if (leader) {
-          for (uint32_t s = 0; s < PSTAGES; ++s)
-            if (issued > s)
-              pair_drain_wait(&full[s], ((issued - 1 - s) / PSTAGES) & 1u, P.budget_ns);
-        } else {
-          pair_pause_ns(200000);  // the even CTA counts our bytes; give copies time to land
-        }
-      }
+      // copies still in flight after an abort are drained at teardown
+      // (pair_teardown: both CTAs' copies are counted on the even CTA)
+      *s_issued = issued;
       grid_dep_launch();  // this CTA is in its last tile
+    }
+  } else if (warp == P_SCHED_WARP) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------------- tile scheduler
+      const int total = s_pre[P.Ex];
+      int ti_slot = 0;
+      uint32_t ti_phase = 0;
+      int u = atomicAdd(P.ticket, 1);
+      for (;;) {
+        PairTile t;
+        t.prob = -1;
+        t.e = t.m0 = t.n0 = t.kb = t.krow0 = 0;
+        if (u < total) {
+          pair_decode(P, s_ord, s_pre, u, t);
+          u = atomicAdd(P.ticket, 1);  // the next ticket, used one tile later
+        }
+        if (!mbar_wait(&ti_empty[ti_slot], ti_phase ^ 1u, wc)) break;
+        s_ti[ti_slot] = t;
+        const uint32_t dst = mapa_shared(smem_u32(&s_ti[ti_slot]), 1);
+        const int* src = reinterpret_cast<const int*>(&t);
+#pragma unroll
+        for (int j = 0; j < static_cast<int>(sizeof(PairTile) / 4); ++j)
+          st_shared_cluster(dst + 4 * j, src[j]);
+        mbar_arrive_cluster(mapa_shared(smem_u32(&ti_full[ti_slot]), 1));
+        mbar_arrive(&ti_full[ti_slot]);
+        if (++ti_slot == P_TI_DEPTH) {
+          ti_slot = 0;
+          ti_phase ^= 1u;
+        }
+        if (t.prob < 0) break;
+      }
+      // the last cluster to finish resets the ticket for the next launch (no
+      // ticket is taken after a cluster's increment of the count)
+      __threadfence();
+      if (atomicAdd(P.ticket + 1, 1) == static_cast<int>(ncluster_x()) - 1) {
+        atomicExch(P.ticket, 0);
+        atomicExch(P.ticket + 1, 0);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------------------ MMA issue
       uint32_t stage = 0, sphase = 0;
       uint32_t acc = 0, acc_phase = 0;
+      int ti_slot = 0;
+      uint32_t ti_phase = 0;
       bool ok = true;
       int lt = 0;
-      for (int u = first; u < total && ok; u += stride) {
-        PairTile t;
-        pair_decode(P, u, t);
+      for (;;) {
+        if (!mbar_wait(&ti_full[ti_slot], ti_phase, wc)) break;
+        const PairTile t = s_ti[ti_slot];
+        mbar_arrive(&ti_empty[ti_slot]);
+        if (++ti_slot == P_TI_DEPTH) {
+          ti_slot = 0;
+          ti_phase ^= 1u;
+        }
+        if (t.prob < 0) break;
         const int split = P.p[t.prob].split;
         uint64_t* rec = pair_rec(P, leader, lt++);
         if (t.kb == 0) continue;
@@ -308,9 +436,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         if (acc == 0) acc_phase ^= 1u;
       }
       umma_commit_pair(mma_done, 0x1);
-      pair_drain_wait(mma_done, 0, P.budget_ns);
+      drain_wait(mma_done, 0, P.budget_ns);
     }
-  } else {
+  } else if (warp >= 2 && warp < 2 + P_EPI_WARPS) {
     // ------------------------------------------------------------- epilogue
     const int q4 = warp & 3;
     const int row_in_half = q4 * 32 + lane;
@@ -319,12 +447,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     uint8_t* obuf = reinterpret_cast<uint8_t*>(xbufs + (warp - 2) * (XBUF_BYTES / 4));
     uint32_t ck = 0;  // chunks this warp has stored
     uint32_t acc = 0, acc_phase = 0;
+    int ti_slot = 0;
+    uint32_t ti_phase = 0;
     const uint32_t tempty_cl[2] = {mapa_shared(smem_u32(&tempty[0]), 0),
                                    mapa_shared(smem_u32(&tempty[1]), 0)};
     int lt = 0;
-    for (int u = first; u < total; u += stride) {
-      PairTile t;
-      pair_decode(P, u, t);
+    for (;;) {
+      bool got = false;
+      if (lane == 0)
+        got = leader ? mbar_wait(&ti_full[ti_slot], ti_phase, wc)
+                     : mbar_wait<true>(&ti_full[ti_slot], ti_phase, wc);
+      __syncwarp();
+      if (!__shfl_sync(0xffffffffu, got, 0)) break;
+      const PairTile t = s_ti[ti_slot];
+      __syncwarp();
+      if (lane == 0) ti_release(ti_slot);
+      if (++ti_slot == P_TI_DEPTH) {
+        ti_slot = 0;
+        ti_phase ^= 1u;
+      }
+      if (t.prob < 0) break;
       const PairProb& pr = P.p[t.prob];
       uint64_t* rec = (warp == 2 && lane == 0) ? pair_rec(P, leader, lt) : nullptr;
       ++lt;
@@ -338,7 +480,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             *reinterpret_cast<uint4*>(orow + col) = make_uint4(0, 0, 0, 0);
         continue;
       }
-      bool got = false;
+      got = false;
       if (lane == 0) got = mbar_wait(&tfull[acc], acc_phase, wc);
       __syncwarp();
       if (!__shfl_sync(0xffffffffu, got, 0)) break;
@@ -408,7 +550,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();  // no peer access to our smem or TMEM after this point
+  // no copy of either CTA in flight, no peer access to our smem or TMEM after this
+  pair_teardown<PSTAGES>(leader, *s_issued, *s_abort, s_peer, full, PSTAGE, P.budget_ns);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, P_TMEM_COLS);  // collective, like the allocation
@@ -457,7 +600,8 @@ int encode2d(const GemmEnv& env, CUtensorMap* m, const void* base, int64_t rows,
 
 }  // namespace
 
-int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, const void* x_perm,
+int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
+                      const void* x_perm,
                       const void* x8, const void* dy_perm, const void* dy8, const void* dH,
                       const void* dH_lo8, const void* wa, const void* wa_lo8, void* dW1,
                       void* dW2, void* dWs1, void* dWs2) {
@@ -467,7 +611,8 @@ int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, const void*
   PairParams P{};
   P.poff = m.poff;
   P.counts = m.counts;
-  P.E = static_cast<int>(E);
+  P.Ex = static_cast<int>(p.Ex);
+  P.ticket = c.tickets + 2;  // [2]: ticket, finished clusters (zero; reset by the launch)
   P.status = env.status;
   P.budget_ns = env.budget_ns;
   if (env.trace && env.trace_which == 2) {
@@ -526,7 +671,7 @@ int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, const void*
   if (cudaFuncSetAttribute(wgrad_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            P_SMEM) != cudaSuccess)
     return HMM_ERR_CUDA;
-  // as many pairs as can be resident at once (tiles are assigned statically)
+  // as many pairs as can be resident at once (each takes tiles by ticket)
   int clusters = env.num_sms / 2;
   {
     cudaLaunchConfig_t cfg = {};

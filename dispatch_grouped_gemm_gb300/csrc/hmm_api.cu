@@ -52,6 +52,7 @@ struct hmm_ctx {
   int profile = 0;
   int pair_rows = 2;  // 0 single CTAs, 1 CTA pairs, 2 automatic, 3 single CTAs, small blocks
   int overlap = 1;    // programmatic dependent launches
+  int fused_combine = 0;  // combine in the GMM2 epilogue
   uint64_t* trace = nullptr;
   size_t trace_bytes = 0;
   int trace_which = 0;
@@ -155,6 +156,10 @@ int make_plan(const hmm_shape* s, bool training, Plan* p) {
   // o: fp32 with the shared expert (its unweighted term in the y combine),
   // else bf16
   const size_t obytes = align_up(static_cast<size_t>(R) * p->H * (p->shared ? 4 : 2), A);
+  // the fused combine's counters: one per token and 32-column segment of H
+  p->cmb_nseg = (p->H + 31) / 32;
+  p->cmb_count = p->T * p->cmb_nseg;
+  const size_t cmb_bytes = align_up(static_cast<size_t>(p->cmb_count) * 4, A);
   if (training) {
     p->sv_meta = 0;
     p->sv_xperm = p->meta_bytes;
@@ -162,13 +167,15 @@ int make_plan(const hmm_shape* s, bool training, Plan* p) {
     p->sv_h = p->sv_x8 + align_up(static_cast<size_t>(R) * p->ld8_h, A);
     p->saved_bytes = p->sv_h + hbytes;
     p->fw_ctrl = 0;
-    p->fw_a = p->ctrl_bytes;
+    p->fw_cmb = p->ctrl_bytes;
+    p->fw_a = p->fw_cmb + cmb_bytes;
     p->fw_o = p->fw_a + abytes;
     p->fwd_ws_bytes = p->fw_o + obytes;
   } else {
     p->saved_bytes = 0;
     p->fw_ctrl = 0;
-    p->fw_meta = p->ctrl_bytes;
+    p->fw_cmb = p->ctrl_bytes;
+    p->fw_meta = p->fw_cmb + cmb_bytes;
     p->fw_xperm = p->fw_meta + p->meta_bytes;
     p->fw_a = p->fw_xperm + xperm;
     p->fw_o = p->fw_a + abytes;
@@ -210,14 +217,8 @@ CtrlPtrs ctrl_at(const Plan& p, void* base) {
   return c;
 }
 
-}  // namespace hmm
-
-using namespace hmm;
-
-namespace {
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
+// Host-side limits of every entry point [HyperMegaMoE §4.2: shapes, dtypes
+// and layouts are rejected at the boundary, before any device work].
 int check_shape(const hmm_shape* s) {
   if (!s) return HMM_ERR_ARG;
   if (s->shared != 0 && s->shared != 1) return HMM_ERR_ARG;
@@ -233,6 +234,14 @@ int check_shape(const hmm_shape* s) {
   if (R >= (int64_t(1) << 31) - 1) return HMM_ERR_SHAPE;
   return HMM_OK;
 }
+
+}  // namespace hmm
+
+using namespace hmm;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct DeviceGuard {
   int prev = -1;
@@ -271,12 +280,16 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? HMM_OK : HMM_ERR_CUDA; }
 
 int read_route_error(hmm_ctx* ctx, cudaStream_t st) {
   unsigned v = 0;
-  if (cudaStreamSynchronize(st) != cudaSuccess) return HMM_ERR_CUDA;
-  if (cudaMemcpy(&v, ctx->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (cudaMemcpyAsync(&v, ctx->status, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
     return HMM_ERR_CUDA;
   if (v & HMM_STATUS_EXPERT_ID) {
+    // clear the bit in stream order (the kernels of this call wrote v; the
+    // timeout bit, if any, stays for hmm_status)
     const unsigned keep = v & ~HMM_STATUS_EXPERT_ID;
-    if (cudaMemcpy(ctx->status, &keep, sizeof keep, cudaMemcpyHostToDevice) != cudaSuccess)
+    if (cudaMemcpyAsync(ctx->status, &keep, sizeof keep, cudaMemcpyHostToDevice, st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
       return HMM_ERR_CUDA;
     return HMM_ERR_EXPERT_ID;
   }
@@ -360,7 +373,8 @@ int hmm_set_option(hmm_ctx* ctx, int option, int64_t value) {
       ctx->budget_ns = static_cast<uint64_t>(value);
       return HMM_OK;
     case HMM_OPT_INJECT_SKIP_READY:
-      ctx->inject_skip_ready = value != 0;
+      if (value < 0 || value > 2) return HMM_ERR_ARG;
+      ctx->inject_skip_ready = static_cast<int>(value);
       return HMM_OK;
     case HMM_OPT_PROFILE:
       ctx->profile = value != 0;
@@ -371,6 +385,9 @@ int hmm_set_option(hmm_ctx* ctx, int option, int64_t value) {
       return HMM_OK;
     case HMM_OPT_OVERLAP_LAUNCHES:
       ctx->overlap = value != 0;
+      return HMM_OK;
+    case HMM_OPT_FUSED_COMBINE:
+      ctx->fused_combine = value != 0;
       return HMM_OK;
     default:
       return HMM_ERR_ARG;
@@ -458,6 +475,8 @@ int forward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* x, const int3
   void* a = ws + p.fw_a;
   void* o = ws + p.fw_o;
 
+  const bool fused = ctx->fused_combine != 0;
+  int32_t* cmb = fused ? reinterpret_cast<int32_t*>(ws + p.fw_cmb) : nullptr;
   {
     PhaseScope ps(ctx, PH_ROUTE, st, route_launches(p));
     rc = cuda_rc(launch_route(p, topk_ids, m, c, nullptr, nullptr, ctx->status, st,
@@ -470,17 +489,20 @@ int forward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* x, const int3
   }
   {
     PhaseScope ps(ctx, PH_DISPATCH_X, st);
-    rc = cuda_rc(launch_dispatch_x(p, x, m, x_perm, x8, st, ctx->overlap != 0));
+    // (with the fused combine the dispatch also zeroes its counters)
+    rc = cuda_rc(launch_dispatch_x(p, x, m, x_perm, x8, cmb, fused ? p.cmb_count : 0, st,
+                                   ctx->overlap != 0));
   }
   if (rc != HMM_OK) return rc;
-  const bool inject = ctx->inject_skip_ready != 0;
-  ctx->inject_skip_ready = 0;
+  const bool inject = ctx->inject_skip_ready == 1;
+  if (inject) ctx->inject_skip_ready = 0;
   {
     PhaseScope ps(ctx, PH_GEMM_FWD, st);
     rc = launch_forward_gemms(env_of(ctx, p, st), p, m, c, x_perm, up_proj_weight, down_proj_weight,
-                              Ws1, Ws2, a, h32, o, inject);
+                              Ws1, Ws2, a, h32, o, inject,
+                              cmb, topk_weights, shape->weights_dtype, fused ? y : nullptr);
   }
-  if (rc != HMM_OK) return rc;
+  if (rc != HMM_OK || fused) return rc;
   PhaseScope ps(ctx, PH_COMBINE_Y, st);
   return cuda_rc(launch_combine_y(p, o, topk_weights, shape->weights_dtype, m, y, st,
                                 ctx->overlap != 0));
@@ -582,7 +604,7 @@ int backward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const vo
   float* dwp = reinterpret_cast<float*>(ws + p.bw_dwp);
   const GemmEnv env = env_of(ctx, p, st);
   auto weight_gemms = [&]() {
-    return launch_wgrad_pair(env, p, m, x_perm, x8, dy_perm, dy8, dH, dH_lo, wa, wa_lo,
+    return launch_wgrad_pair(env, p, m, c, x_perm, x8, dy_perm, dy8, dH, dH_lo, wa, wa_lo,
                              d_up_proj_weight, d_down_proj_weight, dWs1, dWs2);
   };
   const bool weights = d_up_proj_weight || d_down_proj_weight || dWs1 || dWs2;
@@ -599,10 +621,13 @@ int backward_impl(hmm_ctx* ctx, const hmm_shape* shape, const void* dy, const vo
                            st, ctx->overlap != 0));
   }
   if (rc != HMM_OK) return rc;
+  const bool inject = ctx->inject_skip_ready == 2;
+  if (inject) ctx->inject_skip_ready = 0;
   {
     PhaseScope ps(ctx, PH_GEMM_BWD_DATA, st);
     rc = launch_data_grad_gemms(env, p, m, c, dy_perm, wperm, h32, up_proj_weight,
-                                down_proj_weight, Ws1, Ws2, dH, dH_lo, wa, wa_lo, dwp, dx_perm);
+                                down_proj_weight, Ws1, Ws2, dH, dH_lo, wa, wa_lo, dwp, dx_perm,
+                                inject);
   }
   if (rc != HMM_OK) return rc;
   // dx and d_topk_weights need only part 1: combine them on the side stream
@@ -685,12 +710,14 @@ int hmm_status(hmm_ctx* ctx, void* stream, int* device_error) {
   if (!ctx) return HMM_ERR_ARG;
   DeviceGuard g(ctx->device);
   if (!g.ok) return HMM_ERR_CUDA;
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return HMM_ERR_CUDA;
+  // read and clear in the caller's stream order only: no device-wide wait
+  // (work of other streams keeps running)
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned v = 0;
-  if (cudaMemcpy(&v, ctx->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (cudaMemcpyAsync(&v, ctx->status, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemsetAsync(ctx->status, 0, sizeof v, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
     return HMM_ERR_CUDA;
-  if (cudaMemset(ctx->status, 0, sizeof v) != cudaSuccess) return HMM_ERR_CUDA;
-  if (cudaDeviceSynchronize() != cudaSuccess) return HMM_ERR_CUDA;
   if (device_error) *device_error = static_cast<int>(v);
   if (v & HMM_STATUS_TIMEOUT) return HMM_ERR_TIMEOUT;
   if (v & HMM_STATUS_EXPERT_ID) return HMM_ERR_EXPERT_ID;

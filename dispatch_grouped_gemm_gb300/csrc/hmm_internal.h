@@ -57,17 +57,24 @@ struct Plan {
   size_t off_chunk_base, off_tickets, off_ready;                           // inside ctrl
   int64_t ctrl_zero_count;  // int32 counters from off_tickets that each call zeroes
   // forward: saved = [meta | x_perm | x_perm8 | h]   (training)
-  //          workspace = [ctrl | a | o]       (training)
-  //          workspace = [ctrl | meta | x_perm | a | o]   (inference)
+  //          workspace = [ctrl | cmb | a | o]       (training)
+  //          workspace = [ctrl | cmb | meta | x_perm | a | o]   (inference)
+  // cmb: the fused combine's counters, one per (token, 32-column segment of
+  // H): cmb_count int32, zeroed by the dispatch of x when used
   size_t saved_bytes, fwd_ws_bytes;
   size_t sv_meta, sv_xperm, sv_x8, sv_h;
-  size_t fw_ctrl, fw_meta, fw_xperm, fw_a, fw_o;
+  size_t fw_ctrl, fw_cmb, fw_meta, fw_xperm, fw_a, fw_o;
+  int64_t cmb_nseg, cmb_count;
   // backward workspace =
   //   [ctrl | dy_perm | dy_perm8 | wperm | dH | dH_lo8 | wa | wa_lo8 | dX_perm | dwp]
   size_t bwd_ws_bytes;
   size_t bw_ctrl, bw_dyperm, bw_dy8, bw_wperm, bw_dh, bw_dhlo, bw_wa, bw_walo, bw_dxperm, bw_dwp;
 };
 
+// HMM_OK, or the error code for a shape outside the supported range (sizes,
+// dtype, the shared flag, H / I not multiples of 8, a padded row space past
+// 2^31 rows).  Every entry point calls it before any device work.
+int check_shape(const hmm_shape* s);
 int make_plan(const hmm_shape* s, bool training, Plan* p);
 MetaPtrs meta_at(const Plan& p, void* base);
 CtrlPtrs ctrl_at(const Plan& p, void* base);
@@ -128,9 +135,10 @@ cudaError_t launch_route(const Plan& p, const int32_t* ids, MetaPtrs m, CtrlPtrs
                          int32_t* slot2row, int32_t* row2slot, unsigned* status,
                          cudaStream_t st, bool pdl);
 int route_launches(const Plan& p);  // kernels launch_route launches for p
-// x8 (training, else null): also x_perm as e4m3 (ld8_h bytes per row)
+// x8 (training, else null): also x_perm as e4m3 (ld8_h bytes per row).  Also
+// zeroes zero_count int32 at zero_ptr (may be null).
 cudaError_t launch_dispatch_x(const Plan& p, const void* x, MetaPtrs m, void* x_perm, void* x8,
-                              cudaStream_t st, bool pdl);
+                              int32_t* zero_ptr, int64_t zero_count, cudaStream_t st, bool pdl);
 cudaError_t launch_combine_y(const Plan& p, const void* o, const void* w, int w_dtype, MetaPtrs m,
                              void* y, cudaStream_t st, bool pdl);
 // also dy_perm as e5m2 (dy8, ld8_h bytes per row)
@@ -162,22 +170,29 @@ struct GemmEnv {
 // forward GMM1(+SwiGLU) and GMM2 in one persistent launch with per-token-block
 // ready counters, for the routed experts and (p.shared) the shared expert
 // (Ws1 [H, 2I], Ws2 [I, H]).  h32 may be null (inference).
+// fused_y != null: the combine runs in the GMM2 epilogue (counters cmb, the
+// routing weights w of dtype w_dtype) and writes y.
 int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
                          const void* x_perm, const void* W1, const void* W2, const void* Ws1,
-                         const void* Ws2, void* a, float* h32, void* o, bool skip_ready_release);
+                         const void* Ws2, void* a, float* h32, void* o, bool skip_ready_release,
+                         int* cmb, const void* w, int w_dtype, void* fused_y);
 // backward data gradients in one persistent launch: act_grad (+SwiGLU grad,
 // d_w partials; dH and w*a written as a bf16 high part plus an e5m2 low part)
 // and input-grad (released per token block), routed and shared experts.
+// skip_ready_release: test-only fault injection (the input-grad waits run out).
 int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
                            const void* dy_perm, const float* wperm, const float* h32,
                            const void* W1, const void* W2, const void* Ws1, const void* Ws2,
                            void* dH, void* dH_lo, void* wa, void* wa_lo, float* dwp,
-                           void* dx_perm);
+                           void* dx_perm, bool skip_ready_release);
 // weight gradients on CTA pairs (tcgen05 cta_group::2), 256 x 256 tiles:
 // dW1 / dW2 of the routed experts and dWs1 / dWs2 of the shared expert (any
 // may be null).  The low parts (dH_lo8, wa_lo8: e5m2) meet fp8 copies of the
 // other operand (x8: e4m3, dy8: e5m2) in a second, fp8 MMA.
-int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, const void* x_perm,
+// Tiles go out longest first by a ticket in c.tickets[2..3] (zeroed by the
+// backward dispatch; every launch leaves them zero again).
+int launch_wgrad_pair(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
+                      const void* x_perm,
                       const void* x8, const void* dy_perm, const void* dy8, const void* dH,
                       const void* dH_lo8, const void* wa, const void* wa_lo8, void* dW1,
                       void* dW2, void* dWs1, void* dWs2);

@@ -238,13 +238,13 @@ static int move_grid(int64_t warps) {
 }
 
 cudaError_t launch_dispatch_x(const Plan& p, const void* x, MetaPtrs m, void* x_perm, void* x8,
-                              cudaStream_t st, bool pdl) {
+                              int32_t* zero_ptr, int64_t zero_count, cudaStream_t st, bool pdl) {
   const int64_t warps = p.T + p.Ex * BM;
   return launch_kernel(dispatch_rows_kernel<false>, move_grid(warps), MOVE_THREADS, 0, st, pdl, 1,
                        static_cast<const uint4*>(x), p.T, p.K, p.H / 8, m, static_cast<int>(p.E),
                        static_cast<int>(p.Ex), static_cast<uint4*>(x_perm),
-                       static_cast<uint2*>(x8), p.ld8_h / 8, nullptr, 0, nullptr, nullptr,
-                       int64_t(0));
+                       static_cast<uint2*>(x8), p.ld8_h / 8, nullptr, 0, nullptr, zero_ptr,
+                       zero_count);
 }
 
 cudaError_t launch_dispatch_dy(const Plan& p, const void* dy, const void* w, int w_dtype,

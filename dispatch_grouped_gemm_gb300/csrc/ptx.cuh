@@ -45,6 +45,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
       "r"(bytes)
       : "memory");
 }
+// Count `bytes` of transactions on `bar` as completed without any copy (for
+// a CTA pair's teardown: the bytes the peer CTA never loaded).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -451,6 +457,58 @@ __device__ __forceinline__ uint2 pack_fp8x8(const float* v) {
   for (int j = 0; j < 4; ++j)
     q[j] = E5M2 ? cvt_e5m2x2(v[2 * j], v[2 * j + 1]) : cvt_e4m3x2(v[2 * j], v[2 * j + 1]);
   return make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+}
+
+// Bounded wait that ignores the abort flag (used only to drain in-flight
+// copies or MMAs before a CTA exits).
+static __device__ __noinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < (1u << 28); ++it) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((it & 31u) == 31u && globaltimer_ns() - t0 > budget_ns) return;
+  }
+}
+
+// Teardown of a CTA pair whose TMA loads are counted on the even CTA's full
+// barriers (each CTA loads cta_bytes per K block; the even CTA arms every
+// stage it issues for both).  After an abort the two producers may have left
+// their loops after different numbers of K blocks, so loads of the odd CTA
+// can still be in flight (into its own shared memory) or stages the even CTA
+// armed may wait for bytes the odd CTA never requested.  Protocol (called by
+// every thread of both CTAs, after their roles have finished and a
+// __syncthreads):
+//   1. the odd CTA's thread 0 writes its issued K blocks and abort flag into
+//      the even CTA's shared memory; a cluster barrier publishes them;
+//   2. if either CTA aborted, the even CTA's thread 0 arms the stages only
+//      the odd CTA issued (for the odd CTA's bytes), completes the odd CTA's
+//      share of the stages only it issued, and waits (bounded) for the last
+//      phase of every slot: stages older than one ring were complete before
+//      their slot was reused, so after this no copy of either CTA is in
+//      flight;
+//   3. a second cluster barrier holds the odd CTA until then.
+// peer[0], peer[1]: the even CTA's slots for the odd CTA's count and flag.
+template <int NST>
+__device__ __forceinline__ void pair_teardown(bool leader, uint32_t issued, int aborted,
+                                              uint32_t* peer, uint64_t* full, uint32_t cta_bytes,
+                                              uint64_t budget_ns) {
+  if (!leader && threadIdx.x == 0) {
+    st_shared_cluster(mapa_shared(smem_u32(&peer[0]), 0), static_cast<int>(issued));
+    st_shared_cluster(mapa_shared(smem_u32(&peer[1]), 0), aborted);
+  }
+  cluster_sync_all();
+  if (leader && threadIdx.x == 0 && (aborted || peer[1])) {
+    const uint32_t n_e = issued, n_o = peer[0];
+    const uint32_t n = n_e > n_o ? n_e : n_o;
+    for (uint32_t k = n > NST ? n - NST : 0u; k < n; ++k) {
+      uint64_t* b = &full[k % NST];
+      if (k >= n_e)
+        mbar_arrive_expect_tx(b, cta_bytes);  // never armed: count the odd CTA's bytes
+      else if (k >= n_o)
+        mbar_complete_tx(b, cta_bytes);       // armed for both, loaded by the even CTA only
+      drain_wait(b, (k / NST) & 1u, budget_ns);
+    }
+  }
+  cluster_sync_all();
 }
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }

@@ -54,12 +54,9 @@ extern "C" int hmm_route_static(const hmm_shape* shape, const int32_t* topk_ids,
   using namespace hmm;
   // routing of the routed experts only: a shape with the shared expert is refused
   if (!shape || shape->shared != 0) return HMM_ERR_ARG;
-  if (shape->weights_dtype != HMM_DTYPE_BF16 && shape->weights_dtype != HMM_DTYPE_F32)
-    return HMM_ERR_DTYPE;
-  if (shape->T < 0 || shape->H <= 0 || shape->I <= 0 || shape->E <= 0 || shape->K <= 0 ||
-      shape->E > MAX_E || shape->K > 32 || shape->T > (int64_t(1) << 31))
-    return HMM_ERR_SHAPE;
-  if (shape->H % 8 != 0 || shape->I % 8 != 0) return HMM_ERR_LAYOUT;
+  // the same limits as every other entry point (hmm_route included)
+  const int src = check_shape(shape);
+  if (src != HMM_OK) return src;
   Plan p;
   make_plan(shape, false, &p);
   if (!counts || !offsets || (p.TK > 0 && (!topk_ids || !slot2row || !row2slot)))

@@ -112,7 +112,11 @@ int hmm_destroy(hmm_ctx* ctx);
  *                         1, the next hmm_forward launches its GMM1 tiles
  *                         without releasing the GMM2 ready counters, so every
  *                         GMM2 tile's bounded wait runs out and the call
- *                         reports HMM_STATUS_TIMEOUT.  Cleared after one call. */
+ *                         reports HMM_STATUS_TIMEOUT; when 2, the next
+ *                         hmm_backward (or hmm_backward_dx) does the same to
+ *                         its act_grad and input-grad tiles.  Cleared by the
+ *                         call it affects.  No device fault is involved: the
+ *                         waits end by their budget and every CTA leaves. */
 #define HMM_OPT_VALIDATE 1
 #define HMM_OPT_WAIT_BUDGET_NS 2
 #define HMM_OPT_INJECT_SKIP_READY 3
@@ -139,11 +143,26 @@ int hmm_destroy(hmm_ctx* ctx);
  *                         kernel has completed.  Default 1.  Results do not
  *                         depend on it. */
 #define HMM_OPT_OVERLAP_LAUNCHES 8
+/*   HMM_OPT_FUSED_COMBINE  0/1: fold the forward's Combine into the GMM2
+ *                         epilogue [HyperMegaMoE §6.2: the unpermute and the
+ *                         top-k weighted merge inside the fused operator;
+ *                         MoE overlap explainer §6: a per-token completion
+ *                         count publishes a token once all of its branches
+ *                         are in].  Each GMM2 tile counts its token rows per
+ *                         32-column segment; the epilogue warp that completes
+ *                         a token's K expert rows (K + 1 with the shared
+ *                         expert) of a segment sums them in k order and writes
+ *                         y, so no combine launch runs.  y is bit-identical to
+ *                         the separate combine (same fp32 operations in the
+ *                         same order, one bf16 rounding).  Default 0.  Out-of-
+ *                         range expert ids leave the rows of their tokens
+ *                         unwritten (outputs are undefined on that error). */
+#define HMM_OPT_FUSED_COMBINE 9
 int hmm_set_option(hmm_ctx* ctx, int option, int64_t value);
 
 /* Launch phases timed under HMM_OPT_PROFILE (index = phase id):
  *   0 route (2 or 3 kernels)  1 dispatch_x  2 gemm_fwd (GMM1+SwiGLU, GMM2)
- *   3 combine_y          4 dispatch_dy
+ *   3 combine_y (no launch with HMM_OPT_FUSED_COMBINE)   4 dispatch_dy
  *   5 gemm_bwd_data (act_grad + SwiGLU grad, input-grad)
  *   6 gemm_bwd_weight (W2Grad, W1Grad)
  *   7 combine_dx (+ d_topk_weights; on a second stream, beside phase 6)  */
@@ -210,9 +229,14 @@ int hmm_route(hmm_ctx* ctx, const hmm_shape* shape, const int32_t* topk_ids,
  * - Every call shares the one array: calls whose GPU work overlaps (on two
  *   streams, or from two host threads) race and give undefined results.
  *   Serialise them on one stream.
- * - A shape whose scratch exceeds the array returns HMM_ERR_CAPACITY before
- *   any device work; the scratch grows with T*K and E (about 12 bytes per
- *   slot plus 4*E bytes per 1024 slots).
+ * - The scratch of a shape is 256 bytes plus the routing part of the forward
+ *   workspace: with S = T*K slots, C = ceil(S / 1024) and the padded rows
+ *   R = S + 127*min(E, S) rounded up to a multiple of 128, about
+ *   4*S + 4*R + R/16 + 4*E*C + 12*E + 32 bytes, each array rounded up to
+ *   256 bytes (about 8 bytes per slot plus 512 bytes per expert plus 4*E
+ *   bytes per 1024 slots).  A shape whose scratch exceeds the array returns
+ *   HMM_ERR_CAPACITY before any device work.  Shape limits are those of
+ *   hmm_route. 
  * - Ids outside [0, E) are left out: their slot2row is -1 and
  *   offsets[E] < T*K (there is no status word to read). */
 int hmm_route_static(const hmm_shape* shape, const int32_t* topk_ids,
@@ -305,7 +329,9 @@ int hmm_backward_dw(hmm_ctx* ctx, const hmm_shape* shape, const void* saved,
                     void* d_down_proj_weight, void* workspace,
                     size_t workspace_bytes, void* stream);
 
-/* Synchronise `stream`, then read and clear the device status word.
+/* Read and clear the device status word in `stream` order, then wait for
+ * `stream` (only that stream: other streams of the device keep running).
+ * Work queued on `stream` before the call has set its bits by then.
  * *device_error receives the HMM_STATUS_* bits.  Returns HMM_OK, or
  * HMM_ERR_EXPERT_ID / HMM_ERR_TIMEOUT if the corresponding bit was set. */
 int hmm_status(hmm_ctx* ctx, void* stream, int* device_error);

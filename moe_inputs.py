@@ -18,6 +18,7 @@ skewed    16384  7168  2048   32  8  Zipf(1.2) over a seeded expert
                                      permutation, 3 experts never drawn
 decode      128  7168  2048  256  8  uniform
 backward   4096  2048  1408   64  6  uniform, with dy
+skewed_bwd 4096  2048  1408   64  6  Zipf(1.2) as above, with dy
 ========  =====  ====  ====  ===  =  ===============================
 
 x ~ N(0,1), up_proj ~ N(0, 1/H), down_proj ~ N(0, 1/I), dy ~ N(0,1),
@@ -56,6 +57,8 @@ CONFIGS = {
     "skewed": dict(shape=Shape(16384, 7168, 2048, 32, 8), routing="zipf", seed=1002),
     "decode": dict(shape=Shape(128, 7168, 2048, 256, 8), routing="uniform", seed=1003),
     "backward": dict(shape=Shape(4096, 2048, 1408, 64, 6), routing="uniform", seed=1004),
+    # hot-expert backward: the prefill shape with the skewed workload's routing law
+    "skewed_bwd": dict(shape=Shape(4096, 2048, 1408, 64, 6), routing="zipf", seed=1005),
 }
 
 

@@ -4,11 +4,22 @@ compute one by one (rows of y / dx / d_topk_weights are independent per
 token; a weight gradient needs only the slots routed to its expert), plus
 bit-exact routing and invariants that hold at any size.
 
+The sampled tokens are chosen so that every token block of every expert is
+checked: the row-mode GEMMs cut an expert's rows into token blocks (CTA
+pairs at these shapes: blocks of equal size, at most 256 rows, multiples of
+64), and for each block the tokens of its first and last routed rows are in
+the sample (the skewed forward, whose oracle rows cost the most, takes the
+first row of every block and the last row of every expert).  The weight
+gradients are checked for at least eight experts: the first and last ones of
+the schedule, the hot and the coldest expert, and some in between (every
+expert's last W2Grad row tile is a partial one: I = 1408 = 5.5 x 256).
+
 Workloads (seeded, synthetic, see moe_inputs):
-  prefill  T=4096  H=2048 I=1408 E=64  K=6  uniform
-  backward T=4096  H=2048 I=1408 E=64  K=6  uniform, with dy
-  skewed   T=16384 H=7168 I=2048 E=32  K=8  Zipf(1.2), 3 empty experts
-  decode   T=128   H=7168 I=2048 E=256 K=8  uniform (22.5 GB of weights)
+  prefill    T=4096  H=2048 I=1408 E=64  K=6  uniform
+  backward   T=4096  H=2048 I=1408 E=64  K=6  uniform, with dy
+  skewed_bwd T=4096  H=2048 I=1408 E=64  K=6  Zipf(1.2), 3 empty experts, with dy
+  skewed     T=16384 H=7168 I=2048 E=32  K=8  Zipf(1.2), 3 empty experts
+  decode     T=128   H=7168 I=2048 E=256 K=8  uniform (22.5 GB of weights)
 """
 import numpy as np
 import pytest
@@ -19,6 +30,9 @@ import oracle
 from tests import gpu_util as gu
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+TROWS = 64      # token blocks start and end on multiples of 64 rows
+PAIR_NT = 256   # rows per token block at most (CTA-pair tiles)
 
 
 @pytest.fixture(scope="module")
@@ -33,11 +47,42 @@ def _sample_tokens(T, n, seed):
     return np.sort(r.choice(T, size=min(n, T), replace=False))
 
 
-def _upload_small(prob):
+def block_tokens(ids, E, both_ends=True, nt=PAIR_NT):
+    """Tokens whose slots land in every token block of every expert.  An
+    expert of M rows is cut into nb = ceil(M / nt) blocks of equal size (the
+    rows rounded up to 64, divided by nb, rounded up to 64; the last block
+    shorter).  Per block: its first routed row (and its last one with
+    both_ends); always the expert's last row."""
+    counts, offsets, _, row2slot = oracle.route(ids, E)
+    K = ids.shape[1]
+    toks = set()
+    for e in range(E):
+        M = int(counts[e])
+        if M == 0:
+            continue
+        nb = -(-M // nt)
+        rows = -(-M // TROWS) * TROWS
+        blk = -(-(rows // nb) // TROWS) * TROWS
+        picks = {M - 1}
+        for b in range(nb):
+            lo, hi = blk * b, min(blk * (b + 1), M)
+            if lo >= M:
+                continue
+            picks.add(lo)
+            if both_ends:
+                picks.add(hi - 1)
+        for r in picks:
+            toks.add(int(row2slot[offsets[e] + r]) // K)
+    return np.array(sorted(toks), dtype=np.int64)
+
+
+def _upload(prob, dy=False):
     d = gu.SimpleNamespace()
     d.x = gu.bf16(prob.x)
     d.ids = torch.from_numpy(prob.topk_ids).to(gu.dev())
     d.w = gu.bf16(prob.topk_weights)
+    if dy:
+        d.dy = gu.bf16(prob.dy)
     return d
 
 
@@ -52,79 +97,147 @@ def _compact_experts(prob, ids_sub):
     return remap[ids_sub], W1, W2
 
 
+def _rows(t, tok):
+    return gu.f64(t[torch.from_numpy(tok).to(gu.dev())])
+
+
+def _report(workload, name, ratio):
+    # worst |gpu - ref| / (1e-2 + 2e-2 |ref|) of the check (shown with -s)
+    print(f"[tolerance ratio] {workload} {name}: {ratio:.3f}")
+
+
+def _check_weight_grads(prob, dW1, dW2, experts):
+    """dW of each listed expert against the oracle (only its slots matter:
+    one row per slot, in slot order)."""
+    worst = 0.0
+    for e in experts:
+        t_idx, k_idx = np.nonzero(prob.topk_ids == e)
+        if t_idx.size == 0:
+            assert not gu.f64(dW1[e]).any() and not gu.f64(dW2[e]).any(), e
+            continue
+        w_s = np.ascontiguousarray(prob.topk_weights[t_idx, k_idx][:, None])
+        ids_s = np.zeros((t_idx.size, 1), np.int32)
+        rW1, rW2 = oracle.weight_grad(0, prob.x[t_idx], ids_s, w_s, prob.W1[e][None],
+                                      prob.W2[e][None], prob.dy[t_idx])
+        # the weight-gradient GEMMs add the e5m2 low part of their rounded
+        # operand; with the bf16 part alone the worst element of an expert of
+        # ~400 rows lands near 3x the bound, with it the bf16 rounding of dW
+        # itself dominates (a CPU rounding model puts both near 0.2-0.3).  The
+        # low part's own rounding adds up over the rows: the hot expert of the
+        # Zipf routing (3732 rows) reaches 0.63.  A missing low part would
+        # show as a ratio above 1 on these shapes.
+        r1 = gu.check(f"d_up_proj_weight[{e}]", gu.f64(dW1[e]), rW1)
+        r2 = gu.check(f"d_down_proj_weight[{e}]", gu.f64(dW2[e]), rW2)
+        _report(f"expert {e} ({t_idx.size} rows)", "dW1 / dW2", max(r1, r2))
+        margin = 0.6 if t_idx.size <= 1024 else 0.8
+        assert max(r1, r2) < margin, (e, t_idx.size, r1, r2)
+        worst = max(worst, r1, r2)
+    return worst
+
+
+def _wgrad_experts(prob):
+    E = prob.shape.E
+    counts = np.bincount(prob.topk_ids.reshape(-1), minlength=E)
+    order = np.argsort(-counts, kind="stable")
+    nonempty = np.nonzero(counts)[0]
+    pick = [0, 1, E // 2, E - 2, E - 1, int(order[0]), int(order[1]),
+            int(nonempty[np.argmin(counts[nonempty])]), int(np.argsort(counts)[E // 2])]
+    empty = np.nonzero(counts == 0)[0]
+    if empty.size:
+        pick.append(int(empty[0]))
+    out = list(dict.fromkeys(pick))
+    assert len(out) >= 8
+    return out
+
+
+def test_block_tokens_cover_every_block():
+    """The sampler itself (CPU): every block of every expert has a sampled
+    token, on the uniform and the skewed routing."""
+    for name in ("prefill", "skewed"):
+        prob = mi.make(name)
+        ids, E = prob.topk_ids, prob.shape.E
+        tok = block_tokens(ids, E, both_ends=False)
+        counts, offsets, slot2row, _ = oracle.route(ids, E)
+        K = ids.shape[1]
+        hit = set()
+        for t in tok:
+            for k in range(K):
+                s = t * K + k
+                e = int(ids[t, k])
+                hit.add((e, int(slot2row[s]) - int(offsets[e])))
+        for e in range(E):
+            M = int(counts[e])
+            if M == 0:
+                continue
+            nb = -(-M // PAIR_NT)
+            rows = -(-M // TROWS) * TROWS
+            blk = -(-(rows // nb) // TROWS) * TROWS
+            for b in range(nb):
+                lo, hi = blk * b, min(blk * (b + 1), M)
+                assert any((e, r) in hit for r in range(lo, hi)), (name, e, b)
+
+
 def test_prefill_forward_full_size(run):
     prob = mi.make("prefill")
-    d = _upload_small(prob)
-    d.W1, d.W2 = gu.upload_problem_weights(prob)
+    d = _upload(prob)
+    d.W1, d.W2 = gu.bf16(prob.W1), gu.bf16(prob.W2)
     y, _ = run.forward(d, training=False)
     y2, _ = run.forward(d, training=True)
     torch.cuda.synchronize()
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
-    tok = _sample_tokens(prob.shape.T, 48, 1)
-    ids_c, W1c, W2c = _compact_experts(prob, prob.topk_ids[tok])
-    ref = oracle.forward(prob.x[tok], ids_c, prob.topk_weights[tok], W1c, W2c)
-    gu.check("y[sample]", gu.f64(y[torch.from_numpy(tok).to(gu.dev())]), ref)
+    tok = block_tokens(prob.topk_ids, prob.shape.E)
+    ref = oracle.forward(prob.x[tok], prob.topk_ids[tok], prob.topk_weights[tok], prob.W1,
+                         prob.W2)
+    _report("prefill", "y", gu.check("y[every block]", _rows(y, tok), ref))
     assert run.status() == (0, 0)
 
 
-def test_backward_full_size(run):
-    prob = mi.make("backward")
-    d = _upload_small(prob)
-    d.dy = gu.bf16(prob.dy)
-    d.W1, d.W2 = gu.upload_problem_weights(prob)
+@pytest.mark.parametrize("name", ["backward", "skewed_bwd"])
+def test_backward_full_size(run, name):
+    prob = mi.make(name)
+    d = _upload(prob, dy=True)
+    d.W1, d.W2 = gu.bf16(prob.W1), gu.bf16(prob.W2)
     y, saved = run.forward(d)
     dx, dW1, dW2, dw = run.backward(d, saved)
     torch.cuda.synchronize()
-    tok = _sample_tokens(prob.shape.T, 32, 2)
-    ids_c, W1c, W2c = _compact_experts(prob, prob.topk_ids[tok])
-    rdx, rdw = oracle.backward_tokens(prob.x[tok], ids_c, prob.topk_weights[tok], W1c, W2c,
-                                      prob.dy[tok])
-    tk = torch.from_numpy(tok).to(gu.dev())
-    gu.check("dx[sample]", gu.f64(dx[tk]), rdx)
-    gu.check("d_topk_weights[sample]", gu.f64(dw[tk]), rdw)
-    counts = np.bincount(prob.topk_ids.reshape(-1), minlength=prob.shape.E)
-    for e in (int(np.argmax(counts)), int(np.argmin(counts))):
-        # only the slots routed to e matter: one row per slot, in slot order
-        t_idx, k_idx = np.nonzero(prob.topk_ids == e)
-        w_s = np.ascontiguousarray(prob.topk_weights[t_idx, k_idx][:, None])
-        ids_s = np.zeros((t_idx.size, 1), np.int32)
-        rW1, rW2 = oracle.weight_grad(0, prob.x[t_idx], ids_s, w_s, prob.expert_W1(e)[None],
-                                      prob.expert_W2(e)[None], prob.dy[t_idx])
-        # the weight-gradient GEMMs add the e5m2 low part of their rounded
-        # operand; with the bf16 part alone the worst element of these
-        # experts lands near 3x the bound, with it the bf16 rounding of dW
-        # itself dominates (a CPU rounding model puts both near 0.2-0.3)
-        r1 = gu.check(f"d_up_proj_weight[{e}]", gu.f64(dW1[e]), rW1)
-        r2 = gu.check(f"d_down_proj_weight[{e}]", gu.f64(dW2[e]), rW2)
-        assert max(r1, r2) < 0.6, (e, r1, r2)
+    tok = block_tokens(prob.topk_ids, prob.shape.E)
+    ref_y = oracle.forward(prob.x[tok], prob.topk_ids[tok], prob.topk_weights[tok], prob.W1,
+                           prob.W2)
+    _report(name, "y", gu.check("y[every block]", _rows(y, tok), ref_y))
+    rdx, rdw = oracle.backward_tokens(prob.x[tok], prob.topk_ids[tok], prob.topk_weights[tok],
+                                      prob.W1, prob.W2, prob.dy[tok])
+    _report(name, "dx", gu.check("dx[every block]", _rows(dx, tok), rdx))
+    _report(name, "d_topk_weights", gu.check("d_topk_weights[every block]", _rows(dw, tok), rdw))
+    _check_weight_grads(prob, dW1, dW2, _wgrad_experts(prob))
     assert run.status() == (0, 0)
 
 
 def test_skewed_forward_full_size(run):
     prob = mi.make("skewed")
-    d = _upload_small(prob)
-    d.W1, d.W2 = gu.upload_problem_weights(prob)
+    d = _upload(prob)
+    d.W1, d.W2 = gu.bf16(prob.W1), gu.bf16(prob.W2)
     y, _ = run.forward(d, training=False)
     torch.cuda.synchronize()
     counts = np.bincount(prob.topk_ids.reshape(-1), minlength=prob.shape.E)
     assert (counts == 0).sum() >= 3
-    tok = _sample_tokens(prob.shape.T, 24, 3)
-    ids_c, W1c, W2c = _compact_experts(prob, prob.topk_ids[tok])
-    ref = oracle.forward(prob.x[tok], ids_c, prob.topk_weights[tok], W1c, W2c)
-    gu.check("y[sample]", gu.f64(y[torch.from_numpy(tok).to(gu.dev())]), ref)
+    # every block of every expert (the hot one has about 60)
+    tok = block_tokens(prob.topk_ids, prob.shape.E, both_ends=False)
+    ref = oracle.forward(prob.x[tok], prob.topk_ids[tok], prob.topk_weights[tok], prob.W1,
+                         prob.W2)
+    _report("skewed", "y", gu.check("y[every block]", _rows(y, tok), ref))
     assert run.status() == (0, 0)
 
 
 def test_decode_forward_full_size(run):
     prob = mi.make("decode")
-    d = _upload_small(prob)
+    d = _upload(prob)
     d.W1, d.W2 = gu.upload_problem_weights(prob)
     y, _ = run.forward(d, training=False)
     torch.cuda.synchronize()
-    tok = _sample_tokens(prob.shape.T, 16, 4)
+    tok = _sample_tokens(prob.shape.T, 32, 4)
     ids_c, W1c, W2c = _compact_experts(prob, prob.topk_ids[tok])
     ref = oracle.forward(prob.x[tok], ids_c, prob.topk_weights[tok], W1c, W2c)
-    gu.check("y[sample]", gu.f64(y[torch.from_numpy(tok).to(gu.dev())]), ref)
+    _report("decode", "y", gu.check("y[sample]", _rows(y, tok), ref))
     del d
     torch.cuda.empty_cache()
     assert run.status() == (0, 0)

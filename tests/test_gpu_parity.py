@@ -293,3 +293,38 @@ def test_backward_split_dx_then_dw_is_bit_identical(run, rows_mode):
     torch.cuda.synchronize()
     assert torch.equal(dW2.view(torch.int16), dW2c.view(torch.int16))
     assert run.status() == (0, 0)
+
+
+@pytest.mark.parametrize("case", ["multi_tile", "empty_and_hot", "duplicates"])
+def test_backward_split_matches_oracle(run, case, rows_mode):
+    """The W/D split against the fp64 oracle [EP overlap issue §2.3, §4.5:
+    D-only and W-only entry points; HyperMegaMoE §7.2: each optional
+    increment gets its own forward, backward and edge cases]: dx and
+    d_topk_weights from hmm_backward_dx, then the weight gradients from a
+    later hmm_backward_dw (another kernel launched in between on the same
+    stream), each elementwise within the tolerance; empty experts exact
+    zeros."""
+    p = dict(SCEN)[case]
+    d = gu.upload(p)
+    y, saved = run.forward(d)
+    sh = run.shape(d)
+    _, _, bwd = hmm.hmm_workspace_size(sh, True)
+    ws = torch.empty(bwd, dtype=torch.uint8, device=gu.dev())
+    dx = torch.empty_like(d.x)
+    dw = torch.empty_like(d.w)
+    dW1 = torch.full_like(d.W1, float("nan"))
+    dW2 = torch.full_like(d.W2, float("nan"))
+    hmm.hmm_backward_dx(run.ctx.handle, sh, d.dy, d.w, d.W1, d.W2, saved, dx, dw, ws)
+    other = torch.randn(1 << 20, device=gu.dev()).sum()    # unrelated work in between
+    hmm.hmm_backward_dw(run.ctx.handle, sh, saved, dW1, dW2, ws)
+    torch.cuda.synchronize()
+    del other
+    rdx, rdW1, rdW2, rdw = oracle.backward(p.x, p.ids, p.w, p.W1, p.W2, p.dy)
+    gu.check("dx (backward_dx)", gu.f64(dx), rdx)
+    gu.check("d_topk_weights (backward_dx)", gu.f64(dw), rdw)
+    gu.check("d_up_proj_weight (backward_dw)", gu.f64(dW1), rdW1)
+    gu.check("d_down_proj_weight (backward_dw)", gu.f64(dW2), rdW2)
+    counts = np.bincount(p.ids.reshape(-1), minlength=p.E)
+    for e in np.nonzero(counts == 0)[0]:
+        assert not gu.f64(dW1[e]).any() and not gu.f64(dW2[e]).any()
+    assert run.status() == (0, 0)

@@ -26,14 +26,44 @@ def test_route_static_refuses_shapes_beyond_its_scratch():
 
 
 def _ids(case):
+    r = np.random.default_rng(9)
     if case == "prefill":
         return mi.make("prefill").topk_ids, 64
-    r = np.random.default_rng(9)
-    return r.integers(0, 5, size=(3001, 7)).astype(np.int32), 5
+    if case == "ragged_repeats":
+        return r.integers(0, 5, size=(3001, 7)).astype(np.int32), 5
+    # the routing paths with a separate scan launch between the count and
+    # rank kernels: more than 512 experts, and more than 32768 chunk x
+    # expert histogram entries
+    if case == "scan_launch_wide_E":
+        return r.integers(0, 600, size=(3000, 6)).astype(np.int32), 600
+    if case == "scan_launch_many_chunks":
+        return r.integers(0, 256, size=(20000, 8)).astype(np.int32), 256
+    if case == "no_tokens":
+        return np.zeros((0, 4), np.int32), 16
+    raise ValueError(case)
+
+
+def _outs(E, S, dev):
+    return (torch.full((E,), -7, dtype=torch.int32, device=dev),
+            torch.full((E + 1,), -7, dtype=torch.int32, device=dev),
+            torch.full((max(S, 1),), -7, dtype=torch.int32, device=dev),
+            torch.full((max(S, 1),), -7, dtype=torch.int32, device=dev))
+
+
+def _route(sh, ids, E, S, dev):
+    """The existing entry point, with a caller workspace and a context."""
+    ctx = hmm.Context.for_device(dev)
+    fwd, _, _ = hmm.hmm_workspace_size(sh, False)
+    ws = torch.empty(max(fwd, 256), dtype=torch.uint8, device=dev)
+    ref = _outs(E, S, dev)
+    hmm.hmm_route(ctx.handle, sh, ids, *ref, ws)
+    torch.cuda.synchronize()
+    return ref
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("case", ["prefill", "ragged_repeats"])
+@pytest.mark.parametrize("case", ["prefill", "ragged_repeats", "scan_launch_wide_E",
+                                  "scan_launch_many_chunks", "no_tokens"])
 def test_route_static_matches_route_two_calls(case):
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
@@ -41,26 +71,26 @@ def test_route_static_matches_route_two_calls(case):
     torch.cuda.set_device(dev)
     ids_np, E = _ids(case)
     T, K = ids_np.shape
+    S = T * K
     sh = hmm.make_shape(T, 8, 8, E, K)
     ids = torch.from_numpy(ids_np).to(dev)
+    ref = _route(sh, ids, E, S, dev)
 
-    def outs():
-        return (torch.full((E,), -7, dtype=torch.int32, device=dev),
-                torch.full((E + 1,), -7, dtype=torch.int32, device=dev),
-                torch.full((T * K,), -7, dtype=torch.int32, device=dev),
-                torch.full((T * K,), -7, dtype=torch.int32, device=dev))
-
-    # the existing entry point, with a caller workspace and a context
-    ctx = hmm.Context.for_device(dev)
-    fwd, _, _ = hmm.hmm_workspace_size(sh, False)
-    ws = torch.empty(fwd, dtype=torch.uint8, device=dev)
-    ref = outs()
-    hmm.hmm_route(ctx.handle, sh, ids, *ref, ws)
+    # a first call on a larger shape with other ids leaves its contents in the
+    # shared array, so the calls below start from stale scratch
+    r = np.random.default_rng(31)
+    big_np = r.integers(0, 200, size=(9000, 8)).astype(np.int32)
+    big = torch.from_numpy(big_np).to(dev)
+    hmm.hmm_route_static(hmm.make_shape(9000, 8, 8, 200, 8), big, *_outs(200, 9000 * 8, dev))
     torch.cuda.synchronize()
 
+    got = [_outs(E, S, dev) for _ in range(2)]
+    free0, _ = torch.cuda.mem_get_info(dev)
     for call in range(2):
-        got = outs()
-        hmm.hmm_route_static(sh, ids, *got)
+        hmm.hmm_route_static(sh, ids, *got[call])
         torch.cuda.synchronize()
-        for name, g, r in zip(("counts", "offsets", "slot2row", "row2slot"), got, ref):
-            assert torch.equal(g, r), f"call {call}: {name} differs from hmm_route"
+    free1, _ = torch.cuda.mem_get_info(dev)
+    assert free1 == free0, "device memory changed across hmm_route_static calls"
+    for call in range(2):
+        for name, g, rr in zip(("counts", "offsets", "slot2row", "row2slot"), got[call], ref):
+            assert torch.equal(g, rr), f"call {call}: {name} differs from hmm_route"
