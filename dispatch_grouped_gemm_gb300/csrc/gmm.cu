@@ -609,35 +609,95 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
 // a token is published once all of its branches have arrived].  After a warp
 // has stored its 32 columns (segment c0 / 32) of o for the token block of a
 // tile, it counts each routed row on its token's counter of that segment;
-// the lane whose count completes the token's KS rows (K, plus the shared
-// expert's row) owns the token's segment, and the warp then sums those rows
-// and writes y.  The sum is the separate combine's, operation for operation:
-// fp32 fmaf over k = 0 .. K-1 in order with the routing weight (slots with an
-// invalid id skipped), then the shared row with weight 1, one bf16 rounding.
+// the count that completes the token's KS rows (K, plus the shared expert's
+// row) makes this warp the owner of the token's segment, and it sums those
+// rows and writes y.  The sum is the separate combine's, operation for
+// operation: fp32 fmaf over k = 0 .. K-1 in order with the routing weight
+// (slots with an invalid id skipped), then the shared row with weight 1, one
+// bf16 rounding.  Every request is issued in batches (all rows' counts at
+// once; per token, the rows of four slots at once): each step is one round
+// trip to L2, not one per row.
+
+// One token's segment: y[t][c0 .. c0 + 31] (columns below N).
 template <bool F32>
-__device__ __forceinline__ void cmb_acc(float (&acc)[8], const void* o, int64_t row, int64_t ld,
-                                        int col, float s) {
-  if constexpr (F32) {
-    const float4* r = reinterpret_cast<const float4*>(static_cast<const float*>(o) + row * ld + col);
-    const float4 a = __ldcg(r), b = __ldcg(r + 1);
-    acc[0] = fmaf(s, a.x, acc[0]); acc[1] = fmaf(s, a.y, acc[1]);
-    acc[2] = fmaf(s, a.z, acc[2]); acc[3] = fmaf(s, a.w, acc[3]);
-    acc[4] = fmaf(s, b.x, acc[4]); acc[5] = fmaf(s, b.y, acc[5]);
-    acc[6] = fmaf(s, b.z, acc[6]); acc[7] = fmaf(s, b.w, acc[7]);
-  } else {
-    const uint4 v = __ldcg(reinterpret_cast<const uint4*>(
-        static_cast<const __nv_bfloat16*>(o) + row * ld + col));
-    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+__device__ __forceinline__ void finish_token(const Prob& pr, int t, int c0) {
+  constexpr int VPR = F32 ? 8 : 4;  // 16-byte vectors per row of 32 columns
+  constexpr int KB = F32 ? 2 : 4;   // slots whose rows are loaded together
+  float acc[32];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      acc[2 * j] = fmaf(s, bf16_lo(u[j]), acc[2 * j]);
-      acc[2 * j + 1] = fmaf(s, bf16_hi(u[j]), acc[2 * j + 1]);
+  for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+  const int K = pr.cmb_K;
+  const int ncv = min(32, pr.N - c0) / 8;  // 8-column groups inside N
+  auto add_rows = [&](const int32_t (&pk)[KB], const float (&wk)[KB]) {
+    uint4 v[KB][VPR];
+#pragma unroll
+    for (int j = 0; j < KB; ++j)
+#pragma unroll
+      for (int q = 0; q < VPR; ++q) {
+        v[j][q] = make_uint4(0, 0, 0, 0);
+        if (pk[j] >= 0 && q < (F32 ? 2 * ncv : ncv)) {
+          const uint8_t* base = static_cast<const uint8_t*>(pr.out) +
+                                (static_cast<int64_t>(pk[j]) * pr.ld_out + c0) * (F32 ? 4 : 2);
+          v[j][q] = __ldcg(reinterpret_cast<const uint4*>(base) + q);
+        }
+      }
+#pragma unroll
+    for (int j = 0; j < KB; ++j) {
+      if (pk[j] < 0) continue;
+      const float s = wk[j];
+#pragma unroll
+      for (int q = 0; q < VPR; ++q) {
+        const uint32_t u[4] = {v[j][q].x, v[j][q].y, v[j][q].z, v[j][q].w};
+        if constexpr (F32) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[4 * q + i] = fmaf(s, __uint_as_float(u[i]), acc[4 * q + i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[8 * q + 2 * i] = fmaf(s, bf16_lo(u[i]), acc[8 * q + 2 * i]);
+            acc[8 * q + 2 * i + 1] = fmaf(s, bf16_hi(u[i]), acc[8 * q + 2 * i + 1]);
+          }
+        }
+      }
     }
+  };
+  for (int k0 = 0; k0 < K; k0 += KB) {
+    int32_t pk[KB];
+    float wk[KB];
+#pragma unroll
+    for (int j = 0; j < KB; ++j) {
+      const int k = k0 + j;
+      pk[j] = -1;
+      wk[j] = 0.0f;
+      if (k < K) {
+        const int64_t sk = static_cast<int64_t>(t) * K + k;
+        pk[j] = pr.slot2prow[sk];
+        wk[j] = pr.cmb_w_f32 ? static_cast<const float*>(pr.cmb_w)[sk]
+                             : bf16_lo(static_cast<const uint16_t*>(pr.cmb_w)[sk]);
+      }
+    }
+    add_rows(pk, wk);
   }
+  if (pr.cmb_KS > K) {
+    int32_t pk[KB];
+    float wk[KB];
+#pragma unroll
+    for (int j = 0; j < KB; ++j) {
+      pk[j] = j == 0 ? pr.cmb_poff[pr.cmb_E] + t : -1;
+      wk[j] = 1.0f;
+    }
+    add_rows(pk, wk);
+  }
+  __nv_bfloat16* yr = static_cast<__nv_bfloat16*>(pr.cmb_y) + static_cast<int64_t>(t) * pr.N + c0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (q < ncv) reinterpret_cast<uint4*>(yr)[q] = pack_bf16x8(acc + 8 * q);
 }
 
+// list: this warp's shared-memory scratch (NT ints).
 template <bool F32>
-__device__ __noinline__ void combine_tile(const Prob& pr, const TileInfo& ti, int c0, int lane) {
+__device__ __noinline__ void combine_tile(const Prob& pr, const TileInfo& ti, int c0, int lane,
+                                          int* list) {
   if (c0 >= pr.N) return;
   const int seg = c0 >> 5;
   const bool shared = ti.e == pr.cmb_E;
@@ -645,50 +705,41 @@ __device__ __noinline__ void combine_tile(const Prob& pr, const TileInfo& ti, in
   // this warp's stores of o are visible at gpu scope before its counts
   __threadfence();
   __syncwarp();
-#pragma unroll 1
-  for (int j = 0; j < ti.nrow; j += 32) {
-    const int64_t prow = ti.row0 + j + lane;
-    int t = -1;
-    if (shared) {
-      if (prow - srow0 < pr.cmb_T) t = static_cast<int>(prow - srow0);
-    } else {
-      const int32_t sl = pr.prow2slot[prow];
-      if (sl >= 0) t = sl / pr.cmb_K;
-    }
-    bool fin = false;
-    if (t >= 0)
-      fin = atomicAdd(&pr.cmb[static_cast<int64_t>(t) * pr.cmb_nseg + seg], 1) == pr.cmb_KS - 1;
-    const unsigned fmask = __ballot_sync(0xffffffffu, fin);
-    if (fmask == 0) continue;
-    __threadfence();  // the other rows of the completed segments, written by other warps
-    const int nfin = __popc(fmask);
-    const int g = lane >> 2;                // eight tokens per pass,
-    const int col = c0 + 8 * (lane & 3);    // four lanes of eight columns each
-#pragma unroll 1
-    for (int base = 0; base < nfin; base += 8) {
-      const int idx = base + g;
-      const int src = idx < nfin ? static_cast<int>(__fns(fmask, 0, idx + 1)) : 0;
-      const int tt = __shfl_sync(0xffffffffu, t, src);
-      if (idx < nfin && col < pr.N) {
-        float acc[8];
+  // every row of the block at once (lane l: rows l, l + 32, ...)
+  constexpr int MAXG = NT / 32;
+  int tk[MAXG], old[MAXG];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-        for (int k = 0; k < pr.cmb_K; ++k) {
-          const int64_t sk = static_cast<int64_t>(tt) * pr.cmb_K + k;
-          const int32_t pk = pr.slot2prow[sk];
-          const float w = pr.cmb_w_f32
-                              ? static_cast<const float*>(pr.cmb_w)[sk]
-                              : bf16_lo(static_cast<const uint16_t*>(pr.cmb_w)[sk]);
-          if (pk < 0) continue;
-          cmb_acc<F32>(acc, pr.out, pk, pr.ld_out, col, w);
-        }
-        if (pr.cmb_KS > pr.cmb_K)
-          cmb_acc<F32>(acc, pr.out, pr.cmb_poff[pr.cmb_E] + tt, pr.ld_out, col, 1.0f);
-        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(pr.cmb_y) +
-                                  static_cast<int64_t>(tt) * pr.N + col) = pack_bf16x8(acc);
+  for (int i = 0; i < MAXG; ++i) {
+    tk[i] = -1;
+    if (32 * i < ti.nrow) {
+      const int64_t prow = ti.row0 + 32 * i + lane;
+      if (shared) {
+        if (prow - srow0 < pr.cmb_T) tk[i] = static_cast<int>(prow - srow0);
+      } else {
+        const int32_t sl = pr.prow2slot[prow];
+        if (sl >= 0) tk[i] = sl / pr.cmb_K;
       }
     }
   }
+#pragma unroll
+  for (int i = 0; i < MAXG; ++i)
+    old[i] = tk[i] >= 0 ? atomicAdd(&pr.cmb[static_cast<int64_t>(tk[i]) * pr.cmb_nseg + seg], 1)
+                        : -1;
+  // the tokens whose segment this warp completed, compacted
+  int nfin = 0;
+#pragma unroll
+  for (int i = 0; i < MAXG; ++i) {
+    const bool f = old[i] == pr.cmb_KS - 1;
+    const unsigned m = __ballot_sync(0xffffffffu, f);
+    if (f) list[nfin + __popc(m & ((1u << lane) - 1u))] = tk[i];
+    nfin += __popc(m);
+  }
+  if (nfin == 0) return;
+  __syncwarp();
+  __threadfence();  // the other rows of the completed segments, written by other warps
+  for (int b = 0; b < nfin; b += 32)
+    if (b + lane < nfin) finish_token<F32>(pr, list[b + lane], c0);
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------- kernel
@@ -1048,10 +1099,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (pr.cmb) {
         // after the accumulator's release: this overlaps the next tile's MMAs
         const int c0 = ti.w0 + C1::WCOLS * static_cast<int>(rank) + 32 * es.q;
+        int* list = reinterpret_cast<int*>(xbufs + es.q * (XBUF_BYTES / 4));
         if (pr.out_f32)
-          combine_tile<true>(pr, ti, c0, lane);
+          combine_tile<true>(pr, ti, c0, lane, list);
         else
-          combine_tile<false>(pr, ti, c0, lane);
+          combine_tile<false>(pr, ti, c0, lane, list);
       }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
