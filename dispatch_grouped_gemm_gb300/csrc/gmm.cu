@@ -164,8 +164,13 @@ struct Params {
   int trace_cap;
 };
 
+// Token-row maps by block size: t[q][i] loads the token rows of a block of
+// 64 (i + 1) rows, in one box per CTA (pairs: the CTA's half, 32 (i + 1)
+// rows; single CTAs: all of them; small blocks: i = 0 only).
+constexpr int TOK_MAPS = NT / TROWS;
 struct Maps {
-  CUtensorMap m[MAX_PROB][2];  // token rows, weights
+  CUtensorMap w[MAX_PROB];            // weights
+  CUtensorMap t[MAX_PROB][TOK_MAPS];  // token rows
 };
 
 struct TileInfo {
@@ -273,20 +278,20 @@ __device__ void decode_tile(const Params& P, const Prob& pr, int e, int r, TileI
 // coordinate that is a multiple of 8 elements (16 bytes).
 //   PAIR: this CTA's share (its weight columns, its half of the token rows),
 //   counted on the even CTA's full barrier (shared::cluster address bar_cl;
-//   the even CTA arms it for both).  A 128-row token box always lands whole;
-//   the MMA reads the rows it needs.  (64-row boxes sized to each tile cut the
-//   bytes of tiles under 256 rows but made both launches slower: the
-//   pipeline is bound by the latency of a stage's loads, not their bytes.)
+//   the even CTA arms it for both).  The token rows come in one box of exactly
+//   the rows the MMA reads (tT: the map of this block size).  Returns the
+//   bytes this CTA loads.
 template <class C, bool PAIR, bool SMALL>
-__device__ __forceinline__ void load_stage(const Prob& pr, const TileInfo& ti, int kb,
-                                           const CUtensorMap* tT, const CUtensorMap* tW,
-                                           uint8_t* sW, uint8_t* sT, uint64_t* bar,
-                                           uint32_t bar_cl, uint32_t rank) {
+__device__ __forceinline__ uint32_t load_stage(const Prob& pr, const TileInfo& ti, int kb,
+                                               const CUtensorMap* tT, const CUtensorMap* tW,
+                                               uint8_t* sW, uint8_t* sT, uint64_t* bar,
+                                               uint32_t bar_cl, uint32_t rank) {
   const int k = kb * BK;
   const int eb = ti.e - pr.e_lo;  // expert index inside this problem's weight slabs
   const int wc = ti.w0 + C::WCOLS * static_cast<int>(rank);  // this CTA's first column
   if constexpr (PAIR) {
-    if (rank == 0) mbar_arrive_expect_tx(bar, 2 * (W_BYTES + PAIR_T_BYTES));
+    const uint32_t bytes = W_BYTES + (ti.nrow / 2) * BK * 2;
+    if (rank == 0) mbar_arrive_expect_tx(bar, 2 * bytes);
     if constexpr (C::W_MN) {
       // SwiGLU: 64 gate columns, then the same 64 up columns
       const int c2 = C::EPI == EPI_SWIGLU ? pr.half + wc : wc + 64;
@@ -296,10 +301,11 @@ __device__ __forceinline__ void load_stage(const Prob& pr, const TileInfo& ti, i
       tma_load_3d_pair(sW, tW, bar_cl, k, wc, eb);
     }
     tma_load_2d_pair(sT, tT, bar_cl, k, ti.row0 + (ti.nrow / 2) * static_cast<int>(rank));
+    return bytes;
   } else {
-    // small mode: one 64-row box; else one or two 128-row boxes
-    const bool two = !SMALL && ti.nrow > NT / 2;
-    mbar_arrive_expect_tx(bar, W_BYTES + (SMALL ? SMALL_T_BYTES : (two ? 2 : 1) * PAIR_T_BYTES));
+    // one box of the block's rows (small mode: 64)
+    const uint32_t bytes = W_BYTES + ti.nrow * BK * 2;
+    mbar_arrive_expect_tx(bar, bytes);
     if constexpr (C::W_MN) {
       const int c2 = C::EPI == EPI_SWIGLU ? pr.half + wc : wc + 64;
       tma_load_3d(sW, tW, bar, wc, k, eb);
@@ -308,7 +314,7 @@ __device__ __forceinline__ void load_stage(const Prob& pr, const TileInfo& ti, i
       tma_load_3d(sW, tW, bar, k, wc, eb);
     }
     tma_load_2d(sT, tT, bar, k, ti.row0);
-    if (two) tma_load_2d(sT + PAIR_T_BYTES, tT, bar, k, ti.row0 + NT / 2);
+    return bytes;
   }
 }
 
@@ -758,13 +764,6 @@ __device__ __noinline__ void combine_tile(const Prob& pr, const TileInfo& ti, in
   } else {                        \
     F<C1, PAIR>(__VA_ARGS__);     \
   }
-#define HMM_BY_PROB_PS(q, F, ...)     \
-  if (((q) & 1) == 0) {               \
-    F<C0, PAIR, SMALL>(__VA_ARGS__);  \
-  } else {                            \
-    F<C1, PAIR, SMALL>(__VA_ARGS__);  \
-  }
-
 template <bool PAIR, bool SMALL, class C0, class C1>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gmm_kernel(const __grid_constant__ Params P, const __grid_constant__ Maps maps) {
@@ -791,8 +790,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_ti + TI_DEPTH);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   uint32_t* s_issued = s_tmem + 2;  // K blocks this CTA's producer issued
-  uint32_t* s_peer = s_tmem + 3;    // [2] even CTA of a pair: the odd CTA's count, abort flag
-  int* s_pref = reinterpret_cast<int*>(s_tmem + 6);  // [steps + 1]
+  uint32_t* s_sbytes = s_tmem + 3;  // [MAX_STAGES] bytes of this CTA's last loads per slot
+  // [2 + MAX_STAGES] even CTA of a pair: the odd CTA's count, abort flag, bytes per slot
+  uint32_t* s_peer = s_sbytes + MAX_STAGES;
+  int* s_pref = reinterpret_cast<int*>(s_peer + 2 + MAX_STAGES);  // [steps + 1]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -821,7 +822,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     *s_abort = 0;
     *s_issued = 0;
-    s_peer[0] = s_peer[1] = 0;
+    for (int i = 0; i < 2 + MAX_STAGES; ++i) s_peer[i] = 0;
+    for (int i = 0; i < MAX_STAGES; ++i) s_sbytes[i] = 0;
     fence_mbar_init();
   }
   if constexpr (PAIR) cluster_sync_all();  // barriers initialised before any remote arrive
@@ -921,10 +923,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------- TMA producer
-      for (int q = 0; q < P.nprob; ++q) {
-        tma_prefetch_desc(&maps.m[q][0]);
-        tma_prefetch_desc(&maps.m[q][1]);
-      }
+      for (int q = 0; q < P.nprob; ++q) tma_prefetch_desc(&maps.w[q]);
       uint32_t stage = 0, sphase = 0;
       int ti_slot = 0;
       uint32_t ti_phase = 0;
@@ -947,7 +946,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // the scheduler acquired this tile's ready counter (gpu scope) before
         // publishing it; order that with the async-proxy loads below
         if (pr.wait_m) fence_proxy_async_global();
-        const CUtensorMap* mp = maps.m[ti.prob];
+        const CUtensorMap* tW = &maps.w[ti.prob];
+        const CUtensorMap* tT = &maps.t[ti.prob][ti.nrow / TROWS - 1];
         uint64_t* rec = (!PAIR || leader) ? trace_rec(P, lt) : nullptr;
         ++lt;
         for (int kb = 0; kb < ti.kb; ++kb) {
@@ -958,8 +958,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (rec && kb == 0) rec[2] = globaltimer_ns();
           uint8_t* sW = stages + stage * SBYTES;
           const uint32_t full_cl = PAIR ? mapa_shared(smem_u32(&full[stage]), 0) : 0u;
-          HMM_BY_PROB_PS(ti.prob, load_stage, pr, ti, kb, &mp[0], &mp[1], sW, sW + W_BYTES,
-                         &full[stage], full_cl, rank);
+          uint32_t bytes = 0;
+          if ((ti.prob & 1) == 0)
+            bytes = load_stage<C0, PAIR, SMALL>(pr, ti, kb, tT, tW, sW, sW + W_BYTES,
+                                                &full[stage], full_cl, rank);
+          else
+            bytes = load_stage<C1, PAIR, SMALL>(pr, ti, kb, tT, tW, sW, sW + W_BYTES,
+                                                &full[stage], full_cl, rank);
+          s_sbytes[stage] = bytes;
           ++issued;
           if (++stage == NST) {
             stage = 0;
@@ -1114,8 +1120,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   // no copy of either CTA in flight, no peer access to our smem or TMEM after this
   if constexpr (PAIR)
-    pair_teardown<NST>(leader, *s_issued, *s_abort, s_peer, full, W_BYTES + PAIR_T_BYTES,
-                       P.budget_ns);
+    pair_teardown<NST>(leader, *s_issued, *s_abort, s_peer, s_sbytes, full, P.budget_ns);
   if (warp == 1) {
     tc_fence_after();
     if constexpr (PAIR)
@@ -1233,11 +1238,27 @@ void add_shared(Params& P, Maps& maps, int E, const CUtensorMap& B0, const CUten
     P.p[2 + q] = P.p[q];
     P.p[2 + q].e_lo = E;
     P.p[2 + q].e_hi = E + 1;
-    maps.m[2 + q][0] = maps.m[q][0];
+    for (int i = 0; i < TOK_MAPS; ++i) maps.t[2 + q][i] = maps.t[q][i];
   }
-  maps.m[2][1] = B0;
-  maps.m[3][1] = B1;
+  maps.w[2] = B0;
+  maps.w[3] = B1;
   P.nprob = 4;
+}
+
+// The token-row maps of an activation [rows, cols] for the launch's mode:
+// boxes of the rows one CTA loads for a block of 64 (i + 1) rows.
+int map_tokens(const GemmEnv& env, CUtensorMap* t, const void* base, int64_t rows,
+               int64_t cols) {
+  int rc = HMM_OK;
+  for (int i = 0; i < TOK_MAPS; ++i) {
+    if (env.small_rows && i > 0) {
+      t[i] = t[0];  // small token blocks are 64 rows
+      continue;
+    }
+    const uint32_t box = env.pair_rows ? 32u * (i + 1) : 64u * (i + 1);
+    rc |= map_act(env, &t[i], base, rows, cols, box);
+  }
+  return rc;
 }
 
 }  // namespace
@@ -1249,11 +1270,10 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
   const int64_t H = p.H, I = p.I, E = p.E, R = p.R;
   Maps maps;
   int rc = HMM_OK;
-  const uint32_t tbox = env.small_rows ? SMALL_NT : NT / 2;     // token rows per box
-  rc |= map_act(env, &maps.m[0][0], x_perm, R, H, tbox);  // x_perm [R, H], K = H
-  rc |= map_w(env, &maps.m[0][1], W1, E, H, 2 * I, 64);   // W1 [E, H, 2I]: MN-major
-  rc |= map_act(env, &maps.m[1][0], a, R, I, tbox);       // a [R, I], K = I
-  rc |= map_w(env, &maps.m[1][1], W2, E, I, H, 64);         // W2 [E, I, H]: MN-major
+  rc |= map_tokens(env, maps.t[0], x_perm, R, H);        // x_perm [R, H], K = H
+  rc |= map_w(env, &maps.w[0], W1, E, H, 2 * I, 64);      // W1 [E, H, 2I]: MN-major
+  rc |= map_tokens(env, maps.t[1], a, R, I);              // a [R, I], K = I
+  rc |= map_w(env, &maps.w[1], W2, E, I, H, 64);          // W2 [E, I, H]: MN-major
   CUtensorMap s0, s1;
   if (p.shared) {
     rc |= map_w(env, &s0, Ws1, 1, H, 2 * I, 64);  // shared expert's [H, 2I], [I, H]
@@ -1323,12 +1343,11 @@ int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPt
   Maps maps;
   int rc = HMM_OK;
   // act_grad: G = dy_perm . W2^T   (weights: 128 rows of W2 [E, I, H] per CTA, N = I)
-  const uint32_t tbox = env.small_rows ? SMALL_NT : NT / 2;  // token rows per box
-  rc |= map_act(env, &maps.m[0][0], dy_perm, R, H, tbox);
-  rc |= map_w(env, &maps.m[0][1], W2, E, I, H, BW);
+  rc |= map_tokens(env, maps.t[0], dy_perm, R, H);
+  rc |= map_w(env, &maps.w[0], W2, E, I, H, BW);
   // input-grad: dX_perm = dH . W1^T (weights: 128 rows of W1 [E, H, 2I] per CTA, N = H)
-  rc |= map_act(env, &maps.m[1][0], dH, R, 2 * I, tbox);
-  rc |= map_w(env, &maps.m[1][1], W1, E, H, 2 * I, BW);
+  rc |= map_tokens(env, maps.t[1], dH, R, 2 * I);
+  rc |= map_w(env, &maps.w[1], W1, E, H, 2 * I, BW);
   CUtensorMap s0, s1;
   if (p.shared) {
     rc |= map_w(env, &s0, Ws2, 1, I, H, BW);

@@ -204,7 +204,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_ti + P_TI_DEPTH);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   uint32_t* s_issued = s_tmem + 2;  // K blocks this CTA's producer issued
-  uint32_t* s_peer = s_tmem + 3;    // [2] even CTA: the odd CTA's count and abort flag
+  uint32_t* s_sbytes = s_tmem + 3;  // [PSTAGES] bytes of this CTA's loads per slot (fixed)
+  uint32_t* s_peer = s_sbytes + PSTAGES;  // [2 + PSTAGES] even CTA: the odd CTA's count, flag, bytes
   int* s_cnt = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + 1024);
   int* s_ord = s_cnt + (MAX_E + 1);
   int* s_pre = s_ord + (MAX_E + 1);
@@ -232,7 +233,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     }
     *s_abort = 0;
     *s_issued = 0;
-    s_peer[0] = s_peer[1] = 0;
+    for (int i = 0; i < PSTAGES; ++i) s_sbytes[i] = PSTAGE;
+    for (int i = 0; i < 2 + PSTAGES; ++i) s_peer[i] = 0;
     fence_mbar_init();
   }
   cluster_sync_all();  // the peer's barriers are initialised before any remote arrive
@@ -551,7 +553,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   // no copy of either CTA in flight, no peer access to our smem or TMEM after this
-  pair_teardown<PSTAGES>(leader, *s_issued, *s_abort, s_peer, full, PSTAGE, P.budget_ns);
+  pair_teardown<PSTAGES>(leader, *s_issued, *s_abort, s_peer, s_sbytes, full, P.budget_ns);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, P_TMEM_COLS);  // collective, like the allocation

@@ -470,15 +470,16 @@ static __device__ __noinline__ void drain_wait(uint64_t* bar, uint32_t parity, u
 }
 
 // Teardown of a CTA pair whose TMA loads are counted on the even CTA's full
-// barriers (each CTA loads cta_bytes per K block; the even CTA arms every
-// stage it issues for both).  After an abort the two producers may have left
-// their loops after different numbers of K blocks, so loads of the odd CTA
-// can still be in flight (into its own shared memory) or stages the even CTA
-// armed may wait for bytes the odd CTA never requested.  Protocol (called by
-// every thread of both CTAs, after their roles have finished and a
-// __syncthreads):
-//   1. the odd CTA's thread 0 writes its issued K blocks and abort flag into
-//      the even CTA's shared memory; a cluster barrier publishes them;
+// barriers (the even CTA arms every stage it issues for both CTAs' bytes, the
+// two CTAs loading equal shares of a stage).  After an abort the two
+// producers may have left their loops after different numbers of K blocks,
+// so loads of the odd CTA can still be in flight (into its own shared
+// memory) or stages the even CTA armed may wait for bytes the odd CTA never
+// requested.  Protocol (called by every thread of both CTAs, after their
+// roles have finished and a __syncthreads):
+//   1. the odd CTA's thread 0 writes its issued K blocks, abort flag and
+//      bytes per slot into the even CTA's shared memory; a cluster barrier
+//      publishes them;
 //   2. if either CTA aborted, the even CTA's thread 0 arms the stages only
 //      the odd CTA issued (for the odd CTA's bytes), completes the odd CTA's
 //      share of the stages only it issued, and waits (bounded) for the last
@@ -486,25 +487,29 @@ static __device__ __noinline__ void drain_wait(uint64_t* bar, uint32_t parity, u
 //      their slot was reused, so after this no copy of either CTA is in
 //      flight;
 //   3. a second cluster barrier holds the odd CTA until then.
-// peer[0], peer[1]: the even CTA's slots for the odd CTA's count and flag.
+// peer: the even CTA's [2 + NST] slots for the odd CTA's count, flag and
+// bytes; sbytes: this CTA's bytes of its last load into each slot.
 template <int NST>
 __device__ __forceinline__ void pair_teardown(bool leader, uint32_t issued, int aborted,
-                                              uint32_t* peer, uint64_t* full, uint32_t cta_bytes,
-                                              uint64_t budget_ns) {
+                                              uint32_t* peer, const uint32_t* sbytes,
+                                              uint64_t* full, uint64_t budget_ns) {
   if (!leader && threadIdx.x == 0) {
     st_shared_cluster(mapa_shared(smem_u32(&peer[0]), 0), static_cast<int>(issued));
     st_shared_cluster(mapa_shared(smem_u32(&peer[1]), 0), aborted);
+    for (int i = 0; i < NST; ++i)
+      st_shared_cluster(mapa_shared(smem_u32(&peer[2 + i]), 0), static_cast<int>(sbytes[i]));
   }
   cluster_sync_all();
   if (leader && threadIdx.x == 0 && (aborted || peer[1])) {
     const uint32_t n_e = issued, n_o = peer[0];
     const uint32_t n = n_e > n_o ? n_e : n_o;
     for (uint32_t k = n > NST ? n - NST : 0u; k < n; ++k) {
-      uint64_t* b = &full[k % NST];
+      const uint32_t slot = k % NST;
+      uint64_t* b = &full[slot];
       if (k >= n_e)
-        mbar_arrive_expect_tx(b, cta_bytes);  // never armed: count the odd CTA's bytes
+        mbar_arrive_expect_tx(b, peer[2 + slot]);  // never armed: the odd CTA's bytes
       else if (k >= n_o)
-        mbar_complete_tx(b, cta_bytes);       // armed for both, loaded by the even CTA only
+        mbar_complete_tx(b, sbytes[slot]);         // armed for both, loaded by the even CTA only
       drain_wait(b, (k / NST) & 1u, budget_ns);
     }
   }
