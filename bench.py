@@ -468,6 +468,73 @@ SUB = {
 }
 
 
+def unfused_chain(wl, flush, n=20):
+    """The same MoE-FFN step as a chain of separate library operations on the
+    GPU (torch: an index gather for the dispatch, one cuBLAS GEMM per expert
+    for GMM1 and for GMM2, SwiGLU as elementwise ops, an index_add combine in
+    fp32; the backward through autograd): the unfused reference the
+    HyperMegaMoE performance acceptance compares the fused operator with.  A
+    comparison arm only: the fused path never calls it."""
+    import torch
+    import torch.nn.functional as F
+    T, H, I, E, K = wl.T, wl.H, wl.I, wl.E, wl.K
+    W1 = wl.W1.detach().clone().requires_grad_()
+    W2 = wl.W2.detach().clone().requires_grad_()
+    x = wl.x.detach().clone().requires_grad_()
+    w = wl.w.detach().clone().requires_grad_()
+    ids = wl.ids
+    dy = wl.dy
+
+    def step(backward):
+        flat = ids.reshape(-1).long()
+        order = torch.argsort(flat, stable=True)
+        counts = torch.bincount(flat, minlength=E).tolist()  # host sync, as a plain chain has
+        tok = order // K
+        xs = x[tok]
+        # per-expert views (unbind: the backward stacks the experts' gradients
+        # once instead of a full-size gradient per indexed expert)
+        W1s, W2s = W1.unbind(0), W2.unbind(0)
+        outs = []
+        r0 = 0
+        for e in range(E):
+            r1 = r0 + counts[e]
+            if r1 > r0:
+                h = xs[r0:r1] @ W1s[e]
+                a = F.silu(h[:, :I]) * h[:, I:]
+                outs.append(a @ W2s[e])
+            r0 = r1
+        o = torch.cat(outs)
+        ws = w.reshape(-1)[order].float()
+        y = torch.zeros((T, H), dtype=torch.float32, device=x.device)
+        y = y.index_add(0, tok, o.float() * ws[:, None]).to(torch.bfloat16)
+        if backward:
+            y.backward(dy)
+        return y
+
+    res = {}
+    for mode in ("forward", "fwd_bwd"):
+        bw = mode == "fwd_bwd"
+        with torch.set_grad_enabled(bw):
+            for _ in range(3):
+                step(bw)
+            torch.cuda.synchronize()
+            ev = []
+            for _ in range(n):
+                flush.zero_()
+                s0 = torch.cuda.Event(enable_timing=True)
+                s1 = torch.cuda.Event(enable_timing=True)
+                s0.record()
+                step(bw)
+                s1.record()
+                ev.append((s0, s1))
+        torch.cuda.synchronize()
+        res[f"{mode}_ms"] = sum(a.elapsed_time(b) for a, b in ev) / n
+        x.grad = W1.grad = W2.grad = w.grad = None
+    res["ops"] = ("torch on the GPU: gather, per-expert cuBLAS GEMMs, elementwise SwiGLU, "
+                  "fp32 index_add combine; backward by autograd")
+    return res
+
+
 def run_sub(name, hmm, mi, dev, stream, flush, dist, peaks, uniform_phases=None):
     import torch
     cfg, fwd_only, n = SUB[name]
@@ -704,6 +771,12 @@ def run_ours(args, dist: Dist):
     if args.shape:
         out["config"]["workload"] = f"profiling case T={T} H={H} I={I} E={E} K={K}"
     if not args.no_sub:
+        # the fused step against the same step as an unfused chain of library ops
+        uc = unfused_chain(wl, flush)
+        uc["fused_fwd_bwd_ms"] = step_ms_max
+        uc["fused_speedup_fwd_bwd"] = uc["fwd_bwd_ms"] / step_ms_max
+        uc["fused_speedup_forward"] = uc["forward_ms"] / fwd_ms
+        out["unfused_chain"] = uc
         # the other workloads of the acceptance list, each in its own timed loop
         del wl
         torch.cuda.empty_cache()
