@@ -43,6 +43,26 @@ __device__ __forceinline__ void xread(const float* buf, int lane, float (&o)[4][
   }
 }
 
+// Half blocks (16 rows x 32 columns) for two warps per TMEM lane quarter:
+// thread t writes its 16 values down column t of a 16-row buffer (XBUF_HALF
+// bytes per warp), then lane l reads the eight columns 8*(l & 3) .. +7 of
+// the rows (l >> 2) + 8k, k = 0, 1.
+constexpr int XBUF_HALF = 16 * XS * 4;
+__device__ __forceinline__ void xwrite_t16(float* buf, int lane, const uint32_t (&r)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) buf[i * XS + lane] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void xread16(const float* buf, int lane, float (&o)[2][8]) {
+  const float* s = buf + (lane >> 2) * XS + (lane & 3) * 8;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const float4 a = *reinterpret_cast<const float4*>(s + k * 8 * XS);
+    const float4 b = *reinterpret_cast<const float4*>(s + k * 8 * XS + 4);
+    o[k][0] = a.x; o[k][1] = a.y; o[k][2] = a.z; o[k][3] = a.w;
+    o[k][4] = b.x; o[k][5] = b.y; o[k][6] = b.z; o[k][7] = b.w;
+  }
+}
+
 __device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
   uint4 u;
   u.x = pack_bf16(v[0], v[1]);

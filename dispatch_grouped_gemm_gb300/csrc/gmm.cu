@@ -99,13 +99,11 @@ constexpr int MAX_STAGES = SMALL_STAGES;
 static_assert(PAIR_STAGES * PAIR_STAGE_BYTES <= STAGES * STAGE_BYTES, "pair stages");
 static_assert(SMALL_STAGES * SMALL_STAGE_BYTES <= STAGES * STAGE_BYTES, "small stages");
 constexpr int TI_DEPTH = 3;
-// Warp roles: 0 TMA producer, 1 MMA issuer, 2..5 epilogue (one per TMEM lane
-// quarter), 6 tile scheduler.  (Eight epilogue warps, two per quarter, were
-// measured slower: every SM sub-partition then runs two epilogue warps beside
-// the single-thread MMA and TMA loops.)
-constexpr int EPI_WARPS = 4;
-constexpr int SCHED_WARP = 2 + EPI_WARPS;
-constexpr int NUM_THREADS = 32 * (SCHED_WARP + 1);  // 7 warps
+// Warp roles: 0 TMA producer, 1 MMA issuer, 2 .. 1 + EW epilogue (EW = 4: one
+// per TMEM lane quarter; EW = 8, the data-gradient launch: two per quarter,
+// each with 16 rows of every chunk), 2 + EW tile scheduler.
+constexpr int EPI_WARPS = 4;  // the four lane quarters (shared-memory buffers of all EW)
+__host__ __device__ constexpr int gmm_threads(int ew) { return 32 * (ew + 3); }
 constexpr int MAX_PROB = 4;
 constexpr int MAX_STEPS = 2 * MAX_E + 8;
 // alignment slack + stages + epilogue buffers + barriers, tile-info ring and
@@ -383,6 +381,8 @@ __device__ __forceinline__ void store_f32x8(float* dst, const float* v) {
 struct EpiState {
   int q;            // TMEM lane quarter of this warp
   int lane;
+  int hoff;         // eight epilogue warps: the warp's 16 rows of each 32-row chunk (0, 16)
+  float* own;       // this warp's transposition buffer
   float* xbufs;     // the four quarters' transposition buffers
   uint64_t* xfull;  // [2], per gate quarter
   uint64_t* xfree;  // [2]
@@ -406,16 +406,41 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int la
 // the rows (l >> 2) + 8 k.  Column chunks are skipped per lane with plain
 // conditionals, never an early exit: the next chunk's TMEM load is a
 // warp-wide instruction.  ok turns false when a bounded wait gave up.
-template <class C>
+//   EW = 8 (two warps per lane quarter; STORE and SwiGLU grad only): each
+// warp takes 16 rows of every chunk (es.hoff), through a 16-row buffer, and
+// lane l holds columns 8 (l & 3) .. + 7 of the rows (l >> 2) + 8 k, k < 2.
+template <class C, int EW>
 __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti, uint32_t taddr,
                                               uint32_t rank, EpiState& es, const WaitCtl& wc,
                                               bool& ok) {
+  static_assert(EW == 4 || (EW == 8 && C::EPI != EPI_SWIGLU), "epilogue warps");
+  constexpr int KR = EW == 8 ? 2 : 4;  // rows per lane and chunk
   const int cta_col0 = ti.w0 + C::WCOLS * static_cast<int>(rank);
   const int lane = es.lane;
   const int q = es.q;
+  const int hoff = EW == 8 ? es.hoff : 0;
   const int cg = (lane & 3) * 8;  // this lane's first column within a 32-column block
   const int nch = ti.nrow / 32;
-  float* own = es.xbufs + q * (XBUF_BYTES / 4);
+  float* own = es.own;
+  // this warp's rows of chunk j from TMEM, transposed: v[k] = row (l >> 2) + 8 k
+  auto load_chunk = [&](int j, float (&v)[KR][8]) {
+    if constexpr (EW == 8) {
+      uint32_t r[16];
+      tmem_ld16(taddr + j * 32 + hoff, r);
+      tmem_ld_wait();
+      xwrite_t16(own, lane, r);
+      __syncwarp();
+      xread16(own, lane, v);
+    } else {
+      uint32_t r[32];
+      tmem_ld32(taddr + j * 32, r);
+      tmem_ld_wait();
+      xwrite_t(own, lane, r);
+      __syncwarp();
+      xread(own, lane, v);
+    }
+    __syncwarp();
+  };
   if constexpr (C::EPI == EPI_SWIGLU) {
     // a = silu(gate) * up of I columns c .. c + 7; training also saves the
     // fp32 pre-activations (blocked layout)
@@ -481,18 +506,12 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
     const int c = cta_col0 + 32 * q + cg;
 #pragma unroll 1
     for (int j = 0; j < nch; ++j) {
-      uint32_t r[32];
-      tmem_ld32(taddr + j * 32, r);
-      tmem_ld_wait();
-      float v[4][8];
-      xwrite_t(own, lane, r);
-      __syncwarp();
-      xread(own, lane, v);
-      __syncwarp();
+      float v[KR][8];
+      load_chunk(j, v);
       if (c < pr.N) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int64_t row = ti.row0 + 32 * j + (lane >> 2) + 8 * k;
+        for (int k = 0; k < KR; ++k) {
+          const int64_t row = ti.row0 + 32 * j + hoff + (lane >> 2) + 8 * k;
           if (pr.out_f32)
             store_f32x8(static_cast<float*>(pr.out) + row * pr.ld_out + c, v[k]);
           else
@@ -515,12 +534,12 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
     const int c0 = cta_col0 + 32 * q;
     const int c = c0 + cg;
     const bool colok = c < pr.N;
-    float4 gn[4][2], un[4][2];
-    float wn[4];
+    float4 gn[KR][2], un[KR][2];
+    float wn[KR];
     auto load_h = [&](int j) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int64_t row = ti.row0 + 32 * j + (lane >> 2) + 8 * k;
+      for (int k = 0; k < KR; ++k) {
+        const int64_t row = ti.row0 + 32 * j + hoff + (lane >> 2) + 8 * k;
         const float4* p = reinterpret_cast<const float4*>(hb + hblock_offset(row, c, pr.ld_aux));
         const float4* pu = p + 256;  // the up block follows the gate block
         const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -537,8 +556,14 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
     auto prefetch_h = [&](int j) {
       const int64_t row = ti.row0 + 32 * j;
       const char* blk = reinterpret_cast<const char*>(hb + hblock_offset(row, c0, pr.ld_aux));
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(blk + lane * 128));
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(blk + 4096 + lane * 128));
+      if constexpr (EW == 8) {
+        // this warp's 16 rows: lanes 0-15 the gate lines, 16-31 the up lines
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(blk + (lane >> 4) * 4096 +
+                                                       (hoff + (lane & 15)) * 128));
+      } else {
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(blk + lane * 128));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(blk + 4096 + lane * 128));
+      }
     };
     constexpr int PF_H = 2;
     load_h(0);
@@ -547,9 +572,9 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
 #pragma unroll 1
     for (int j = 0; j < nch; ++j) {
       if (j + PF_H < nch && c0 < pr.N) prefetch_h(j + PF_H);
-      float gv[4][8], uv[4][8], w[4];
+      float gv[KR][8], uv[KR][8], w[KR];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < KR; ++k) {
         gv[k][0] = gn[k][0].x; gv[k][1] = gn[k][0].y; gv[k][2] = gn[k][0].z; gv[k][3] = gn[k][0].w;
         gv[k][4] = gn[k][1].x; gv[k][5] = gn[k][1].y; gv[k][6] = gn[k][1].z; gv[k][7] = gn[k][1].w;
         uv[k][0] = un[k][0].x; uv[k][1] = un[k][0].y; uv[k][2] = un[k][0].z; uv[k][3] = un[k][0].w;
@@ -557,18 +582,12 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
         w[k] = wn[k];
       }
       if (j + 1 < nch) load_h(j + 1);
-      uint32_t r[32];
-      tmem_ld32(taddr + j * 32, r);
-      tmem_ld_wait();
-      float Gv[4][8];
-      xwrite_t(own, lane, r);
-      __syncwarp();
-      xread(own, lane, Gv);
-      __syncwarp();
-      float dwp[4];
+      float Gv[KR][8];
+      load_chunk(j, Gv);
+      float dwp[KR];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int64_t row = ti.row0 + 32 * j + (lane >> 2) + 8 * k;
+      for (int k = 0; k < KR; ++k) {
+        const int64_t row = ti.row0 + 32 * j + hoff + (lane >> 2) + 8 * k;
         float dg[8], du[8], wa[8];
         dwp[k] = 0.0f;
 #pragma unroll
@@ -594,14 +613,14 @@ __device__ __forceinline__ void epilogue_tile(const Prob& pr, const TileInfo& ti
       // one partial per (row, 32-column block): the four lanes of a row add
       // theirs in a fixed tree, the combine sums the blocks in order
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < KR; ++k) {
         dwp[k] += __shfl_xor_sync(0xffffffffu, dwp[k], 1);
         dwp[k] += __shfl_xor_sync(0xffffffffu, dwp[k], 2);
       }
       if (cg == 0 && c0 < pr.N) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int64_t row = ti.row0 + 32 * j + (lane >> 2) + 8 * k;
+        for (int k = 0; k < KR; ++k) {
+          const int64_t row = ti.row0 + 32 * j + hoff + (lane >> 2) + 8 * k;
           static_cast<float*>(pr.out3)[row * pr.ld_out3 + c0 / 32] = dwp[k];
         }
       }
@@ -764,10 +783,13 @@ __device__ __noinline__ void combine_tile(const Prob& pr, const TileInfo& ti, in
   } else {                        \
     F<C1, PAIR>(__VA_ARGS__);     \
   }
-template <bool PAIR, bool SMALL, class C0, class C1>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <bool PAIR, bool SMALL, int EW, class C0, class C1>
+__global__ void __launch_bounds__(gmm_threads(EW), 1)
     gmm_kernel(const __grid_constant__ Params P, const __grid_constant__ Maps maps) {
   static_assert(!(PAIR && SMALL), "small token blocks run on single CTAs");
+  static_assert(EW == 4 || EW == 8, "epilogue warps");
+  static_assert(EW * XBUF_HALF <= EPI_WARPS * XBUF_BYTES, "transposition buffers");
+  constexpr int SCHED_WARP = 2 + EW;
   constexpr int NST = PAIR ? PAIR_STAGES : (SMALL ? SMALL_STAGES : STAGES);
   constexpr int SBYTES = PAIR ? PAIR_STAGE_BYTES : (SMALL ? SMALL_STAGE_BYTES : STAGE_BYTES);
   extern __shared__ uint8_t smem_raw[];
@@ -807,13 +829,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], PAIR ? 2 * EPI_WARPS : EPI_WARPS);
+      mbar_init(&tempty[a], PAIR ? 2 * EW : EW);
     }
     for (int i = 0; i < TI_DEPTH; ++i) {
       mbar_init(&ti_full[i], 1);
       // consumers: TMA producer, MMA issuer, epilogue warps (+ the odd CTA's
       // producer and epilogue warps in a pair)
-      mbar_init(&ti_empty[i], PAIR ? 2 * (1 + EPI_WARPS) + 1 : 2 + EPI_WARPS);
+      mbar_init(&ti_empty[i], PAIR ? 2 * (1 + EW) + 1 : 2 + EW);
     }
     mbar_init(mma_done, 1);
     for (int i = 0; i < 2; ++i) {
@@ -1045,11 +1067,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         umma_commit(mma_done);
       drain_wait(mma_done, 0, P.budget_ns);
     }
-  } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
+  } else if (warp >= 2 && warp < 2 + EW) {
     // ------------------------------------------------------------- epilogue
     EpiState es;
     es.q = warp & 3;
     es.lane = lane;
+    es.hoff = EW == 8 ? 16 * ((warp - 2) >> 2) : 0;
+    es.own = EW == 8 ? xbufs + (warp - 2) * (XBUF_HALF / 4) : xbufs + es.q * (XBUF_BYTES / 4);
     es.xbufs = xbufs;
     es.xfull = xfull;
     es.xfree = xfree;
@@ -1086,7 +1110,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (rec) rec[6] = globaltimer_ns();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(es.q * 32) << 16) + acc * NT;
       bool eok = true;
-      HMM_BY_PROB(ti.prob, epilogue_tile, pr, ti, taddr, rank, es, wc, eok);
+      if ((ti.prob & 1) == 0)
+        epilogue_tile<C0, EW>(pr, ti, taddr, rank, es, wc, eok);
+      else
+        epilogue_tile<C1, EW>(pr, ti, taddr, rank, es, wc, eok);
       if (!eok) break;
       tc_fence_before();
       __syncwarp();
@@ -1167,14 +1194,15 @@ int map_w(const GemmEnv& env, CUtensorMap* m, const void* base, int64_t E, int64
   return encode(env, m, base, 3, dims, str, box);
 }
 
-template <bool PAIR, bool SMALL, class C0, class C1>
+template <bool PAIR, bool SMALL, int EW, class C0, class C1>
 int launch(const GemmEnv& env, Params& P, const Maps& maps, int64_t max_tiles, int kind) {
   if (max_tiles <= 0 || P.nprob == 0) return HMM_OK;
   if (env.trace && env.trace_which == kind) {
     P.trace = env.trace;
     P.trace_cap = env.trace_cap;
   }
-  auto kern = gmm_kernel<PAIR, SMALL, C0, C1>;
+  auto kern = gmm_kernel<PAIR, SMALL, EW, C0, C1>;
+  constexpr int NUM_THREADS = gmm_threads(EW);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
       cudaSuccess)
     return HMM_ERR_CUDA;
@@ -1225,6 +1253,9 @@ using CfgGmm1 = Cfg<EPI_SWIGLU, true>;     // tokens x_perm, weights W1 (MN-majo
 using CfgGmm2 = Cfg<EPI_STORE, true>;      // tokens a, weights W2 (MN-major)
 using CfgActGrad = Cfg<EPI_DSWIGLU, false>; // tokens dy_perm, weights W2 rows (K-major)
 using CfgInGrad = Cfg<EPI_STORE, false>;   // tokens dH, weights W1 rows (K-major)
+// epilogue warps of the data-gradient launch: two per TMEM lane quarter, so
+// every SM sub-partition holds two SwiGLU-grad epilogue warps
+constexpr int DATA_EW = 8;
 
 namespace {
 
@@ -1329,9 +1360,9 @@ int launch_forward_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs
   }
   if (p.shared) add_shared(P, maps, static_cast<int>(E), s0, s1);
   const int64_t max_tiles = (p.R / TROWS) * (g1.n_tiles + g2.n_tiles);
-  if (env.pair_rows) return launch<true, false, CfgGmm1, CfgGmm2>(env, P, maps, max_tiles, 0);
-  if (env.small_rows) return launch<false, true, CfgGmm1, CfgGmm2>(env, P, maps, max_tiles, 0);
-  return launch<false, false, CfgGmm1, CfgGmm2>(env, P, maps, max_tiles, 0);
+  if (env.pair_rows) return launch<true, false, 4, CfgGmm1, CfgGmm2>(env, P, maps, max_tiles, 0);
+  if (env.small_rows) return launch<false, true, 4, CfgGmm1, CfgGmm2>(env, P, maps, max_tiles, 0);
+  return launch<false, false, 4, CfgGmm1, CfgGmm2>(env, P, maps, max_tiles, 0);
 }
 
 int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPtrs c,
@@ -1392,15 +1423,15 @@ int launch_data_grad_gemms(const GemmEnv& env, const Plan& p, MetaPtrs m, CtrlPt
   ig.e_lo = 0;
   ig.e_hi = static_cast<int>(E);
   ig.wait_m = c.ready;
-  ig.wait_unit = EPI_WARPS * ncta * ag.n_tiles;
+  ig.wait_unit = DATA_EW * ncta * ag.n_tiles;  // every epilogue warp of every act_grad tile
   ig.lag = static_cast<int>(p.Ex);  // input-grad after every act_grad tile is handed out
   if (p.shared) add_shared(P, maps, static_cast<int>(E), s0, s1);
   const int64_t data_tiles = (p.R / TROWS) * (ag.n_tiles + ig.n_tiles);
   if (env.pair_rows)
-    return launch<true, false, CfgActGrad, CfgInGrad>(env, P, maps, data_tiles, 1);
+    return launch<true, false, DATA_EW, CfgActGrad, CfgInGrad>(env, P, maps, data_tiles, 1);
   if (env.small_rows)
-    return launch<false, true, CfgActGrad, CfgInGrad>(env, P, maps, data_tiles, 1);
-  return launch<false, false, CfgActGrad, CfgInGrad>(env, P, maps, data_tiles, 1);
+    return launch<false, true, DATA_EW, CfgActGrad, CfgInGrad>(env, P, maps, data_tiles, 1);
+  return launch<false, false, DATA_EW, CfgActGrad, CfgInGrad>(env, P, maps, data_tiles, 1);
 }
 
 }  // namespace hmm
