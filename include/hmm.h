@@ -50,6 +50,12 @@
  *   receives no token are written as exact zeros).
  * - A context may be used from one host thread at a time.  Concurrent calls
  *   on different streams need distinct workspace and saved buffers.
+ * - hmm_route, hmm_forward*, hmm_backward* can be captured into a CUDA graph
+ *   on `stream` and replayed (the pointers and shape are fixed in the graph;
+ *   the inputs may change in place between replays): they allocate nothing,
+ *   reset their own counters in every call, and the backward's second stream
+ *   joins the capture through its fork and join events.  HMM_OPT_VALIDATE
+ *   (a host synchronisation) and HMM_OPT_PROFILE must be off while capturing.
  */
 #ifndef HMM_H_
 #define HMM_H_
