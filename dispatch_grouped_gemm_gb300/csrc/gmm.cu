@@ -61,7 +61,6 @@ enum Epi : int { EPI_SWIGLU = 0, EPI_STORE = 1, EPI_DSWIGLU = 2 };
 // accumulator columns) and the granularity of a token block's end.
 constexpr int BW = 128;
 constexpr int NT = 256;
-constexpr int TROWS = 64;  // also the weight-gradient GEMMs' K block: rows they read are written
 
 // EPI: epilogue; W_MN: weights MN-major (forward), else K-major (data
 // gradients).  Token rows are K-major.  IDESC / IDESC2: instruction

@@ -48,6 +48,7 @@ namespace {
 // 24 KB stages of 32 rows made the launch 23 % slower than four of 64: more,
 // smaller copies and barrier round trips per byte.
 constexpr int PK = 64;
+static_assert(PK == TROWS, "K blocks end where the zeroed padding rows end");
 constexpr int PSTAGES = 4 * 64 / PK;
 constexpr int PA_BYTES = 128 * PK * 2;  // this CTA's 128 rows of A, PK deep (bf16)
 constexpr int PB_BYTES = 128 * PK * 2;  // this CTA's 128 columns of B, PK deep (bf16)

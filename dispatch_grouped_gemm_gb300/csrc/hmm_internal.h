@@ -16,6 +16,10 @@ namespace hmm {
 // zero (x_perm, dy_perm) or computed from zeros (a, h, dH, w*a).
 constexpr int BM = 128;
 constexpr int BK = 64;    // K per pipeline stage (one 128-byte swizzle row of bf16)
+// Token blocks of the row-mode GEMMs end at the first multiple of TROWS at or
+// past an expert's last row, and so do the weight gradients' K blocks: the
+// padding rows up to there are the only ones any kernel reads.
+constexpr int TROWS = 64;
 constexpr int RCHUNK = 1024;  // slots per routing warp-chunk
 constexpr int RWARPS = 8;     // warps per routing block
 constexpr int MAX_E = 1024;   // experts supported (routing keeps per-expert counters in smem)

@@ -11,6 +11,8 @@
 // All row traffic uses 16-byte vectors (H is a multiple of 8 bf16).
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "hmm_internal.h"
 #include "ptx.cuh"
 
@@ -73,18 +75,27 @@ constexpr int DISPATCH_UNROLL = 8;  // dispatch: a whole 2048-wide row per pass
 }  // namespace
 
 // Dispatch: token t's row of src goes to the padded rows of its K slots and,
-// with the shared expert (E < Ex), to the shared expert's row poff[E] + t; the
-// warps past T zero the padding rows of each expert (so every padded row of
-// the GEMM operands is defined).  Optionally also scatters the routing weight
+// with the shared expert (E < Ex), to the shared expert's row poff[E] + t.
+// The warps past T (launched when training) zero each expert's padding rows up
+// to the first multiple of TROWS = 64 at or past its last row: the GEMMs'
+// token blocks and the weight gradients' K blocks end there, so those rows
+// are read and must be zero (the weight gradients sum over them), while the
+// rows past it are never read.  In inference no padding row is written: the
+// forward GEMMs compute outputs for the padding rows of a block, which no
+// one reads.  Optionally also scatters the routing weight
 // of every slot to its padded row (wperm: 1 on the shared rows, 0 on padding
 // rows), and writes an fp8 copy of every row (dst8, ld8 8-byte groups per
 // row; E5M2: e5m2, else e4m3), the weight-gradient GEMMs' operand for the
 // low parts of their split operand.
+//   spw: slots per warp.  A warp copies the row of one token to spw of its
+// slots (K, plus the shared expert's row): with all of them (large T) the row
+// is read once; with one (few tokens, e.g. decode) K times as many warps share
+// the writes, the repeated reads hit L2.
 template <bool E5M2>
 __global__ void __launch_bounds__(MOVE_THREADS) dispatch_rows_kernel(
     const uint4* __restrict__ src, int64_t T, int64_t K, int64_t H8, MetaPtrs m, int E, int Ex,
     uint4* __restrict__ dst, uint2* __restrict__ dst8, int64_t ld8, const void* w, int w_dtype,
-    float* wperm, int32_t* zero_ptr, int64_t zero_count) {
+    float* wperm, int32_t* zero_ptr, int64_t zero_count, int spw) {
   const int lane = threadIdx.x & 31;
   const int64_t g = static_cast<int64_t>(blockIdx.x) * MOVE_WARPS + (threadIdx.x >> 5);
   grid_dep_wait();
@@ -94,17 +105,23 @@ __global__ void __launch_bounds__(MOVE_THREADS) dispatch_rows_kernel(
          i < zero_count; i += static_cast<int64_t>(gridDim.x) * MOVE_THREADS)
       zero_ptr[i] = 0;
   }
-  if (g < T) {
+  const int64_t KS = K + (E < Ex ? 1 : 0);
+  const int64_t G = (KS + spw - 1) / spw;  // warps per token
+  if (g < T * G) {
+    const int64_t t = g / G;
+    const int k0 = static_cast<int>(g % G) * spw;
+    const int k1 = min(static_cast<int>(KS), k0 + spw);
+    const bool mine = lane >= k0 && lane < k1;
     int32_t prow_l = -1;
-    if (lane < K) prow_l = m.slot2prow[g * K + lane];
-    if (wperm && lane < K && prow_l >= 0) wperm[prow_l] = ld_weight(w, g * K + lane, w_dtype);
+    if (mine && lane < K) prow_l = m.slot2prow[t * K + lane];
+    if (wperm && mine && lane < K && prow_l >= 0)
+      wperm[prow_l] = ld_weight(w, t * K + lane, w_dtype);
     // the shared expert's row of this token, handled as slot K
-    if (E < Ex && lane == K) {
-      prow_l = m.poff[E] + static_cast<int32_t>(g);
+    if (E < Ex && lane == K && mine) {
+      prow_l = m.poff[E] + static_cast<int32_t>(t);
       if (wperm) wperm[prow_l] = 1.0f;
     }
-    const int64_t KS = K + (E < Ex ? 1 : 0);
-    const uint4* s = src + g * H8;
+    const uint4* s = src + t * H8;
     // every lane runs every iteration (the shuffles below read other lanes'
     // slots); only the loads and stores are guarded
     for (int64_t c0 = lane; c0 - lane < H8; c0 += 32 * DISPATCH_UNROLL) {
@@ -114,7 +131,7 @@ __global__ void __launch_bounds__(MOVE_THREADS) dispatch_rows_kernel(
         const int64_t c = c0 + 32 * u;
         if (c < H8) v[u] = s[c];
       }
-      for (int k = 0; k < KS; ++k) {
+      for (int k = k0; k < k1; ++k) {
         const int32_t prow = __shfl_sync(0xffffffffu, prow_l, k);
         if (prow < 0) continue;
         uint4* d = dst + static_cast<int64_t>(prow) * H8;
@@ -134,11 +151,13 @@ __global__ void __launch_bounds__(MOVE_THREADS) dispatch_rows_kernel(
       }
     }
   } else {
-    const int64_t q = g - T;
-    const int64_t e = q / BM;
+    const int64_t q = g - T * G;
+    const int64_t e = q / TROWS;
     if (e >= Ex) return;
-    const int32_t row = m.poff[e] + m.counts[e] + static_cast<int32_t>(q % BM);
-    if (row >= m.poff[e + 1]) return;
+    const int32_t cnt = m.counts[e];
+    const int32_t pad = (cnt + TROWS - 1) / TROWS * TROWS - cnt;
+    if (q % TROWS >= pad) return;
+    const int32_t row = m.poff[e] + cnt + static_cast<int32_t>(q % TROWS);
     if (wperm && lane == 0) wperm[row] = 0.0f;
     uint4* d = dst + static_cast<int64_t>(row) * H8;
     const uint4 z = make_uint4(0, 0, 0, 0);
@@ -176,6 +195,9 @@ __device__ __forceinline__ void acc_group(float (&acc)[8], const void* rows, int
 // With dwp != null (backward) lane k also writes
 //   d_topk_weights[t,k] = sum over the act_grad N tiles of the per-row
 //   partial dot products <G_s, a_s> (fixed order).
+//   The grid's y dimension splits each token's row over several warps, each
+// taking every gridDim.y-th group of 32 * UNROLL vectors (1 for large T;
+// several for a few tokens, e.g. decode, so that enough rows are in flight).
 template <bool WEIGHTED, bool F32>
 __global__ void __launch_bounds__(MOVE_THREADS) combine_rows_kernel(
     const void* __restrict__ rows, const void* w, int w_dtype, int64_t T, int64_t K, int64_t H8,
@@ -183,6 +205,8 @@ __global__ void __launch_bounds__(MOVE_THREADS) combine_rows_kernel(
     const float* dwp, int64_t dwp_ld, void* dw) {
   const int lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * MOVE_WARPS + (threadIdx.x >> 5);
+  const int part = static_cast<int>(blockIdx.y);
+  const int parts = static_cast<int>(gridDim.y);
   grid_dep_wait();
   grid_dep_launch();
   if (t >= T) return;
@@ -192,7 +216,7 @@ __global__ void __launch_bounds__(MOVE_THREADS) combine_rows_kernel(
     prow_l = slot2prow[t * K + lane];
     w_l = WEIGHTED ? ld_weight(w, t * K + lane, w_dtype) : 1.0f;
   }
-  if (dwp && lane < K) {
+  if (dwp && part == 0 && lane < K) {
     float d = 0.0f;
     if (prow_l >= 0)
       for (int64_t j = 0; j < dwp_ld; ++j) d += dwp[static_cast<int64_t>(prow_l) * dwp_ld + j];
@@ -202,7 +226,8 @@ __global__ void __launch_bounds__(MOVE_THREADS) combine_rows_kernel(
   const int64_t srow = shared_row0 ? *shared_row0 + t : -1;
   // every lane runs every iteration (the shuffles below read other lanes'
   // slots); only the loads and stores are guarded
-  for (int64_t c0 = lane; c0 - lane < H8; c0 += 32 * UNROLL) {
+  for (int64_t c0 = lane + static_cast<int64_t>(part) * 32 * UNROLL; c0 - lane < H8;
+       c0 += static_cast<int64_t>(parts) * 32 * UNROLL) {
     float acc[UNROLL][8];
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u)
@@ -237,34 +262,54 @@ static int move_grid(int64_t warps) {
   return static_cast<int>((warps + MOVE_WARPS - 1) / MOVE_WARPS);
 }
 
+// Below this many tokens a warp per token leaves too few rows in flight to
+// keep HBM busy: the dispatch gives each slot its own warp, the combine
+// splits each token's row over several warps.
+constexpr int64_t FEW_TOKENS = 1024;
+static int dispatch_spw(const Plan& p) {
+  return p.T >= FEW_TOKENS ? static_cast<int>(p.K + p.shared) : 1;
+}
+static int64_t dispatch_token_warps(const Plan& p) {
+  const int64_t ks = p.K + p.shared, spw = dispatch_spw(p);
+  return p.T * ((ks + spw - 1) / spw);
+}
+static int combine_parts(const Plan& p) {
+  if (p.T >= FEW_TOKENS) return 1;
+  const int64_t groups = (p.H / 8 + 32 * UNROLL - 1) / (32 * UNROLL);
+  return static_cast<int>(std::min<int64_t>(groups, 8));
+}
+
 cudaError_t launch_dispatch_x(const Plan& p, const void* x, MetaPtrs m, void* x_perm, void* x8,
                               int32_t* zero_ptr, int64_t zero_count, cudaStream_t st, bool pdl) {
-  const int64_t warps = p.T + p.Ex * BM;
+  // padding warps only when training (x8: the weight gradients will read them)
+  const int64_t warps = dispatch_token_warps(p) + (x8 ? p.Ex * TROWS : 0);
   return launch_kernel(dispatch_rows_kernel<false>, move_grid(warps), MOVE_THREADS, 0, st, pdl, 1,
                        static_cast<const uint4*>(x), p.T, p.K, p.H / 8, m, static_cast<int>(p.E),
                        static_cast<int>(p.Ex), static_cast<uint4*>(x_perm),
                        static_cast<uint2*>(x8), p.ld8_h / 8, nullptr, 0, nullptr, zero_ptr,
-                       zero_count);
+                       zero_count, dispatch_spw(p));
 }
 
 cudaError_t launch_dispatch_dy(const Plan& p, const void* dy, const void* w, int w_dtype,
                                MetaPtrs m, CtrlPtrs c, void* dy_perm, void* dy8, float* wperm,
                                cudaStream_t st, bool pdl) {
-  const int64_t warps = p.T + p.Ex * BM;
+  const int64_t warps = dispatch_token_warps(p) + p.Ex * TROWS;
   // also zero the backward launch counters (tickets and per-token-block ready
   // counters are contiguous in the control block)
   const int64_t nzero = p.ctrl_zero_count;
   return launch_kernel(dispatch_rows_kernel<true>, move_grid(warps), MOVE_THREADS, 0, st, pdl, 1,
                        static_cast<const uint4*>(dy), p.T, p.K, p.H / 8, m, static_cast<int>(p.E),
                        static_cast<int>(p.Ex), static_cast<uint4*>(dy_perm),
-                       static_cast<uint2*>(dy8), p.ld8_h / 8, w, w_dtype, wperm, c.tickets, nzero);
+                       static_cast<uint2*>(dy8), p.ld8_h / 8, w, w_dtype, wperm, c.tickets, nzero,
+                       dispatch_spw(p));
 }
 
 cudaError_t launch_combine_y(const Plan& p, const void* o, const void* w, int w_dtype, MetaPtrs m,
                              void* y, cudaStream_t st, bool pdl) {
   auto kern = p.shared ? combine_rows_kernel<true, true> : combine_rows_kernel<true, false>;
-  return launch_kernel(kern, move_grid(p.T), MOVE_THREADS, 0, st, pdl, 1, o, w, w_dtype, p.T, p.K,
-                       p.H / 8, static_cast<const int32_t*>(m.slot2prow),
+  const dim3 grid(move_grid(p.T), combine_parts(p));
+  return launch_kernel(kern, grid, MOVE_THREADS, 0, st, pdl, 1, o, w, w_dtype,
+                       p.T, p.K, p.H / 8, static_cast<const int32_t*>(m.slot2prow),
                        static_cast<const int32_t*>(p.shared ? m.poff + p.E : nullptr),
                        static_cast<uint4*>(y), static_cast<const float*>(nullptr), int64_t(0),
                        static_cast<void*>(nullptr));
@@ -273,7 +318,8 @@ cudaError_t launch_combine_y(const Plan& p, const void* o, const void* w, int w_
 cudaError_t launch_combine_dx(const Plan& p, const void* dx_perm, const float* dwp, MetaPtrs m,
                               void* dx, void* dw, int w_dtype, cudaStream_t st, bool pdl) {
   auto kern = p.shared ? combine_rows_kernel<false, true> : combine_rows_kernel<false, false>;
-  return launch_kernel(kern, move_grid(p.T), MOVE_THREADS, 0, st, pdl, 1, dx_perm,
+  const dim3 grid(move_grid(p.T), combine_parts(p));
+  return launch_kernel(kern, grid, MOVE_THREADS, 0, st, pdl, 1, dx_perm,
                        static_cast<const void*>(nullptr), w_dtype, p.T, p.K, p.H / 8,
                        static_cast<const int32_t*>(m.slot2prow),
                        static_cast<const int32_t*>(p.shared ? m.poff + p.E : nullptr),

@@ -83,3 +83,44 @@ def test_fp32_weights_with_shared_expert(run):
     gu.check("d_shared_up_proj_weight", gu.f64(dWs1), sdW1)
     gu.check("d_shared_down_proj_weight", gu.f64(dWs2), sdW2)
     assert run.status() == (0, 0)
+
+
+@pytest.mark.parametrize("pair_rows", [0, 1, 3], ids=["cta", "pair", "small"])
+@pytest.mark.parametrize("case", ["multi_tile", "empty_and_hot", "one_token", "duplicates"])
+def test_buffers_full_of_nan_bytes(run, case, pair_rows):
+    """Workspace and `saved` filled with 0xFF bytes (NaN as bf16 and fp32)
+    before every call: the kernels write every byte they later read (the
+    padding rows up to each expert's last 64-row block when training, none in
+    inference), so the outputs match the oracle and stay finite."""
+    from tests.test_gpu_parity import SCEN
+    p = dict(SCEN)[case]
+    d = gu.upload(p)
+    h = run.ctx.handle
+    hmm.hmm_set_option(h, hmm.HMM_OPT_PAIR_ROWS, pair_rows)
+    try:
+        sh = run.shape(d)
+        dev = gu.dev()
+        ref_y = oracle.forward(p.x, p.ids, p.w, p.W1, p.W2)
+        for training in (False, True):
+            fwd, sv, bwd = hmm.hmm_workspace_size(sh, training)
+            ws = torch.full((max(fwd, 16),), 255, dtype=torch.uint8, device=dev)
+            saved = torch.full((max(sv, 16),), 255, dtype=torch.uint8, device=dev) if training else None
+            y = torch.empty_like(d.x)
+            hmm.hmm_forward(h, sh, d.x, d.ids, d.w, d.W1, d.W2, y, saved, ws)
+            torch.cuda.synchronize()
+            gu.check(f"y (training={training})", gu.f64(y), ref_y)
+        wsb = torch.full((bwd,), 255, dtype=torch.uint8, device=dev)
+        dx = torch.empty_like(d.x)
+        dW1 = torch.full_like(d.W1, float("nan"))
+        dW2 = torch.full_like(d.W2, float("nan"))
+        dw = torch.empty_like(d.w)
+        hmm.hmm_backward(h, sh, d.dy, d.w, d.W1, d.W2, saved, dx, dW1, dW2, dw, wsb)
+        torch.cuda.synchronize()
+        rdx, rdW1, rdW2, rdw = oracle.backward(p.x, p.ids, p.w, p.W1, p.W2, p.dy)
+        gu.check("dx", gu.f64(dx), rdx)
+        gu.check("d_up_proj_weight", gu.f64(dW1), rdW1)
+        gu.check("d_down_proj_weight", gu.f64(dW2), rdW2)
+        gu.check("d_topk_weights", gu.f64(dw), rdw)
+        assert run.status() == (0, 0)
+    finally:
+        hmm.hmm_set_option(h, hmm.HMM_OPT_PAIR_ROWS, 2)
