@@ -199,7 +199,7 @@ __device__ __forceinline__ void acc_group(float (&acc)[8], const void* rows, int
 // taking every gridDim.y-th group of 32 * UNROLL vectors (1 for large T;
 // several for a few tokens, e.g. decode, so that enough rows are in flight).
 template <bool WEIGHTED, bool F32>
-__global__ void __launch_bounds__(MOVE_THREADS) combine_rows_kernel(
+__global__ void __launch_bounds__(MOVE_THREADS, F32 ? 2 : 4) combine_rows_kernel(
     const void* __restrict__ rows, const void* w, int w_dtype, int64_t T, int64_t K, int64_t H8,
     const int32_t* __restrict__ slot2prow, const int32_t* shared_row0, uint4* __restrict__ out,
     const float* dwp, int64_t dwp_ld, void* dw) {
