@@ -10,6 +10,10 @@ elementwise within |gpu - ref| <= 1e-2 + 2e-2 |ref|
 [HyperMegaMoE §7.1, §7.2: shapes, dtypes and routings beyond the named
 configurations, each against the reference].
 
+A second set (test_random_large_shape_matches_oracle) draws larger shapes: H
+up to 1024 and I up to 768, so every tiling runs several weight tiles along
+the MMA's M side and several token blocks per expert.
+
 The family is that of the five workloads (K >= 2, I >= 64).  Outside it the
 16-bit storage the bound allows for can exceed the bound by itself: with
 I = 24 and the shared expert one y element came out at 1.14x (fp64 with only
@@ -38,13 +42,21 @@ def run():
     return gu.Runner()
 
 
-def _case(i):
-    r = np.random.default_rng(9000 + i)
-    T = int(r.integers(1, 901))
-    H = 8 * int(r.integers(1, 65))
-    I = 8 * int(r.integers(8, 49))
-    E = int(r.integers(1, 49))
-    K = int(r.integers(2, 9))
+def _case(i, large=False):
+    seed = (9500 if large else 9000) + i
+    r = np.random.default_rng(seed)
+    if large:
+        T = int(r.integers(300, 1201))
+        H = 8 * int(r.integers(64, 129))
+        I = 8 * int(r.integers(48, 97))
+        E = int(r.integers(2, 25))
+        K = int(r.integers(2, 7))
+    else:
+        T = int(r.integers(1, 901))
+        H = 8 * int(r.integers(1, 65))
+        I = 8 * int(r.integers(8, 49))
+        E = int(r.integers(1, 49))
+        K = int(r.integers(2, 9))
     repeats = K > E or r.random() < 0.5
     if repeats:
         # a random subset of the experts is used (others stay empty), repeats allowed
@@ -52,7 +64,7 @@ def _case(i):
         ids = used[r.integers(0, used.size, size=(T, K))].astype(np.int32)
     else:
         ids = None
-    p = gu.problem(T, H, I, E, K, seed=9000 + i, ids=ids)
+    p = gu.problem(T, H, I, E, K, seed=seed, ids=ids)
     if ids is not None:
         lg = r.standard_normal((T, K)).astype(np.float32)
         ex = np.exp(lg - lg.max(axis=1, keepdims=True))
@@ -61,20 +73,31 @@ def _case(i):
     mode = [0, 1, 3][i % 3]
     shared = K < 32 and r.random() < 0.25
     if shared:
-        p.Ws1 = mi.normal_bf16(mi._rng(9000 + i, 8), (H, 2 * I), 1.0 / np.sqrt(H))
-        p.Ws2 = mi.normal_bf16(mi._rng(9000 + i, 9), (I, H), 1.0 / np.sqrt(I))
+        p.Ws1 = mi.normal_bf16(mi._rng(seed, 8), (H, 2 * I), 1.0 / np.sqrt(H))
+        p.Ws2 = mi.normal_bf16(mi._rng(seed, 9), (I, H), 1.0 / np.sqrt(I))
     return p, wdt, mode, shared
 
 
-def _id(i):
-    p, wdt, mode, shared = _case(i)
+N_LARGE = 18
+
+
+def _id(i, large=False):
+    p, wdt, mode, shared = _case(i, large)
     return (f"{i}-T{p.T}-H{p.H}-I{p.I}-E{p.E}-K{p.K}-{wdt}-{['cta', 'pair', '', 'small'][mode]}"
             + ("-shared" if shared else ""))
 
 
 @pytest.mark.parametrize("i", range(N_CASES), ids=_id)
 def test_random_shape_matches_oracle(run, i):
-    p, wdt, mode, shared = _case(i)
+    _check(run, *_case(i))
+
+
+@pytest.mark.parametrize("i", range(N_LARGE), ids=lambda i: _id(i, True))
+def test_random_large_shape_matches_oracle(run, i):
+    _check(run, *_case(i, True))
+
+
+def _check(run, p, wdt, mode, shared):
     d = gu.upload(p, weights_dtype=wdt)
     c = run.ctx
     hmm.hmm_set_option(c.handle, hmm.HMM_OPT_PAIR_ROWS, mode)
