@@ -59,6 +59,15 @@ MUTANTS = [
     ("shared expert's dWs2 with a transposed output",
      "dWs2[j * H + c] += aj * ld(dy, t * H + c, dt);",
      "dWs2[c * I + j] += aj * ld(dy, t * H + c, dt);"),
+    ("up_proj rows read with the stride of I",
+     "int64_t row = w1_off + i * 2 * I;",
+     "int64_t row = w1_off + i * I;"),
+    ("act_grad without the routing weight",
+     "acc += dO[c] * ld(W2, row + c, dt);",
+     "acc += ld(dy, dy_off + c, dt) * ld(W2, row + c, dt);"),
+    ("weight gradients with slot s read as token s mod T",
+     "int64_t s = slots[r], t = s / K;",
+     "int64_t s = slots[r], t = s % T;"),
 ]
 
 
